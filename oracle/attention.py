@@ -1,0 +1,67 @@
+"""Masked and segment-batch attention in float64 (test infrastructure only).
+
+[AKV-blog] section 2 "The Drop Primitive": attention over a cache with dropped
+tokens is softmax(Q K^T / sqrt(d_k) + M) V with M = -inf on dropped columns and
+0 elsewhere.  [AKV-notes] section 3 "Segment-Batch Attention": each segment of
+queries selects its KV pages and runs standard causal attention over them.
+
+Readings fixed here: the softmax scale is an explicit argument (1/sqrt(d_k) is
+the usual value); inside a segment the causal rule is aligned bottom-right, so
+the segment's own q_len new tokens are its last q_len KV entries and query row
+i (0-based) sees entries j <= kv_len - q_len + i.  A row that sees nothing gets
+o = 0 and lse = -inf.
+"""
+import numpy as np
+
+
+def masked_attention(q, k, v, visible, scale):
+    """Dense masked attention for one head.
+
+    q [n, d], k [N, d], v [N, dv], visible [n, N] bool -> (o [n, dv], lse [n]),
+    lse the natural-log sum of exp(scale * q.k) over the visible columns.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    s = scale * (q @ k.T)
+    s = np.where(visible, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    empty = ~np.isfinite(m[:, 0])
+    m = np.where(np.isfinite(m), m, 0.0)
+    p = np.exp(s - m)
+    l = p.sum(axis=1)
+    o = (p @ v) / np.where(empty, 1.0, l)[:, None]
+    o[empty] = 0.0
+    with np.errstate(divide="ignore"):
+        lse = m[:, 0] + np.log(l)
+    lse[empty] = -np.inf
+    return o, lse
+
+
+def causal_visibility(q_len, kv_len):
+    """Bottom-right causal mask [q_len, kv_len]: row i sees j <= kv_len - q_len + i."""
+    i = np.arange(q_len)[:, None]
+    j = np.arange(kv_len)[None, :]
+    return j <= (kv_len - q_len + i)
+
+
+def segment_attention(q, k, v, scale, rows=None):
+    """Causal attention of one segment over its own KV entry list, all heads.
+
+    q [q_len, Hq, d], k [kv_len, Hkv, d], v [kv_len, Hkv, dv]; query head h reads
+    kv head h // (Hq / Hkv) (grouped-query attention).  rows: optional subset of
+    query rows to evaluate (each against the full visible list).
+    Returns o [len(rows), Hq, dv], lse [len(rows), Hq].
+    """
+    q_len, hq, _ = q.shape
+    kv_len, hkv, _ = k.shape
+    if hq % hkv:
+        raise ValueError("query heads must be a multiple of kv heads")
+    group = hq // hkv
+    rows = np.arange(q_len) if rows is None else np.asarray(rows)
+    vis = causal_visibility(q_len, kv_len)[rows]
+    o = np.empty((len(rows), hq, v.shape[-1]))
+    lse = np.empty((len(rows), hq))
+    for h in range(hq):
+        o[:, h], lse[:, h] = masked_attention(q[rows, h], k[:, h // group], v[:, h // group], vis, scale)
+    return o, lse

@@ -1,0 +1,90 @@
+// Internal interface between the host engine (engine.cpp) and the CUDA
+// kernels.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace akv {
+
+// Device error word, written by kernels with atomicCAS from 0 so the first
+// failure wins.  code is an akv_status value; info holds where it happened.
+struct DevErr {
+  int32_t code;
+  int32_t info[3];
+};
+
+// One flush run: rows [lo, hi) of K page src are rotated by the shift whose
+// (cos, sin) table row is didx and written to the same rows of page dst
+// (dst == src: in place; dst != src: copy-on-write).
+struct RunDesc {
+  int32_t src;
+  int32_t dst;
+  int32_t lohi;  // lo | hi << 16
+  int32_t didx;
+};
+
+// One attention run: rows [lo, hi) of K page kp / V page vp hold the
+// segment's entries es .. es + (hi - lo) - 1.
+struct AttnRun {
+  int32_t kp;
+  int32_t vp;
+  int32_t lohi;  // lo | hi << 16
+  int32_t es;
+};
+
+struct AttnSeg {
+  int32_t run_off;  // first run in the run table
+  int32_t n_runs;
+  int32_t kv_len;
+  int32_t q_len;
+  int32_t q_row0;
+  int32_t pad[3];
+};
+
+// One CTA's work: query tile qt of segment seg for kv head kvh, covering
+// n_tiles KV tiles (the causal limit of the tile's last row).
+struct AttnWork {
+  int32_t seg;
+  int32_t kvh;
+  int32_t qt;
+  int32_t n_tiles;
+};
+
+struct AttnParams {
+  CUtensorMap q_map;  // Q [n_q_rows][Hq][d_qk], box {64, G, 128/G}
+  CUtensorMap k_map;  // rotated pool, [L*P][H][page][d_rot], box {64, page, 1, 1}
+  CUtensorMap v_map;  // value pool,  [L*P][H][page][d_v],   box {64, page, 1, 1}
+  const AttnRun* runs;
+  const AttnSeg* segs;
+  const AttnWork* work;
+  void* o;            // bf16 [n_q_rows][Hq][d_v]
+  float* lse;         // float [n_q_rows][Hq] or null
+  DevErr* err;
+  float scale_log2;   // softmax scale * log2(e)
+  int32_t n_work;
+  int32_t layer;
+  int32_t n_pages;
+  int32_t n_layers;
+  int32_t hq;
+  int32_t group;      // query heads per kv head
+  int32_t page;
+};
+
+// Launchers; each returns the launch's cudaError_t.
+cudaError_t launch_kv_write(const void* src, void* pool, const int32_t* rows, int64_t n, int n_layers,
+                            int heads, int dim, int page, int64_t n_pages, cudaStream_t st);
+
+cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs,
+                                int n_layers, int heads, int d_rot, int page, int64_t n_pages,
+                                bool half_layout, cudaStream_t st);
+
+// dim: d_rot = d_v (GQA, 64 or 128).
+cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st);
+
+// Shared-memory bytes the attention kernel needs for head dimension dim.
+int segment_attn_smem_bytes(int dim);
+
+}  // namespace akv

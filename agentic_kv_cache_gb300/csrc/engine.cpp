@@ -1,0 +1,1150 @@
+// Host engine of the agentic KV cache: page pools, sequences, the
+// append / drop / repos / splice contract, composition of shifts, flush run
+// lists and the (cos, sin) table, segment run lists and the attention work
+// list, staging of host buffers, and the C ABI of include/akv.h.
+//
+// Sources, cited by page title and section:
+//   [AKV-blog]  "AKV: Cache Engineering for Autonomous Agents and
+//               State-Preserving Prefix Invalidation Bypass"
+//   [AKV-notes] "Cache Engineering for Agents" (reading notes on Fu et al.)
+//   [Leyline]   "Leyline: KV Cache Directives for Agentic Inference"
+//
+// Bookkeeping rules (the pages leave these open; the float64 oracle states
+// the same rules independently and the tests compare the two bit for bit):
+//   * two pools of equal size: "K" holds the rotated key part, "V" the rest;
+//     each page has a reference count = live sequences with a token in it;
+//     a fresh page is the lowest free id of its pool.
+//   * append fills the last token's page at slot + 1 when its K and V pages
+//     both have one reference; otherwise it opens a K page and a V page.
+//   * drop only hides ([AKV-blog] section 2 "The Drop Primitive": no
+//     deallocation).  repos only adds to a token's pending shift.
+//   * flush rotates visible tokens with a pending shift once by the composed
+//     shift ([Leyline] "Method": R(a)R(b) = R(a+b)).  A shared K page is
+//     copied first with every visible token of the sequence in it ([AKV-notes]
+//     section 3 "Cache Management": rotate copies that form a new branch).
+//   * splice removes [s, e), writes the stub to fresh pages, inserts it at s
+//     and shifts later tokens by n_stub - (e - s) ([Leyline] "Method").
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <new>
+#include <queue>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/akv.h"
+#include "akv_internal.h"
+
+namespace {
+
+constexpr int64_t kI32Min = INT32_MIN;
+constexpr int64_t kI32Max = INT32_MAX;
+
+struct Fail {
+  akv_status st;
+  std::string msg;
+};
+
+[[noreturn]] void fail(akv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  throw Fail{st, buf};
+}
+
+void cuda_check(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) fail(AKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct Tok {
+  int32_t kp, vp, slot, pos, delta;
+  uint8_t vis;
+  int64_t eff() const { return int64_t(pos) + delta; }
+};
+
+// Reference counts of one pool with lowest-free-id-first allocation.
+class Pool {
+ public:
+  void init(int32_t n) {
+    rc_.assign(n, 0);
+    std::vector<int32_t> ids(n);
+    for (int32_t i = 0; i < n; ++i) ids[i] = i;
+    free_ = decltype(free_)(std::greater<int32_t>(), std::move(ids));
+    n_free_ = n;
+  }
+  int32_t alloc() {
+    int32_t p = free_.top();
+    free_.pop();
+    rc_[p] = 1;
+    --n_free_;
+    return p;
+  }
+  void inc(int32_t p) { ++rc_[p]; }
+  void dec(int32_t p) {
+    if (--rc_[p] == 0) {
+      free_.push(p);
+      ++n_free_;
+    }
+  }
+  int32_t rc(int32_t p) const { return rc_[p]; }
+  int32_t n_free() const { return n_free_; }
+  const std::vector<int32_t>& counts() const { return rc_; }
+
+ private:
+  std::vector<int32_t> rc_;
+  std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_;
+  int32_t n_free_ = 0;
+};
+
+// Epoch-stamped marks over page ids: distinct-page sets in O(tokens).
+class Marks {
+ public:
+  void init(int32_t n) { m_.assign(n, 0); }
+  void next() {
+    if (++epoch_ == 0) {
+      std::fill(m_.begin(), m_.end(), 0);
+      epoch_ = 1;
+    }
+  }
+  bool test_set(int32_t p) {
+    if (m_[p] == epoch_) return false;
+    m_[p] = epoch_;
+    return true;
+  }
+  bool test(int32_t p) const { return m_[p] == epoch_; }
+
+ private:
+  std::vector<uint32_t> m_;
+  uint32_t epoch_ = 0;
+};
+
+// A pinned-host + device buffer pair reused across calls.  acquire() waits
+// for the event recorded by the previous user, so a buffer is never
+// overwritten while a copy or kernel that reads it is still queued.
+struct Staging {
+  void* host = nullptr;
+  void* dev = nullptr;
+  size_t cap = 0;
+  cudaEvent_t ev = nullptr;
+  bool pending = false;
+  bool want_host = true;
+
+  void acquire(size_t bytes) {
+    if (!ev) cuda_check(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "cudaEventCreate");
+    if (pending) {
+      cuda_check(cudaEventSynchronize(ev), "cudaEventSynchronize");
+      pending = false;
+    }
+    if (bytes <= cap) return;
+    size_t want = std::max<size_t>(bytes + bytes / 2, 4096);
+    if (host) cudaFreeHost(host);
+    if (dev) cudaFree(dev);
+    host = dev = nullptr;
+    cap = 0;
+    if (want_host) cuda_check(cudaMallocHost(&host, want), "cudaMallocHost");
+    cuda_check(cudaMalloc(&dev, want), "cudaMalloc");
+    cap = want;
+  }
+  void release(cudaStream_t st) {
+    cuda_check(cudaEventRecord(ev, st), "cudaEventRecord");
+    pending = true;
+  }
+  void destroy() {
+    if (ev) {
+      cudaEventSynchronize(ev);
+      cudaEventDestroy(ev);
+    }
+    if (host) cudaFreeHost(host);
+    if (dev) cudaFree(dev);
+    host = dev = nullptr;
+    ev = nullptr;
+    cap = 0;
+  }
+};
+
+// Uploads several host arrays to one device block through a ring of
+// staging buffers; returns device pointers (16-byte aligned pieces).
+class Uploader {
+ public:
+  static constexpr int kRing = 4;
+  struct Piece {
+    const void* src;
+    size_t bytes;
+    void** dst_dev;
+  };
+  void upload(std::initializer_list<Piece> pieces, cudaStream_t st) {
+    size_t total = 0;
+    for (auto& p : pieces) total += (p.bytes + 15) & ~size_t(15);
+    Staging& s = ring_[next_];
+    next_ = (next_ + 1) % kRing;
+    s.acquire(std::max<size_t>(total, 16));
+    size_t off = 0;
+    for (auto& p : pieces) {
+      if (p.bytes) std::memcpy(static_cast<char*>(s.host) + off, p.src, p.bytes);
+      *p.dst_dev = static_cast<char*>(s.dev) + off;
+      off += (p.bytes + 15) & ~size_t(15);
+    }
+    cuda_check(cudaMemcpyAsync(s.dev, s.host, std::max<size_t>(off, 16), cudaMemcpyHostToDevice, st),
+               "descriptor upload");
+    last_ = &s;
+  }
+  // Record the event after the kernel that reads the last upload.
+  void done(cudaStream_t st) {
+    if (last_) last_->release(st);
+    last_ = nullptr;
+  }
+  void destroy() {
+    for (auto& s : ring_) s.destroy();
+  }
+
+ private:
+  Staging ring_[kRing];
+  int next_ = 0;
+  Staging* last_ = nullptr;
+};
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn) return fn;
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cuda_check(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q),
+             "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+  if (q != cudaDriverEntryPointSuccess || !ptr) fail(AKV_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+  fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  return fn;
+}
+
+// Row-major bf16 tensor map; dims/strides innermost first, strides in bytes
+// for dims 1.., box in elements, 128-byte swizzle, zero fill out of bounds.
+void encode_map(CUtensorMap* m, void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                const uint32_t* box) {
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides[i];
+  CUresult r = get_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, d, s, b, e,
+                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) fail(AKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+}
+
+enum KernelId { kKvWrite = 0, kRepos = 1, kAttn = 2 };
+
+}  // namespace
+
+struct akv_ctx {
+  akv_config cfg{};
+  bool meta = false;
+  void* kpool = nullptr;
+  void* vpool = nullptr;
+  Pool K, V;
+  Marks mk, mv;
+  std::vector<std::vector<Tok>> seqs;
+  std::vector<uint8_t> live;
+  std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ids;
+  std::string err;
+  std::vector<int32_t> last_runs;  // 5 per run
+
+  // device side
+  int device = -1;
+  akv::DevErr* dev_err = nullptr;
+  Uploader up;
+  Staging st_k, st_v, st_q, st_o, st_lse;
+  CUtensorMap k_map{}, v_map{};
+  bool maps_ok = false;
+
+  // profiling
+  bool prof = false;
+  struct Timed {
+    int kernel;
+    cudaEvent_t a, b;
+    double bytes, flops;
+  };
+  std::vector<Timed> timed;
+  std::vector<cudaEvent_t> ev_pool;
+  akv_kernel_stats stats{};
+
+  int64_t row_elems_k() const { return int64_t(cfg.n_kv_heads) * cfg.page_size * cfg.d_rot; }
+
+  std::vector<Tok>& seq(int32_t id) {
+    if (id < 0 || id >= int32_t(seqs.size()) || !live[id]) fail(AKV_ERR_ARG, "sequence %d is not live", id);
+    return seqs[id];
+  }
+
+  int32_t new_id() {
+    if (!free_ids.empty()) {
+      int32_t id = free_ids.top();
+      free_ids.pop();
+      live[id] = 1;
+      return id;
+    }
+    seqs.emplace_back();
+    live.push_back(1);
+    return int32_t(seqs.size() - 1);
+  }
+
+  // distinct K and V pages of toks[a, b)
+  void pages_of(const std::vector<Tok>& toks, size_t a, size_t b, std::vector<int32_t>& kps,
+                std::vector<int32_t>& vps) {
+    mk.next();
+    mv.next();
+    kps.clear();
+    vps.clear();
+    for (size_t i = a; i < b; ++i) {
+      if (mk.test_set(toks[i].kp)) kps.push_back(toks[i].kp);
+      if (mv.test_set(toks[i].vp)) vps.push_back(toks[i].vp);
+    }
+  }
+
+  // ------------------------------------------------------------ profiling
+  cudaEvent_t take_event() {
+    if (!ev_pool.empty()) {
+      cudaEvent_t e = ev_pool.back();
+      ev_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e;
+    cuda_check(cudaEventCreate(&e), "cudaEventCreate");
+    return e;
+  }
+  void begin_timed(int kernel, double bytes, double flops, cudaStream_t st, Timed& t) {
+    t.kernel = kernel;
+    t.bytes = bytes;
+    t.flops = flops;
+    t.a = t.b = nullptr;
+    if (!prof) return;
+    t.a = take_event();
+    t.b = take_event();
+    cuda_check(cudaEventRecord(t.a, st), "cudaEventRecord");
+  }
+  void end_timed(Timed& t, cudaStream_t st) {
+    if (!prof) return;
+    cuda_check(cudaEventRecord(t.b, st), "cudaEventRecord");
+    timed.push_back(t);
+  }
+  void collect() {
+    for (auto& t : timed) {
+      cuda_check(cudaEventSynchronize(t.b), "cudaEventSynchronize");
+      float ms = 0.f;
+      cuda_check(cudaEventElapsedTime(&ms, t.a, t.b), "cudaEventElapsedTime");
+      stats.launches[t.kernel] += 1;
+      stats.ms[t.kernel] += ms;
+      stats.bytes[t.kernel] += t.bytes;
+      stats.flops[t.kernel] += t.flops;
+      ev_pool.push_back(t.a);
+      ev_pool.push_back(t.b);
+    }
+    timed.clear();
+  }
+
+  // ------------------------------------------------------------- device IO
+  // Returns a device pointer holding `bytes` of `src` (device: as is; host: staged).
+  const void* device_input(const void* src, size_t bytes, Staging& s, cudaStream_t st) {
+    if (is_device_ptr(src)) return src;
+    s.want_host = false;
+    s.acquire(bytes);
+    cuda_check(cudaMemcpyAsync(s.dev, src, bytes, cudaMemcpyHostToDevice, st), "host input copy");
+    return s.dev;
+  }
+
+  void write_rows(const std::vector<int32_t>& krow, const std::vector<int32_t>& vrow, const void* k,
+                  const void* v, cudaStream_t st) {
+    const int64_t n = int64_t(krow.size());
+    if (meta || n == 0) return;
+    if (!k || !v) fail(AKV_ERR_ARG, "null K/V data pointer");
+    const size_t kbytes = size_t(cfg.n_layers) * n * cfg.n_kv_heads * cfg.d_rot * 2;
+    const size_t vbytes = size_t(cfg.n_layers) * n * cfg.n_kv_heads * cfg.d_v * 2;
+    const void* kd = device_input(k, kbytes, st_k, st);
+    const void* vd = device_input(v, vbytes, st_v, st);
+    void* dk = nullptr;
+    void* dv = nullptr;
+    up.upload({{krow.data(), krow.size() * 4, &dk}, {vrow.data(), vrow.size() * 4, &dv}}, st);
+    Timed t;
+    begin_timed(kKvWrite, double(kbytes + vbytes) * 2.0, 0.0, st, t);
+    cuda_check(akv::launch_kv_write(kd, kpool, static_cast<int32_t*>(dk), n, cfg.n_layers, cfg.n_kv_heads,
+                                    cfg.d_rot, cfg.page_size, cfg.n_pages, st),
+               "kv_write launch");
+    cuda_check(akv::launch_kv_write(vd, vpool, static_cast<int32_t*>(dv), n, cfg.n_layers, cfg.n_kv_heads,
+                                    cfg.d_v, cfg.page_size, cfg.n_pages, st),
+               "kv_write launch");
+    end_timed(t, st);
+    up.done(st);
+    if (st_k.dev && !is_device_ptr(k)) st_k.release(st);
+    if (st_v.dev && !is_device_ptr(v)) st_v.release(st);
+  }
+
+  // ---------------------------------------------------------- operations
+  void append(int32_t sid, int64_t n, const void* k, const void* v, const int32_t* pos, cudaStream_t st) {
+    auto& toks = seq(sid);
+    if (n < 0) fail(AKV_ERR_ARG, "negative token count");
+    if (n > kI32Max) fail(AKV_ERR_RANGE, "too many tokens");
+    std::vector<int32_t> p(n);
+    if (pos) {
+      std::memcpy(p.data(), pos, size_t(n) * 4);
+    } else {
+      int64_t start = toks.empty() ? 0 : toks.back().eff() + 1;
+      if (n && start + n - 1 > kI32Max) fail(AKV_ERR_OVERFLOW, "position %lld leaves int32", (long long)(start + n - 1));
+      for (int64_t i = 0; i < n; ++i) p[i] = int32_t(start + i);
+    }
+    int64_t room = 0;
+    int32_t kp = -1, vp = -1, slot = -1;
+    if (!toks.empty()) {
+      const Tok& last = toks.back();
+      if (K.rc(last.kp) == 1 && V.rc(last.vp) == 1) {
+        room = cfg.page_size - 1 - last.slot;
+        kp = last.kp;
+        vp = last.vp;
+        slot = last.slot;
+      }
+    }
+    int64_t need = n <= room ? 0 : (n - room + cfg.page_size - 1) / cfg.page_size;
+    if (need > K.n_free() || need > V.n_free()) fail(AKV_ERR_NO_PAGES, "append needs %lld pages", (long long)need);
+    if (int64_t(toks.size()) + n > kI32Max) fail(AKV_ERR_RANGE, "sequence too long");
+    std::vector<int32_t> krow(n), vrow(n);
+    toks.reserve(toks.size() + n);
+    for (int64_t i = 0; i < n; ++i) {
+      if (room > 0) {
+        ++slot;
+        --room;
+      } else {
+        kp = K.alloc();
+        vp = V.alloc();
+        slot = 0;
+        room = cfg.page_size - 1;
+      }
+      toks.push_back(Tok{kp, vp, slot, p[i], 0, 1});
+      krow[i] = kp * cfg.page_size + slot;
+      vrow[i] = vp * cfg.page_size + slot;
+    }
+    write_rows(krow, vrow, k, v, st);
+  }
+
+  void check_span(const std::vector<Tok>& toks, int64_t s, int64_t e, const char* what) {
+    if (s < 0 || s > e || e > int64_t(toks.size())) fail(AKV_ERR_RANGE, "%s span [%lld, %lld) outside the sequence", what, (long long)s, (long long)e);
+  }
+
+  void drop(int32_t sid, int64_t s, int64_t e) {
+    auto& toks = seq(sid);
+    check_span(toks, s, e, "drop");
+    for (int64_t i = s; i < e; ++i) toks[i].vis = 0;
+  }
+
+  void check_shift(const std::vector<Tok>& toks, int64_t a, int64_t b, int64_t delta) {
+    for (int64_t i = a; i < b; ++i) {
+      const Tok& t = toks[i];
+      if (int64_t(t.delta) + delta < kI32Min || int64_t(t.delta) + delta > kI32Max)
+        fail(AKV_ERR_OVERFLOW, "composed shift of token %lld leaves int32", (long long)i);
+      if (t.eff() + delta < kI32Min || t.eff() + delta > kI32Max)
+        fail(AKV_ERR_OVERFLOW, "position of token %lld leaves int32", (long long)i);
+    }
+  }
+
+  void repos(int32_t sid, int64_t s, int64_t e, int32_t delta) {
+    auto& toks = seq(sid);
+    check_span(toks, s, e, "repos");
+    check_shift(toks, s, e, delta);
+    for (int64_t i = s; i < e; ++i) toks[i].delta += delta;
+  }
+
+  void splice(int32_t sid, int64_t s, int64_t e, int64_t n_stub, const void* k, const void* v, const int32_t* pos,
+              cudaStream_t st) {
+    auto& toks = seq(sid);
+    check_span(toks, s, e, "splice");
+    if (n_stub < 0 || n_stub > kI32Max) fail(AKV_ERR_RANGE, "bad stub length");
+    const int64_t delta = n_stub - (e - s);
+    if (delta < kI32Min || delta > kI32Max) fail(AKV_ERR_OVERFLOW, "splice shift leaves int32");
+    std::vector<int32_t> p(n_stub);
+    if (pos) {
+      std::memcpy(p.data(), pos, size_t(n_stub) * 4);
+    } else {
+      int64_t p0 = s < int64_t(toks.size()) ? toks[s].eff() : (toks.empty() ? 0 : toks.back().eff() + 1);
+      if (n_stub && p0 + n_stub - 1 > kI32Max) fail(AKV_ERR_OVERFLOW, "stub position leaves int32");
+      for (int64_t i = 0; i < n_stub; ++i) p[i] = int32_t(p0 + i);
+    }
+    check_shift(toks, e, int64_t(toks.size()), delta);
+    if (int64_t(toks.size()) - (e - s) + n_stub > kI32Max) fail(AKV_ERR_RANGE, "sequence too long");
+    // pages referenced only by the removed tokens are released
+    std::vector<int32_t> kk, vv, kr, vr;
+    pages_of(toks, 0, size_t(s), kk, vv);
+    for (size_t i = size_t(e); i < toks.size(); ++i) {
+      mk.test_set(toks[i].kp);
+      mv.test_set(toks[i].vp);
+    }
+    for (int64_t i = s; i < e; ++i) {
+      const Tok& t = toks[i];
+      if (mk.test_set(t.kp)) kr.push_back(t.kp);
+      if (mv.test_set(t.vp)) vr.push_back(t.vp);
+    }
+    const int64_t need = (n_stub + cfg.page_size - 1) / cfg.page_size;
+    int64_t kf = K.n_free(), vf = V.n_free();
+    for (int32_t q : kr) kf += K.rc(q) == 1;
+    for (int32_t q : vr) vf += V.rc(q) == 1;
+    if (need > kf || need > vf) fail(AKV_ERR_NO_PAGES, "splice needs %lld pages", (long long)need);
+    for (int32_t q : kr) K.dec(q);
+    for (int32_t q : vr) V.dec(q);
+    std::vector<Tok> stub(n_stub);
+    std::vector<int32_t> krow(n_stub), vrow(n_stub);
+    int32_t kp = -1, vp = -1;
+    for (int64_t i = 0; i < n_stub; ++i) {
+      const int32_t slot = int32_t(i % cfg.page_size);
+      if (slot == 0) {
+        kp = K.alloc();
+        vp = V.alloc();
+      }
+      stub[i] = Tok{kp, vp, slot, p[i], 0, 1};
+      krow[i] = kp * cfg.page_size + slot;
+      vrow[i] = vp * cfg.page_size + slot;
+    }
+    for (size_t i = size_t(e); i < toks.size(); ++i) toks[i].delta += int32_t(delta);
+    std::vector<Tok> out;
+    out.reserve(toks.size() - (e - s) + n_stub);
+    out.insert(out.end(), toks.begin(), toks.begin() + s);
+    out.insert(out.end(), stub.begin(), stub.end());
+    out.insert(out.end(), toks.begin() + e, toks.end());
+    toks.swap(out);
+    write_rows(krow, vrow, k, v, st);
+  }
+
+  void fork(int32_t src, int64_t n_prefix, int32_t* out) {
+    auto& toks = seq(src);
+    if (n_prefix < 0 || n_prefix > int64_t(toks.size())) fail(AKV_ERR_RANGE, "fork prefix outside the sequence");
+    std::vector<Tok> child(toks.begin(), toks.begin() + n_prefix);
+    std::vector<int32_t> kps, vps;
+    pages_of(child, 0, child.size(), kps, vps);
+    for (int32_t q : kps) K.inc(q);
+    for (int32_t q : vps) V.inc(q);
+    int32_t id = new_id();
+    seqs[id] = std::move(child);
+    *out = id;
+  }
+
+  void free_seq(int32_t sid) {
+    auto& toks = seq(sid);
+    std::vector<int32_t> kps, vps;
+    pages_of(toks, 0, toks.size(), kps, vps);
+    for (int32_t q : kps) K.dec(q);
+    for (int32_t q : vps) V.dec(q);
+    std::vector<Tok>().swap(toks);
+    live[sid] = 0;
+    free_ids.push(sid);
+  }
+
+  // ----------------------------------------------------------------- flush
+  // Pages holding visible tokens with a pending shift, first-appearance order.
+  void moving_pages(const std::vector<Tok>& toks, std::vector<int32_t>& order) {
+    mk.next();
+    order.clear();
+    for (const Tok& t : toks)
+      if (t.vis && t.delta != 0 && mk.test_set(t.kp)) order.push_back(t.kp);
+  }
+
+  void flush(const std::vector<int32_t>& ids, cudaStream_t st) {
+    // Budget check on simulated reference counts, so a failure changes nothing.
+    std::unordered_map<int32_t, int32_t> rc_sim;
+    auto rc_of = [&](int32_t q) {
+      auto it = rc_sim.find(q);
+      return it == rc_sim.end() ? K.rc(q) : it->second;
+    };
+    int64_t need = 0;
+    std::vector<int32_t> order;
+    for (int32_t sid : ids) {
+      auto& toks = seqs[sid];
+      moving_pages(toks, order);
+      std::vector<int32_t> cow;
+      for (int32_t q : order)
+        if (rc_of(q) > 1) cow.push_back(q);
+      need += int64_t(cow.size());
+      if (cow.empty()) continue;
+      mk.next();
+      for (int32_t q : cow) mk.test_set(q);
+      std::unordered_map<int32_t, bool> stays;
+      for (const Tok& t : toks)
+        if (!t.vis && mk.test(t.kp)) stays[t.kp] = true;
+      for (int32_t q : cow)
+        if (!stays.count(q)) rc_sim[q] = rc_of(q) - 1;
+    }
+    if (need > K.n_free()) fail(AKV_ERR_NO_PAGES, "flush needs %lld copy-on-write pages", (long long)need);
+
+    std::vector<akv::RunDesc> runs;
+    std::vector<int32_t> deltas;          // distinct shifts, first-appearance order
+    std::unordered_map<int32_t, int32_t> didx;
+    std::vector<int32_t> flat;
+    for (int32_t sid : ids) flush_seq(seqs[sid], runs, deltas, didx, flat);
+    if (!runs.empty()) last_runs.swap(flat);
+    if (meta || runs.empty()) return;
+
+    // (cos, sin)(delta * theta_j) evaluated in float64, stored as float32.
+    const int half = cfg.d_rot / 2;
+    std::vector<float2> cs(deltas.size() * half);
+    for (size_t d = 0; d < deltas.size(); ++d)
+      for (int j = 0; j < half; ++j) {
+        const double th = std::pow(cfg.rope_base, -2.0 * j / cfg.d_rot);
+        const double a = double(deltas[d]) * th;
+        cs[d * half + j] = make_float2(float(std::cos(a)), float(std::sin(a)));
+      }
+    void* druns = nullptr;
+    void* dcs = nullptr;
+    up.upload({{runs.data(), runs.size() * sizeof(akv::RunDesc), &druns}, {cs.data(), cs.size() * sizeof(float2), &dcs}},
+              st);
+    int64_t rows = 0;
+    for (auto& r : runs) rows += (r.lohi >> 16) - (r.lohi & 0xffff);
+    Timed t;
+    const double bytes = 2.0 * double(rows) * cfg.n_layers * cfg.n_kv_heads * cfg.d_rot * 2.0;
+    begin_timed(kRepos, bytes, 0.0, st, t);
+    cuda_check(akv::launch_repos_rotate(kpool, static_cast<akv::RunDesc*>(druns), static_cast<float2*>(dcs),
+                                        int(runs.size()), cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.page_size,
+                                        cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, st),
+               "repos_rotate launch");
+    end_timed(t, st);
+    up.done(st);
+  }
+
+  void flush_seq(std::vector<Tok>& toks, std::vector<akv::RunDesc>& runs, std::vector<int32_t>& deltas,
+                 std::unordered_map<int32_t, int32_t>& didx, std::vector<int32_t>& flat) {
+    std::vector<int32_t> order;
+    moving_pages(toks, order);
+    if (order.empty()) return;
+    std::unordered_map<int32_t, int32_t> dst;  // source page -> destination page
+    std::vector<int32_t> cow;
+    for (int32_t q : order) {
+      if (K.rc(q) > 1) {
+        cow.push_back(q);
+        dst[q] = K.alloc();
+      } else {
+        dst[q] = q;
+      }
+    }
+    mk.next();
+    for (int32_t q : cow) mk.test_set(q);  // marked = copied page
+    // Runs: maximal groups of consecutive emitted tokens with equal
+    // (source, destination, shift) and consecutive slots.
+    bool open = false;
+    int32_t c_src = 0, c_dst = 0, c_delta = 0, c_lo = 0, c_hi = 0;
+    auto close = [&]() {
+      if (!open) return;
+      auto it = didx.find(c_delta);
+      int32_t di;
+      if (it == didx.end()) {
+        di = int32_t(deltas.size());
+        didx.emplace(c_delta, di);
+        deltas.push_back(c_delta);
+      } else {
+        di = it->second;
+      }
+      runs.push_back(akv::RunDesc{c_src, c_dst, c_lo | (c_hi << 16), di});
+      flat.insert(flat.end(), {c_src, c_dst, c_lo, c_hi, c_delta});
+      open = false;
+    };
+    for (Tok& t : toks) {
+      const bool copied = mk.test(t.kp);
+      const bool emit = t.vis && (t.delta != 0 || copied);
+      if (!emit) {
+        close();
+        continue;
+      }
+      const int32_t d = dst.count(t.kp) ? dst[t.kp] : t.kp;
+      if (open && c_src == t.kp && c_dst == d && c_delta == t.delta && t.slot == c_hi) {
+        ++c_hi;
+      } else {
+        close();
+        open = true;
+        c_src = t.kp;
+        c_dst = d;
+        c_delta = t.delta;
+        c_lo = t.slot;
+        c_hi = t.slot + 1;
+      }
+    }
+    close();
+    for (Tok& t : toks) {
+      const bool copied = mk.test(t.kp);
+      if (t.vis && (t.delta != 0 || copied)) {
+        if (copied) t.kp = dst[t.kp];
+        t.pos += t.delta;
+        t.delta = 0;
+      }
+    }
+    // A copied page loses this sequence's reference unless a dropped token stays in it.
+    mk.next();
+    for (const Tok& t : toks) mk.test_set(t.kp);
+    for (int32_t q : cow)
+      if (!mk.test(q)) K.dec(q);
+  }
+
+  // -------------------------------------------------------------- segments
+  struct SegPlan {
+    std::vector<akv::AttnRun> runs;
+    int64_t kv_len = 0;
+  };
+
+  void validate_segment(const akv_segment& g, int64_t n_q_rows) {
+    auto& toks = seq(g.seq);
+    if (g.reserved != 0) fail(AKV_ERR_ARG, "segment reserved field must be 0");
+    if (g.q_len < 1 || g.kv_end < g.q_len || g.kv_end > int64_t(toks.size()))
+      fail(AKV_ERR_RANGE, "segment outside the sequence");
+    if (n_q_rows >= 0 && (g.q_row0 < 0 || g.q_row0 + g.q_len > n_q_rows)) fail(AKV_ERR_RANGE, "segment rows outside Q");
+    if (g.n_hide < 0 || (g.n_hide > 0 && !g.hide)) fail(AKV_ERR_ARG, "bad hidden span list");
+    for (int32_t h = 0; h < g.n_hide; ++h) {
+      int64_t a = g.hide[2 * h], b = g.hide[2 * h + 1];
+      if (a < 0 || a > b || b > g.kv_end) fail(AKV_ERR_RANGE, "hidden span outside the segment");
+      if (b > g.kv_end - g.q_len && a < b) fail(AKV_ERR_ARG, "a query token of the segment is hidden");
+    }
+    for (int64_t i = g.kv_end - g.q_len; i < g.kv_end; ++i)
+      if (!toks[i].vis) fail(AKV_ERR_ARG, "a query token of the segment is dropped");
+  }
+
+  SegPlan plan_segment(const akv_segment& g) {
+    auto& toks = seq(g.seq);
+    std::vector<uint8_t> hidden;
+    if (g.n_hide > 0) {
+      hidden.assign(size_t(g.kv_end), 0);
+      for (int32_t h = 0; h < g.n_hide; ++h)
+        for (int64_t i = g.hide[2 * h]; i < g.hide[2 * h + 1]; ++i) hidden[i] = 1;
+    }
+    SegPlan sp;
+    bool open = false;
+    akv::AttnRun cur{};
+    int32_t lo = 0, hi = 0;
+    for (int64_t i = 0; i < g.kv_end; ++i) {
+      const Tok& t = toks[i];
+      if (!t.vis || (!hidden.empty() && hidden[i])) continue;
+      if (t.delta != 0) fail(AKV_ERR_ARG, "segment reads token %lld with a pending shift", (long long)i);
+      if (open && cur.kp == t.kp && cur.vp == t.vp && t.slot == hi) {
+        ++hi;
+      } else {
+        if (open) {
+          cur.lohi = lo | (hi << 16);
+          sp.runs.push_back(cur);
+        }
+        open = true;
+        cur.kp = t.kp;
+        cur.vp = t.vp;
+        cur.es = int32_t(sp.kv_len);
+        lo = t.slot;
+        hi = t.slot + 1;
+      }
+      ++sp.kv_len;
+    }
+    if (open) {
+      cur.lohi = lo | (hi << 16);
+      sp.runs.push_back(cur);
+    }
+    return sp;
+  }
+
+  void attend(int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q, int64_t n_q_rows, void* o,
+              float* lse, float scale, cudaStream_t st) {
+    if (n_segs < 0 || (n_segs > 0 && !segs)) fail(AKV_ERR_ARG, "bad segment list");
+    if (layer < 0 || layer >= cfg.n_layers) fail(AKV_ERR_RANGE, "layer outside the pools");
+    if (n_q_rows < 0 || n_q_rows > kI32Max) fail(AKV_ERR_RANGE, "bad query row count");
+    if (!meta && n_segs > 0 && (!q || !o)) fail(AKV_ERR_ARG, "null Q or O pointer");
+    for (int32_t i = 0; i < n_segs; ++i) validate_segment(segs[i], n_q_rows);
+    std::vector<int32_t> ids;
+    for (int32_t i = 0; i < n_segs; ++i) ids.push_back(segs[i].seq);
+    std::sort(ids.begin(), ids.end());
+    ids.erase(std::unique(ids.begin(), ids.end()), ids.end());
+    flush(ids, st);
+    if (n_segs == 0) return;
+
+    const int G = cfg.n_q_heads / cfg.n_kv_heads;
+    const int tpt = 128 / G;                   // query tokens per 128-row tile
+    const int rpt = 128 / cfg.page_size;       // runs per 128-key tile
+    std::vector<akv::AttnRun> runs;
+    std::vector<akv::AttnSeg> tab;
+    std::vector<akv::AttnWork> work;
+    double flops = 0.0;
+    const int dqk = cfg.layout == AKV_LAYOUT_MLA ? cfg.d_v + cfg.d_rot : cfg.d_rot;
+    for (int32_t i = 0; i < n_segs; ++i) {
+      SegPlan sp = plan_segment(segs[i]);
+      if (sp.kv_len > kI32Max) fail(AKV_ERR_RANGE, "segment too long");
+      akv::AttnSeg s{};
+      s.run_off = int32_t(runs.size());
+      s.n_runs = int32_t(sp.runs.size());
+      s.kv_len = int32_t(sp.kv_len);
+      s.q_len = segs[i].q_len;
+      s.q_row0 = int32_t(segs[i].q_row0);
+      const int64_t ql = s.q_len, kl = s.kv_len;
+      flops += double(cfg.n_q_heads) * 2.0 * (dqk + cfg.d_v) * double(ql * (kl - ql) + ql * (ql + 1) / 2);
+      const int n_qt = (s.q_len + tpt - 1) / tpt;
+      for (int qt = 0; qt < n_qt; ++qt) {
+        const int64_t last = std::min<int64_t>(ql, int64_t(qt + 1) * tpt) - 1;
+        const int64_t limit = kl - ql + last;  // largest entry index the tile reads
+        // runs whose first entry is <= limit
+        int64_t lo_r = 0, hi_r = int64_t(sp.runs.size());
+        while (lo_r < hi_r) {
+          int64_t mid = (lo_r + hi_r) / 2;
+          if (sp.runs[mid].es <= limit) lo_r = mid + 1; else hi_r = mid;
+        }
+        const int32_t n_tiles = int32_t((lo_r + rpt - 1) / rpt);
+        for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, n_tiles});
+      }
+      runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
+      tab.push_back(s);
+    }
+    if (meta) return;
+    // Longest first (LPT); ties in (segment, head, tile) order.
+    std::stable_sort(work.begin(), work.end(),
+                     [](const akv::AttnWork& a, const akv::AttnWork& b) { return a.n_tiles > b.n_tiles; });
+    if (cfg.layout != AKV_LAYOUT_GQA || !(cfg.d_rot == 64 || cfg.d_rot == 128))
+      fail(AKV_ERR_ARG, "segment attention supports GQA with head_dim 64 or 128");
+
+    const size_t qbytes = size_t(n_q_rows) * cfg.n_q_heads * dqk * 2;
+    const size_t obytes = size_t(n_q_rows) * cfg.n_q_heads * cfg.d_v * 2;
+    const void* qd = device_input(q, qbytes, st_q, st);
+    const bool o_host = !is_device_ptr(o);
+    void* od = o;
+    if (o_host) {
+      st_o.want_host = false;
+      st_o.acquire(obytes);
+      od = st_o.dev;
+    }
+    float* lsed = lse;
+    const bool lse_host = lse && !is_device_ptr(lse);
+    if (lse_host) {
+      st_lse.want_host = false;
+      st_lse.acquire(size_t(n_q_rows) * cfg.n_q_heads * 4);
+      lsed = static_cast<float*>(st_lse.dev);
+    }
+    if (reinterpret_cast<uintptr_t>(qd) % 16) fail(AKV_ERR_ARG, "Q must be 16-byte aligned");
+
+    akv::AttnParams p{};
+    {
+      const uint64_t dims[3] = {uint64_t(dqk), uint64_t(cfg.n_q_heads), uint64_t(std::max<int64_t>(n_q_rows, 1))};
+      const uint64_t strides[2] = {uint64_t(dqk) * 2, uint64_t(cfg.n_q_heads) * dqk * 2};
+      const uint32_t box[3] = {64, uint32_t(G), uint32_t(tpt)};
+      encode_map(&p.q_map, const_cast<void*>(qd), 3, dims, strides, box);
+    }
+    p.k_map = k_map;
+    p.v_map = v_map;
+    void* druns = nullptr;
+    void* dsegs = nullptr;
+    void* dwork = nullptr;
+    up.upload({{runs.data(), runs.size() * sizeof(akv::AttnRun), &druns},
+               {tab.data(), tab.size() * sizeof(akv::AttnSeg), &dsegs},
+               {work.data(), work.size() * sizeof(akv::AttnWork), &dwork}},
+              st);
+    p.runs = static_cast<akv::AttnRun*>(druns);
+    p.segs = static_cast<akv::AttnSeg*>(dsegs);
+    p.work = static_cast<akv::AttnWork*>(dwork);
+    p.o = od;
+    p.lse = lsed;
+    p.err = dev_err;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.n_work = int32_t(work.size());
+    p.layer = layer;
+    p.n_pages = cfg.n_pages;
+    p.n_layers = cfg.n_layers;
+    p.hq = cfg.n_q_heads;
+    p.group = G;
+    p.page = cfg.page_size;
+    Timed t;
+    begin_timed(kAttn, 0.0, flops, st, t);
+    cuda_check(akv::launch_segment_attn(p, cfg.d_rot, st), "segment_attn launch");
+    end_timed(t, st);
+    up.done(st);
+    if (st_q.dev && !is_device_ptr(q)) st_q.release(st);
+    if (o_host) {
+      cuda_check(cudaMemcpyAsync(o, od, obytes, cudaMemcpyDeviceToHost, st), "O copy to host");
+      st_o.release(st);
+    }
+    if (lse_host) {
+      cuda_check(cudaMemcpyAsync(lse, lsed, size_t(n_q_rows) * cfg.n_q_heads * 4, cudaMemcpyDeviceToHost, st),
+                 "LSE copy to host");
+      st_lse.release(st);
+    }
+  }
+
+  // ------------------------------------------------------------ lifecycle
+  void create(const akv_config& c, const akv_pools* pools) {
+    cfg = c;
+    if (c.n_layers <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.n_pages <= 0 || c.reserved != 0)
+      fail(AKV_ERR_ARG, "bad config sizes");
+    if (c.page_size != 16 && c.page_size != 32 && c.page_size != 64 && c.page_size != 128)
+      fail(AKV_ERR_ARG, "page_size must be 16, 32, 64 or 128");
+    if (c.d_rot <= 0 || c.d_rot % 8 || c.d_v <= 0 || c.d_v % 8) fail(AKV_ERR_ARG, "d_rot and d_v must be multiples of 8");
+    if (c.n_q_heads % c.n_kv_heads) fail(AKV_ERR_ARG, "n_q_heads must be a multiple of n_kv_heads");
+    const int G = c.n_q_heads / c.n_kv_heads;
+    if (G > 128 || 128 % G) fail(AKV_ERR_ARG, "n_q_heads / n_kv_heads must divide 128");
+    if (c.layout != AKV_LAYOUT_GQA && c.layout != AKV_LAYOUT_MLA) fail(AKV_ERR_ARG, "bad layout");
+    if (c.layout == AKV_LAYOUT_MLA && c.n_kv_heads != 1) fail(AKV_ERR_ARG, "MLA needs n_kv_heads = 1");
+    if (c.layout == AKV_LAYOUT_GQA && c.d_v != c.d_rot) fail(AKV_ERR_ARG, "GQA needs d_v = d_rot");
+    if (c.rope_layout != AKV_ROPE_INTERLEAVED && c.rope_layout != AKV_ROPE_HALF) fail(AKV_ERR_ARG, "bad rope layout");
+    if (c.rope_layout == AKV_ROPE_HALF && c.d_rot % 16) fail(AKV_ERR_ARG, "half layout needs d_rot % 16 == 0");
+    if (!(c.rope_base > 0.0)) fail(AKV_ERR_ARG, "rope_base must be positive");
+    if (int64_t(c.n_pages) * c.page_size > kI32Max) fail(AKV_ERR_ARG, "pool too large for int32 rows");
+    K.init(c.n_pages);
+    V.init(c.n_pages);
+    mk.init(c.n_pages);
+    mv.init(c.n_pages);
+    if (!pools) {
+      meta = true;
+      return;
+    }
+    if (!pools->k_pool || !pools->v_pool) fail(AKV_ERR_ARG, "null pool pointer");
+    if (reinterpret_cast<uintptr_t>(pools->k_pool) % 16 || reinterpret_cast<uintptr_t>(pools->v_pool) % 16)
+      fail(AKV_ERR_ARG, "pools must be 16-byte aligned");
+    kpool = pools->k_pool;
+    vpool = pools->v_pool;
+    cuda_check(cudaGetDevice(&device), "cudaGetDevice");
+    cuda_check(cudaMalloc(&dev_err, sizeof(akv::DevErr)), "cudaMalloc");
+    cuda_check(cudaMemset(dev_err, 0, sizeof(akv::DevErr)), "cudaMemset");
+    if (c.d_rot % 64 == 0 && c.d_v % 64 == 0) {
+      const uint64_t lp = uint64_t(c.n_layers) * c.n_pages;
+      const uint32_t box[4] = {64, uint32_t(c.page_size), 1, 1};
+      const uint64_t kd[4] = {uint64_t(c.d_rot), uint64_t(c.page_size), uint64_t(c.n_kv_heads), lp};
+      const uint64_t ks[3] = {uint64_t(c.d_rot) * 2, uint64_t(c.page_size) * c.d_rot * 2,
+                              uint64_t(c.n_kv_heads) * c.page_size * c.d_rot * 2};
+      encode_map(&k_map, kpool, 4, kd, ks, box);
+      const uint64_t vd[4] = {uint64_t(c.d_v), uint64_t(c.page_size), uint64_t(c.n_kv_heads), lp};
+      const uint64_t vs[3] = {uint64_t(c.d_v) * 2, uint64_t(c.page_size) * c.d_v * 2,
+                              uint64_t(c.n_kv_heads) * c.page_size * c.d_v * 2};
+      encode_map(&v_map, vpool, 4, vd, vs, box);
+      maps_ok = true;
+    }
+  }
+
+  void destroy() {
+    if (meta) return;
+    cudaDeviceSynchronize();
+    up.destroy();
+    st_k.destroy();
+    st_v.destroy();
+    st_q.destroy();
+    st_o.destroy();
+    st_lse.destroy();
+    for (auto& t : timed) {
+      cudaEventDestroy(t.a);
+      cudaEventDestroy(t.b);
+    }
+    for (auto e : ev_pool) cudaEventDestroy(e);
+    if (dev_err) cudaFree(dev_err);
+  }
+};
+
+namespace {
+
+template <typename F>
+akv_status guard(akv_ctx* ctx, F&& f) {
+  if (!ctx) return AKV_ERR_ARG;
+  try {
+    ctx->err.clear();
+    f();
+    return AKV_OK;
+  } catch (const Fail& e) {
+    ctx->err = e.msg;
+    return e.st;
+  } catch (const std::bad_alloc&) {
+    ctx->err = "host out of memory";
+    return AKV_ERR_NO_PAGES;
+  } catch (...) {
+    ctx->err = "internal error";
+    return AKV_ERR_ARG;
+  }
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+akv_status akv_create(const akv_config* cfg, const akv_pools* pools, akv_ctx** out) {
+  if (!cfg || !out) return AKV_ERR_ARG;
+  *out = nullptr;
+  akv_ctx* ctx = new (std::nothrow) akv_ctx();
+  if (!ctx) return AKV_ERR_ARG;
+  akv_status s = guard(ctx, [&] { ctx->create(*cfg, pools); });
+  if (s != AKV_OK) {
+    ctx->destroy();
+    delete ctx;
+    return s;
+  }
+  *out = ctx;
+  return AKV_OK;
+}
+
+akv_status akv_destroy(akv_ctx* ctx) {
+  if (!ctx) return AKV_ERR_ARG;
+  ctx->destroy();
+  delete ctx;
+  return AKV_OK;
+}
+
+const char* akv_last_error(const akv_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+akv_status akv_seq_alloc(akv_ctx* ctx, int32_t* seq_out) {
+  return guard(ctx, [&] {
+    if (!seq_out) fail(AKV_ERR_ARG, "null output");
+    *seq_out = ctx->new_id();
+    ctx->seqs[*seq_out].clear();
+  });
+}
+
+akv_status akv_seq_fork(akv_ctx* ctx, int32_t src, int64_t n_prefix, int32_t* seq_out) {
+  return guard(ctx, [&] {
+    if (!seq_out) fail(AKV_ERR_ARG, "null output");
+    ctx->fork(src, n_prefix, seq_out);
+  });
+}
+
+akv_status akv_seq_free(akv_ctx* ctx, int32_t seq) {
+  return guard(ctx, [&] { ctx->free_seq(seq); });
+}
+
+akv_status akv_seq_len(akv_ctx* ctx, int32_t seq, int64_t* n_out) {
+  return guard(ctx, [&] {
+    if (!n_out) fail(AKV_ERR_ARG, "null output");
+    *n_out = int64_t(ctx->seq(seq).size());
+  });
+}
+
+akv_status akv_append(akv_ctx* ctx, int32_t seq, int64_t n, const void* k, const void* v, const int32_t* pos,
+                      void* stream) {
+  return guard(ctx, [&] { ctx->append(seq, n, k, v, pos, as_stream(stream)); });
+}
+
+akv_status akv_drop(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e) {
+  return guard(ctx, [&] { ctx->drop(seq, s, e); });
+}
+
+akv_status akv_repos(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int32_t delta) {
+  return guard(ctx, [&] { ctx->repos(seq, s, e, delta); });
+}
+
+akv_status akv_splice(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int64_t n_stub, const void* k_stub,
+                      const void* v_stub, const int32_t* pos, void* stream) {
+  return guard(ctx, [&] { ctx->splice(seq, s, e, n_stub, k_stub, v_stub, pos, as_stream(stream)); });
+}
+
+akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream) {
+  return guard(ctx, [&] {
+    std::vector<int32_t> ids;
+    if (seq == -1) {
+      for (int32_t i = 0; i < int32_t(ctx->seqs.size()); ++i)
+        if (ctx->live[i]) ids.push_back(i);
+    } else {
+      ctx->seq(seq);
+      ids.push_back(seq);
+    }
+    ctx->flush(ids, as_stream(stream));
+  });
+}
+
+akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
+                      int64_t n_q_rows, void* o, float* lse, float scale, void* stream) {
+  return guard(ctx, [&] { ctx->attend(layer, segs, n_segs, q, n_q_rows, o, lse, scale, as_stream(stream)); });
+}
+
+akv_status akv_export_state(akv_ctx* ctx, int32_t seq, int32_t* k_page, int32_t* v_page, int32_t* slot,
+                            int32_t* pos, int32_t* delta, uint8_t* visible) {
+  return guard(ctx, [&] {
+    const auto& toks = ctx->seq(seq);
+    for (size_t i = 0; i < toks.size(); ++i) {
+      if (k_page) k_page[i] = toks[i].kp;
+      if (v_page) v_page[i] = toks[i].vp;
+      if (slot) slot[i] = toks[i].slot;
+      if (pos) pos[i] = toks[i].pos;
+      if (delta) delta[i] = toks[i].delta;
+      if (visible) visible[i] = toks[i].vis;
+    }
+  });
+}
+
+akv_status akv_refcounts(akv_ctx* ctx, int32_t* k_rc, int32_t* v_rc) {
+  return guard(ctx, [&] {
+    if (k_rc) std::memcpy(k_rc, ctx->K.counts().data(), ctx->K.counts().size() * 4);
+    if (v_rc) std::memcpy(v_rc, ctx->V.counts().data(), ctx->V.counts().size() * 4);
+  });
+}
+
+akv_status akv_last_flush_runs(akv_ctx* ctx, int32_t* out, int64_t cap, int64_t* n_runs) {
+  return guard(ctx, [&] {
+    const int64_t n = int64_t(ctx->last_runs.size() / 5);
+    if (n_runs) *n_runs = n;
+    if (out && cap > 0) std::memcpy(out, ctx->last_runs.data(), size_t(std::min(n, cap)) * 5 * 4);
+  });
+}
+
+akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_t* out, int64_t cap, int64_t* n_runs,
+                            int64_t* kv_len) {
+  return guard(ctx, [&] {
+    if (!seg) fail(AKV_ERR_ARG, "null segment");
+    ctx->validate_segment(*seg, -1);
+    auto sp = ctx->plan_segment(*seg);
+    if (n_runs) *n_runs = int64_t(sp.runs.size());
+    if (kv_len) *kv_len = sp.kv_len;
+    for (int64_t i = 0; out && i < std::min<int64_t>(cap, int64_t(sp.runs.size())); ++i) {
+      const auto& r = sp.runs[i];
+      out[4 * i + 0] = r.kp;
+      out[4 * i + 1] = r.vp;
+      out[4 * i + 2] = r.lohi & 0xffff;
+      out[4 * i + 3] = r.lohi >> 16;
+    }
+  });
+}
+
+akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code) {
+  akv_status inner = AKV_OK;
+  akv_status s = guard(ctx, [&] {
+    int32_t c = 0;
+    if (!ctx->meta) {
+      akv::DevErr e{};
+      cuda_check(cudaStreamSynchronize(as_stream(stream)), "cudaStreamSynchronize");
+      cuda_check(cudaMemcpy(&e, ctx->dev_err, sizeof e, cudaMemcpyDeviceToHost), "error word read");
+      cuda_check(cudaMemset(ctx->dev_err, 0, sizeof e), "error word clear");
+      c = e.code;
+      if (c) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "device error %d (info %d %d %d)", e.code, e.info[0], e.info[1], e.info[2]);
+        ctx->err = buf;
+      }
+    }
+    if (code) *code = c;
+    inner = akv_status(c);
+  });
+  return s != AKV_OK ? s : inner;
+}
+
+akv_status akv_profile_enable(akv_ctx* ctx, int32_t on) {
+  return guard(ctx, [&] {
+    if (ctx->meta) return;
+    ctx->collect();
+    ctx->stats = akv_kernel_stats{};
+    ctx->prof = on != 0;
+  });
+}
+
+akv_status akv_profile_read(akv_ctx* ctx, akv_kernel_stats* out) {
+  return guard(ctx, [&] {
+    if (!out) fail(AKV_ERR_ARG, "null output");
+    if (!ctx->meta) ctx->collect();
+    *out = ctx->stats;
+  });
+}
+
+}  // extern "C"

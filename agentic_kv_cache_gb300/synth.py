@@ -20,6 +20,7 @@ Operation tuples (sequence operands are symbolic names):
     ("drop", name, s, e)
     ("repos", name, s, e, delta)
     ("splice", name, s, e, n_stub, key) stub K/V drawn under ``key``
+    ("flush", name)                     materialise pending shifts now
 Segments: dict(seq=name, kv_end, q_len, hide=[(a, b), ...], q_row0).
 """
 import dataclasses
@@ -279,6 +280,7 @@ def llama70b_128k(seed=0, n_layers=80, total=131072, n_spans=64, n_branches=32, 
     ops = [("alloc", "M"), ("append", "M", total, "ctx")]
     for k in range(n_spans):
         ops.append(("repos", "M", k * ln, (k + 1) * ln, int(rng.integers(-max_shift, max_shift + 1))))
+    ops.append(("flush", "M"))  # the sweep is in place, before any branch shares the pages
     segs = []
     for b in range(n_branches):
         name = f"B{b}"

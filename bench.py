@@ -1,0 +1,388 @@
+"""Benchmark: one post-drop agent turn on a Llama-3.1-8B-shaped layer at 32K context.
+
+A step is one pass of the whole hot path over one turn of synthetic input:
+fork the 32K-token trajectory (a new branch), drop the oldest 20 tool
+responses and reposition every retained suffix token by its composed shift
+(host bookkeeping), append the 2,048 new tokens' K/V (kv_write), flush the
+shifts (repos_rotate, copy-on-write into the branch), and run segment-batch
+attention of the 2,048 new queries over the edited history
+(segment_batch_attn); the branch is then released.  Inputs are resident in HBM
+when the timed region starts; L2 is flushed (a 512 MiB write) between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own
+independent sessions (weak scaling, no data-path collective); the time is the
+max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "repos rotated tokens/s (HBM GB/s) + segment-batch attn TFLOP/s at 32K ctx"
+UNIT = "post-drop turns/s"
+WORKLOAD = ("llama8b_32k: Llama-3.1-8B-shaped layer (32 q / 8 kv heads, d 128, RoPE theta 5e5, page 16), "
+            "32K-token 40-turn trajectory, drop oldest 20 tool responses + repos of the retained suffix "
+            "(copy-on-write branch), 2,048 new query tokens in one segment")
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+class Turn:
+    """The engine, the resident 32K-token trajectory and the per-step inputs."""
+
+    def __init__(self, seed=0, host_inputs=False):
+        import torch
+        from agentic_kv_cache_gb300 import akv, build, runner, synth
+        build.build()
+        self.torch, self.akv, self.runner = torch, akv, runner
+        self.w = w = synth.llama8b_32k(seed=seed, fork=True)
+        s = w.shape
+        self.cfg = akv.config_from_shape(s, w.n_pages)
+        self.pools = akv.make_pools(self.cfg)
+        self.eng = akv.Engine(self.cfg, self.pools)
+        self.stream = torch.cuda.current_stream()
+        fork_at = next(i for i, op in enumerate(w.ops) if op[0] == "fork")
+        self.setup_ops, self.step_ops = w.ops[:fork_at], w.ops[fork_at:]
+        src = runner.torch_kv_source(w)
+        self.names = runner.run_ops(self.eng, w, kv_source=src, ops=self.setup_ops, stream=self.stream)
+        new_op = next(op for op in self.step_ops if op[0] == "append")
+        self.new_k, self.new_v = src(new_op[3], new_op[2])
+        q32 = synth.q_array(w)
+        self.q = torch.from_numpy(q32).cuda().to(torch.bfloat16)
+        self.nq = q32.shape[0]
+        self.o = torch.empty((self.nq, s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
+        if host_inputs:
+            self.h_k = self.new_k.cpu().pin_memory()
+            self.h_v = self.new_v.cpu().pin_memory()
+            self.h_q = self.q.cpu().pin_memory()
+            self.h_o = torch.empty(self.o.shape, dtype=torch.bfloat16).pin_memory()
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+
+    def step(self, host=False):
+        k, v = (self.h_k, self.h_v) if host else (self.new_k, self.new_v)
+        names = dict(self.names)
+        self.runner.run_ops(self.eng, self.w, kv_source=lambda *_: (k, v), ops=self.step_ops, names=names,
+                            stream=self.stream)
+        segs = self.runner.engine_segments(self.w, names)
+        q, o = (self.h_q, self.h_o) if host else (self.q, self.o)
+        self.eng.attend(0, segs, q, self.nq, o, None, self.w.shape.scale, stream=self.stream)
+        self.eng.seq_free(names["F"])
+
+    def flush_l2(self):
+        self.flush_buf.zero_()
+
+    def io_bytes(self):
+        b = lambda t: t.numel() * t.element_size()
+        return b(self.new_k) + b(self.new_v) + b(self.q), b(self.o)
+
+
+def gpu_arm(args, rank, world):
+    import torch
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    t = Turn(seed=rank, host_inputs=True)
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        if dist:
+            tdist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        t.step()
+        t.flush_l2()
+    assert t.eng.check_device_error(t.stream) == 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    t.eng.profile_enable(True)
+    with ClockSampler(dev) as clk:
+        for i in range(args.steps):
+            ev[i][0].record(t.stream)
+            t.step()
+            ev[i][1].record(t.stream)
+            t.flush_l2()
+        barrier()
+    stats = t.eng.profile_read()
+    t.eng.profile_enable(False)
+    assert t.eng.check_device_error(t.stream) == 0
+    ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(ms)
+
+    # end to end through the C ABI with pinned host buffers
+    for _ in range(2):
+        t.step(host=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        t.flush_l2()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        t.step(host=True)
+        torch.cuda.synchronize()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_total = sum(e2e_ms)
+
+    if dist:
+        x = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device="cuda")
+        tdist.all_reduce(x, op=tdist.ReduceOp.MAX)
+        total_ms, e2e_total = x.tolist()
+    if rank != 0:
+        return None
+
+    hbm, bf16_peak, bf16_sus, peak_kind = load_peaks()
+    rep, att, kvw = stats["repos_rotate"], stats["segment_attn"], stats["kv_write"]
+    rep_ms = rep["ms"] / max(rep["launches"], 1)
+    att_ms = att["ms"] / max(att["launches"], 1)
+    rep_bytes = rep["bytes"] / max(rep["launches"], 1)
+    att_flops = att["flops"] / max(att["launches"], 1)
+    rot_tokens = rep_bytes / (2 * 8 * 128 * 2)  # token-layers per launch: read + write of 8 x 128 bf16
+    rep_gbs = rep_bytes / (rep_ms * 1e-3) / 1e9
+    att_tf = att_flops / (att_ms * 1e-3) / 1e12
+    share = {k: v["ms"] for k, v in stats.items()}
+    dominant = max(share, key=share.get)
+    h2d, d2h = t.io_bytes()
+    value = world * args.steps / (total_ms * 1e-3)
+    e2e_value = world * args.steps / (e2e_total * 1e-3)
+    if dominant == "segment_attn":
+        roof = {"kernel": "segment_attn", "bound": "tensor", "achieved": att_tf, "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": att_tf / bf16_peak, "traffic": None,
+                "peak_kind": f"{peak_kind} bf16 dense burst (sustained {bf16_sus})"}
+    else:
+        roof = {"kernel": "repos_rotate", "bound": "hbm", "achieved": rep_gbs, "peak": hbm, "unit": "GB/s",
+                "frac": rep_gbs / hbm, "traffic": None, "peak_kind": f"{peak_kind} HBM copy"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "flushed between steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "repos_rotate": {"rotated_tokens_per_s": rot_tokens / (rep_ms * 1e-3), "rotated_tokens_per_launch": rot_tokens,
+                         "GB/s": rep_gbs, "frac_of_hbm": rep_gbs / hbm, "frac_of_8TBs": rep_gbs / 8000.0,
+                         "ms_per_launch": rep_ms},
+        "segment_batch_attn": {"TFLOP/s": att_tf, "frac_of_bf16_dense": att_tf / bf16_peak,
+                               "frac_of_bf16_sustained": att_tf / bf16_sus if bf16_sus else None,
+                               "ms_per_launch": att_ms, "flops_per_launch": att_flops},
+        "kv_write": {"ms_per_step": kvw["ms"] / args.steps, "GB/s": kvw["bytes"] / max(kvw["ms"], 1e-9) / 1e6},
+        "ttft_equiv_ms": total_ms / args.steps,
+        "kernel_share": {k: v / max(sum(share.values()), 1e-9) for k, v in share.items()},
+        "roofline": roof,
+        "gpu_launches": int(sum(v["launches"] for v in stats.values())),
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_total / args.steps},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+class OracleTurn:
+    """The float64 oracle on the same turn: resident trajectory built once, then per step
+    the turn's bookkeeping, the full repos and attention on a sample of query rows."""
+
+    def __init__(self, seed=0):
+        from agentic_kv_cache_gb300 import synth
+        from oracle import attention, bf16, kernels
+        from oracle.cache import CacheModel
+        self.synth, self.bf16, self.kernels, self.attention = synth, bf16, kernels, attention
+        self.w = w = synth.llama8b_32k(seed=seed, fork=True)
+        s = w.shape
+        fork_at = next(i for i, op in enumerate(w.ops) if op[0] == "fork")
+        self.step_ops = w.ops[fork_at:]
+        self.model = CacheModel(w.n_pages, s.page_size)
+        self.kp = np.zeros((1, w.n_pages, s.n_kv_heads, s.page_size, s.d_rot), np.float32)
+        self.vp = np.zeros_like(self.kp)
+        self.names = {}
+        self.values = {}
+        for op in w.ops[:fork_at]:
+            if op[0] == "alloc":
+                self.names[op[1]] = self.model.seq_alloc()
+            elif op[0] == "append":
+                self._write(self.model.append(self.names[op[1]], op[2]), op[3], op[2])
+        new = next(op for op in self.step_ops if op[0] == "append")
+        self._values(new[3], new[2])
+        self.qb = bf16.round_bf16(synth.q_array(w).astype(np.float64))
+
+    def _values(self, key, n):
+        if key not in self.values:
+            k32, v32 = self.synth.kv_arrays(self.w, key, n)
+            self.values[key] = (self.bf16.round_bf16(k32.astype(np.float64)).astype(np.float32),
+                                self.bf16.round_bf16(v32.astype(np.float64)).astype(np.float32))
+        return self.values[key]
+
+    def _write(self, slots, key, n):
+        kb, vb = self._values(key, n)
+        idx = np.array(slots)
+        self.kp[:, idx[:, 0], :, idx[:, 2]] = kb.transpose(1, 0, 2, 3)
+        self.vp[:, idx[:, 1], :, idx[:, 2]] = vb.transpose(1, 0, 2, 3)
+
+    def step(self, rows):
+        """Run one turn (attention on `rows` sampled query rows); returns (seconds per full turn, parts)."""
+        s, m = self.w.shape, self.model
+        names = dict(self.names)
+        t0 = time.perf_counter()
+        for op in self.step_ops:
+            if op[0] == "fork":
+                names[op[1]] = m.seq_fork(names[op[2]], op[3])
+            elif op[0] == "drop":
+                m.drop(names[op[1]], op[2], op[3])
+            elif op[0] == "repos":
+                m.repos(names[op[1]], op[2], op[3], op[4])
+            elif op[0] == "append":
+                self._write(m.append(names[op[1]], op[2]), op[3], op[2])
+        g = self.w.segments[0]
+        runs = m.flush([names[g["seq"]]])
+        seg_runs, _ = m.segment_runs(names[g["seq"]], g["kv_end"], g["q_len"], g["hide"])
+        t_book = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        self.kernels.repos_runs(self.kp, runs, s.rope_base, s.rope_layout, out=self.kp)
+        t_rep = time.perf_counter() - t0
+        sample = np.linspace(0, g["q_len"] - 1, rows).astype(np.int64)
+        # attention = gather of the segment's KV (once per turn) + per-row work (scaled to all rows)
+        t0 = time.perf_counter()
+        k = self.kernels.gather(self.kp, 0, seg_runs, 0).astype(np.float64)
+        v = self.kernels.gather(self.vp, 0, seg_runs, 1).astype(np.float64)
+        t_gather = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        self.attention.segment_attention(self.qb, k, v, s.scale, rows=sample)
+        t_att = t_gather + (time.perf_counter() - t0) * g["q_len"] / rows
+        m.seq_free(names["F"])
+        return t_book + t_rep + t_att, dict(bookkeeping_s=t_book, repos_s=t_rep, attention_s=t_att,
+                                            gather_s=t_gather, rows=rows)
+
+
+def cpu_baseline(seconds=15.0):
+    ot = OracleTurn()
+    est, parts = ot.step(rows=16)
+    att_per_row = (parts["attention_s"] - parts["gather_s"]) / 2048
+    fixed = parts["bookkeeping_s"] + parts["repos_s"] + parts["gather_s"]
+    rows = int(np.clip((seconds - fixed) / max(att_per_row, 1e-6), 16, 2048))
+    est, parts = ot.step(rows=rows)
+    return {"value": 1.0 / est, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"float64 numpy oracle, one turn: full bookkeeping and repos, attention on {rows} of 2048 "
+                       f"query rows (all heads, full visible KV) scaled to 2048; BLAS threads = all host cores"),
+            "seconds_per_turn": est, "parts": parts}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    ot = OracleTurn()
+    for _ in range(args.warmup):
+        ot.step(rows=16)
+    times = [ot.step(rows=16)[0] for _ in range(args.steps)]
+    total = sum(times)
+    value = args.steps / total
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "n/a (host)", "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "per step: full bookkeeping and repos, attention on 16 of 2048 query rows "
+                                       "scaled to the full turn"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as tdist
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            tdist.init_process_group("nccl")
+        line = gpu_arm(args, rank, world)
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,250 @@
+/*
+ * akv.h -- C ABI of the GB300 agentic KV-cache engine (libakv.so).
+ *
+ * The engine keeps a paged bf16 KV cache for agent trajectories and applies
+ * the cache operations an agent harness issues instead of editing its prompt:
+ *
+ *   append  add the K/V of new tokens            ("Cache Engineering for Agents"
+ *   drop    hide a span from later attention       reading notes, section 1
+ *   repos   move retained keys to new positions    "Problem & Solution")
+ *   splice  replace a span by a stub (Leyline AMORTIZE)
+ *   attend  segment-batch attention of new queries over each segment's pages
+ *
+ * Sources, cited by page title and section:
+ *   [AKV-blog]  "AKV: Cache Engineering for Autonomous Agents and
+ *               State-Preserving Prefix Invalidation Bypass"
+ *   [AKV-notes] "Cache Engineering for Agents" (reading notes on Fu et al.)
+ *   [Leyline]   "Leyline: KV Cache Directives for Agentic Inference"
+ *
+ * Conventions (apply to every function):
+ *   - Every function returns akv_status.  A call that fails with AKV_ERR_ARG,
+ *     AKV_ERR_RANGE, AKV_ERR_NO_PAGES or AKV_ERR_OVERFLOW changes nothing.
+ *     AKV_ERR_CUDA means a CUDA call failed; the context should then be
+ *     destroyed.  akv_last_error() gives a message for the last failure.
+ *   - Spans [s, e) are half-open logical token indices of a sequence as the
+ *     harness sees it.  splice shifts the logical indices of later tokens.
+ *   - Positions and shifts are int32; an operation that would take a
+ *     position or a composed shift outside int32 fails with AKV_ERR_OVERFLOW.
+ *     A shift delta moves a key from position p to p + delta.
+ *   - The K/V pools are device memory owned by the caller and must stay
+ *     allocated while the context lives.  Pool memory must hold finite values
+ *     before first use (zero it): attention reads whole pages and masks the
+ *     slots it does not need, and a NaN there would leak through 0 * NaN.
+ *   - Data pointers passed to append / splice / attend may be device memory
+ *     or host memory (pinned for asynchronous copies).  Host inputs are copied
+ *     into library-owned device staging memory on the given stream; a host
+ *     output is copied back on the stream, so synchronise the stream before
+ *     reading it.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work of a call is enqueued on it asynchronously;
+ *     host bookkeeping changes at call time.  Use one stream per context, or
+ *     order the streams yourself.
+ *   - A context is not thread-safe; one host thread at a time.
+ *   - No C++ exception crosses this boundary.
+ */
+#ifndef AKV_H
+#define AKV_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define AKV_API __attribute__((visibility("default")))
+#else
+#define AKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum akv_status {
+  AKV_OK = 0,
+  AKV_ERR_ARG = 1,            /* bad argument (null pointer, dead sequence, bad config) */
+  AKV_ERR_RANGE = 2,          /* a span or index outside the sequence or buffer */
+  AKV_ERR_NO_PAGES = 4,       /* the page pool cannot supply the pages needed */
+  AKV_ERR_OVERFLOW = 5,       /* a position or composed shift would leave int32 */
+  AKV_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed */
+  AKV_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up a bounded wait (see akv_check_device_error) */
+  AKV_ERR_DEVICE = 8          /* a kernel's own bounds check failed */
+} akv_status;
+
+typedef enum akv_layout {
+  AKV_LAYOUT_GQA = 0, /* K and V per kv head; all of K is rotated */
+  AKV_LAYOUT_MLA = 1  /* K_pe (rotated) + one latent shared as K_nope and V ([Leyline] "Method") */
+} akv_layout;
+
+typedef enum akv_rope_layout {
+  AKV_ROPE_INTERLEAVED = 0, /* pairs (2j, 2j+1), as [AKV-blog] section 2 writes the rotation */
+  AKV_ROPE_HALF = 1         /* pairs (j, j + d_rot/2) */
+} akv_rope_layout;
+
+/* Model and pool shape of one context. */
+typedef struct akv_config {
+  int32_t layout;       /* akv_layout */
+  int32_t n_layers;     /* layers held in each pool */
+  int32_t n_q_heads;    /* query heads; a multiple of n_kv_heads, n_q_heads/n_kv_heads divides 128 */
+  int32_t n_kv_heads;   /* kv heads (GQA); must be 1 under MLA */
+  int32_t d_rot;        /* rotated key width: head_dim (GQA) or K_pe width (MLA); even */
+  int32_t d_v;          /* value width: head_dim (GQA, = d_rot) or latent width (MLA) */
+  int32_t page_size;    /* tokens per page: 16, 32, 64 or 128 */
+  int32_t n_pages;      /* pages in each pool */
+  int32_t rope_layout;  /* akv_rope_layout */
+  int32_t reserved;     /* must be 0 */
+  double rope_base;     /* RoPE base: theta_j = rope_base^(-2j/d_rot) */
+} akv_config;
+
+/* Caller-owned device pools (bf16).  Row-major layouts:
+ *   k_pool [n_layers][n_pages][n_kv_heads][page_size][d_rot]   (K, or K_pe under MLA)
+ *   v_pool [n_layers][n_pages][n_kv_heads][page_size][d_v]     (V, or the latent under MLA)
+ * Both base addresses must be 16-byte aligned (TMA). */
+typedef struct akv_pools {
+  void* k_pool;
+  void* v_pool;
+} akv_pools;
+
+/* One attention segment ([AKV-notes] section 3 "Segment-Batch Attention").
+ * The segment sees the visible (not dropped) tokens of sequence `seq` in
+ * logical indices [0, kv_end), minus the `n_hide` extra spans in `hide`
+ * (host array of [a, b) pairs), in logical order.  Its queries are tokens
+ * [kv_end - q_len, kv_end), which must be visible, not hidden, and hence the
+ * last q_len entries; query row i sees entries j <= kv_len - q_len + i
+ * (causal, aligned bottom-right).  Their Q rows are q[q_row0 .. q_row0+q_len). */
+typedef struct akv_segment {
+  int32_t seq;
+  int32_t q_len;
+  int64_t kv_end;
+  int64_t q_row0;
+  const int64_t* hide;
+  int32_t n_hide;
+  int32_t reserved;   /* must be 0 */
+} akv_segment;
+
+/* Per-kernel launch statistics collected while profiling is enabled. */
+typedef struct akv_kernel_stats {
+  int64_t launches[4];   /* [0] kv_write  [1] repos_rotate  [2] segment_attn  [3] reserved */
+  double ms[4];          /* summed CUDA-event time of those launches, milliseconds */
+  double bytes[4];       /* algorithmic bytes moved (kv_write, repos_rotate) */
+  double flops[4];       /* algorithmic FLOPs (segment_attn) */
+} akv_kernel_stats;
+
+typedef struct akv_ctx akv_ctx;
+
+/* Create a context.  pools == NULL gives a metadata-only context: every
+ * bookkeeping rule runs, no CUDA call is made and data pointers are ignored
+ * (for planning and for checking the bookkeeping on hosts without a GPU).
+ * Otherwise the current CUDA device is used and TMA descriptors of the
+ * pools are built once here.  *out receives the context. */
+AKV_API akv_status akv_create(const akv_config* cfg, const akv_pools* pools, akv_ctx** out);
+
+/* Destroy a context and free the library-owned device and host memory.
+ * Synchronises the device work the context has enqueued. */
+AKV_API akv_status akv_destroy(akv_ctx* ctx);
+
+/* Message of the last failure on this context ("" if none).  Valid until the next call. */
+AKV_API const char* akv_last_error(const akv_ctx* ctx);
+
+/* "kv_alloc": a new empty sequence; ids are the lowest unused non-negative integers. */
+AKV_API akv_status akv_seq_alloc(akv_ctx* ctx, int32_t* seq_out);
+
+/* A new sequence sharing tokens [0, n_prefix) of `src` by page reference
+ * (a shared radix prefix; [AKV-blog] section 3, copy-on-write page references).
+ * Copies no data.  Pending shifts and drop marks are inherited. */
+AKV_API akv_status akv_seq_fork(akv_ctx* ctx, int32_t src, int64_t n_prefix, int32_t* seq_out);
+
+/* Release a sequence; pages no live sequence references return to the pool. */
+AKV_API akv_status akv_seq_free(akv_ctx* ctx, int32_t seq);
+
+/* Logical length of a sequence (tokens, including dropped ones). */
+AKV_API akv_status akv_seq_len(akv_ctx* ctx, int32_t seq, int64_t* n_out);
+
+/* "append" ([AKV-notes] section 1): add n tokens whose keys are already
+ * RoPE-rotated at their positions.
+ *   k: bf16 [n_layers][n][n_kv_heads][d_rot]   v: bf16 [n_layers][n][n_kv_heads][d_v]
+ *   pos: host int32[n], or NULL = last position + 1 counting up (0 if empty).
+ * The page of the last token is filled further when both its K and V page
+ * are referenced by this sequence only; otherwise new pages are opened
+ * (lowest free id first). */
+AKV_API akv_status akv_append(akv_ctx* ctx, int32_t seq, int64_t n, const void* k, const void* v,
+                      const int32_t* pos, void* stream);
+
+/* "drop" ([AKV-blog] section 2 "The Drop Primitive"): tokens [s, e) become
+ * invisible to later attention.  Frees nothing and writes no device memory. */
+AKV_API akv_status akv_drop(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e);
+
+/* "repos" ([AKV-blog] section 2 "The Repos Primitive and Rotary Position
+ * Embeddings"; [Leyline] "Method", composition R(a)R(b) = R(a+b)): record a
+ * shift `delta` for tokens [s, e).  Shifts compose per token by addition; the
+ * keys are rotated once, by the composed shift, at the next flush. */
+AKV_API akv_status akv_repos(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int32_t delta);
+
+/* Leyline AMORTIZE splice ([Leyline] "Method", D = (s, e, R, AMORTIZE)):
+ * remove tokens [s, e) from the sequence, insert n_stub stub tokens at s
+ * (written to fresh pages), and shift every later token by
+ * n_stub - (e - s).  Under MLA only K_pe is rotated; the latent (K_nope and V)
+ * is untouched.  k_stub / v_stub as in akv_append with n = n_stub; pos NULL =
+ * the position of token s counting up. */
+AKV_API akv_status akv_splice(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int64_t n_stub,
+                      const void* k_stub, const void* v_stub, const int32_t* pos, void* stream);
+
+/* Materialise pending shifts (the repos_rotate kernel): every visible token
+ * with a pending shift is rotated once, K'[i] = R(delta_i) K[i], in fp32 with
+ * one rounding to bf16.  A K page referenced by this sequence only is rotated
+ * in place; a shared one is first copied (copy-on-write of the K page only,
+ * [AKV-notes] section 3 "Cache Management").  seq = -1 flushes every live
+ * sequence in increasing id order. */
+AKV_API akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream);
+
+/* Segment-batch attention for one layer (the segment_batch_attn kernel):
+ * flushes the segments' sequences first, then one launch covers every segment.
+ *   q:   bf16 [n_q_rows][n_q_heads][d_qk]  (d_qk = d_rot under GQA; d_v + d_rot
+ *        under MLA, laid out [latent part | rope part]); already RoPE'd.
+ *   o:   bf16 [n_q_rows][n_q_heads][d_v]; rows outside the segments are not written.
+ *   lse: float [n_q_rows][n_q_heads] natural-log softmax normaliser, or NULL.
+ *   scale: softmax scale (1/sqrt(d_k)).
+ * Query head h reads kv head h / (n_q_heads / n_kv_heads). */
+AKV_API akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs,
+                      const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
+                      void* stream);
+
+/* --- inspection (host memory only; used by the bookkeeping tests) -------- */
+
+/* Per-token state of a sequence into caller arrays of akv_seq_len entries
+ * (any may be NULL): K page, V page, slot, stored position, pending shift,
+ * visibility (1 visible, 0 dropped). */
+AKV_API akv_status akv_export_state(akv_ctx* ctx, int32_t seq, int32_t* k_page, int32_t* v_page,
+                            int32_t* slot, int32_t* pos, int32_t* delta, uint8_t* visible);
+
+/* Reference counts of every page: k_rc, v_rc int32[n_pages] (either may be NULL). */
+AKV_API akv_status akv_refcounts(akv_ctx* ctx, int32_t* k_rc, int32_t* v_rc);
+
+/* Run list of the last flush that had work: 5 int32 per run
+ * (src K page, dst K page, slot_lo, slot_hi, delta), at most `cap` runs
+ * written; *n_runs receives the full count. */
+AKV_API akv_status akv_last_flush_runs(akv_ctx* ctx, int32_t* out, int64_t cap, int64_t* n_runs);
+
+/* Run list a segment would attend over (after its sequence is flushed):
+ * 4 int32 per run (K page, V page, slot_lo, slot_hi); *kv_len the entry count.
+ * Fails with AKV_ERR_ARG if a visible token of the segment has a pending shift. */
+AKV_API akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_t* out, int64_t cap,
+                            int64_t* n_runs, int64_t* kv_len);
+
+/* --- device status and measurement --------------------------------------- */
+
+/* Synchronise `stream` and read the device error word of the context's
+ * kernels: *code = 0, AKV_ERR_DEVICE_TIMEOUT or AKV_ERR_DEVICE.  The word
+ * is cleared after reading.  Returns the same status as *code. */
+AKV_API akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code);
+
+/* Enable (1) or disable (0) per-launch CUDA-event timing of the context's
+ * kernels; enabling clears the statistics. */
+AKV_API akv_status akv_profile_enable(akv_ctx* ctx, int32_t on);
+
+/* Synchronise the timed launches and return the statistics gathered since
+ * profiling was enabled. */
+AKV_API akv_status akv_profile_read(akv_ctx* ctx, akv_kernel_stats* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AKV_H */

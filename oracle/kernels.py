@@ -18,14 +18,17 @@ import numpy as np
 from . import attention, bf16, rope
 
 
-def repos_runs(kpool, runs, base, layout="interleaved"):
+def repos_runs(kpool, runs, base, layout="interleaved", out=None):
     """Apply a flush run list [(src, dst, lo, hi, delta)] to a copy of kpool.
 
     Every run reads rows [lo, hi) of page src in every layer and head of the
     pool as it was before the flush, rotates them by delta in float64, rounds
-    to bfloat16 and writes them to the same rows of page dst.
+    to bfloat16 and writes them to the same rows of page dst.  ``out=kpool``
+    updates the pool in place: no run reads a row another run writes (a
+    destination page is either the run's own source or a fresh copy).
     """
-    out = np.array(kpool, dtype=np.float64, copy=True)
+    if out is None:
+        out = np.array(kpool, dtype=np.float64, copy=True)
     for src, dst, lo, hi, delta in runs:
         rows = kpool[:, src, :, lo:hi, :]
         out[:, dst, :, lo:hi, :] = bf16.round_bf16(rope.repos(rows, np.full(rows.shape[:-1], delta), base, layout))

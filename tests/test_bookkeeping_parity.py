@@ -1,0 +1,183 @@
+"""The engine's bookkeeping (metadata-only context, no GPU) must equal the
+oracle's independent model bit for bit: per-token page map, slots, positions,
+pending shifts, visibility, page reference counts, flush run lists and segment
+run lists, and the status of every rejected operation."""
+import numpy as np
+import pytest
+
+from agentic_kv_cache_gb300 import akv, build, runner, synth
+from oracle.cache import CacheError, CacheModel
+from drive import oracle_model, oracle_run_ops
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+
+
+def engine_for(w):
+    return akv.Engine(akv.config_from_shape(w.shape, w.n_pages))
+
+
+def assert_same_state(eng, model, names_e, names_o):
+    for name in names_e:
+        if names_o[name] not in model.seqs:
+            continue
+        a = eng.export_state(names_e[name])
+        b = model.state(names_o[name])
+        for k in ("k_page", "v_page", "slot", "pos", "delta", "visible"):
+            assert np.array_equal(a[k], np.asarray(b[k], np.int32)), (name, k)
+    ke, ve = eng.refcounts()
+    ko, vo = model.refcounts()
+    assert np.array_equal(ke, ko) and np.array_equal(ve, vo)
+
+
+WORKLOADS = [
+    ("tiny", lambda: synth.tiny()),
+    ("llama8b_32k", lambda: synth.llama8b_32k()),
+    ("llama8b_32k_fork", lambda: synth.llama8b_32k(fork=True)),
+    ("sessions_64k_small", lambda: synth.sessions_64k(n_layers=2, n_sessions=3, prefix=1024, per_session=8192,
+                                                      q_per_seg=128, span_len=(64, 512))),
+    ("mla_c4", lambda: synth.mla_dsv2lite(n_layers=2, concurrency=4)),
+    ("llama70b_small", lambda: synth.llama70b_128k(n_layers=2, total=16384, n_branches=6, q_per_branch=256)),
+]
+
+
+@pytest.mark.parametrize("name,make", WORKLOADS, ids=[n for n, _ in WORKLOADS])
+def test_workload_bookkeeping_matches_oracle(name, make):
+    w = make()
+    eng, model = engine_for(w), oracle_model(w)
+    ne = runner.run_ops(eng, w)
+    no = oracle_run_ops(model, w)
+    assert ne == no
+    assert_same_state(eng, model, ne, no)
+    # the flush that attention triggers: sequences of the segments, in id order
+    ids = sorted({no[s["seq"]] for s in w.segments})
+    runs_o = model.flush(ids)
+    for i in ids:
+        eng.flush(i)
+    assert_same_state(eng, model, ne, no)
+    for s in w.segments:
+        seg = dict(seq=ne[s["seq"]], kv_end=s["kv_end"], q_len=s["q_len"], hide=np.asarray(s["hide"]).reshape(-1))
+        runs_e, kv_e = eng.segment_runs(seg)
+        runs_m, kv_m = model.segment_runs(no[s["seq"]], s["kv_end"], s["q_len"], s["hide"])
+        assert kv_e == kv_m
+        assert np.array_equal(runs_e, np.asarray(runs_m, np.int32).reshape(-1, 4))
+
+
+@pytest.mark.parametrize("name,make", WORKLOADS[:3] + WORKLOADS[4:5], ids=[n for n, _ in WORKLOADS[:3] + WORKLOADS[4:5]])
+def test_flush_run_lists_match_oracle(name, make):
+    w = make()
+    eng, model = engine_for(w), oracle_model(w)
+    ne = runner.run_ops(eng, w)
+    no = oracle_run_ops(model, w)
+    runs_o = model.flush()          # every live sequence, increasing id
+    eng.flush(-1)
+    assert np.array_equal(eng.last_flush_runs(), np.asarray(runs_o, np.int32).reshape(-1, 5))
+    assert_same_state(eng, model, ne, no)
+
+
+def apply_both(eng, model, op, args):
+    """Run one operation on both sides; both must succeed or fail with the same status."""
+    err_e = err_o = None
+    out_e = out_o = None
+    try:
+        out_e = getattr(eng, op)(*args)
+    except akv.AKVError as x:
+        err_e = x.code
+    try:
+        out_o = getattr(model, op)(*args)
+    except CacheError as x:
+        err_o = x.code
+    assert err_e == err_o, (op, args, err_e, err_o)
+    return out_e, out_o, err_e
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_operations_match_oracle(seed):
+    rng = np.random.default_rng(100 + seed)
+    P = int(rng.choice([16, 32]))
+    n_pages = int(rng.integers(12, 80))
+    cfg = dict(layout=0, n_layers=1, n_q_heads=4, n_kv_heads=1, d_rot=64, d_v=64, page_size=P, n_pages=n_pages,
+               rope_layout=0, rope_base=1e4)
+    eng, model = akv.Engine(cfg), CacheModel(n_pages, P)
+    ids = [eng.seq_alloc()]
+    assert model.seq_alloc() == ids[0]
+    for step in range(150):
+        live = sorted(model.seqs)
+        s = live[int(rng.integers(len(live)))]
+        n = len(model.seqs[s])
+        op = rng.choice(["append", "fork", "drop", "repos", "splice", "flush", "flush_all", "free", "seg", "bad"])
+        if op == "append":
+            apply_both(eng, model, "append", (s, int(rng.integers(0, 3 * P))))
+        elif op == "fork" and len(live) < 8:
+            e_id, o_id, err = apply_both(eng, model, "seq_fork", (s, int(rng.integers(0, n + 1))))
+            assert e_id == o_id
+        elif op == "drop":
+            a = int(rng.integers(0, n + 1))
+            apply_both(eng, model, "drop", (s, a, int(rng.integers(a, n + 1))))
+        elif op == "repos":
+            a = int(rng.integers(0, n + 1))
+            d = int(rng.integers(-3000, 3000)) if rng.random() < 0.9 else int(rng.choice([2 ** 31 - 1, -2 ** 31]))
+            apply_both(eng, model, "repos", (s, a, int(rng.integers(a, n + 1)), d))
+        elif op == "splice":
+            a = int(rng.integers(0, n + 1))
+            apply_both(eng, model, "splice", (s, a, int(rng.integers(a, n + 1)), int(rng.integers(0, 2 * P))))
+        elif op == "flush":
+            try:
+                runs_o = model.flush([s])
+                err_o = None
+            except CacheError as x:
+                err_o, runs_o = x.code, []
+            try:
+                eng.flush(s)
+                err_e = None
+            except akv.AKVError as x:
+                err_e = x.code
+            assert err_e == err_o
+            if runs_o:
+                assert np.array_equal(eng.last_flush_runs(), np.asarray(runs_o, np.int32).reshape(-1, 5))
+        elif op == "flush_all":
+            try:
+                runs_o = model.flush()
+                err_o = None
+            except CacheError as x:
+                err_o, runs_o = x.code, []
+            try:
+                eng.flush(-1)
+                err_e = None
+            except akv.AKVError as x:
+                err_e = x.code
+            assert err_e == err_o
+            if runs_o:
+                assert np.array_equal(eng.last_flush_runs(), np.asarray(runs_o, np.int32).reshape(-1, 5))
+        elif op == "free" and len(live) > 1:
+            apply_both(eng, model, "seq_free", (s,))
+        elif op == "seg" and n:
+            q = int(rng.integers(1, min(n, 8) + 1))
+            a = int(rng.integers(0, n - q + 1))
+            hide = [(a, int(rng.integers(a, n - q + 1)))] if rng.random() < 0.5 else []
+            try:
+                ro, ko = model.segment_runs(s, n, q, hide)
+                err_o = None
+            except CacheError as x:
+                err_o = x.code
+            try:
+                re_, ke = eng.segment_runs(dict(seq=s, kv_end=n, q_len=q, hide=np.asarray(hide).reshape(-1)))
+                err_e = None
+            except akv.AKVError as x:
+                err_e = x.code
+            assert err_e == err_o
+            if err_o is None:
+                assert ke == ko and np.array_equal(re_, np.asarray(ro, np.int32).reshape(-1, 4))
+        elif op == "bad":
+            apply_both(eng, model, "drop", (s, -1, 2))
+            apply_both(eng, model, "repos", (s, 0, n + 1, 1))
+        # full comparison after every step
+        for sid in model.seqs:
+            a, b = eng.export_state(sid), model.state(sid)
+            for k in b:
+                assert np.array_equal(a[k], np.asarray(b[k], np.int32)), (step, op, k)
+        ke, ve = eng.refcounts()
+        ko, vo = model.refcounts()
+        assert np.array_equal(ke, ko) and np.array_equal(ve, vo), (step, op)

@@ -77,6 +77,7 @@ def load(path=LIB_PATH):
         "akv_splice": [P, I32, I64, I64, I64, P, P, P, P],
         "akv_flush": [P, I32, P],
         "akv_attend": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
+        "akv_debug_rotate_f32": [P, P, I32, P, P],
         "akv_export_state": [P, I32, P, P, P, P, P, P],
         "akv_refcounts": [P, P, P],
         "akv_last_flush_runs": [P, P, I64, pi64],
@@ -213,6 +214,12 @@ class Engine:
         arr, keep = self.make_segments(segs)
         self._check(self.lib.akv_attend(self.h, layer, arr, len(segs), _ptr(q), n_q_rows, _ptr(o), _ptr(lse),
                                         float(scale), _stream(stream)))
+
+    def debug_rotate_f32(self, runs, out, stream=None):
+        """runs: int array [n, 4] (K page, lo, hi, delta); out: device float32 tensor
+        [n_layers][sum(hi - lo)][n_kv_heads][d_rot]."""
+        r = np.ascontiguousarray(np.asarray(runs, dtype=np.int32).reshape(-1, 4))
+        self._check(self.lib.akv_debug_rotate_f32(self.h, r.ctypes.data, r.shape[0], _ptr(out), _stream(stream)))
 
     # ----------------------------------------------------------- inspection
     def export_state(self, seq):

@@ -81,6 +81,13 @@ cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* 
                                 int n_layers, int heads, int d_rot, int page, int64_t n_pages,
                                 bool half_layout, cudaStream_t st);
 
+// Float32 debug mode of repos_rotate: rotated rows of each run go to
+// out[L][total_rows][H][d_rot] (rows of run r start at row_off[r]); the pool
+// is only read.
+cudaError_t launch_repos_rotate_f32(const void* kpool, const RunDesc* runs, const float2* cs, const int32_t* row_off,
+                                    int64_t total_rows, float* out, int n_runs, int n_layers, int heads, int d_rot,
+                                    int page, int64_t n_pages, bool half_layout, cudaStream_t st);
+
 // dim: d_rot = d_v (GQA, 64 or 128).
 cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st);
 

@@ -282,6 +282,7 @@ struct akv_ctx {
   bool prof = false;
   struct Timed {
     int kernel;
+    int launches;
     cudaEvent_t a, b;
     double bytes, flops;
   };
@@ -332,8 +333,9 @@ struct akv_ctx {
     cuda_check(cudaEventCreate(&e), "cudaEventCreate");
     return e;
   }
-  void begin_timed(int kernel, double bytes, double flops, cudaStream_t st, Timed& t) {
+  void begin_timed(int kernel, double bytes, double flops, cudaStream_t st, Timed& t, int launches = 1) {
     t.kernel = kernel;
+    t.launches = launches;
     t.bytes = bytes;
     t.flops = flops;
     t.a = t.b = nullptr;
@@ -352,7 +354,7 @@ struct akv_ctx {
       cuda_check(cudaEventSynchronize(t.b), "cudaEventSynchronize");
       float ms = 0.f;
       cuda_check(cudaEventElapsedTime(&ms, t.a, t.b), "cudaEventElapsedTime");
-      stats.launches[t.kernel] += 1;
+      stats.launches[t.kernel] += t.launches;
       stats.ms[t.kernel] += ms;
       stats.bytes[t.kernel] += t.bytes;
       stats.flops[t.kernel] += t.flops;
@@ -385,7 +387,7 @@ struct akv_ctx {
     void* dv = nullptr;
     up.upload({{krow.data(), krow.size() * 4, &dk}, {vrow.data(), vrow.size() * 4, &dv}}, st);
     Timed t;
-    begin_timed(kKvWrite, double(kbytes + vbytes) * 2.0, 0.0, st, t);
+    begin_timed(kKvWrite, double(kbytes + vbytes) * 2.0, 0.0, st, t, 2);
     cuda_check(akv::launch_kv_write(kd, kpool, static_cast<int32_t*>(dk), n, cfg.n_layers, cfg.n_kv_heads,
                                     cfg.d_rot, cfg.page_size, cfg.n_pages, st),
                "kv_write launch");
@@ -598,15 +600,7 @@ struct akv_ctx {
     if (!runs.empty()) last_runs.swap(flat);
     if (meta || runs.empty()) return;
 
-    // (cos, sin)(delta * theta_j) evaluated in float64, stored as float32.
-    const int half = cfg.d_rot / 2;
-    std::vector<float2> cs(deltas.size() * half);
-    for (size_t d = 0; d < deltas.size(); ++d)
-      for (int j = 0; j < half; ++j) {
-        const double th = std::pow(cfg.rope_base, -2.0 * j / cfg.d_rot);
-        const double a = double(deltas[d]) * th;
-        cs[d * half + j] = make_float2(float(std::cos(a)), float(std::sin(a)));
-      }
+    std::vector<float2> cs = angle_table(deltas);
     void* druns = nullptr;
     void* dcs = nullptr;
     up.upload({{runs.data(), runs.size() * sizeof(akv::RunDesc), &druns}, {cs.data(), cs.size() * sizeof(float2), &dcs}},
@@ -621,6 +615,57 @@ struct akv_ctx {
                                         cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, st),
                "repos_rotate launch");
     end_timed(t, st);
+    up.done(st);
+  }
+
+  // (cos, sin)(delta * theta_j) for each distinct shift, evaluated in float64
+  // and stored as float32: [deltas][d_rot / 2].
+  std::vector<float2> angle_table(const std::vector<int32_t>& deltas) const {
+    const int half = cfg.d_rot / 2;
+    std::vector<float2> cs(deltas.size() * half);
+    for (size_t d = 0; d < deltas.size(); ++d)
+      for (int j = 0; j < half; ++j) {
+        const double th = std::pow(cfg.rope_base, -2.0 * j / cfg.d_rot);
+        const double a = double(deltas[d]) * th;
+        cs[d * half + j] = make_float2(float(std::cos(a)), float(std::sin(a)));
+      }
+    return cs;
+  }
+
+  void debug_rotate_f32(const int32_t* in, int32_t n_runs, float* out, cudaStream_t st) {
+    if (meta) fail(AKV_ERR_ARG, "metadata-only context has no pools");
+    if (n_runs < 0 || (n_runs > 0 && (!in || !out))) fail(AKV_ERR_ARG, "bad run list");
+    std::vector<akv::RunDesc> runs(n_runs);
+    std::vector<int32_t> row_off(n_runs), deltas;
+    std::unordered_map<int32_t, int32_t> didx;
+    int64_t rows = 0;
+    for (int32_t r = 0; r < n_runs; ++r) {
+      const int32_t pg = in[4 * r], lo = in[4 * r + 1], hi = in[4 * r + 2], d = in[4 * r + 3];
+      if (pg < 0 || pg >= cfg.n_pages || lo < 0 || lo >= hi || hi > cfg.page_size)
+        fail(AKV_ERR_RANGE, "run %d outside the pool", r);
+      auto it = didx.find(d);
+      if (it == didx.end()) {
+        it = didx.emplace(d, int32_t(deltas.size())).first;
+        deltas.push_back(d);
+      }
+      runs[r] = akv::RunDesc{pg, pg, lo | (hi << 16), it->second};
+      row_off[r] = int32_t(rows);
+      rows += hi - lo;
+    }
+    if (n_runs == 0) return;
+    std::vector<float2> cs = angle_table(deltas);
+    void* druns = nullptr;
+    void* dcs = nullptr;
+    void* doff = nullptr;
+    up.upload({{runs.data(), runs.size() * sizeof(akv::RunDesc), &druns},
+               {cs.data(), cs.size() * sizeof(float2), &dcs},
+               {row_off.data(), row_off.size() * 4, &doff}},
+              st);
+    cuda_check(akv::launch_repos_rotate_f32(kpool, static_cast<akv::RunDesc*>(druns), static_cast<float2*>(dcs),
+                                            static_cast<int32_t*>(doff), rows, out, n_runs, cfg.n_layers,
+                                            cfg.n_kv_heads, cfg.d_rot, cfg.page_size, cfg.n_pages,
+                                            cfg.rope_layout == AKV_ROPE_HALF, st),
+               "repos_rotate f32 launch");
     up.done(st);
   }
 
@@ -1058,6 +1103,10 @@ akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream) {
 akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
                       int64_t n_q_rows, void* o, float* lse, float scale, void* stream) {
   return guard(ctx, [&] { ctx->attend(layer, segs, n_segs, q, n_q_rows, o, lse, scale, as_stream(stream)); });
+}
+
+akv_status akv_debug_rotate_f32(akv_ctx* ctx, const int32_t* runs, int32_t n_runs, float* out, void* stream) {
+  return guard(ctx, [&] { ctx->debug_rotate_f32(runs, n_runs, out, as_stream(stream)); });
 }
 
 akv_status akv_export_state(akv_ctx* ctx, int32_t seq, int32_t* k_page, int32_t* v_page, int32_t* slot,

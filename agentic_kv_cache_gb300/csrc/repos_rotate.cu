@@ -11,6 +11,10 @@
 // every layer and kv head.  dst == src rotates in place; dst != src is the
 // copy-on-write of a shared page ([AKV-notes] section 3 "Cache Management").
 //
+// A float32-output debug mode of the same kernel (launch_repos_rotate_f32)
+// writes the unrounded rotation of given rows to a dense array instead of the
+// pool, so the rotation arithmetic can be checked against float64 directly.
+//
 // Design: HBM-bound streaming (0.75 FLOP/B).  A CTA takes one (layer, run)
 // unit: H * (hi - lo) rows of d_rot bf16, i.e. up to 32 KiB for a full page of
 // 8 heads x 16 slots x 128 dims, contiguous in the pool.  Every thread moves
@@ -27,46 +31,46 @@
 namespace akv {
 namespace {
 
-__device__ __forceinline__ uint32_t rot_pair(uint32_t xy, float c, float s) {
+__device__ __forceinline__ float2 rot2(uint32_t xy, float c, float s) {
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&xy);
   const float2 f = __bfloat1622float2(b);
-  const float y0 = fmaf(c, f.x, -s * f.y);
-  const float y1 = fmaf(s, f.x, c * f.y);
-  __nv_bfloat162 r = __floats2bfloat162_rn(y0, y1);
+  return make_float2(fmaf(c, f.x, -s * f.y), fmaf(s, f.x, c * f.y));
+}
+
+__device__ __forceinline__ uint32_t pack(float2 y) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(y.x, y.y);
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// Interleaved pairs (2j, 2j+1): one 16-byte vector holds pairs 4v .. 4v+3.
-__device__ __forceinline__ uint4 rot_vec_interleaved(uint4 x, const float2* __restrict__ cs_row, int v) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v + 2));
-  x.x = rot_pair(x.x, a.x, a.y);
-  x.y = rot_pair(x.y, a.z, a.w);
-  x.z = rot_pair(x.z, b.x, b.y);
-  x.w = rot_pair(x.w, b.z, b.w);
-  return x;
-}
-
-__device__ __forceinline__ void rot_halves(uint32_t& a, uint32_t& b, float c0, float s0, float c1, float s1) {
-  // a holds first-half elements e, e+1; b the matching second-half elements.
+// Both halves of a (j, j + D/2) pair: a holds first-half elements e, e+1; b
+// the matching second-half elements.
+__device__ __forceinline__ void rot_halves(uint32_t a, uint32_t b, float c0, float s0, float c1, float s1,
+                                           float2& ya, float2& yb) {
   __nv_bfloat162 ab = *reinterpret_cast<__nv_bfloat162*>(&a);
   __nv_bfloat162 bb = *reinterpret_cast<__nv_bfloat162*>(&b);
   const float2 fa = __bfloat1622float2(ab), fb = __bfloat1622float2(bb);
-  __nv_bfloat162 ra = __floats2bfloat162_rn(fmaf(c0, fa.x, -s0 * fb.x), fmaf(c1, fa.y, -s1 * fb.y));
-  __nv_bfloat162 rb = __floats2bfloat162_rn(fmaf(s0, fa.x, c0 * fb.x), fmaf(s1, fa.y, c1 * fb.y));
-  a = *reinterpret_cast<uint32_t*>(&ra);
-  b = *reinterpret_cast<uint32_t*>(&rb);
+  ya = make_float2(fmaf(c0, fa.x, -s0 * fb.x), fmaf(c1, fa.y, -s1 * fb.y));
+  yb = make_float2(fmaf(s0, fa.x, c0 * fb.x), fmaf(s1, fa.y, c1 * fb.y));
 }
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
-template <int D>
+// Where a rotated 16-byte vector goes: back into the pool as bf16 (the
+// product path), or, in the float32 debug mode, into a dense float32 array
+// [L][rows][H][D] so the rotation can be checked before rounding.
+struct F32Out {
+  float* out;
+  const int32_t* row_off;  // first output row of each run
+  int64_t total_rows;
+};
+
+template <int D, bool F32>
 __global__ void __launch_bounds__(kThreads) repos_interleaved_kernel(uint4* __restrict__ pool,
                                                                    const RunDesc* __restrict__ runs,
                                                                    const float2* __restrict__ cs, int n_runs,
                                                                    int n_layers, int heads, int page,
-                                                                   int64_t n_pages) {
+                                                                   int64_t n_pages, F32Out f32) {
   constexpr int V = D / 8;  // vectors per row
   const int64_t page_vecs = int64_t(heads) * page * V;
   const int64_t layer_vecs = page_vecs * n_pages;
@@ -83,31 +87,43 @@ __global__ void __launch_bounds__(kThreads) repos_interleaved_kernel(uint4* __re
     const int total = heads * per_head;
     for (int base = 0; base < total; base += kThreads * kUnroll) {
       uint4 x[kUnroll];
-      int off[kUnroll];
+      int idx[kUnroll];
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
-        const int i = base + k * kThreads + int(threadIdx.x);
-        off[k] = -1;
-        if (i < total) {
-          const int h = i / per_head;
-          const int rem = i - h * per_head;  // (slot - lo) * V + v
-          off[k] = (h * page + lo) * V + rem;
-          x[k] = __ldcs(src + off[k]);
+        idx[k] = base + k * kThreads + int(threadIdx.x);
+        if (idx[k] < total) {
+          const int h = idx[k] / per_head;
+          x[k] = __ldcs(src + (h * page + lo) * V + (idx[k] - h * per_head));
         }
       }
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
-        if (off[k] >= 0) __stcs(dst + off[k], rot_vec_interleaved(x[k], cs_row, off[k] % V));
+        if (idx[k] >= total) continue;
+        const int h = idx[k] / per_head;
+        const int rem = idx[k] - h * per_head;  // (slot - lo) * V + v
+        const int v = rem % V;
+        const float4 a = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v + 2));
+        const float2 y0 = rot2(x[k].x, a.x, a.y), y1 = rot2(x[k].y, a.z, a.w);
+        const float2 y2 = rot2(x[k].z, b.x, b.y), y3 = rot2(x[k].w, b.z, b.w);
+        if constexpr (F32) {
+          const int64_t row = layer * f32.total_rows + f32.row_off[r] + rem / V;
+          float4* o = reinterpret_cast<float4*>(f32.out + (row * heads + h) * D + v * 8);
+          o[0] = make_float4(y0.x, y0.y, y1.x, y1.y);
+          o[1] = make_float4(y2.x, y2.y, y3.x, y3.y);
+        } else {
+          __stcs(dst + (h * page + lo) * V + rem, make_uint4(pack(y0), pack(y1), pack(y2), pack(y3)));
+        }
       }
     }
   }
 }
 
-template <int D>
+template <int D, bool F32>
 __global__ void __launch_bounds__(kThreads) repos_half_kernel(uint4* __restrict__ pool,
                                                             const RunDesc* __restrict__ runs,
                                                             const float2* __restrict__ cs, int n_runs, int n_layers,
-                                                            int heads, int page, int64_t n_pages) {
+                                                            int heads, int page, int64_t n_pages, F32Out f32) {
   constexpr int V = D / 8;
   constexpr int HV = V / 2;  // vector pairs per row: (v, v + V/2)
   const int64_t page_vecs = int64_t(heads) * page * V;
@@ -128,23 +144,34 @@ __global__ void __launch_bounds__(kThreads) repos_half_kernel(uint4* __restrict_
       const int rem = i - h * per_head;
       const int row = rem / HV, v = rem % HV;
       const int off = (h * page + lo + row) * V + v;
-      uint4 a = __ldcs(src + off), b = __ldcs(src + off + HV);
+      const uint4 a = __ldcs(src + off), b = __ldcs(src + off + HV);
       const float4* c4 = reinterpret_cast<const float4*>(cs_row + 8 * v);
       const float4 c01 = __ldg(c4), c23 = __ldg(c4 + 1), c45 = __ldg(c4 + 2), c67 = __ldg(c4 + 3);
-      rot_halves(a.x, b.x, c01.x, c01.y, c01.z, c01.w);
-      rot_halves(a.y, b.y, c23.x, c23.y, c23.z, c23.w);
-      rot_halves(a.z, b.z, c45.x, c45.y, c45.z, c45.w);
-      rot_halves(a.w, b.w, c67.x, c67.y, c67.z, c67.w);
-      __stcs(dst + off, a);
-      __stcs(dst + off + HV, b);
+      float2 ya[4], yb[4];
+      rot_halves(a.x, b.x, c01.x, c01.y, c01.z, c01.w, ya[0], yb[0]);
+      rot_halves(a.y, b.y, c23.x, c23.y, c23.z, c23.w, ya[1], yb[1]);
+      rot_halves(a.z, b.z, c45.x, c45.y, c45.z, c45.w, ya[2], yb[2]);
+      rot_halves(a.w, b.w, c67.x, c67.y, c67.z, c67.w, ya[3], yb[3]);
+      if constexpr (F32) {
+        const int64_t orow = layer * f32.total_rows + f32.row_off[r] + row;
+        float* o = f32.out + (orow * heads + h) * D;
+        float4* oa = reinterpret_cast<float4*>(o + v * 8);
+        float4* ob = reinterpret_cast<float4*>(o + D / 2 + v * 8);
+        oa[0] = make_float4(ya[0].x, ya[0].y, ya[1].x, ya[1].y);
+        oa[1] = make_float4(ya[2].x, ya[2].y, ya[3].x, ya[3].y);
+        ob[0] = make_float4(yb[0].x, yb[0].y, yb[1].x, yb[1].y);
+        ob[1] = make_float4(yb[2].x, yb[2].y, yb[3].x, yb[3].y);
+      } else {
+        __stcs(dst + off, make_uint4(pack(ya[0]), pack(ya[1]), pack(ya[2]), pack(ya[3])));
+        __stcs(dst + off + HV, make_uint4(pack(yb[0]), pack(yb[1]), pack(yb[2]), pack(yb[3])));
+      }
     }
   }
 }
 
-}  // namespace
-
-cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs, int n_layers,
-                                int heads, int d_rot, int page, int64_t n_pages, bool half_layout, cudaStream_t st) {
+template <bool F32>
+cudaError_t launch(void* kpool, const RunDesc* runs, const float2* cs, int n_runs, int n_layers, int heads,
+                   int d_rot, int page, int64_t n_pages, bool half_layout, F32Out f32, cudaStream_t st) {
   if (n_runs <= 0) return cudaSuccess;
   int sms = 152;
   int dev = 0;
@@ -152,13 +179,14 @@ cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* 
   const int64_t units = int64_t(n_layers) * n_runs;
   const unsigned blocks = unsigned(std::min<int64_t>(units, int64_t(sms) * 8));
   uint4* p = static_cast<uint4*>(kpool);
-#define AKV_REPOS_CASE(DIM)                                                                              \
-  case DIM:                                                                                              \
-    if (half_layout)                                                                                     \
-      repos_half_kernel<DIM><<<blocks, kThreads, 0, st>>>(p, runs, cs, n_runs, n_layers, heads, page, n_pages); \
-    else                                                                                                 \
-      repos_interleaved_kernel<DIM><<<blocks, kThreads, 0, st>>>(p, runs, cs, n_runs, n_layers, heads, page,  \
-                                                                 n_pages);                              \
+#define AKV_REPOS_CASE(DIM)                                                                                    \
+  case DIM:                                                                                                    \
+    if (half_layout)                                                                                           \
+      repos_half_kernel<DIM, F32><<<blocks, kThreads, 0, st>>>(p, runs, cs, n_runs, n_layers, heads, page,     \
+                                                               n_pages, f32);                                  \
+    else                                                                                                       \
+      repos_interleaved_kernel<DIM, F32><<<blocks, kThreads, 0, st>>>(p, runs, cs, n_runs, n_layers, heads,    \
+                                                                      page, n_pages, f32);                    \
     break;
   switch (d_rot) {
     AKV_REPOS_CASE(16)
@@ -171,6 +199,21 @@ cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* 
   }
 #undef AKV_REPOS_CASE
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs, int n_layers,
+                                int heads, int d_rot, int page, int64_t n_pages, bool half_layout, cudaStream_t st) {
+  return launch<false>(kpool, runs, cs, n_runs, n_layers, heads, d_rot, page, n_pages, half_layout,
+                       F32Out{nullptr, nullptr, 0}, st);
+}
+
+cudaError_t launch_repos_rotate_f32(const void* kpool, const RunDesc* runs, const float2* cs, const int32_t* row_off,
+                                    int64_t total_rows, float* out, int n_runs, int n_layers, int heads, int d_rot,
+                                    int page, int64_t n_pages, bool half_layout, cudaStream_t st) {
+  return launch<true>(const_cast<void*>(kpool), runs, cs, n_runs, n_layers, heads, d_rot, page, n_pages,
+                      half_layout, F32Out{out, row_off, total_rows}, st);
 }
 
 }  // namespace akv

@@ -206,6 +206,18 @@ AKV_API akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* se
                       const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
                       void* stream);
 
+/* Float32 debug mode of the repos_rotate kernel: rotate rows of the K pool
+ * (K_pe under MLA) by given shifts exactly as akv_flush would, but write the
+ * unrounded float32 results to `out` instead of rounding them back into the
+ * pool (the pool is only read).  Checks the rotation arithmetic against
+ * float64 without the bf16 storage rounding ([Leyline] "Limitations": the
+ * rotation runs in fp32; storage adds its own rounding).
+ *   runs: host int32, 4 per run: K page, slot_lo, slot_hi, delta.
+ *   out:  device float [n_layers][sum of (slot_hi - slot_lo)][n_kv_heads][d_rot],
+ *         rows in run order. */
+AKV_API akv_status akv_debug_rotate_f32(akv_ctx* ctx, const int32_t* runs, int32_t n_runs, float* out,
+                                        void* stream);
+
 /* --- inspection (host memory only; used by the bookkeeping tests) -------- */
 
 /* Per-token state of a sequence into caller arrays of akv_seq_len entries

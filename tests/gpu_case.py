@@ -25,6 +25,9 @@ class Case:
         self.model = CacheModel(w.n_pages, s.page_size)
         L, P, H, S = s.n_layers, w.n_pages, s.n_kv_heads, s.page_size
         self.kp = np.zeros((L, P, H, S, s.d_rot), np.float32)
+        # per rotated element: the float32 rounding allowance of the rotation,
+        # 2^-20 * (|x_a| + |x_b|) of its input pair (see compare_rotated)
+        self.kterm = np.zeros((L, P, H, S, s.d_rot), np.float32)
         self.vp = np.zeros((L, P, H, S, s.d_v), np.float32)
         self.stream = torch.cuda.current_stream()
         self.names_e = {}
@@ -70,6 +73,13 @@ class Case:
 
     def _apply_runs(self, runs):
         s = self.w.shape
+        from oracle import rope
+        for src, dst, lo, hi, d in runs:
+            x = np.abs(self.kp[:, src, :, lo:hi, :].astype(np.float64))
+            a, b = rope.pair_indices(s.d_rot, s.rope_layout)
+            t = 2.0 ** -20 * (x[..., a] + x[..., b])
+            self.kterm[:, dst, :, lo:hi, a] = t
+            self.kterm[:, dst, :, lo:hi, b] = t
         kernels.repos_runs(self.kp, runs, s.rope_base, s.rope_layout, out=self.kp)
         self.flush_runs.extend(runs)
 

@@ -1,10 +1,14 @@
 """repos_rotate and kv_write on the GPU against the oracle.
 
-Bar (see the tolerance reading for rotated keys): every rotated bf16 value is
-within one bf16 ulp of RNE_bf16(float64 rotation) and at least 99.9% are
-bit-identical (only near-ties may differ, because the kernel rotates in
-float32); every row a flush does not rotate, and every V / latent row, is
-bit-identical.  kv_write is a pure copy: bit-exact."""
+Bars (the tolerance reading for rotated keys):
+* bf16 in the pool: every rotated value is within one bf16 ulp of
+  RNE_bf16(float64 rotation) plus the float32 rounding allowance of the
+  rotation, 2^-20 (|x_a| + |x_b|) of its input pair (which only matters where
+  the result cancels towards zero), and at least 99.9% are bit-identical;
+* the float32 debug mode of the same kernel meets the stated rotated-key
+  tolerance against float64: |err| <= 2e-3 + 1e-3 |ref|;
+* every row a flush does not rotate, and every V / latent row, is
+  bit-identical; kv_write is a pure copy: bit-exact."""
 import numpy as np
 import pytest
 
@@ -16,16 +20,19 @@ from oracle import bf16
 pytestmark = pytest.mark.gpu
 
 
-def compare_rotated(gpu, want, rows_mask):
-    """gpu/want float32 pools holding bf16 values; rows_mask marks rotated rows (broadcast over d)."""
-    g, w_ = gpu[rows_mask], want[rows_mask]
-    ulp = bf16.ulp_bf16(w_)
-    diff = np.abs(g.astype(np.float64) - w_.astype(np.float64))
-    assert np.all(diff <= ulp), f"max diff {diff.max()} vs ulp"
-    eq = np.mean(g == w_)
-    assert eq >= 0.999, f"bit-equal fraction {eq}"
+def compare_rotated(gpu, want, rows_mask, term):
+    """gpu/want float32 pools holding bf16 values; rows_mask marks rotated rows (broadcast over d);
+    term: the float32 rounding allowance per element."""
     rest_g, rest_w = gpu[~rows_mask], want[~rows_mask]
     assert np.array_equal(rest_g, rest_w)
+    if not rows_mask.any():
+        return 1.0
+    g, w_ = gpu[rows_mask], want[rows_mask]
+    bound = bf16.ulp_bf16(w_) + term[rows_mask]
+    diff = np.abs(g.astype(np.float64) - w_.astype(np.float64))
+    assert np.all(diff <= bound), f"worst diff / bound {np.max(diff / bound)}"
+    eq = np.mean(g == w_)
+    assert eq >= 0.999, f"bit-equal fraction {eq}"
     return eq
 
 
@@ -42,12 +49,12 @@ def run_case(w):
     c = Case(w)
     c.run_ops()
     kg, vg = c.gpu_pools()
-    assert np.array_equal(kg, c.kp), "K pool after appends / explicit flushes"
+    compare_rotated(kg, c.kp, rotated_mask(c, c.flush_runs), c.kterm)   # appends + explicit flushes
     assert np.array_equal(vg, c.vp), "V pool after appends"
     runs = c.flush_segments()
     kg, vg = c.gpu_pools()
     assert np.array_equal(vg, c.vp)
-    eq = compare_rotated(kg, c.kp, rotated_mask(c, runs))
+    eq = compare_rotated(kg, c.kp, rotated_mask(c, c.flush_runs), c.kterm)
     assert c.eng.check_device_error() == 0
     return c, runs, eq
 
@@ -106,3 +113,36 @@ def test_zero_shift_is_identity_bitwise():
     kg, _ = c.gpu_pools()
     assert np.array_equal(kg, c.kp)   # delta 0 copies (cos 1, sin 0) are exact
     assert any(r[4] == 0 for r in runs)
+
+
+@pytest.mark.parametrize("layout", ["interleaved", "half"])
+def test_f32_debug_mode_meets_rotated_key_tolerance(layout):
+    # The pre-flush pool of the 32K trajectory, every flush run of the turn plus
+    # shifts up to +-64K, rotated without rounding and compared with float64.
+    from gpu_case import Case
+    from oracle import rope
+    w = synth.llama8b_32k(total=8192, n_new=128, n_layers=2)
+    w.shape.rope_layout = layout
+    c = Case(w)
+    c.run_ops()
+    ids = sorted({c.names_o[g["seq"]] for g in w.segments})
+    import copy
+    runs = copy.deepcopy(c.model).flush(ids)
+    rng = np.random.default_rng(5)
+    req = [(src, lo, hi, d) for src, dst, lo, hi, d in runs]
+    req += [(int(rng.integers(0, 40)), 0, 16, int(rng.integers(-65536, 65537))) for _ in range(32)]
+    req = np.array(req, np.int32)
+    n_rows = int((req[:, 2] - req[:, 1]).sum())
+    s = w.shape
+    out = torch.empty((s.n_layers, n_rows, s.n_kv_heads, s.d_rot), dtype=torch.float32, device="cuda")
+    c.eng.debug_rotate_f32(req, out, stream=c.stream)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    want = np.concatenate([rope.repos(c.kp[:, pg, :, lo:hi, :].transpose(0, 2, 1, 3),
+                                      np.full((s.n_layers, hi - lo, s.n_kv_heads), d, np.float64),
+                                      s.rope_base, layout) for pg, lo, hi, d in req], axis=1)
+    err = np.abs(got - want)
+    assert np.all(err <= 2e-3 + 1e-3 * np.abs(want)), err.max()
+    assert err.max() < 1e-5          # float32 rotation: far inside the tolerance
+    kg, _ = c.gpu_pools()
+    assert np.array_equal(kg, c.kp)  # the debug mode only reads the pool

@@ -78,8 +78,9 @@ class Case:
             x = np.abs(self.kp[:, src, :, lo:hi, :].astype(np.float64))
             a, b = rope.pair_indices(s.d_rot, s.rope_layout)
             t = 2.0 ** -20 * (x[..., a] + x[..., b])
-            self.kterm[:, dst, :, lo:hi, a] = t
-            self.kterm[:, dst, :, lo:hi, b] = t
+            view = self.kterm[:, dst, :, lo:hi, :]
+            view[..., a] = t
+            view[..., b] = t
         kernels.repos_runs(self.kp, runs, s.rope_base, s.rope_layout, out=self.kp)
         self.flush_runs.extend(runs)
 

@@ -90,6 +90,8 @@ def load(path=LIB_PATH):
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    lib.akv_repos_rotate_noalloc.argtypes = [P, I32, I32, I32, I32, I32, I32, ctypes.c_double, P, I32, P]
+    lib.akv_repos_rotate_noalloc.restype = ctypes.c_int
     lib.akv_last_error.argtypes = [P]
     lib.akv_last_error.restype = ctypes.c_char_p
     _lib = lib
@@ -270,6 +272,18 @@ class Engine:
         self._check(self.lib.akv_profile_read(self.h, ctypes.byref(s)))
         return {name: dict(launches=s.launches[i], ms=s.ms[i], bytes=s.bytes[i], flops=s.flops[i])
                 for i, name in enumerate(KERNEL_NAMES)}
+
+
+def repos_rotate_noalloc(k_pool, cfg, runs, stream=None):
+    """akv_repos_rotate_noalloc: rotate runs [n, 5] (src, dst, lo, hi, delta) of k_pool in the
+    library's fixed device scratch array, without a context and without allocating."""
+    lib = load()
+    r = np.ascontiguousarray(np.asarray(runs, dtype=np.int32).reshape(-1, 5))
+    st = lib.akv_repos_rotate_noalloc(_ptr(k_pool), cfg["n_layers"], cfg["n_kv_heads"], cfg["page_size"],
+                                      cfg["n_pages"], cfg["d_rot"], cfg["rope_layout"], float(cfg["rope_base"]),
+                                      r.ctypes.data, r.shape[0], _stream(stream))
+    if st != OK:
+        raise AKVError(st, "akv_repos_rotate_noalloc failed")
 
 
 def config_from_shape(shape, n_pages):

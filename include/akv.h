@@ -218,6 +218,34 @@ AKV_API akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* se
 AKV_API akv_status akv_debug_rotate_f32(akv_ctx* ctx, const int32_t* runs, int32_t n_runs, float* out,
                                         void* stream);
 
+/* The repos_rotate kernel for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * such as a serving process that reserves nearly all of HBM for its KV pool
+ * up front (no room for more cudaMalloc calls) or a latency-critical path
+ * that must avoid cudaMalloc / cudaFree because they can synchronise the
+ * whole device.  It needs no context and allocates nothing: the run list and
+ * the (cos, sin) table are copied into a fixed 256 KiB array in the library's
+ * own device memory (every GPU that loads the library holds it until exit).
+ *   k_pool: device bf16 [n_layers][n_pages][n_kv_heads][page_size][d_rot],
+ *           read and written (the same layout as akv_pools.k_pool).
+ *   runs:   host int32, 5 per run: src page, dst page, slot_lo, slot_hi,
+ *           delta -- rows [slot_lo, slot_hi) of page src, every layer and
+ *           head, rotated by delta and stored to the same rows of page dst
+ *           (the run format of akv_last_flush_runs).
+ *   d_rot: 16, 32, 64, 128 or 256; page_size: 16, 32, 64 or 128.
+ * Returns AKV_ERR_RANGE when a run is outside the pool or when the runs plus
+ * the table (16 B per run, rounded up to 256 B, plus 4 * d_rot B per distinct
+ * delta) exceed 256 KiB, AKV_ERR_ARG for a bad shape.  Every call overwrites
+ * the part of the array it uses, so nothing needs clearing between calls, but
+ * calls that overlap on the GPU (e.g. unordered streams) race on the array;
+ * calls on one stream are ordered.  The first call on a device, with that
+ * device current, looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it: make that first call before any stream capture. */
+AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_layers, int32_t n_kv_heads,
+                                            int32_t page_size, int32_t n_pages, int32_t d_rot,
+                                            int32_t rope_layout, double rope_base, const int32_t* runs,
+                                            int32_t n_runs, void* stream);
+
 /* --- inspection (host memory only; used by the bookkeeping tests) -------- */
 
 /* Per-token state of a sequence into caller arrays of akv_seq_len entries

@@ -44,13 +44,16 @@ struct AttnSeg {
   int32_t pad[3];
 };
 
-// One CTA's work: query tile qt of segment seg for kv head kvh, covering
-// n_tiles KV tiles (the causal limit of the tile's last row).
+// One CTA's work: two consecutive 128-row query tiles (A = qt0, B = qt0 + 1)
+// of segment seg for kv head kvh.  n_a / n_b: KV tiles each reads (up to the
+// causal limit of its last row); n_b = 0 when the segment has no tile B.
 struct AttnWork {
   int32_t seg;
   int32_t kvh;
-  int32_t qt;
-  int32_t n_tiles;
+  int32_t qt0;
+  int32_t n_a;
+  int32_t n_b;
+  int32_t pad[3];
 };
 
 struct AttnParams {

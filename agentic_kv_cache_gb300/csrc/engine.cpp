@@ -836,25 +836,31 @@ struct akv_ctx {
       const int64_t ql = s.q_len, kl = s.kv_len;
       flops += double(cfg.n_q_heads) * 2.0 * (dqk + cfg.d_v) * double(ql * (kl - ql) + ql * (ql + 1) / 2);
       const int n_qt = (s.q_len + tpt - 1) / tpt;
-      for (int qt = 0; qt < n_qt; ++qt) {
+      // KV tiles query tile qt reads: runs whose first entry is <= the
+      // largest entry index its last row may see.
+      auto tiles_of = [&](int qt) -> int32_t {
+        if (qt >= n_qt) return 0;
         const int64_t last = std::min<int64_t>(ql, int64_t(qt + 1) * tpt) - 1;
-        const int64_t limit = kl - ql + last;  // largest entry index the tile reads
-        // runs whose first entry is <= limit
+        const int64_t limit = kl - ql + last;
         int64_t lo_r = 0, hi_r = int64_t(sp.runs.size());
         while (lo_r < hi_r) {
           int64_t mid = (lo_r + hi_r) / 2;
           if (sp.runs[mid].es <= limit) lo_r = mid + 1; else hi_r = mid;
         }
-        const int32_t n_tiles = int32_t((lo_r + rpt - 1) / rpt);
-        for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, n_tiles});
+        return int32_t((lo_r + rpt - 1) / rpt);
+      };
+      for (int qt = 0; qt < n_qt; qt += 2) {
+        const int32_t na = tiles_of(qt), nb = tiles_of(qt + 1);
+        for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, na, nb, {0, 0, 0}});
       }
       runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
       tab.push_back(s);
     }
     if (meta) return;
     // Longest first (LPT); ties in (segment, head, tile) order.
-    std::stable_sort(work.begin(), work.end(),
-                     [](const akv::AttnWork& a, const akv::AttnWork& b) { return a.n_tiles > b.n_tiles; });
+    std::stable_sort(work.begin(), work.end(), [](const akv::AttnWork& a, const akv::AttnWork& b) {
+      return a.n_a + a.n_b > b.n_a + b.n_b;
+    });
     if (cfg.layout != AKV_LAYOUT_GQA || !(cfg.d_rot == 64 || cfg.d_rot == 128))
       fail(AKV_ERR_ARG, "segment attention supports GQA with head_dim 64 or 128");
 

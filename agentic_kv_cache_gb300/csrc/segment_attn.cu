@@ -10,20 +10,23 @@
 // dense mask.  [AKV-blog] section 2 "The Drop Primitive" fixes what is
 // computed: softmax(Q K^T * scale + M) V with M = -inf on invisible entries.
 //
-// GB300 design (one CTA = one 128-row query tile of one kv head):
-//   * rows are (query token, query head of the kv group) pairs, so the G query
-//     heads that share a kv head share every K/V tile load (GQA packing);
-//   * warp 0 issues TMA loads: the Q tile once, then per 128-key tile one box
-//     of page_size rows per run ("page") straight from the paged pool into a
-//     128-byte-swizzled shared-memory tile, double buffered; slots of a tile
-//     past the segment's last run load the segment's first page again (finite
-//     data, masked out like every slot outside a run);
-//   * warp 1 owns TMEM (512 columns: S0, S1, O) and issues tcgen05.mma from one
-//     thread: S_j = Q K_j^T into TMEM, then O += P_j V_j with P from shared memory;
-//   * warps 2-5 (128 threads, one per row = one TMEM lane) run the online
-//     softmax: each thread holds a whole score row, so row max and row sum need
-//     no shuffles; rescaling of O is lazy (only when the running max grows by
-//     more than 2^8), done in TMEM; the epilogue normalises O and writes bf16.
+// GB300 design (one CTA = two consecutive 128-row query tiles A, B of one kv
+// head; rows are (query token, query head of the kv group) pairs so the G
+// query heads sharing a kv head share every K/V load):
+//   * warp 0 issues TMA loads: both Q tiles once, then K_j and V_j of every
+//     128-key tile into a ring of three shared-memory slots (K0 V0 K1 V1 ...),
+//     one box of page_size rows per run (page), 128-byte swizzled; slots past
+//     the segment's last run reload its first page (finite, masked out);
+//   * warp 1 owns TMEM (S_A, S_B, O_A, O_B: 4 x 128 columns) and issues
+//     tcgen05.mma from one thread, per KV tile j and per query tile T:
+//     O_T += P_T(j-1) V_{j-1}, then S_T(j) = Q_T K_j^T, then one commit -- so
+//     "S_T(j) is ready" also means "O_T is stable and P_T may be rewritten";
+//   * warps 2-5 (tile A) and 6-9 (tile B) run the online softmax, one thread
+//     per row = one TMEM lane: a whole score row comes in with one 128-column
+//     TMEM load, row max and row sum need no shuffles, O is rescaled lazily in
+//     TMEM (only when the running max grows by more than 2^8), P goes to shared
+//     memory for the next PV.  While one warpgroup computes exponentials the
+//     tensor core runs the other tile's MMAs;
 //   * every wait is bounded; on time-out the CTA records AKV_ERR_DEVICE_TIMEOUT
 //     in the device error word, drains its copies and MMAs, frees TMEM, exits.
 #include <cuda_bf16.h>
@@ -37,29 +40,40 @@
 namespace akv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kTileKeys = 128;
 constexpr int kRows = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
-constexpr int32_t kErrTimeout = 7;                 // AKV_ERR_DEVICE_TIMEOUT
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+constexpr int32_t kErrTimeout = 7;  // AKV_ERR_DEVICE_TIMEOUT
+constexpr int32_t kErrDevice = 8;   // AKV_ERR_DEVICE
+constexpr int kSlots = 3;
 
 template <int D>
 struct Layout {
-  static constexpr int kBlocks = D / 64;                 // 64-element (128-byte) K blocks
-  static constexpr uint32_t kBlockBytes = 128 * 128;     // 128 rows x 128 bytes
-  static constexpr uint32_t kTileBytes = kBlocks * kBlockBytes;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK0 = kQ + kTileBytes;
-  static constexpr uint32_t kV0 = kK0 + 2 * kTileBytes;
-  static constexpr uint32_t kP = kV0 + 2 * kTileBytes;
-  static constexpr uint32_t kBars = kP + 2 * kBlockBytes;  // P: 128 rows x 128 keys
-  static constexpr uint32_t kColE = kBars + 256;           // int32 [2][128]: entry index per key column
-  static constexpr uint32_t kBytes = kColE + 2 * 128 * 4;
+  static constexpr int kBlocks = D / 64;              // 64-element (128-byte) column blocks
+  static constexpr uint32_t kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
+  static constexpr uint32_t kTile = kBlocks * kBlockBytes;
+  static constexpr uint32_t kQ = 0;                          // Q_A, Q_B
+  static constexpr uint32_t kSlot = kQ + 2 * kTile;          // 3 K/V slots
+  static constexpr uint32_t kP = kSlot + kSlots * kTile;     // P_A, P_B: 128 rows x 128 keys each
+  static constexpr uint32_t kColE = kP + 2 * 2 * kBlockBytes;  // int32 [2][128]: entry per key column
+  static constexpr uint32_t kBars = kColE + 2 * 128 * 4;
+  static constexpr uint32_t kBytes = kBars + 128;
 };
 
-// barrier slots (8 bytes each) after the tiles
-enum Bar { kBarQ = 0, kBarK0, kBarK1, kBarV0, kBarV1, kBarE0, kBarE1, kBarS0, kBarS1, kBarP, kBarO, kBarFin, kNumBars };
+enum Bar {
+  kBarQ = 0,
+  kBarFull0,  // + slot
+  kBarEmpty0 = kBarFull0 + kSlots,
+  kBarS0 = kBarEmpty0 + kSlots,  // + tile
+  kBarP0 = kBarS0 + 2,
+  kBarO0 = kBarP0 + 2,
+  kBarFin = kBarO0 + 2,
+  kNumBars
+};
+static_assert(kNumBars * 8 + 8 <= 128, "barrier area");
 
 __device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
   if (atomicCAS(&err->code, 0, code) == 0) {
@@ -74,31 +88,309 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// ---------------------------------------------------------------- producer
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_constant__ AttnParams p) {
+__device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
+                        volatile int* abort_flag) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = ptx::smem_addr(smem);
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kNumBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kNumBars + 8);
+  const int G = p.group, tpt = kRows / G, rpt = kTileKeys / p.page;
+  const int n_max = max(w.n_a, w.n_b);
+  const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
+  ptx::mbar_arrive_expect_tx(bar(kBarQ), (w.n_b > 0 ? 2 : 1) * L::kTile);
+  for (int t = 0; t < (w.n_b > 0 ? 2 : 1); ++t)
+    for (int kb = 0; kb < L::kBlocks; ++kb)
+      ptx::tma_load_3d(sbase + L::kQ + t * L::kTile + kb * L::kBlockBytes, &p.q_map, bar(kBarQ), kb * 64,
+                       w.kvh * G, q_tok0 + t * tpt);
+  const int layer_base = p.layer * p.n_pages;
+  const AttnRun first = p.runs[seg.run_off];
+  int armed[kSlots] = {0, 0, 0};
+  bool ok = true;
+  for (int ld = 0; ld < 2 * n_max; ++ld) {
+    const int j = ld >> 1, is_v = ld & 1, slot = ld % kSlots, use = ld / kSlots;
+    if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+      ok = false;
+      break;
+    }
+    const uint32_t dst = sbase + L::kSlot + slot * L::kTile;
+    const CUtensorMap* map = is_v ? &p.v_map : &p.k_map;
+    ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), L::kTile);
+    for (int g = 0; g < rpt; ++g) {
+      const int ri = j * rpt + g;
+      const AttnRun run = ri < seg.n_runs ? p.runs[seg.run_off + ri] : first;
+      const int pg = layer_base + (is_v ? run.vp : run.kp);
+      for (int kb = 0; kb < L::kBlocks; ++kb)
+        ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, map, bar(kBarFull0 + slot), kb * 64, 0, w.kvh,
+                         pg);
+    }
+    armed[slot] = use + 1;
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 0, 0);
+    *abort_flag = 1;
+  }
+  // Drain: every copy issued here has landed before the CTA may exit.
+  ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kDrainLimitNs);
+  for (int s = 0; s < kSlots; ++s)
+    if (armed[s]) ptx::mbar_wait(bar(kBarFull0 + s), (armed[s] - 1) & 1, abort_flag, kDrainLimitNs);
+}
 
+// --------------------------------------------------------------------- MMA
+// Per KV tile j and query tile T: O_T += P_T(j-1) V_{j-1} (once P_T(j-1) is
+// written), then S_T(j) = Q_T K_j^T, then one commit to S_T's barrier.  Slots
+// are released (commit to their empty barrier) after their last reader.
+template <int D>
+__device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
+                          volatile int* abort_flag) {
+  using L = Layout<D>;
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kTileKeys, false);
+  constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, D, true);
+  const int n_t[2] = {w.n_a, w.n_b};
+  const int n_max = max(w.n_a, w.n_b);
+  auto slot_of = [](int ld) { return ld % kSlots; };
+  auto full_parity = [](int ld) { return (ld / kSlots) & 1; };
+  bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
+  for (int j = 0; j <= n_max && ok; ++j) {
+    bool k_ready = false, v_ready = false;
+    for (int t = 0; t < 2 && ok; ++t) {
+      const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
+      if (j >= 1 && j - 1 < n_t[t]) {
+        if (!v_ready) {
+          const int ld = 2 * (j - 1) + 1;
+          if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs))) break;
+          v_ready = true;
+        }
+        if (!(ok = ptx::mbar_wait(bar(kBarP0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        ptx::tc_fence_after();
+        const uint32_t vt = sbase + L::kSlot + slot_of(2 * (j - 1) + 1) * L::kTile;
+        const uint32_t pt = sbase + L::kP + t * 2 * L::kBlockBytes;
+        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
+          const uint32_t poff = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
+          ptx::mma_bf16(tO, ptx::smem_desc(pt + poff, 16, 1024), ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024),
+                        idesc_pv, (j > 1 || ks > 0));
+        }
+        if (j - 1 == n_t[t] - 1) ptx::mma_commit(bar(kBarO0 + t));
+      }
+      if (j < n_t[t]) {
+        if (!k_ready) {
+          const int ld = 2 * j;
+          if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs))) break;
+          k_ready = true;
+          ptx::tc_fence_after();
+        }
+        const uint32_t kt = sbase + L::kSlot + slot_of(2 * j) * L::kTile;
+        const uint32_t qt = sbase + L::kQ + t * L::kTile;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
+          ptx::mma_bf16(tS, ptx::smem_desc(qt + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024), idesc_qk, ks > 0);
+        }
+        ptx::mma_commit(bar(kBarS0 + t));
+      }
+    }
+    if (!ok) break;
+    if (j >= 1) ptx::mma_commit(bar(kBarEmpty0 + slot_of(2 * (j - 1) + 1)));  // V_{j-1} done
+    if (j < n_max) ptx::mma_commit(bar(kBarEmpty0 + slot_of(2 * j)));        // K_j done
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 1, 0);
+    *abort_flag = 1;
+  }
+  // Every MMA issued above has completed before TMEM is released.
+  ptx::mma_commit(bar(kBarFin));
+  ptx::mbar_wait(bar(kBarFin), 0, abort_flag, kDrainLimitNs);
+}
+
+// ----------------------------------------------------------------- softmax
+// One warpgroup per query tile t; thread = row r = TMEM lane r.
+template <int D>
+__device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint8_t* smem,
+                             uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
+  using L = Layout<D>;
+  const int n_t = t == 0 ? w.n_a : w.n_b;
+  if (n_t == 0) return;
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int wg_warp = (threadIdx.x / 32 - 2) % 4;
+  const int quad = (threadIdx.x / 32) & 3;  // TMEM lane quadrant this warp may access
+  const int lane = threadIdx.x % 32;
+  const int r = quad * 32 + lane;
+  (void)wg_warp;
+  const uint32_t lane_addr = uint32_t(quad * 32) << 16;
+  const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
+  const int G = p.group, tpt = kRows / G, rpt = kTileKeys / p.page;
+  const int t_loc = r / G, g = r % G;
+  const int qi = (w.qt0 + t) * tpt + t_loc;  // query index inside the segment
+  const bool row_valid = qi < seg.q_len;
+  const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
+  const float sl2 = p.scale_log2;
+  const int bar_id = 1 + t;  // named barrier of this warpgroup
+  int* colE = reinterpret_cast<int*>(smem + L::kColE) + t * 128;
+  uint8_t* prow = smem + L::kP + t * 2 * L::kBlockBytes + r * 128;
+  int page_shift = 4;
+  while ((1 << page_shift) < p.page) ++page_shift;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n_t; ++j) {
+    ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(bar_id, 128, ok)) {
+      ok = false;
+      break;
+    }
+    // Entry index of key column r of tile j (INT_MAX: no entry there);
+    // columns are (run c / page, slot c % page) of the tile's runs.
+    int e = INT_MAX;
+    {
+      const int ri = j * rpt + (r >> page_shift), sl = r & (p.page - 1);
+      if (ri < seg.n_runs) {
+        const AttnRun ar = p.runs[seg.run_off + ri];
+        const int lo = ar.lohi & 0xffff, hi = ar.lohi >> 16;
+        if (sl >= lo && sl < hi) e = ar.es + (sl - lo);
+      }
+      colE[r] = e;
+    }
+    const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
+    ptx::tc_fence_after();
+    // With every column valid the entries are consecutive, so the last column
+    // holds the tile's largest entry index.
+    const bool need_mask = !all_valid || colE[kTileKeys - 1] > lim;
+    const int4* ce4 = reinterpret_cast<const int4*>(colE);
+    // Pass 1: row max over two 64-column halves read from TMEM.
+    float mx[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;  // -inf
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(u[c]));
+    }
+    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+    const float m_new = fmaxf(m_run, mt);
+    const bool resc = m_new > m_run + 8.0f;
+    const float m_use = resc ? m_new : m_run;
+    const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
+    const float msub = m_use == -INFINITY ? 0.f : m_use;
+    // O_T is stable here: S_T(j) completes after PV_T(j-1).
+    if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_load32(tO + lane_addr + c * 32, o);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+        ptx::tmem_store32(tO + lane_addr + c * 32, o);
+      }
+    }
+    // Pass 2: P = exp2(s * scale * log2 e - m) -> shared memory, K-major with
+    // the 128-byte swizzle (16-byte chunk c of row r lands in chunk c ^ (r & 7)),
+    // one 64-key block per half.
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = c * 8 + 2 * q;
+          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[col]), sl2, -msub));
+          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[col + 1]), sl2, -msub));
+          sum[2 * q] += p0;
+          sum[2 * q + 1] += p1;
+          pk[q] = pack_bf16(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(prow + h * L::kBlockBytes + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+    const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+    l_run = l_run * alpha + rowsum;
+    m_run = m_use;
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(bar(kBarP0 + t));
+  }
+  if (ok) {
+    ok = ptx::mbar_wait(bar(kBarO0 + t), 0, abort_flag, kWaitLimitNs);
+    ok = ptx::bar_red_and(bar_id, 128, ok);
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 2 + t, 0);
+    *abort_flag = 1;
+    return;
+  }
+  ptx::tc_fence_after();
+  const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+  __nv_bfloat16* orow =
+      static_cast<__nv_bfloat16*>(p.o) + (int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g) * D;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    ptx::tmem_load32(tO + lane_addr + c * 32, o);
+    if (row_valid) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 8) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(o[k + 0]) * inv, __uint_as_float(o[k + 1]) * inv);
+        v.y = pack_bf16(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+        v.z = pack_bf16(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+        v.w = pack_bf16(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+        *reinterpret_cast<uint4*>(orow + c * 32 + k) = v;
+      }
+    }
+  }
+  if (row_valid && p.lse) {
+    const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    p.lse[int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g] = lse;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_constant__ AttnParams p, int smem_bytes) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  uint8_t* smem = reinterpret_cast<uint8_t*>((raw + 1023) & ~uintptr_t(1023));
+  if (smem + L::kBytes > smem_raw + smem_bytes) {  // layout does not fit: report, touch nothing
+    if (threadIdx.x == 0) raise_error(p.err, kErrDevice, blockIdx.x, int(raw & 1023), 0);
+    return;
+  }
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t bars = sbase + L::kBars;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const AttnWork w = p.work[blockIdx.x];
   const AttnSeg seg = p.segs[w.seg];
-  const int G = p.group;
-  const int tpt = kRows / G;  // query tokens per tile
-  const int n_tiles = w.n_tiles;
-  const int rpt = kTileKeys / p.page;  // runs (pages) per key tile
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
-      uint32_t count = 1;
-      if (i == kBarP) count = 128;
-      ptx::mbar_init(bar(i), count);
-    }
+    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, (i == kBarP0 || i == kBarP0 + 1) ? 128 : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -115,254 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const int q_tok0 = seg.q_row0 + w.qt * tpt;
-      int armed[2] = {0, 0};
-      bool ok = true;
-      ptx::mbar_arrive_expect_tx(bar(kBarQ), L::kTileBytes);
-      for (int kb = 0; kb < L::kBlocks; ++kb)
-        ptx::tma_load_3d(sbase + L::kQ + kb * L::kBlockBytes, &p.q_map, bar(kBarQ), kb * 64, w.kvh * G, q_tok0);
-      const int layer_base = p.layer * p.n_pages;
-      // Slots past the last run: reload the first run's pages (finite, masked out).
-      const int fill_k = layer_base + __ldg(&p.runs[seg.run_off].kp);
-      const int fill_v = layer_base + __ldg(&p.runs[seg.run_off].vp);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !ptx::mbar_wait(bar(kBarE0 + s), ((j >> 1) - 1) & 1, abort_flag, kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        const uint32_t kdst = sbase + L::kK0 + s * L::kTileBytes;
-        const uint32_t vdst = sbase + L::kV0 + s * L::kTileBytes;
-        ptx::mbar_arrive_expect_tx(bar(kBarK0 + s), L::kTileBytes);
-        for (int g = 0; g < rpt; ++g) {
-          const int ri = j * rpt + g;
-          const int pg = ri < seg.n_runs ? layer_base + __ldg(&p.runs[seg.run_off + ri].kp) : fill_k;
-          for (int kb = 0; kb < L::kBlocks; ++kb)
-            ptx::tma_load_4d(kdst + kb * L::kBlockBytes + g * p.page * 128, &p.k_map, bar(kBarK0 + s), kb * 64, 0,
-                             w.kvh, pg);
-        }
-        ptx::mbar_arrive_expect_tx(bar(kBarV0 + s), L::kTileBytes);
-        for (int g = 0; g < rpt; ++g) {
-          const int ri = j * rpt + g;
-          const int pg = ri < seg.n_runs ? layer_base + __ldg(&p.runs[seg.run_off + ri].vp) : fill_v;
-          for (int kb = 0; kb < L::kBlocks; ++kb)
-            ptx::tma_load_4d(vdst + kb * L::kBlockBytes + g * p.page * 128, &p.v_map, bar(kBarV0 + s), kb * 64, 0,
-                             w.kvh, pg);
-        }
-        ++armed[s];
-      }
-      if (!ok) {
-        raise_error(p.err, kErrTimeout, blockIdx.x, 0, 0);
-        *abort_flag = 1;
-      }
-      // Drain: every copy this thread issued has landed before the CTA can exit.
-      ptx::mbar_wait(bar(kBarQ), 0, abort_flag, 100000000ull);
-      for (int s = 0; s < 2; ++s)
-        if (armed[s]) {
-          ptx::mbar_wait(bar(kBarK0 + s), (armed[s] - 1) & 1, abort_flag, 100000000ull);
-          ptx::mbar_wait(bar(kBarV0 + s), (armed[s] - 1) & 1, abort_flag, 100000000ull);
-        }
-    }
+    if (lane == 0) produce<D>(p, w, seg, sbase, abort_flag);
   } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kTileKeys, false);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, D, true);
-      auto issue_qk = [&](int j) {
-        const int s = j & 1;
-        const uint32_t kt = sbase + L::kK0 + s * L::kTileBytes;
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
-          ptx::mma_bf16(tS[s], ptx::smem_desc(sbase + L::kQ + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024),
-                        idesc_qk, ks > 0);
-        }
-        ptx::mma_commit(bar(kBarS0 + s));
-      };
-      bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
-      if (ok && n_tiles > 0) {
-        ok = ptx::mbar_wait(bar(kBarK0), 0, abort_flag, kWaitLimitNs);
-        if (ok) {
-          ptx::tc_fence_after();
-          issue_qk(0);
-        }
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        if (j + 1 < n_tiles) {
-          const int s1 = (j + 1) & 1;
-          if (!(ok = ptx::mbar_wait(bar(kBarK0 + s1), ((j + 1) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
-          ptx::tc_fence_after();
-          issue_qk(j + 1);
-        }
-        if (!(ok = ptx::mbar_wait(bar(kBarP), j & 1, abort_flag, kWaitLimitNs))) break;
-        if (!(ok = ptx::mbar_wait(bar(kBarV0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs))) break;
-        ptx::tc_fence_after();
-        const uint32_t vt = sbase + L::kV0 + (j & 1) * L::kTileBytes;
-        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-          const uint32_t poff = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
-          ptx::mma_bf16(tO, ptx::smem_desc(sbase + L::kP + poff, 16, 1024),
-                        ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024), idesc_pv, (j > 0 || ks > 0));
-        }
-        ptx::mma_commit(bar(kBarE0 + (j & 1)));
-        ptx::mma_commit(bar(kBarO));
-      }
-      if (!ok) {
-        raise_error(p.err, kErrTimeout, blockIdx.x, 1, 0);
-        *abort_flag = 1;
-      }
-      // Every MMA issued above has completed before TMEM is released.
-      ptx::mma_commit(bar(kBarFin));
-      ptx::mbar_wait(bar(kBarFin), 0, abort_flag, 100000000ull);
-    }
+    if (lane == 0) issue_mma<D>(p, w, sbase, tmem, abort_flag);
   } else {
-    // ------------------------------------------------------------- softmax
-    const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // tile row == TMEM lane
-    const uint32_t lane_addr = uint32_t(quad * 32) << 16;
-    const int t_loc = r / G, g = r % G;
-    const int qi = w.qt * tpt + t_loc;  // query index inside the segment
-    const bool row_valid = qi < seg.q_len;
-    const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
-    const float sl2 = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    uint8_t* prow = smem + L::kP + r * 128;
-    int* colE = reinterpret_cast<int*>(smem + L::kColE);
-    int page_shift = 4;
-    while ((1 << page_shift) < p.page) ++page_shift;
-    for (int j = 0; j < n_tiles; ++j) {
-      // Entry index of key column r of this tile (INT_MAX: no entry there).
-      // Columns are (run g = c / page, slot = c % page) of the tile's runs.
-      int e = INT_MAX;
-      {
-        const int gg = r >> page_shift, sl = r & (p.page - 1);
-        const int ri = j * rpt + gg;
-        if (ri < seg.n_runs) {
-          const AttnRun ar = p.runs[seg.run_off + ri];
-          const int lo = ar.lohi & 0xffff, hi = ar.lohi >> 16;
-          if (sl >= lo && sl < hi) e = ar.es + (sl - lo);
-        }
-        colE[(j & 1) * 128 + r] = e;
-      }
-      ok = ptx::mbar_wait(bar(kBarS0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs);
-      if (!ptx::bar_red_and(1, 128, ok)) {
-        ok = false;
-        break;
-      }
-      const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
-      ptx::tc_fence_after();
-      float sc[kTileKeys];
-#pragma unroll
-      for (int c = 0; c < kTileKeys / 32; ++c) {
-        uint32_t u[32];
-        ptx::tmem_load32(tS[j & 1] + lane_addr + c * 32, u);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) sc[c * 32 + k] = __uint_as_float(u[k]);
-      }
-      // Visibility: missing slots of partial runs, missing runs, causal limit.
-      // With every column valid the entries are consecutive, so the last
-      // column holds the tile's largest entry index.
-      const int* ce = colE + (j & 1) * 128;
-      if (!all_valid || ce[kTileKeys - 1] > lim) {
-#pragma unroll
-        for (int c = 0; c < kTileKeys; ++c)
-          if (ce[c] > lim) sc[c] = -INFINITY;
-      }
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kTileKeys; ++c) mt = fmaxf(mt, sc[c]);
-      mt *= sl2;
-      const float m_new = fmaxf(m_run, mt);
-      const bool resc = m_new > m_run + 8.0f;
-      const float m_use = resc ? m_new : m_run;
-      const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
-      const float msub = m_use == -INFINITY ? 0.f : m_use;
-      float rowsum = 0.f;
-      uint32_t pk[kTileKeys / 2];
-#pragma unroll
-      for (int c = 0; c < kTileKeys; c += 2) {
-        const float p0 = ptx::ex2_approx(fmaf(sc[c], sl2, -msub));
-        const float p1 = ptx::ex2_approx(fmaf(sc[c + 1], sl2, -msub));
-        rowsum += p0 + p1;
-        pk[c / 2] = pack_bf16(p0, p1);
-      }
-      if (j > 0) {
-        ok = ptx::mbar_wait(bar(kBarO), (j - 1) & 1, abort_flag, kWaitLimitNs);
-        if (!ptx::bar_red_and(1, 128, ok)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-      }
-      // P row -> shared memory, K-major 128-byte swizzle (16-byte chunk c of
-      // row r lands in chunk c ^ (r & 7)), two 64-key blocks.
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int k0 = kb * 32 + c * 4;
-          uint4 v = make_uint4(pk[k0], pk[k0 + 1], pk[k0 + 2], pk[k0 + 3]);
-          *reinterpret_cast<uint4*>(prow + kb * L::kBlockBytes + ((c ^ (r & 7)) << 4)) = v;
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          ptx::tmem_load32(tO + lane_addr + c * 32, u);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
-          ptx::tmem_store32(tO + lane_addr + c * 32, u);
-        }
-      }
-      l_run = l_run * alpha + rowsum;
-      m_run = m_use;
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kBarP));
-    }
-    if (ok && n_tiles > 0) {
-      ok = ptx::mbar_wait(bar(kBarO), (n_tiles - 1) & 1, abort_flag, kWaitLimitNs);
-      ok = ptx::bar_red_and(1, 128, ok);
-    }
-    if (!ok) {
-      raise_error(p.err, kErrTimeout, blockIdx.x, 2, 0);
-      *abort_flag = 1;
-    } else {
-      ptx::tc_fence_after();
-      const float inv = (n_tiles > 0 && l_run > 0.f) ? 1.0f / l_run : 0.f;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
-                            (int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        ptx::tmem_load32(tO + lane_addr + c * 32, u);
-        if (n_tiles == 0) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) u[k] = 0u;
-        }
-        if (row_valid) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 8) {
-            uint4 v;
-            v.x = pack_bf16(__uint_as_float(u[k + 0]) * inv, __uint_as_float(u[k + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(u[k + 2]) * inv, __uint_as_float(u[k + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(u[k + 4]) * inv, __uint_as_float(u[k + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(u[k + 6]) * inv, __uint_as_float(u[k + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + k) = v;
-          }
-        }
-      }
-      if (row_valid && p.lse) {
-        const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-        p.lse[int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g] = lse;
-      }
-    }
+    softmax_tile<D>(p, w, seg, warp < 6 ? 0 : 1, smem, sbase, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -376,8 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
 }  // namespace
 
 // Every CTA allocates all 512 TMEM columns, so exactly one CTA may live on an
-// SM: both head dims request the d=128 footprint, which is over half of the
-// shared memory of an SM.
+// SM; both head dims request enough shared memory to guarantee that.
 int segment_attn_smem_bytes(int dim) {
   if (dim != 64 && dim != 128) return -1;
   return int(Layout<128>::kBytes) + 1024;
@@ -391,11 +441,11 @@ cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st) {
   if (dim == 64) {
     e = cudaFuncSetAttribute(segment_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    segment_attn_kernel<64><<<p.n_work, kThreads, smem, st>>>(p);
+    segment_attn_kernel<64><<<p.n_work, kThreads, smem, st>>>(p, smem);
   } else {
     e = cudaFuncSetAttribute(segment_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    segment_attn_kernel<128><<<p.n_work, kThreads, smem, st>>>(p);
+    segment_attn_kernel<128><<<p.n_work, kThreads, smem, st>>>(p, smem);
   }
   return cudaGetLastError();
 }

@@ -14,7 +14,7 @@
 // head; rows are (query token, query head of the kv group) pairs so the G
 // query heads sharing a kv head share every K/V load):
 //   * warp 0 issues TMA loads: both Q tiles once, then K_j and V_j of every
-//     128-key tile into a ring of three shared-memory slots (K0 V0 K1 V1 ...),
+//     128-key tile into a ring of five shared-memory slots (K0 V0 K1 V1 ...),
 //     one box of page_size rows per run (page), 128-byte swizzled; slots past
 //     the segment's last run reload its first page (finite, masked out);
 //   * warp 1 owns TMEM (S_A, S_B, O_A, O_B: 4 x 128 columns) and issues
@@ -24,9 +24,12 @@
 //   * warps 2-5 (tile A) and 6-9 (tile B) run the online softmax, one thread
 //     per row = one TMEM lane: a whole score row comes in with one 128-column
 //     TMEM load, row max and row sum need no shuffles, O is rescaled lazily in
-//     TMEM (only when the running max grows by more than 2^8), P goes to shared
-//     memory for the next PV.  While one warpgroup computes exponentials the
-//     tensor core runs the other tile's MMAs;
+//     TMEM (only when the running max grows by more than 2^8), and P (bf16) is
+//     written back into the S columns already consumed, where the next PV MMA
+//     reads it as its TMEM A operand (the MMA thread issues that PV before the
+//     QK that overwrites S, and one thread's MMAs execute in issue order).
+//     While one warpgroup computes exponentials the tensor core runs the other
+//     tile's MMAs;
 //   * every wait is bounded; on time-out the CTA records AKV_ERR_DEVICE_TIMEOUT
 //     in the device error word, drains its copies and MMAs, frees TMEM, exits.
 #include <cuda_bf16.h>
@@ -48,7 +51,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitim
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;  // AKV_ERR_DEVICE_TIMEOUT
 constexpr int32_t kErrDevice = 8;   // AKV_ERR_DEVICE
-constexpr int kSlots = 3;
+constexpr int kSlots = 5;
 
 template <int D>
 struct Layout {
@@ -56,11 +59,10 @@ struct Layout {
   static constexpr uint32_t kBlockBytes = 128 * 128;  // 128 rows x 128 bytes
   static constexpr uint32_t kTile = kBlocks * kBlockBytes;
   static constexpr uint32_t kQ = 0;                          // Q_A, Q_B
-  static constexpr uint32_t kSlot = kQ + 2 * kTile;          // 3 K/V slots
-  static constexpr uint32_t kP = kSlot + kSlots * kTile;     // P_A, P_B: 128 rows x 128 keys each
-  static constexpr uint32_t kColE = kP + 2 * 2 * kBlockBytes;  // int32 [2][128]: entry per key column
+  static constexpr uint32_t kSlot = kQ + 2 * kTile;          // K/V slots
+  static constexpr uint32_t kColE = kSlot + kSlots * kTile;  // int32 [2][128]: entry per key column
   static constexpr uint32_t kBars = kColE + 2 * 128 * 4;
-  static constexpr uint32_t kBytes = kBars + 128;
+  static constexpr uint32_t kBytes = kBars + 256;
 };
 
 enum Bar {
@@ -73,7 +75,7 @@ enum Bar {
   kBarFin = kBarO0 + 2,
   kNumBars
 };
-static_assert(kNumBars * 8 + 8 <= 128, "barrier area");
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
 __device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
   if (atomicCAS(&err->code, 0, code) == 0) {
@@ -166,12 +168,9 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
         if (!(ok = ptx::mbar_wait(bar(kBarP0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
         ptx::tc_fence_after();
         const uint32_t vt = sbase + L::kSlot + slot_of(2 * (j - 1) + 1) * L::kTile;
-        const uint32_t pt = sbase + L::kP + t * 2 * L::kBlockBytes;
-        for (int ks = 0; ks < kTileKeys / 16; ++ks) {
-          const uint32_t poff = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
-          ptx::mma_bf16(tO, ptx::smem_desc(pt + poff, 16, 1024), ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024),
-                        idesc_pv, (j > 1 || ks > 0));
-        }
+        for (int ks = 0; ks < kTileKeys / 16; ++ks)  // P: 16 keys = 8 packed TMEM columns per step
+          ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024), idesc_pv,
+                               (j > 1 || ks > 0));
         if (j - 1 == n_t[t] - 1) ptx::mma_commit(bar(kBarO0 + t));
       }
       if (j < n_t[t]) {
@@ -228,11 +227,13 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   const float sl2 = p.scale_log2;
   const int bar_id = 1 + t;  // named barrier of this warpgroup
   int* colE = reinterpret_cast<int*>(smem + L::kColE) + t * 128;
-  uint8_t* prow = smem + L::kP + t * 2 * L::kBlockBytes + r * 128;
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
+  const int sl_own = r & (p.page - 1);
+  bool run_ok = (r >> page_shift) < seg.n_runs;
+  AttnRun run_cur = run_ok ? p.runs[seg.run_off + (r >> page_shift)] : AttnRun{0, 0, 0, 0};
   for (int j = 0; j < n_t; ++j) {
     ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
     if (!ptx::bar_red_and(bar_id, 128, ok)) {
@@ -240,16 +241,16 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       break;
     }
     // Entry index of key column r of tile j (INT_MAX: no entry there);
-    // columns are (run c / page, slot c % page) of the tile's runs.
+    // columns are (run c / page, slot c % page) of the tile's runs.  The run
+    // of the next tile is fetched now so its latency hides behind this tile.
     int e = INT_MAX;
     {
-      const int ri = j * rpt + (r >> page_shift), sl = r & (p.page - 1);
-      if (ri < seg.n_runs) {
-        const AttnRun ar = p.runs[seg.run_off + ri];
-        const int lo = ar.lohi & 0xffff, hi = ar.lohi >> 16;
-        if (sl >= lo && sl < hi) e = ar.es + (sl - lo);
-      }
+      const int lo = run_cur.lohi & 0xffff, hi = run_cur.lohi >> 16;
+      if (run_ok && sl_own >= lo && sl_own < hi) e = run_cur.es + (sl_own - lo);
       colE[r] = e;
+      const int ri = (j + 1) * rpt + (r >> page_shift);
+      run_ok = ri < seg.n_runs;
+      if (run_ok) run_cur = p.runs[seg.run_off + ri];
     }
     const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
     ptx::tc_fence_after();
@@ -295,9 +296,9 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
         ptx::tmem_store32(tO + lane_addr + c * 32, o);
       }
     }
-    // Pass 2: P = exp2(s * scale * log2 e - m) -> shared memory, K-major with
-    // the 128-byte swizzle (16-byte chunk c of row r lands in chunk c ^ (r & 7)),
-    // one 64-key block per half.
+    // Pass 2: P = exp2(s * scale * log2 e - m), packed to bf16 pairs and
+    // stored over the S columns already read (keys 2c, 2c+1 -> column c), where
+    // the PV MMA reads it as its A operand.
     float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -313,26 +314,20 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
           if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
         }
       }
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = c * 8 + 2 * q;
-          const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[col]), sl2, -msub));
-          const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[col + 1]), sl2, -msub));
-          sum[2 * q] += p0;
-          sum[2 * q + 1] += p1;
-          pk[q] = pack_bf16(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(prow + h * L::kBlockBytes + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
+        const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
+        sum[(2 * c) & 7] += p0;
+        sum[(2 * c + 1) & 7] += p1;
+        pk[c] = pack_bf16(p0, p1);
       }
+      ptx::tmem_store32(tS + lane_addr + h * 32, pk);
     }
     const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
     l_run = l_run * alpha + rowsum;
     m_run = m_use;
-    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     ptx::mbar_arrive(bar(kBarP0 + t));
   }

@@ -45,8 +45,8 @@ namespace {
 
 constexpr int kThreads = 384;  // 3 warpgroups: control (producer, MMA), softmax A, softmax B
 constexpr int kLaunchRegs = 168;  // per thread at launch: 65536 / 384, rounded down to 8
-constexpr int kCtlRegs = 56;      // control warpgroup after re-allocation
-constexpr int kSoftmaxRegs = 224; // each softmax warpgroup after re-allocation
+constexpr int kCtlRegs = 120;     // control warpgroup after re-allocation (producer + MMA loops)
+constexpr int kSoftmaxRegs = 192; // each softmax warpgroup after re-allocation
 static_assert(4 * 32 * kCtlRegs + 8 * 32 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
 constexpr int kTileKeys = 128;
 constexpr int kRows = 128;
@@ -95,7 +95,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // ---------------------------------------------------------------- producer
 template <int D>
-__device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
+__device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
                         volatile int* abort_flag) {
   using L = Layout<D>;
   const uint32_t bars = sbase + L::kBars;
@@ -149,7 +149,7 @@ __device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& s
 // written), then S_T(j) = Q_T K_j^T, then one commit to S_T's barrier.  Slots
 // are released (commit to their empty barrier) after their last reader.
 template <int D>
-__device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
+__device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
                           volatile int* abort_flag) {
   using L = Layout<D>;
   const uint32_t bars = sbase + L::kBars;
@@ -163,7 +163,7 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
   bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
   for (int j = 0; j <= n_max && ok; ++j) {
     bool k_ready = false, v_ready = false;
-#pragma unroll
+#pragma unroll 1
     for (int t = 0; t < 2; ++t) {
       if (!ok) break;
       const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
@@ -176,6 +176,7 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
         if (!(ok = ptx::mbar_wait(bar(kBarP0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
         ptx::tc_fence_after();
         const uint32_t vt = sbase + L::kSlot + slot_of(2 * (j - 1) + 1) * L::kTile;
+#pragma unroll 1
         for (int ks = 0; ks < kTileKeys / 16; ++ks)  // P: 16 keys = 8 packed TMEM columns per step
           ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024), idesc_pv,
                                (j > 1 || ks > 0));
@@ -190,6 +191,7 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
         }
         const uint32_t kt = sbase + L::kSlot + slot_of(2 * j) * L::kTile;
         const uint32_t qt = sbase + L::kQ + t * L::kTile;
+#pragma unroll 1
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
           ptx::mma_bf16(tS, ptx::smem_desc(qt + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024), idesc_qk, ks > 0);
@@ -222,33 +224,25 @@ struct TileMask {
   bool all_full;
 
   __device__ __forceinline__ void build(const AttnRun* runs, int first, int n_runs, int lim) {
-    int2 rr[kRuns];
-#pragma unroll
-    for (int g = 0; g < kRuns; ++g) {
-      const int ri = first + g;
-      rr[g] = ri < n_runs ? *reinterpret_cast<const int2*>(&runs[ri].lohi) : make_int2(0, INT_MIN);
-    }
-    // Fast path: every run a full page and the last entry within the limit.
+    // One run at a time: its visible slots are [lo, min(hi, lo + (lim - es) + 1)).
     bool full = true;
-#pragma unroll
-    for (int g = 0; g < kRuns; ++g) full = full && rr[g].x == (PAGE << 16) && rr[g].y != INT_MIN;
-    full = full && rr[kRuns - 1].y + PAGE - 1 <= lim;
-    all_full = full;
-    if (full) {
-      m[0] = m[1] = m[2] = m[3] = 0xffffffffu;
-      return;
-    }
     m[0] = m[1] = m[2] = m[3] = 0u;
 #pragma unroll
     for (int g = 0; g < kRuns; ++g) {
-      if (rr[g].y == INT_MIN) continue;
-      const int lo = rr[g].x & 0xffff, hi = rr[g].x >> 16;
-      // visible slots: [lo, min(hi, lo + (lim - es) + 1))
-      const int64_t cap = int64_t(lo) + int64_t(lim) - int64_t(rr[g].y) + 1;
+      const int ri = first + g;
+      if (ri >= n_runs) {
+        full = false;
+        continue;
+      }
+      const int2 rr = *reinterpret_cast<const int2*>(&runs[ri].lohi);
+      const int lo = rr.x & 0xffff, hi = rr.x >> 16;
+      const int64_t cap = int64_t(lo) + int64_t(lim) - int64_t(rr.y) + 1;
       const int vhi = int(cap < hi ? (cap < lo ? lo : cap) : hi);
+      full = full && lo == 0 && vhi == PAGE;
       const int a = g * PAGE + lo, b = g * PAGE + vhi;  // bit range [a, b)
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
+        if (32 * w + 32 <= g * PAGE || 32 * w >= (g + 1) * PAGE) continue;  // word outside this run
         const int wa = min(max(a - 32 * w, 0), 32), wb = min(max(b - 32 * w, 0), 32);
         if (wb > wa) {
           const uint32_t upper = wb == 32 ? 0xffffffffu : ((1u << wb) - 1u);
@@ -256,6 +250,7 @@ struct TileMask {
         }
       }
     }
+    all_full = full;
   }
 };
 
@@ -263,7 +258,7 @@ struct TileMask {
 // across warps inside the loop: each warp synchronises only through mbarriers
 // and its own warp-collective TMEM accesses.
 template <int D, int PAGE>
-__device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint32_t sbase,
+__device__ __forceinline__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint32_t sbase,
                              uint32_t tmem, volatile int* abort_flag) {
   using L = Layout<D>;
   constexpr int kRuns = kTileKeys / PAGE;
@@ -291,6 +286,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs));
     if (!ok) break;
     ptx::tc_fence_after();
+    if (lane == 0 && (j + 1) * kRuns < seg.n_runs) ptx::prefetch_l1(runs + (j + 1) * kRuns);
     uint32_t u[kTileKeys];
     ptx::tmem_load64_async(tS + lane_addr, u);
     ptx::tmem_load64_async(tS + lane_addr + 64, u + 64);
@@ -338,6 +334,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
         ptx::tmem_store32(tO + lane_addr + c * 32, o);
       }
     }
+    // The next tile's visibility (its runs were prefetched into L1 above).
     if (j + 1 < n_t) mask.build(runs, (j + 1) * kRuns, seg.n_runs, lim);
     l_run = l_run * alpha + rowsum;
     m_run = m_use;
@@ -391,8 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const AttnWork w = p.work[blockIdx.x];
-  const AttnSeg seg = p.segs[w.seg];
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, (i == kBarP0 || i == kBarP0 + 1) ? 128 : 1);
@@ -413,13 +408,23 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Each role loads its work item itself, so nothing but a few addresses is
+  // live across the register re-allocation.
   if (warp < 4) {
     ptx::regs_decrease<kCtlRegs>();
-    if (warp == 0 && lane == 0) produce<D>(p, w, seg, sbase, abort_flag);
-    if (warp == 1 && lane == 0) issue_mma<D>(p, w, sbase, tmem, abort_flag);
+    if (warp == 0 && lane == 0) {
+      const AttnWork w = p.work[blockIdx.x];
+      produce<D>(p, w, p.segs[w.seg], sbase, abort_flag);
+    }
+    if (warp == 1 && lane == 0) issue_mma<D>(p, p.work[blockIdx.x], sbase, tmem, abort_flag);
+    __syncwarp();
+    ptx::regs_increase<kLaunchRegs>();
   } else {
     ptx::regs_increase<kSoftmaxRegs>();
-    softmax_tile<D, PAGE>(p, w, seg, warp < 8 ? 0 : 1, sbase, tmem, abort_flag);
+    const AttnWork w = p.work[blockIdx.x];
+    softmax_tile<D, PAGE>(p, w, p.segs[w.seg], warp < 8 ? 0 : 1, sbase, tmem, abort_flag);
+    __syncwarp();
+    ptx::regs_decrease<kLaunchRegs>();
   }
 
   ptx::tc_fence_before();

@@ -21,7 +21,7 @@
 //     tcgen05.mma from one thread, per KV tile j and per query tile T:
 //     O_T += P_T(j-1) V_{j-1}, then S_T(j) = Q_T K_j^T, then one commit -- so
 //     "S_T(j) is ready" also means "O_T is stable and P_T may be rewritten";
-//   * warpgroups 1 (tile A) and 2 (tile B) run the online softmax, one thread
+//   * warps 2-5 (tile A) and 6-9 (tile B) run the online softmax, one thread
 //     per row = one TMEM lane: a whole score row comes in with one 128-column
 //     TMEM load, row max and row sum need no shuffles, O is rescaled lazily in
 //     TMEM (only when the running max grows by more than 2^8), and P (bf16) is
@@ -43,11 +43,7 @@
 namespace akv {
 namespace {
 
-constexpr int kThreads = 384;  // 3 warpgroups: control (producer, MMA), softmax A, softmax B
-constexpr int kLaunchRegs = 168;  // per thread at launch: 65536 / 384, rounded down to 8
-constexpr int kCtlRegs = 120;     // control warpgroup after re-allocation (producer + MMA loops)
-constexpr int kSoftmaxRegs = 192; // each softmax warpgroup after re-allocation
-static_assert(4 * 32 * kCtlRegs + 8 * 32 * kSoftmaxRegs <= kThreads * kLaunchRegs, "register split");
+constexpr int kThreads = 320;
 constexpr int kTileKeys = 128;
 constexpr int kRows = 128;
 constexpr uint32_t kTmemCols = 512;
@@ -64,7 +60,8 @@ struct Layout {
   static constexpr uint32_t kTile = kBlocks * kBlockBytes;
   static constexpr uint32_t kQ = 0;                          // Q_A, Q_B
   static constexpr uint32_t kSlot = kQ + 2 * kTile;          // K/V slots
-  static constexpr uint32_t kBars = kSlot + kSlots * kTile;
+  static constexpr uint32_t kColE = kSlot + kSlots * kTile;  // int32 [2][128]: entry per key column
+  static constexpr uint32_t kBars = kColE + 2 * 128 * 4;
   static constexpr uint32_t kBytes = kBars + 256;
 };
 
@@ -95,7 +92,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // ---------------------------------------------------------------- producer
 template <int D>
-__device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
+__device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
                         volatile int* abort_flag) {
   using L = Layout<D>;
   const uint32_t bars = sbase + L::kBars;
@@ -110,8 +107,8 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
                        w.kvh * G, q_tok0 + t * tpt);
   const int layer_base = p.layer * p.n_pages;
   const AttnRun first = p.runs[seg.run_off];
+  int armed[kSlots] = {0, 0, 0};
   bool ok = true;
-  int issued = 0;  // loads issued
   for (int ld = 0; ld < 2 * n_max; ++ld) {
     const int j = ld >> 1, is_v = ld & 1, slot = ld % kSlots, use = ld / kSlots;
     if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
@@ -129,7 +126,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
         ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, map, bar(kBarFull0 + slot), kb * 64, 0, w.kvh,
                          pg);
     }
-    issued = ld + 1;
+    armed[slot] = use + 1;
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 0, 0);
@@ -137,11 +134,8 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
   }
   // Drain: every copy issued here has landed before the CTA may exit.
   ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kDrainLimitNs);
-#pragma unroll
-  for (int s = 0; s < kSlots; ++s) {
-    const int uses = issued > s ? (issued - s + kSlots - 1) / kSlots : 0;  // loads that went to slot s
-    if (uses) ptx::mbar_wait(bar(kBarFull0 + s), (uses - 1) & 1, abort_flag, kDrainLimitNs);
-  }
+  for (int s = 0; s < kSlots; ++s)
+    if (armed[s]) ptx::mbar_wait(bar(kBarFull0 + s), (armed[s] - 1) & 1, abort_flag, kDrainLimitNs);
 }
 
 // --------------------------------------------------------------------- MMA
@@ -149,7 +143,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
 // written), then S_T(j) = Q_T K_j^T, then one commit to S_T's barrier.  Slots
 // are released (commit to their empty barrier) after their last reader.
 template <int D>
-__device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
+__device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
                           volatile int* abort_flag) {
   using L = Layout<D>;
   const uint32_t bars = sbase + L::kBars;
@@ -163,9 +157,7 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
   bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
   for (int j = 0; j <= n_max && ok; ++j) {
     bool k_ready = false, v_ready = false;
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-      if (!ok) break;
+    for (int t = 0; t < 2 && ok; ++t) {
       const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
       if (j >= 1 && j - 1 < n_t[t]) {
         if (!v_ready) {
@@ -176,7 +168,6 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
         if (!(ok = ptx::mbar_wait(bar(kBarP0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
         ptx::tc_fence_after();
         const uint32_t vt = sbase + L::kSlot + slot_of(2 * (j - 1) + 1) * L::kTile;
-#pragma unroll 1
         for (int ks = 0; ks < kTileKeys / 16; ++ks)  // P: 16 keys = 8 packed TMEM columns per step
           ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024), idesc_pv,
                                (j > 1 || ks > 0));
@@ -191,7 +182,6 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
         }
         const uint32_t kt = sbase + L::kSlot + slot_of(2 * j) * L::kTile;
         const uint32_t qt = sbase + L::kQ + t * L::kTile;
-#pragma unroll 1
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
           ptx::mma_bf16(tS, ptx::smem_desc(qt + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024), idesc_qk, ks > 0);
@@ -213,117 +203,89 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
 }
 
 // ----------------------------------------------------------------- softmax
-// Visibility of the 128 key columns of one KV tile for one query row, as a
-// 128-bit mask: column c = run c / PAGE, slot c % PAGE of the tile's runs is
-// visible when the slot lies in the run and its entry index is within the
-// row's causal limit.  all_full tells whether every column is visible.
-template <int PAGE>
-struct TileMask {
-  static constexpr int kRuns = kTileKeys / PAGE;
-  uint32_t m[4];
-  bool all_full;
-
-  __device__ __forceinline__ void build(const AttnRun* runs, int first, int n_runs, int lim) {
-    // One run at a time: its visible slots are [lo, min(hi, lo + (lim - es) + 1)).
-    bool full = true;
-    m[0] = m[1] = m[2] = m[3] = 0u;
-#pragma unroll
-    for (int g = 0; g < kRuns; ++g) {
-      const int ri = first + g;
-      if (ri >= n_runs) {
-        full = false;
-        continue;
-      }
-      const int2 rr = *reinterpret_cast<const int2*>(&runs[ri].lohi);
-      const int lo = rr.x & 0xffff, hi = rr.x >> 16;
-      const int64_t cap = int64_t(lo) + int64_t(lim) - int64_t(rr.y) + 1;
-      const int vhi = int(cap < hi ? (cap < lo ? lo : cap) : hi);
-      full = full && lo == 0 && vhi == PAGE;
-      const int a = g * PAGE + lo, b = g * PAGE + vhi;  // bit range [a, b)
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        if (32 * w + 32 <= g * PAGE || 32 * w >= (g + 1) * PAGE) continue;  // word outside this run
-        const int wa = min(max(a - 32 * w, 0), 32), wb = min(max(b - 32 * w, 0), 32);
-        if (wb > wa) {
-          const uint32_t upper = wb == 32 ? 0xffffffffu : ((1u << wb) - 1u);
-          m[w] |= upper & ~((1u << wa) - 1u);
-        }
-      }
-    }
-    all_full = full;
-  }
-};
-
-// One warpgroup per query tile t; thread = row r = TMEM lane r.  No barrier
-// across warps inside the loop: each warp synchronises only through mbarriers
-// and its own warp-collective TMEM accesses.
-template <int D, int PAGE>
-__device__ __forceinline__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint32_t sbase,
-                             uint32_t tmem, volatile int* abort_flag) {
+// One warpgroup per query tile t; thread = row r = TMEM lane r.
+template <int D>
+__device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint8_t* smem,
+                             uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
   using L = Layout<D>;
-  constexpr int kRuns = kTileKeys / PAGE;
   const int n_t = t == 0 ? w.n_a : w.n_b;
   if (n_t == 0) return;
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
-  const int quad = (threadIdx.x / 32) & 3;  // TMEM lane quadrant this warp may access (warp % 4)
+  const int wg_warp = (threadIdx.x / 32 - 2) % 4;
+  const int quad = (threadIdx.x / 32) & 3;  // TMEM lane quadrant this warp may access
   const int lane = threadIdx.x % 32;
   const int r = quad * 32 + lane;
+  (void)wg_warp;
   const uint32_t lane_addr = uint32_t(quad * 32) << 16;
   const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
-  const int G = p.group, tpt = kRows / G;
+  const int G = p.group, tpt = kRows / G, rpt = kTileKeys / p.page;
   const int t_loc = r / G, g = r % G;
   const int qi = (w.qt0 + t) * tpt + t_loc;  // query index inside the segment
   const bool row_valid = qi < seg.q_len;
   const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
   const float sl2 = p.scale_log2;
-  const AttnRun* runs = p.runs + seg.run_off;
+  const int bar_id = 1 + t;  // named barrier of this warpgroup
+  int* colE = reinterpret_cast<int*>(smem + L::kColE) + t * 128;
+  int page_shift = 4;
+  while ((1 << page_shift) < p.page) ++page_shift;
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
-  TileMask<PAGE> mask;
-  mask.build(runs, 0, seg.n_runs, lim);
+  const int sl_own = r & (p.page - 1);
+  bool run_ok = (r >> page_shift) < seg.n_runs;
+  AttnRun run_cur = run_ok ? p.runs[seg.run_off + (r >> page_shift)] : AttnRun{0, 0, 0, 0};
   for (int j = 0; j < n_t; ++j) {
-    ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs));
-    if (!ok) break;
-    ptx::tc_fence_after();
-    if (lane == 0 && (j + 1) * kRuns < seg.n_runs) ptx::prefetch_l1(runs + (j + 1) * kRuns);
-    uint32_t u[kTileKeys];
-    ptx::tmem_load64_async(tS + lane_addr, u);
-    ptx::tmem_load64_async(tS + lane_addr + 64, u + 64);
-    ptx::tmem_wait_load128(u);
-    if (!mask.all_full) {
-#pragma unroll
-      for (int c = 0; c < kTileKeys; ++c)
-        if (!((mask.m[c >> 5] >> (c & 31)) & 1u)) u[c] = 0xff800000u;  // -inf
+    ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(bar_id, 128, ok)) {
+      ok = false;
+      break;
     }
-    float mx[4];
+    // Entry index of key column r of tile j (INT_MAX: no entry there);
+    // columns are (run c / page, slot c % page) of the tile's runs.  The run
+    // of the next tile is fetched now so its latency hides behind this tile.
+    int e = INT_MAX;
+    {
+      const int lo = run_cur.lohi & 0xffff, hi = run_cur.lohi >> 16;
+      if (run_ok && sl_own >= lo && sl_own < hi) e = run_cur.es + (sl_own - lo);
+      colE[r] = e;
+      const int ri = (j + 1) * rpt + (r >> page_shift);
+      run_ok = ri < seg.n_runs;
+      if (run_ok) run_cur = p.runs[seg.run_off + ri];
+    }
+    const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
+    ptx::tc_fence_after();
+    // With every column valid the entries are consecutive, so the last column
+    // holds the tile's largest entry index.
+    const bool need_mask = !all_valid || colE[kTileKeys - 1] > lim;
+    const int4* ce4 = reinterpret_cast<const int4*>(colE);
+    // Pass 1: row max over two 64-column halves read from TMEM.
+    float mx[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) mx[k] = __uint_as_float(u[k]);
+    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
-    for (int c = 4; c < kTileKeys; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(u[c]));
-    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;  // -inf
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(u[c]));
+    }
+    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
     const float m_new = fmaxf(m_run, mt);
     const bool resc = m_new > m_run + 8.0f;
     const float m_use = resc ? m_new : m_run;
     const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
     const float msub = m_use == -INFINITY ? 0.f : m_use;
-    // P = exp2(s * scale * log2 e - m) as bf16 pairs (keys 2c, 2c+1 -> column c),
-    // stored over the S columns already read; the PV MMA reads it from TMEM.
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int c = 0; c < kTileKeys / 2; ++c) {
-      const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
-      const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
-      sum[(2 * c) & 3] += p0;
-      sum[(2 * c + 1) & 3] += p1;
-      u[c] = pack_bf16(p0, p1);  // u[c] was consumed by an earlier pair
-    }
-    ptx::tmem_store32_async(tS + lane_addr, u);
-    ptx::tmem_store32_async(tS + lane_addr + 32, u + 32);
-    const float rowsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
-    ptx::tmem_wait_store64(u);
-    // Lazy rescale of O (after P is stored, before PV_T(j) may start): O_T is
-    // stable here because S_T(j) completes after PV_T(j-1).
+    // O_T is stable here: S_T(j) completes after PV_T(j-1).
     if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -334,14 +296,45 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& p, const AttnWork
         ptx::tmem_store32(tO + lane_addr + c * 32, o);
       }
     }
-    // The next tile's visibility (its runs were prefetched into L1 above).
-    if (j + 1 < n_t) mask.build(runs, (j + 1) * kRuns, seg.n_runs, lim);
+    // Pass 2: P = exp2(s * scale * log2 e - m), packed to bf16 pairs and
+    // stored over the S columns already read (keys 2c, 2c+1 -> column c), where
+    // the PV MMA reads it as its A operand.
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
+        const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
+        sum[(2 * c) & 7] += p0;
+        sum[(2 * c + 1) & 7] += p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      ptx::tmem_store32(tS + lane_addr + h * 32, pk);
+    }
+    const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
     l_run = l_run * alpha + rowsum;
     m_run = m_use;
     ptx::tc_fence_before();
     ptx::mbar_arrive(bar(kBarP0 + t));
   }
-  if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarO0 + t), 0, abort_flag, kWaitLimitNs));
+  if (ok) {
+    ok = ptx::mbar_wait(bar(kBarO0 + t), 0, abort_flag, kWaitLimitNs);
+    ok = ptx::bar_red_and(bar_id, 128, ok);
+  }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 2 + t, 0);
     *abort_flag = 1;
@@ -373,7 +366,7 @@ __device__ __forceinline__ void softmax_tile(const AttnParams& p, const AttnWork
   }
 }
 
-template <int D, int PAGE>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_constant__ AttnParams p, int smem_bytes) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -388,6 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const AttnWork w = p.work[blockIdx.x];
+  const AttnSeg seg = p.segs[w.seg];
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, (i == kBarP0 || i == kBarP0 + 1) ? 128 : 1);
@@ -408,23 +403,12 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Each role loads its work item itself, so nothing but a few addresses is
-  // live across the register re-allocation.
-  if (warp < 4) {
-    ptx::regs_decrease<kCtlRegs>();
-    if (warp == 0 && lane == 0) {
-      const AttnWork w = p.work[blockIdx.x];
-      produce<D>(p, w, p.segs[w.seg], sbase, abort_flag);
-    }
-    if (warp == 1 && lane == 0) issue_mma<D>(p, p.work[blockIdx.x], sbase, tmem, abort_flag);
-    __syncwarp();
-    ptx::regs_increase<kLaunchRegs>();
+  if (warp == 0) {
+    if (lane == 0) produce<D>(p, w, seg, sbase, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) issue_mma<D>(p, w, sbase, tmem, abort_flag);
   } else {
-    ptx::regs_increase<kSoftmaxRegs>();
-    const AttnWork w = p.work[blockIdx.x];
-    softmax_tile<D, PAGE>(p, w, p.segs[w.seg], warp < 8 ? 0 : 1, sbase, tmem, abort_flag);
-    __syncwarp();
-    ptx::regs_decrease<kLaunchRegs>();
+    softmax_tile<D>(p, w, seg, warp < 6 ? 0 : 1, smem, sbase, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -444,29 +428,21 @@ int segment_attn_smem_bytes(int dim) {
   return int(Layout<128>::kBytes) + 1024;
 }
 
-template <int D, int PAGE>
-cudaError_t launch_one(const AttnParams& p, int smem, cudaStream_t st) {
-  // The register re-allocation inside the kernel needs the launch to hold
-  // kLaunchRegs per thread; refuse to launch otherwise (it would never finish).
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, segment_attn_kernel<D, PAGE>);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs < kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(segment_attn_kernel<D, PAGE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  segment_attn_kernel<D, PAGE><<<p.n_work, kThreads, smem, st>>>(p, smem);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st) {
   if (p.n_work <= 0) return cudaSuccess;
   const int smem = segment_attn_smem_bytes(dim);
   if (smem < 0) return cudaErrorInvalidValue;
-  if (dim == 64 && p.page == 16) return launch_one<64, 16>(p, smem, st);
-  if (dim == 64 && p.page == 64) return launch_one<64, 64>(p, smem, st);
-  if (dim == 128 && p.page == 16) return launch_one<128, 16>(p, smem, st);
-  if (dim == 128 && p.page == 64) return launch_one<128, 64>(p, smem, st);
-  return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (dim == 64) {
+    e = cudaFuncSetAttribute(segment_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    segment_attn_kernel<64><<<p.n_work, kThreads, smem, st>>>(p, smem);
+  } else {
+    e = cudaFuncSetAttribute(segment_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    segment_attn_kernel<128><<<p.n_work, kThreads, smem, st>>>(p, smem);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace akv

@@ -90,10 +90,6 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l1(const void* ptr) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
-}
-
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor core reading P from shared memory).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -202,31 +198,6 @@ __device__ __forceinline__ void tmem_store32(uint32_t taddr, const uint32_t (&r)
 }
 
 
-// Split-phase TMEM access: issue loads / stores, then one wait for all of
-// them.  The wait names the loaded registers as in-out operands so that no use
-// of them can be scheduled before it.
-__device__ __forceinline__ void tmem_load64_async(uint32_t taddr, uint32_t* x) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n"
-               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5]), "=r"(x[6]), "=r"(x[7]), "=r"(x[8]), "=r"(x[9]), "=r"(x[10]), "=r"(x[11]), "=r"(x[12]), "=r"(x[13]), "=r"(x[14]), "=r"(x[15]), "=r"(x[16]), "=r"(x[17]), "=r"(x[18]), "=r"(x[19]), "=r"(x[20]), "=r"(x[21]), "=r"(x[22]), "=r"(x[23]), "=r"(x[24]), "=r"(x[25]), "=r"(x[26]), "=r"(x[27]), "=r"(x[28]), "=r"(x[29]), "=r"(x[30]), "=r"(x[31]), "=r"(x[32]), "=r"(x[33]), "=r"(x[34]), "=r"(x[35]), "=r"(x[36]), "=r"(x[37]), "=r"(x[38]), "=r"(x[39]), "=r"(x[40]), "=r"(x[41]), "=r"(x[42]), "=r"(x[43]), "=r"(x[44]), "=r"(x[45]), "=r"(x[46]), "=r"(x[47]), "=r"(x[48]), "=r"(x[49]), "=r"(x[50]), "=r"(x[51]), "=r"(x[52]), "=r"(x[53]), "=r"(x[54]), "=r"(x[55]), "=r"(x[56]), "=r"(x[57]), "=r"(x[58]), "=r"(x[59]), "=r"(x[60]), "=r"(x[61]), "=r"(x[62]), "=r"(x[63])
-               : "r"(taddr)
-               : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_load128(uint32_t (&x)[128]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]), "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]), "+r"(x[14]), "+r"(x[15]), "+r"(x[16]), "+r"(x[17]), "+r"(x[18]), "+r"(x[19]), "+r"(x[20]), "+r"(x[21]), "+r"(x[22]), "+r"(x[23]), "+r"(x[24]), "+r"(x[25]), "+r"(x[26]), "+r"(x[27]), "+r"(x[28]), "+r"(x[29]), "+r"(x[30]), "+r"(x[31]), "+r"(x[32]), "+r"(x[33]), "+r"(x[34]), "+r"(x[35]), "+r"(x[36]), "+r"(x[37]), "+r"(x[38]), "+r"(x[39]), "+r"(x[40]), "+r"(x[41]), "+r"(x[42]), "+r"(x[43]), "+r"(x[44]), "+r"(x[45]), "+r"(x[46]), "+r"(x[47]), "+r"(x[48]), "+r"(x[49]), "+r"(x[50]), "+r"(x[51]), "+r"(x[52]), "+r"(x[53]), "+r"(x[54]), "+r"(x[55]), "+r"(x[56]), "+r"(x[57]), "+r"(x[58]), "+r"(x[59]), "+r"(x[60]), "+r"(x[61]), "+r"(x[62]), "+r"(x[63]), "+r"(x[64]), "+r"(x[65]), "+r"(x[66]), "+r"(x[67]), "+r"(x[68]), "+r"(x[69]), "+r"(x[70]), "+r"(x[71]), "+r"(x[72]), "+r"(x[73]), "+r"(x[74]), "+r"(x[75]), "+r"(x[76]), "+r"(x[77]), "+r"(x[78]), "+r"(x[79]), "+r"(x[80]), "+r"(x[81]), "+r"(x[82]), "+r"(x[83]), "+r"(x[84]), "+r"(x[85]), "+r"(x[86]), "+r"(x[87]), "+r"(x[88]), "+r"(x[89]), "+r"(x[90]), "+r"(x[91]), "+r"(x[92]), "+r"(x[93]), "+r"(x[94]), "+r"(x[95]), "+r"(x[96]), "+r"(x[97]), "+r"(x[98]), "+r"(x[99]), "+r"(x[100]), "+r"(x[101]), "+r"(x[102]), "+r"(x[103]), "+r"(x[104]), "+r"(x[105]), "+r"(x[106]), "+r"(x[107]), "+r"(x[108]), "+r"(x[109]), "+r"(x[110]), "+r"(x[111]), "+r"(x[112]), "+r"(x[113]), "+r"(x[114]), "+r"(x[115]), "+r"(x[116]), "+r"(x[117]), "+r"(x[118]), "+r"(x[119]), "+r"(x[120]), "+r"(x[121]), "+r"(x[122]), "+r"(x[123]), "+r"(x[124]), "+r"(x[125]), "+r"(x[126]), "+r"(x[127])::"memory");
-}
-
-__device__ __forceinline__ void tmem_store32_async(uint32_t taddr, const uint32_t* x) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n" ::"r"(taddr), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3]), "r"(x[4]), "r"(x[5]), "r"(x[6]), "r"(x[7]), "r"(x[8]), "r"(x[9]), "r"(x[10]), "r"(x[11]), "r"(x[12]), "r"(x[13]), "r"(x[14]), "r"(x[15]), "r"(x[16]), "r"(x[17]), "r"(x[18]), "r"(x[19]), "r"(x[20]), "r"(x[21]), "r"(x[22]), "r"(x[23]), "r"(x[24]), "r"(x[25]), "r"(x[26]), "r"(x[27]), "r"(x[28]), "r"(x[29]), "r"(x[30]), "r"(x[31])
-               : "memory");
-}
-
-// Wait for this thread's TMEM stores; the stored registers are in-out
-// operands, so they stay untouched until the stores have read them.
-__device__ __forceinline__ void tmem_wait_store64(uint32_t (&x)[128]) {
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5]), "+r"(x[6]), "+r"(x[7]), "+r"(x[8]), "+r"(x[9]), "+r"(x[10]), "+r"(x[11]), "+r"(x[12]), "+r"(x[13]), "+r"(x[14]), "+r"(x[15]), "+r"(x[16]), "+r"(x[17]), "+r"(x[18]), "+r"(x[19]), "+r"(x[20]), "+r"(x[21]), "+r"(x[22]), "+r"(x[23]), "+r"(x[24]), "+r"(x[25]), "+r"(x[26]), "+r"(x[27]), "+r"(x[28]), "+r"(x[29]), "+r"(x[30]), "+r"(x[31]), "+r"(x[32]), "+r"(x[33]), "+r"(x[34]), "+r"(x[35]), "+r"(x[36]), "+r"(x[37]), "+r"(x[38]), "+r"(x[39]), "+r"(x[40]), "+r"(x[41]), "+r"(x[42]), "+r"(x[43]), "+r"(x[44]), "+r"(x[45]), "+r"(x[46]), "+r"(x[47]), "+r"(x[48]), "+r"(x[49]), "+r"(x[50]), "+r"(x[51]), "+r"(x[52]), "+r"(x[53]), "+r"(x[54]), "+r"(x[55]), "+r"(x[56]), "+r"(x[57]), "+r"(x[58]), "+r"(x[59]), "+r"(x[60]), "+r"(x[61]), "+r"(x[62]), "+r"(x[63])::"memory");
-}
-
 // 64 consecutive 32-bit TMEM columns of this thread's lane, then the wait.
 __device__ __forceinline__ void tmem_load64(uint32_t taddr, uint32_t (&x)[64]) {
   asm volatile(
@@ -266,18 +237,6 @@ __device__ __forceinline__ bool bar_red_and(int id, int nthreads, bool pred) {
       : "r"(uint32_t(pred)), "r"(id), "r"(nthreads)
       : "memory");
   return out != 0;
-}
-
-// Warpgroup-wide register re-allocation (all four warps of a warpgroup run
-// the same one).  The launch's registers (threads x per-thread count) must
-// cover the sum of the new per-warpgroup counts.
-template <int N>
-__device__ __forceinline__ void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

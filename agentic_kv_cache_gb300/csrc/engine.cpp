@@ -266,6 +266,11 @@ struct akv_ctx {
   Marks mk, mv;
   std::vector<std::vector<Tok>> seqs;
   std::vector<uint8_t> live;
+  // Per sequence: an upper bound on |position| and |pending shift| of its
+  // tokens; while bound + |delta| fits in int32 no per-token overflow check is needed.
+  std::vector<int64_t> bound;
+  std::vector<int32_t> page_dst;  // flush scratch: destination of each moving K page
+  std::vector<int32_t> sim_rc;    // flush scratch: simulated reference-count changes
   std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ids;
   std::string err;
   std::vector<int32_t> last_runs;  // 5 per run
@@ -302,10 +307,12 @@ struct akv_ctx {
       int32_t id = free_ids.top();
       free_ids.pop();
       live[id] = 1;
+      bound[id] = 0;
       return id;
     }
     seqs.emplace_back();
     live.push_back(1);
+    bound.push_back(0);
     return int32_t(seqs.size() - 1);
   }
 
@@ -440,6 +447,7 @@ struct akv_ctx {
         room = cfg.page_size - 1;
       }
       toks.push_back(Tok{kp, vp, slot, p[i], 0, 1});
+      bound[sid] = std::max<int64_t>(bound[sid], std::abs(int64_t(p[i])));
       krow[i] = kp * cfg.page_size + slot;
       vrow[i] = vp * cfg.page_size + slot;
     }
@@ -456,7 +464,8 @@ struct akv_ctx {
     for (int64_t i = s; i < e; ++i) toks[i].vis = 0;
   }
 
-  void check_shift(const std::vector<Tok>& toks, int64_t a, int64_t b, int64_t delta) {
+  void check_shift(const std::vector<Tok>& toks, int64_t a, int64_t b, int64_t delta, int64_t seq_bound) {
+    if (seq_bound + std::abs(delta) <= kI32Max) return;  // cannot leave int32
     for (int64_t i = a; i < b; ++i) {
       const Tok& t = toks[i];
       if (int64_t(t.delta) + delta < kI32Min || int64_t(t.delta) + delta > kI32Max)
@@ -466,11 +475,24 @@ struct akv_ctx {
     }
   }
 
+  // Exact bound of a sequence (used when the running bound grew too loose).
+  static int64_t exact_bound(const std::vector<Tok>& toks) {
+    int64_t b = 0;
+    for (const Tok& t : toks) b = std::max({b, std::abs(t.eff()), std::abs(int64_t(t.delta))});
+    return b;
+  }
+
+  void grow_bound(int32_t sid, int64_t by) {
+    bound[sid] += by;
+    if (bound[sid] > kI32Max) bound[sid] = exact_bound(seqs[sid]);
+  }
+
   void repos(int32_t sid, int64_t s, int64_t e, int32_t delta) {
     auto& toks = seq(sid);
     check_span(toks, s, e, "repos");
-    check_shift(toks, s, e, delta);
+    check_shift(toks, s, e, delta, bound[sid]);
     for (int64_t i = s; i < e; ++i) toks[i].delta += delta;
+    grow_bound(sid, std::abs(int64_t(delta)));
   }
 
   void splice(int32_t sid, int64_t s, int64_t e, int64_t n_stub, const void* k, const void* v, const int32_t* pos,
@@ -488,7 +510,7 @@ struct akv_ctx {
       if (n_stub && p0 + n_stub - 1 > kI32Max) fail(AKV_ERR_OVERFLOW, "stub position leaves int32");
       for (int64_t i = 0; i < n_stub; ++i) p[i] = int32_t(p0 + i);
     }
-    check_shift(toks, e, int64_t(toks.size()), delta);
+    check_shift(toks, e, int64_t(toks.size()), delta, bound[sid]);
     if (int64_t(toks.size()) - (e - s) + n_stub > kI32Max) fail(AKV_ERR_RANGE, "sequence too long");
     // pages referenced only by the removed tokens are released
     std::vector<int32_t> kk, vv, kr, vr;
@@ -529,6 +551,10 @@ struct akv_ctx {
     out.insert(out.end(), stub.begin(), stub.end());
     out.insert(out.end(), toks.begin() + e, toks.end());
     toks.swap(out);
+    int64_t pmax = 0;
+    for (int32_t q : p) pmax = std::max<int64_t>(pmax, std::abs(int64_t(q)));
+    bound[sid] = std::max(bound[sid], pmax);
+    grow_bound(sid, std::abs(delta));
     write_rows(krow, vrow, k, v, st);
   }
 
@@ -540,8 +566,10 @@ struct akv_ctx {
     pages_of(child, 0, child.size(), kps, vps);
     for (int32_t q : kps) K.inc(q);
     for (int32_t q : vps) V.inc(q);
+    const int64_t parent_bound = bound[src];
     int32_t id = new_id();
     seqs[id] = std::move(child);
+    bound[id] = parent_bound;
     *out = id;
   }
 
@@ -567,11 +595,7 @@ struct akv_ctx {
 
   void flush(const std::vector<int32_t>& ids, cudaStream_t st) {
     // Budget check on simulated reference counts, so a failure changes nothing.
-    std::unordered_map<int32_t, int32_t> rc_sim;
-    auto rc_of = [&](int32_t q) {
-      auto it = rc_sim.find(q);
-      return it == rc_sim.end() ? K.rc(q) : it->second;
-    };
+    std::vector<int32_t> touched;  // pages with a simulated change
     int64_t need = 0;
     std::vector<int32_t> order;
     for (int32_t sid : ids) {
@@ -579,17 +603,19 @@ struct akv_ctx {
       moving_pages(toks, order);
       std::vector<int32_t> cow;
       for (int32_t q : order)
-        if (rc_of(q) > 1) cow.push_back(q);
+        if (K.rc(q) + sim_rc[q] > 1) cow.push_back(q);
       need += int64_t(cow.size());
       if (cow.empty()) continue;
       mk.next();
-      for (int32_t q : cow) mk.test_set(q);
-      std::unordered_map<int32_t, bool> stays;
       for (const Tok& t : toks)
-        if (!t.vis && mk.test(t.kp)) stays[t.kp] = true;
+        if (!t.vis) mk.test_set(t.kp);  // marked: a dropped token of this sequence sits in the page
       for (int32_t q : cow)
-        if (!stays.count(q)) rc_sim[q] = rc_of(q) - 1;
+        if (!mk.test(q)) {
+          if (sim_rc[q] == 0) touched.push_back(q);
+          sim_rc[q] -= 1;
+        }
     }
+    for (int32_t q : touched) sim_rc[q] = 0;
     if (need > K.n_free()) fail(AKV_ERR_NO_PAGES, "flush needs %lld copy-on-write pages", (long long)need);
 
     std::vector<akv::RunDesc> runs;
@@ -674,14 +700,13 @@ struct akv_ctx {
     std::vector<int32_t> order;
     moving_pages(toks, order);
     if (order.empty()) return;
-    std::unordered_map<int32_t, int32_t> dst;  // source page -> destination page
     std::vector<int32_t> cow;
-    for (int32_t q : order) {
+    for (int32_t q : order) {  // page_dst: source page -> destination page
       if (K.rc(q) > 1) {
         cow.push_back(q);
-        dst[q] = K.alloc();
+        page_dst[q] = K.alloc();
       } else {
-        dst[q] = q;
+        page_dst[q] = q;
       }
     }
     mk.next();
@@ -712,7 +737,7 @@ struct akv_ctx {
         close();
         continue;
       }
-      const int32_t d = dst.count(t.kp) ? dst[t.kp] : t.kp;
+      const int32_t d = page_dst[t.kp];  // emitted tokens sit in moving pages
       if (open && c_src == t.kp && c_dst == d && c_delta == t.delta && t.slot == c_hi) {
         ++c_hi;
       } else {
@@ -729,7 +754,7 @@ struct akv_ctx {
     for (Tok& t : toks) {
       const bool copied = mk.test(t.kp);
       if (t.vis && (t.delta != 0 || copied)) {
-        if (copied) t.kp = dst[t.kp];
+        if (copied) t.kp = page_dst[t.kp];
         t.pos += t.delta;
         t.delta = 0;
       }
@@ -952,6 +977,8 @@ struct akv_ctx {
     V.init(c.n_pages);
     mk.init(c.n_pages);
     mv.init(c.n_pages);
+    page_dst.assign(c.n_pages, -1);
+    sim_rc.assign(c.n_pages, 0);
     if (!pools) {
       meta = true;
       return;

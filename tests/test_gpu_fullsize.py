@@ -1,0 +1,79 @@
+"""Parity at the workloads' full sizes, on sampled outputs (see tests/gpu_sampled.py).
+
+* eight 64K-token sessions sharing a 4K prefix, 32 layers (~72 GB of pools):
+  sampled rotated rows of every session and layer; attention on layers 0 and
+  31 for sampled query rows of first / middle / last segments;
+* the Llama-3.1-70B-shaped 128K cache, 80 layers (~54 GB of pools): the
+  in-place full-cache sweep with shifts up to +-64K, sampled rows; attention
+  of four of the 32 branch segments on layers 0 and 79;
+* 16 DeepSeek-V2-Lite MLA sessions, 27 layers: the splice's K_pe rotation.
+Bars as in the other GPU tests (rotated keys: one bf16 ulp plus the float32
+rotation allowance, >= 99.9% bit-identical; attention: 2e-2 max-abs)."""
+import gc
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from agentic_kv_cache_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def release(c):
+    del c
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_sampled_harness_on_small_cases():
+    # the same sampled harness on scaled workloads (fast): fails early if the harness is wrong
+    from gpu_sampled import SampledCase
+    for w in (synth.sessions_64k(n_layers=2, n_sessions=3, prefix=1024, per_session=8192, q_per_seg=128,
+                                 span_len=(64, 512)),
+              synth.llama70b_128k(n_layers=2, total=16384, n_branches=4, q_per_branch=200)):
+        c = SampledCase(w)
+        c.run()
+        rng = np.random.default_rng(3)
+        n_rot, _ = c.check_repos(512, rng)
+        assert n_rot > 50
+        c.check_attention(1, 6, rng, segments=[0, len(w.segments) - 1])
+        release(c)
+
+
+def test_sessions_64k_full_size_sampled():
+    from gpu_sampled import SampledCase
+    w = synth.sessions_64k()
+    c = SampledCase(w)
+    c.run()
+    rng = np.random.default_rng(11)
+    n_rot, worst = c.check_repos(4096, rng)
+    assert n_rot > 1000
+    last = len(w.segments) - 1
+    for layer in (0, w.shape.n_layers - 1):
+        c.check_attention(layer, 12, rng, segments=[0, last // 2, last])
+    release(c)
+
+
+def test_llama70b_128k_full_size_sampled():
+    from gpu_sampled import SampledCase
+    w = synth.llama70b_128k()
+    c = SampledCase(w)
+    c.run()
+    rng = np.random.default_rng(12)
+    n_rot, worst = c.check_repos(4096, rng)
+    assert n_rot > 1000
+    for layer in (0, w.shape.n_layers - 1):
+        c.check_attention(layer, 8, rng, segments=[0, 13, 22, 31])
+    release(c)
+
+
+def test_mla_16_sessions_full_size_repos_sampled():
+    from gpu_sampled import SampledCase
+    w = synth.mla_dsv2lite(concurrency=16)
+    c = SampledCase(w)
+    c.run()
+    n_rot, worst = c.check_repos(4096, np.random.default_rng(13))
+    assert n_rot > 1000
+    release(c)

@@ -232,8 +232,6 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
   const int sl_own = r & (p.page - 1);
-  bool run_ok = (r >> page_shift) < seg.n_runs;
-  AttnRun run_cur = run_ok ? p.runs[seg.run_off + (r >> page_shift)] : AttnRun{0, 0, 0, 0};
   for (int j = 0; j < n_t; ++j) {
     ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
     // Entry index of key column r of tile j (INT_MAX: no entry there);
@@ -241,12 +239,14 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // of the next tile is fetched now so its latency hides behind this tile.
     int e = INT_MAX;
     {
-      const int lo = run_cur.lohi & 0xffff, hi = run_cur.lohi >> 16;
-      if (run_ok && sl_own >= lo && sl_own < hi) e = run_cur.es + (sl_own - lo);
+      const int ri = j * rpt + (r >> page_shift);
+      if (ri < seg.n_runs) {
+        const int2 rr = *reinterpret_cast<const int2*>(&p.runs[seg.run_off + ri].lohi);  // L1 hit: prefetched
+        const int lo = rr.x & 0xffff, hi = rr.x >> 16;
+        if (sl_own >= lo && sl_own < hi) e = rr.y + (sl_own - lo);
+      }
       colE[r] = e;
-      const int ri = (j + 1) * rpt + (r >> page_shift);
-      run_ok = ri < seg.n_runs;
-      if (run_ok) run_cur = p.runs[seg.run_off + ri];
+      if (ri + rpt < seg.n_runs) ptx::prefetch_l1(&p.runs[seg.run_off + ri + rpt]);  // next tile's run
     }
     // One warpgroup-wide reduction on the common path: every wait succeeded
     // and every column holds an entry.  (Rewriting colE here is safe: S_T(j)
@@ -267,7 +267,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // One half (64 key columns) of the row: load from TMEM, mask, then
     // p = exp2(s * scale * log2 e - msub) packed to bf16 pairs, row sum, and the
     // raw maximum of the half on the side.
-    auto half = [&](int h, float msub, uint32_t (&pk)[32], float (&sum)[4], float& mx) {
+    auto half = [&](int h, float msub, uint32_t (&pk)[32], float (&sum)[2], float& mx) {
       uint32_t u[64];
       ptx::tmem_load64(tS + lane_addr + h * 64, u);
       if (need_mask) {
@@ -280,25 +280,22 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
           if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
         }
       }
-      float m2[2] = {mx, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         const float s0 = __uint_as_float(u[2 * c]), s1 = __uint_as_float(u[2 * c + 1]);
-        m2[0] = fmaxf(m2[0], s0);
-        m2[1] = fmaxf(m2[1], s1);
+        mx = fmaxf(mx, fmaxf(s0, s1));
         const float p0 = ptx::ex2_approx(fmaf(s0, sl2, -msub));
         const float p1 = ptx::ex2_approx(fmaf(s1, sl2, -msub));
-        sum[(2 * c) & 3] += p0;
-        sum[(2 * c + 1) & 3] += p1;
+        sum[0] += p0;
+        sum[1] += p1;
         pk[c] = pack_bf16(p0, p1);
       }
-      mx = fmaxf(m2[0], m2[1]);
     };
     // Stale-max pass: P with the running max of the earlier tiles.  Only if a
     // row's maximum grows by more than 2^8 (always on the first tile) does its
     // warp reload S -- still intact, P is not stored yet -- and recompute.
     uint32_t pk0[32], pk1[32];
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    float sum[2] = {0.f, 0.f};
     float mraw = -INFINITY;
     const float msub0 = m_run == -INFINITY ? 0.f : m_run;
     half(0, msub0, pk0, sum, mraw);
@@ -312,7 +309,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
         alpha = ptx::ex2_approx(m_run - m_use);  // 0 when m_run is -inf
       }
       const float msub = m_use == -INFINITY ? 0.f : m_use;
-      sum[0] = sum[1] = sum[2] = sum[3] = 0.f;
+      sum[0] = sum[1] = 0.f;
       float unused = -INFINITY;
       half(0, msub, pk0, sum, unused);
       half(1, msub, pk1, sum, unused);
@@ -332,7 +329,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // MMA reads it from TMEM as its A operand.
     ptx::tmem_store32_async(tS + lane_addr, pk0);
     ptx::tmem_store32_async(tS + lane_addr + 32, pk1);
-    const float rowsum = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    const float rowsum = sum[0] + sum[1];
     ptx::tmem_wait_store_keep(pk0, pk1);
     l_run = l_run * alpha + rowsum;
     m_run = m_use;

@@ -232,42 +232,38 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
   const int sl_own = r & (p.page - 1);
+  bool run_ok = (r >> page_shift) < seg.n_runs;
+  AttnRun run_cur = run_ok ? p.runs[seg.run_off + (r >> page_shift)] : AttnRun{0, 0, 0, 0};
   for (int j = 0; j < n_t; ++j) {
     ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(bar_id, 128, ok)) {
+      ok = false;
+      break;
+    }
     // Entry index of key column r of tile j (INT_MAX: no entry there);
     // columns are (run c / page, slot c % page) of the tile's runs.  The run
     // of the next tile is fetched now so its latency hides behind this tile.
     int e = INT_MAX;
     {
-      const int ri = j * rpt + (r >> page_shift);
-      if (ri < seg.n_runs) {
-        const int2 rr = *reinterpret_cast<const int2*>(&p.runs[seg.run_off + ri].lohi);  // L1 hit: prefetched
-        const int lo = rr.x & 0xffff, hi = rr.x >> 16;
-        if (sl_own >= lo && sl_own < hi) e = rr.y + (sl_own - lo);
-      }
+      const int lo = run_cur.lohi & 0xffff, hi = run_cur.lohi >> 16;
+      if (run_ok && sl_own >= lo && sl_own < hi) e = run_cur.es + (sl_own - lo);
       colE[r] = e;
-      if (ri + rpt < seg.n_runs) ptx::prefetch_l1(&p.runs[seg.run_off + ri + rpt]);  // next tile's run
+      const int ri = (j + 1) * rpt + (r >> page_shift);
+      run_ok = ri < seg.n_runs;
+      if (run_ok) run_cur = p.runs[seg.run_off + ri];
     }
-    // One warpgroup-wide reduction on the common path: every wait succeeded
-    // and every column holds an entry.  (Rewriting colE here is safe: S_T(j)
-    // is only ready after all 128 threads finished reading colE of tile j-1.)
-    bool all_valid = true;
-    if (!ptx::bar_red_and(bar_id, 128, ok && e != INT_MAX)) {
-      if (!ptx::bar_red_and(bar_id, 128, ok)) {
-        ok = false;
-        break;
-      }
-      all_valid = false;
-    }
+    const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
     ptx::tc_fence_after();
     // With every column valid the entries are consecutive, so the last column
     // holds the tile's largest entry index.
     const bool need_mask = !all_valid || colE[kTileKeys - 1] > lim;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
-    // One half (64 key columns) of the row: load from TMEM, mask, then
-    // p = exp2(s * scale * log2 e - msub) packed to bf16 pairs, row sum, and the
-    // raw maximum of the half on the side.
-    auto half = [&](int h, float msub, uint32_t (&pk)[32], float (&sum)[2], float& mx) {
+    // Pass 1: row max over two 64-column halves read from TMEM.
+    float mx[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
       uint32_t u[64];
       ptx::tmem_load64(tS + lane_addr + h * 64, u);
       if (need_mask) {
@@ -281,56 +277,55 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
         }
       }
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float s0 = __uint_as_float(u[2 * c]), s1 = __uint_as_float(u[2 * c + 1]);
-        mx = fmaxf(mx, fmaxf(s0, s1));
-        const float p0 = ptx::ex2_approx(fmaf(s0, sl2, -msub));
-        const float p1 = ptx::ex2_approx(fmaf(s1, sl2, -msub));
-        sum[0] += p0;
-        sum[1] += p1;
-        pk[c] = pack_bf16(p0, p1);
-      }
-    };
-    // Stale-max pass: P with the running max of the earlier tiles.  Only if a
-    // row's maximum grows by more than 2^8 (always on the first tile) does its
-    // warp reload S -- still intact, P is not stored yet -- and recompute.
-    uint32_t pk0[32], pk1[32];
-    float sum[2] = {0.f, 0.f};
-    float mraw = -INFINITY;
-    const float msub0 = m_run == -INFINITY ? 0.f : m_run;
-    half(0, msub0, pk0, sum, mraw);
-    half(1, msub0, pk1, sum, mraw);
-    const float mt = mraw * sl2;
-    const bool resc = mt > m_run + 8.0f;
-    float alpha = 1.0f, m_use = m_run;
-    if (__any_sync(0xffffffffu, resc)) {
-      if (resc) {
-        m_use = fmaxf(m_run, mt);
-        alpha = ptx::ex2_approx(m_run - m_use);  // 0 when m_run is -inf
-      }
-      const float msub = m_use == -INFINITY ? 0.f : m_use;
-      sum[0] = sum[1] = 0.f;
-      float unused = -INFINITY;
-      half(0, msub, pk0, sum, unused);
-      half(1, msub, pk1, sum, unused);
-      // O_T is stable here: S_T(j) completes after PV_T(j-1).
-      if (j > 0) {
+      for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(u[c]));
+    }
+    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+    const float m_new = fmaxf(m_run, mt);
+    const bool resc = m_new > m_run + 8.0f;
+    const float m_use = resc ? m_new : m_run;
+    const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
+    const float msub = m_use == -INFINITY ? 0.f : m_use;
+    // O_T is stable here: S_T(j) completes after PV_T(j-1).
+    if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          ptx::tmem_load32(tO + lane_addr + c * 32, o);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_load32(tO + lane_addr + c * 32, o);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          ptx::tmem_store32(tO + lane_addr + c * 32, o);
-        }
+        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+        ptx::tmem_store32(tO + lane_addr + c * 32, o);
       }
     }
-    // P over the S columns already read (keys 2c, 2c+1 -> column c); the PV
-    // MMA reads it from TMEM as its A operand.
-    ptx::tmem_store32_async(tS + lane_addr, pk0);
-    ptx::tmem_store32_async(tS + lane_addr + 32, pk1);
-    const float rowsum = sum[0] + sum[1];
-    ptx::tmem_wait_store_keep(pk0, pk1);
+    // Pass 2: P = exp2(s * scale * log2 e - m), packed to bf16 pairs and
+    // stored over the S columns already read (keys 2c, 2c+1 -> column c), where
+    // the PV MMA reads it as its A operand.
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
+        const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
+        sum[(2 * c) & 7] += p0;
+        sum[(2 * c + 1) & 7] += p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      ptx::tmem_store32(tS + lane_addr + h * 32, pk);
+    }
+    const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
     l_run = l_run * alpha + rowsum;
     m_run = m_use;
     ptx::tc_fence_before();

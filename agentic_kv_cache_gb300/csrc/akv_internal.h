@@ -94,6 +94,10 @@ cudaError_t launch_repos_rotate_f32(const void* kpool, const RunDesc* runs, cons
 // dim: d_rot = d_v (GQA, 64 or 128).
 cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st);
 
+// MLA variant: 16 query heads over one latent (d_v 512) + K_pe (64) per token;
+// work items carry the output half (0 or 1) in n_b.
+cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st);
+
 // Shared-memory bytes the attention kernel needs for head dimension dim.
 int segment_attn_smem_bytes(int dim);
 

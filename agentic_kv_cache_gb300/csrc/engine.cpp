@@ -874,20 +874,33 @@ struct akv_ctx {
         }
         return int32_t((lo_r + rpt - 1) / rpt);
       };
-      for (int qt = 0; qt < n_qt; qt += 2) {
-        const int32_t na = tiles_of(qt), nb = tiles_of(qt + 1);
-        for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, na, nb, {0, 0, 0}});
+      if (cfg.layout == AKV_LAYOUT_MLA) {
+        // one query tile per item, one item per half of the 512 output columns (n_b = half)
+        for (int qt = 0; qt < n_qt; ++qt) {
+          const int32_t nt = tiles_of(qt);
+          for (int half = 0; half < 2; ++half) work.push_back(akv::AttnWork{i, 0, qt, nt, half, {0, 0, 0}});
+        }
+      } else {
+        for (int qt = 0; qt < n_qt; qt += 2) {
+          const int32_t na = tiles_of(qt), nb = tiles_of(qt + 1);
+          for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, na, nb, {0, 0, 0}});
+        }
       }
       runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
       tab.push_back(s);
     }
     if (meta) return;
+    const bool mla = cfg.layout == AKV_LAYOUT_MLA;
     // Longest first (LPT); ties in (segment, head, tile) order.
-    std::stable_sort(work.begin(), work.end(), [](const akv::AttnWork& a, const akv::AttnWork& b) {
-      return a.n_a + a.n_b > b.n_a + b.n_b;
+    std::stable_sort(work.begin(), work.end(), [mla](const akv::AttnWork& a, const akv::AttnWork& b) {
+      return mla ? a.n_a > b.n_a : a.n_a + a.n_b > b.n_a + b.n_b;
     });
-    if (cfg.layout != AKV_LAYOUT_GQA || !(cfg.d_rot == 64 || cfg.d_rot == 128))
-      fail(AKV_ERR_ARG, "segment attention supports GQA with head_dim 64 or 128");
+    if (mla) {
+      if (cfg.d_v != 512 || cfg.d_rot != 64)
+        fail(AKV_ERR_ARG, "MLA segment attention supports a 512-wide latent and a 64-wide K_pe");
+    } else if (!(cfg.d_rot == 64 || cfg.d_rot == 128)) {
+      fail(AKV_ERR_ARG, "GQA segment attention supports head_dim 64 or 128");
+    }
 
     const size_t qbytes = size_t(n_q_rows) * cfg.n_q_heads * dqk * 2;
     const size_t obytes = size_t(n_q_rows) * cfg.n_q_heads * cfg.d_v * 2;
@@ -940,7 +953,8 @@ struct akv_ctx {
     p.page = cfg.page_size;
     Timed t;
     begin_timed(kAttn, 0.0, flops, st, t);
-    cuda_check(akv::launch_segment_attn(p, cfg.d_rot, st), "segment_attn launch");
+    cuda_check(mla ? akv::launch_segment_attn_mla(p, st) : akv::launch_segment_attn(p, cfg.d_rot, st),
+               "segment_attn launch");
     end_timed(t, st);
     up.done(st);
     if (st_q.dev && !is_device_ptr(q)) st_q.release(st);

@@ -1,0 +1,406 @@
+// segment_batch_attn, MLA variant ([Leyline] "Method": under MLA the cached
+// key is a position-free latent -- which also serves as the value -- plus a
+// RoPE'd K_pe; 16 query heads share one latent).  What it computes is the
+// same as the GQA kernel ([AKV-notes] section 3 "Segment-Batch Attention";
+// [AKV-blog] section 2 "The Drop Primitive"): per segment, causal softmax
+// attention of its queries over its visible entries, with
+//   score = q_latent . c + q_pe . k_pe   (d_qk = 512 + 64)
+//   out   = sum_j p_j c_j                (d_v = 512).
+//
+// GB300 design.  One CTA = one 128-row query tile (8 tokens x 16 heads) and
+// one half of the 512 output columns: O for all 512 columns would fill TMEM
+// by itself, so each half recomputes S (+53% MMA over the algorithmic count;
+// the two halves run as separate CTAs).  TMEM: S0, S1 (double-buffered, P
+// written back over the consumed S columns as bf16 pairs) and the 256-column O
+// half.  The Q tile (144 KiB) stays in shared memory; keys stream through a
+// 4-slot ring of 16 KiB chunks: per 128-key tile, the 8 latent chunks and the
+// K_pe chunk for QK^T, then the 4 latent chunks of this half for PV.
+// Warp 0: TMA producer; warp 1: TMEM owner and single-thread MMA issuer;
+// warps 2-5: softmax (one row per thread).  Every wait is bounded.
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "akv_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace akv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kKeys = 128;     // keys per KV tile
+constexpr int kRows = 128;     // rows per query tile
+constexpr int kLat = 512;      // latent width
+constexpr int kPe = 64;        // K_pe width
+constexpr int kQChunks = (kLat + kPe) / 64;  // 9 chunks of the QK contraction
+constexpr int kVChunks = 256 / 64;           // 4 chunks of one output half
+constexpr int kRing = 4;
+constexpr uint32_t kChunk = 128 * 128;       // 128 rows x 64 bf16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+constexpr int32_t kErrTimeout = 7;
+
+// shared memory layout (bytes)
+constexpr uint32_t kQ = 0;                          // 9 chunks of Q
+constexpr uint32_t kSlots = kQ + kQChunks * kChunk;  // ring
+constexpr uint32_t kColE = kSlots + kRing * kChunk;  // int32[128]
+constexpr uint32_t kBars = kColE + 128 * 4;
+constexpr uint32_t kBytes = kBars + 256;
+
+enum Bar { kBarQ = 0, kBarFull0, kBarEmpty0 = kBarFull0 + kRing, kBarS0 = kBarEmpty0 + kRing, kBarP = kBarS0 + 2,
+           kBarO, kBarFin, kNumBars };
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+
+__device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
+  if (atomicCAS(&err->code, 0, code) == 0) {
+    err->info[0] = a;
+    err->info[1] = b;
+    err->info[2] = c;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Chunks are loaded in the order the MMA thread consumes them:
+//   QK chunks of tile 0, then for each tile j: QK chunks of tile j+1 (if
+//   any), PV chunks of tile j.
+// Stream position ld goes to ring slot ld % kRing.  chunk_at() maps a stream
+// position to (tile, chunk), chunk < 9: QK (latent 0..7, K_pe 8), 9..12: PV.
+constexpr int kPerTile = kQChunks + kVChunks;
+
+__device__ __forceinline__ void chunk_at(int ld, int n_tiles, int& tile, int& chunk) {
+  if (ld < kQChunks) {
+    tile = 0;
+    chunk = ld;
+    return;
+  }
+  int rest = ld - kQChunks;
+  // blocks of (QK of j+1, PV of j) for j = 0 .. n-2 (13 chunks each), then PV of n-1
+  const int j = rest / kPerTile;
+  if (j < n_tiles - 1) {
+    const int c = rest % kPerTile;
+    if (c < kQChunks) {
+      tile = j + 1;
+      chunk = c;
+    } else {
+      tile = j;
+      chunk = c;
+    }
+  } else {
+    tile = n_tiles - 1;
+    chunk = kQChunks + (rest - (n_tiles - 1) * kPerTile);
+  }
+}
+
+__device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
+                                        volatile int* abort_flag) {
+  const uint32_t bars = sbase + kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
+  const int half = w.n_b;  // which 256 output columns
+  const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
+  ptx::mbar_arrive_expect_tx(bar(kBarQ), kQChunks * kChunk);
+  for (int c = 0; c < kQChunks; ++c)
+    ptx::tma_load_3d(sbase + kQ + c * kChunk, &p.q_map, bar(kBarQ), c * 64, 0, q_tok0);
+  const int layer_base = p.layer * p.n_pages;
+  const AttnRun first = p.runs[seg.run_off];
+  bool ok = true;
+  int issued = 0;
+  for (int ld = 0; ld < w.n_a * kPerTile; ++ld) {
+    int j, c;
+    chunk_at(ld, w.n_a, j, c);
+    const int slot = ld % kRing, use = ld / kRing;
+    if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+      ok = false;
+      break;
+    }
+    // chunk c < 8: latent columns 64c (QK); c == 8: K_pe; c > 8: latent columns of this half (PV)
+    const bool pe = c == kLat / 64;
+    const int col = c < kQChunks ? (pe ? 0 : 64 * c) : 256 * half + 64 * (c - kQChunks);
+    const CUtensorMap* map = pe ? &p.k_map : &p.v_map;
+    const uint32_t dst = sbase + kSlots + slot * kChunk;
+    ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), kChunk);
+    for (int g = 0; g < rpt; ++g) {
+      const int ri = j * rpt + g;
+      const AttnRun run = ri < seg.n_runs ? p.runs[seg.run_off + ri] : first;
+      const int pg = layer_base + (pe ? run.kp : run.vp);
+      ptx::tma_load_4d(dst + g * p.page * 128, map, bar(kBarFull0 + slot), col, 0, 0, pg);
+    }
+    issued = ld + 1;
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 10, 0);
+    *abort_flag = 1;
+  }
+  ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kDrainLimitNs);
+#pragma unroll
+  for (int s = 0; s < kRing; ++s) {
+    const int uses = issued > s ? (issued - s + kRing - 1) / kRing : 0;
+    if (uses) ptx::mbar_wait(bar(kBarFull0 + s), (uses - 1) & 1, abort_flag, kDrainLimitNs);
+  }
+}
+
+// --------------------------------------------------------------------- MMA
+__device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
+                                          volatile int* abort_flag) {
+  const uint32_t bars = sbase + kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kKeys, false);
+  constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, 64, true);
+  const uint32_t tO = tmem + 256;
+  const int n = w.n_a;
+  int ld = 0;
+  bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
+  auto next_chunk = [&]() -> uint32_t {  // wait for the chunk at stream position ld; its slot address
+    const int slot = ld % kRing;
+    ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (ld / kRing) & 1, abort_flag, kWaitLimitNs);
+    ptx::tc_fence_after();
+    return sbase + kSlots + slot * kChunk;
+  };
+  auto release = [&]() {
+    ptx::mma_commit(bar(kBarEmpty0 + ld % kRing));
+    ++ld;
+  };
+  auto qk = [&](int j) {
+    const uint32_t tS = tmem + 128u * (j & 1);
+#pragma unroll 1
+    for (int c = 0; c < kQChunks && ok; ++c) {
+      const uint32_t kt = next_chunk();
+      if (!ok) break;
+      const uint32_t qt = sbase + kQ + c * kChunk;
+#pragma unroll 1
+      for (int ks = 0; ks < 4; ++ks)
+        ptx::mma_bf16(tS, ptx::smem_desc(qt + ks * 32, 16, 1024), ptx::smem_desc(kt + ks * 32, 16, 1024), idesc_qk,
+                      (c > 0 || ks > 0));
+      release();
+    }
+    if (ok) ptx::mma_commit(bar(kBarS0 + (j & 1)));
+  };
+  if (ok && n > 0) qk(0);
+  for (int j = 0; j < n && ok; ++j) {
+    if (j + 1 < n) qk(j + 1);
+    if (!ok) break;
+    if (!(ok = ptx::mbar_wait(bar(kBarP), j & 1, abort_flag, kWaitLimitNs))) break;
+    ptx::tc_fence_after();
+    const uint32_t tP = tmem + 128u * (j & 1);  // P of tile j, packed over S
+#pragma unroll 1
+    for (int i = 0; i < kVChunks && ok; ++i) {
+      const uint32_t vt = next_chunk();
+      if (!ok) break;
+#pragma unroll 1
+      for (int ks = 0; ks < kKeys / 16; ++ks)
+        ptx::mma_bf16_tmem_a(tO + 64u * i, tP + 8u * ks, ptx::smem_desc(vt + ks * 2048, kChunk, 1024), idesc_pv,
+                             (j > 0 || ks > 0));
+      release();
+    }
+    if (ok) ptx::mma_commit(bar(kBarO));
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 11, 0);
+    *abort_flag = 1;
+  }
+  ptx::mma_commit(bar(kBarFin));
+  ptx::mbar_wait(bar(kBarFin), 0, abort_flag, kDrainLimitNs);
+}
+
+// ----------------------------------------------------------------- softmax
+__device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint8_t* smem,
+                                        uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
+  const int n = w.n_a;
+  const uint32_t bars = sbase + kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int quad = (threadIdx.x / 32) & 3;  // warps 2..5 -> TMEM lane quadrants 2, 3, 0, 1
+  const int lane = threadIdx.x % 32;
+  const int r = quad * 32 + lane;
+  const uint32_t lane_addr = uint32_t(quad * 32) << 16;
+  const uint32_t tO = tmem + 256;
+  const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
+  const int t_loc = r / G, g = r % G;
+  const int qi = w.qt0 * tpt + t_loc;
+  const bool row_valid = qi < seg.q_len;
+  const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
+  const float sl2 = p.scale_log2;
+  int* colE = reinterpret_cast<int*>(smem + kColE);
+  int page_shift = 4;
+  while ((1 << page_shift) < p.page) ++page_shift;
+  const int sl_own = r & (p.page - 1);
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const uint32_t tS = tmem + 128u * (j & 1);
+    ok = ptx::mbar_wait(bar(kBarS0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(1, 128, ok)) {
+      ok = false;
+      break;
+    }
+    int e = INT_MAX;  // entry index of key column r (INT_MAX: none)
+    {
+      const int ri = j * rpt + (r >> page_shift);
+      if (ri < seg.n_runs) {
+        const AttnRun ar = p.runs[seg.run_off + ri];
+        const int lo = ar.lohi & 0xffff, hi = ar.lohi >> 16;
+        if (sl_own >= lo && sl_own < hi) e = ar.es + (sl_own - lo);
+      }
+      colE[r] = e;
+    }
+    const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
+    ptx::tc_fence_after();
+    const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
+    const int4* ce4 = reinterpret_cast<const int4*>(colE);
+    auto masked = [&](int h, uint32_t (&u)[64]) {
+      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+    };
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      masked(h, u);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(u[c]));
+    }
+    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+    const float m_new = fmaxf(m_run, mt);
+    const bool resc = m_new > m_run + 8.0f;
+    const float m_use = resc ? m_new : m_run;
+    const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
+    const float msub = m_use == -INFINITY ? 0.f : m_use;
+    if (j > 0) {  // O stable (PV of tile j-1 done) before any rescale
+      ok = ptx::mbar_wait(bar(kBarO), (j - 1) & 1, abort_flag, kWaitLimitNs);
+      if (!ptx::bar_red_and(1, 128, ok)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < 256 / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_load32(tO + lane_addr + c * 32, o);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          ptx::tmem_store32(tO + lane_addr + c * 32, o);
+        }
+      }
+    }
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      masked(h, u);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
+        const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
+        sum[(2 * c) & 3] += p0;
+        sum[(2 * c + 1) & 3] += p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      ptx::tmem_store32(tS + lane_addr + h * 32, pk);  // over S columns already read
+    }
+    l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+    m_run = m_use;
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(bar(kBarP));
+  }
+  if (ok && n > 0) {
+    ok = ptx::mbar_wait(bar(kBarO), (n - 1) & 1, abort_flag, kWaitLimitNs);
+    ok = ptx::bar_red_and(1, 128, ok);
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 12, 0);
+    *abort_flag = 1;
+    return;
+  }
+  ptx::tc_fence_after();
+  const int half = w.n_b;
+  const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+  __nv_bfloat16* orow =
+      static_cast<__nv_bfloat16*>(p.o) + (int64_t(seg.q_row0 + qi) * p.hq + g) * kLat + 256 * half;
+#pragma unroll 1
+  for (int c = 0; c < 256 / 32; ++c) {
+    uint32_t o[32];
+    ptx::tmem_load32(tO + lane_addr + c * 32, o);
+    if (row_valid) {
+#pragma unroll
+      for (int k = 0; k < 32; k += 8) {
+        uint4 v;
+        v.x = pack_bf16(__uint_as_float(o[k + 0]) * inv, __uint_as_float(o[k + 1]) * inv);
+        v.y = pack_bf16(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+        v.z = pack_bf16(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+        v.w = pack_bf16(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+        *reinterpret_cast<uint4*>(orow + c * 32 + k) = v;
+      }
+    }
+  }
+  if (row_valid && p.lse && half == 0) {
+    const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+    p.lse[int64_t(seg.q_row0 + qi) * p.hq + g] = lse;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) segment_attn_mla_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t bars = sbase + kBars;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBars + 8 * kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + 8 * kNumBars + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const AttnWork w = p.work[blockIdx.x];
+  const AttnSeg seg = p.segs[w.seg];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, i == kBarP ? 128 : 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp == 0) {
+    if (lane == 0) produce(p, w, seg, sbase, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) issue_mma(p, w, sbase, tmem, abort_flag);
+  } else {
+    softmax(p, w, seg, smem, sbase, tmem, abort_flag);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st) {
+  if (p.n_work <= 0) return cudaSuccess;
+  const int smem = int(kBytes) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(segment_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  segment_attn_mla_kernel<<<p.n_work, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace akv

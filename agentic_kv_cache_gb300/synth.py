@@ -255,7 +255,9 @@ def mla_dsv2lite(seed=0, n_layers=27, concurrency=1, prompt=17408, span=2016, st
     ops, segs = [], []
     for c in range(concurrency):
         name = f"C{c}"
-        s = int(rng.integers(1024, prompt - 3072 + 1))
+        # the span starts after a kept prefix and leaves a downstream suffix to rotate
+        lo, tail = min(1024, prompt // 4), min(1056, prompt // 4)
+        s = int(rng.integers(lo, prompt - span - tail + 1))
         ops += [("alloc", name), ("append", name, prompt, f"prompt{c}"),
                 ("splice", name, s, s + span, stub, f"stub{c}"),
                 ("append", name, n_new, f"new{c}")]

@@ -93,3 +93,13 @@ def test_partial_pages_everywhere():
     w.ops = ops
     w.segments = [dict(seq="A", kv_end=770, q_len=70, hide=[(300, 333)], q_row0=0)]
     check(w)
+
+
+def test_mla_spliced_sessions():
+    # DeepSeek-V2-Lite MLA shape: 16 heads over one latent (d_qk 512 + 64, d_v 512), page 64,
+    # two ~17K-token sessions each spliced (2,016 -> 32 tokens), 256 new queries per session
+    check(synth.mla_dsv2lite(n_layers=2, concurrency=2), k_rows=48)
+
+
+def test_mla_small_full_compare():
+    check(synth.mla_dsv2lite(n_layers=1, concurrency=1, prompt=3000, span=700, stub=20, n_new=100))

@@ -69,11 +69,14 @@ def test_llama70b_128k_full_size_sampled():
     release(c)
 
 
-def test_mla_16_sessions_full_size_repos_sampled():
+def test_mla_16_sessions_full_size_sampled():
     from gpu_sampled import SampledCase
     w = synth.mla_dsv2lite(concurrency=16)
     c = SampledCase(w)
     c.run()
-    n_rot, worst = c.check_repos(4096, np.random.default_rng(13))
+    rng = np.random.default_rng(13)
+    n_rot, worst = c.check_repos(4096, rng)
     assert n_rot > 1000
+    for layer in (0, w.shape.n_layers - 1):
+        c.check_attention(layer, 16, rng, segments=[0, 7, 15])
     release(c)

@@ -146,6 +146,50 @@ class Turn:
         return b(self.new_k) + b(self.new_v) + b(self.q), b(self.o)
 
 
+def repos_sweep(steps, warmup=2, n_layers=80):
+    """repos_rotate on the Llama-3.1-70B-shaped 128K cache: 80 layers, 64 spans with shifts in
+    +-64K, flushed in place (42.95 GB of algorithmic traffic per flush; the launch large enough for
+    HBM to be the bound).  Steps alternate the sign of every shift so the work repeats exactly."""
+    import torch
+    from agentic_kv_cache_gb300 import akv, runner, synth
+    w = synth.llama70b_128k(n_branches=0, n_layers=n_layers)
+    cfg = akv.config_from_shape(w.shape, w.n_pages)
+    pools = akv.make_pools(cfg)
+    eng = akv.Engine(cfg, pools)
+    st = torch.cuda.current_stream()
+    names = runner.run_ops(eng, w, kv_source=runner.torch_device_kv_source(w),
+                           ops=[op for op in w.ops if op[0] in ("alloc", "append")], stream=st)
+    spans = [op for op in w.ops if op[0] == "repos"]
+    torch.cuda.synchronize()
+
+    def sweep(sign):
+        for op in spans:
+            eng.repos(names[op[1]], op[2], op[3], sign * op[4])
+        eng.flush(names["M"], stream=st)
+
+    for i in range(warmup):
+        sweep(1 if i % 2 == 0 else -1)
+    torch.cuda.synchronize()
+    eng.profile_enable(True)
+    for i in range(steps):
+        sweep(1 if (warmup + i) % 2 == 0 else -1)
+    stats = eng.profile_read()["repos_rotate"]
+    eng.profile_enable(False)
+    assert eng.check_device_error(st) == 0
+    hbm = load_peaks()[0]
+    ms = stats["ms"] / stats["launches"]
+    gbs = stats["bytes"] / stats["launches"] / (ms * 1e-3) / 1e9
+    tokens = stats["bytes"] / stats["launches"] / (2 * 8 * 128 * 2)
+    del eng, pools
+    torch.cuda.empty_cache()
+    return {"workload": f"llama70b_128k full-cache sweep: {n_layers} layers x 131,072 tokens x 8 kv heads x d 128, "
+                        "64 spans, shifts in +-64K, in place", "launches": stats["launches"],
+            "ms_per_launch": ms, "bytes_per_launch": stats["bytes"] / stats["launches"], "GB/s": gbs,
+            "frac_of_hbm": gbs / hbm, "frac_of_8TBs": gbs / 8000.0,
+            "rotated_token_layers_per_s": tokens / (ms * 1e-3),
+            "rotated_tokens_per_s": tokens / n_layers / (ms * 1e-3)}
+
+
 def gpu_arm(args, rank, world):
     import torch
     dev = int(os.environ.get("LOCAL_RANK", 0))
@@ -243,6 +287,8 @@ def gpu_arm(args, rank, world):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_total / args.steps},
     }
+    if not args.no_sweep:
+        line["repos_rotate_sweep"] = repos_sweep(steps=4, n_layers=args.sweep_layers)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return line
@@ -363,11 +409,21 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the large repos_rotate sweep measurement")
+    ap.add_argument("--only-sweep", action="store_true", help="run only the repos_rotate sweep (for profiling)")
+    ap.add_argument("--sweep-layers", type=int, default=80)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))
+    if args.only_sweep:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        from agentic_kv_cache_gb300 import build
+        build.build()
+        print(json.dumps(repos_sweep(args.steps, args.warmup, args.sweep_layers)), flush=True)
+        return
     if args.impl == "reference":
         line = reference_arm(args, rank, world)
     else:

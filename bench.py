@@ -45,6 +45,23 @@ def load_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel's source
+    has changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
+            return None
+    return rec
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples during the timed region."""
 
@@ -182,7 +199,12 @@ def repos_sweep(steps, warmup=2, n_layers=80):
     tokens = stats["bytes"] / stats["launches"] / (2 * 8 * 128 * 2)
     del eng, pools
     torch.cuda.empty_cache()
-    return {"workload": f"llama70b_128k full-cache sweep: {n_layers} layers x 131,072 tokens x 8 kv heads x d 128, "
+    tr = measured_traffic("repos_rotate")
+    traffic = None
+    if tr:  # the capture's bytes scaled to this launch by the rotated token-layers (traffic grows in proportion)
+        traffic = tr["dram_bytes_per_launch"] * (131072 * n_layers) / tr["units_per_launch"]
+    return {"traffic_per_launch": traffic,
+            "workload": f"llama70b_128k full-cache sweep: {n_layers} layers x 131,072 tokens x 8 kv heads x d 128, "
                         "64 spans, shifts in +-64K, in place", "launches": stats["launches"],
             "ms_per_launch": ms, "bytes_per_launch": stats["bytes"] / stats["launches"], "GB/s": gbs,
             "frac_of_hbm": gbs / hbm, "frac_of_8TBs": gbs / 8000.0,
@@ -260,10 +282,13 @@ def gpu_arm(args, rank, world):
     value = world * args.steps / (total_ms * 1e-3)
     e2e_value = world * args.steps / (e2e_total * 1e-3)
     if dominant == "segment_attn":
+        tr = measured_traffic("segment_attn")
         roof = {"kernel": "segment_attn", "bound": "tensor", "achieved": att_tf, "peak": bf16_peak,
-                "unit": "TFLOP/s", "frac": att_tf / bf16_peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": att_tf / bf16_peak,
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
                 "peak_kind": f"{peak_kind} bf16 dense burst (sustained {bf16_sus})"}
     else:
+        tr = measured_traffic("repos_rotate")
         roof = {"kernel": "repos_rotate", "bound": "hbm", "achieved": rep_gbs, "peak": hbm, "unit": "GB/s",
                 "frac": rep_gbs / hbm, "traffic": None, "peak_kind": f"{peak_kind} HBM copy"}
     line = {

@@ -84,6 +84,7 @@ def load(path=LIB_PATH):
         "akv_segment_runs": [P, ctypes.POINTER(Segment), P, I64, pi64, pi64],
         "akv_check_device_error": [P, P, pi32],
         "akv_profile_enable": [P, I32],
+        "akv_set_attention_split": [P, I32],
         "akv_profile_read": [P, ctypes.POINTER(KernelStats)],
     }
     for name, args in sig.items():
@@ -263,6 +264,10 @@ class Engine:
         if st not in (OK, ERR_DEVICE_TIMEOUT, ERR_DEVICE):
             self._check(st)
         return code.value
+
+    def set_attention_split(self, split):
+        """0: automatic split-KV; n >= 1: exactly n KV chunks per work item (1 = never split)."""
+        self._check(self.lib.akv_set_attention_split(self.h, int(split)))
 
     def profile_enable(self, on=True):
         self._check(self.lib.akv_profile_enable(self.h, int(on)))

@@ -45,15 +45,32 @@ struct AttnSeg {
 };
 
 // One CTA's work: two consecutive 128-row query tiles (A = qt0, B = qt0 + 1)
-// of segment seg for kv head kvh.  n_a / n_b: KV tiles each reads (up to the
-// causal limit of its last row); n_b = 0 when the segment has no tile B.
+// of segment seg for kv head kvh (GQA), or one query tile qt0 and output half
+// n_b (MLA).  n_a / n_b: KV tiles each query tile reads in all (up to the causal
+// limit of its last row); n_b = 0 when the segment has no tile B.  The CTA
+// reads KV tiles [t0, t1) of those.  part < 0: it owns the whole range and
+// writes the final output; part >= 0: it writes unnormalised partial results
+// to partial slot `part`; the part that finishes last merges them all.
 struct AttnWork {
   int32_t seg;
   int32_t kvh;
   int32_t qt0;
   int32_t n_a;
   int32_t n_b;
-  int32_t pad[3];
+  int32_t t0;
+  int32_t t1;
+  int32_t part;  // partial slot of this split part, -1 when the item is not split
+  int32_t comb;  // its CombineItem
+};
+
+// One split work item: its parts own partial slots [part0, part0 + n_parts);
+// count[t] is the ticket counter of query tile t, zero at launch (the host
+// uploads it with the work list), taken by each part once its partial is
+// written; the part that draws the last ticket merges.
+struct CombineItem {
+  int32_t part0;
+  int32_t n_parts;
+  int32_t count[2];
 };
 
 struct AttnParams {
@@ -65,6 +82,9 @@ struct AttnParams {
   const AttnWork* work;
   void* o;            // bf16 [n_q_rows][Hq][d_v]
   float* lse;         // float [n_q_rows][Hq] or null
+  float* partial;     // split-KV scratch: per part [tile][width + 2][128 rows] floats (O columns, m, l)
+  CombineItem* comb;  // split items (ticket counters), null when nothing is split
+  int32_t comb_tiles; // query tiles per partial slot (2 for GQA pairs, 1 under MLA)
   DevErr* err;
   float scale_log2;   // softmax scale * log2(e)
   int32_t n_work;
@@ -74,7 +94,12 @@ struct AttnParams {
   int32_t hq;
   int32_t group;      // query heads per kv head
   int32_t page;
+  int32_t width;      // output columns one CTA writes (d_v, or d_v / 2 under MLA)
+  int32_t dv;         // output row width (d_v)
 };
+
+// Floats of one partial slot: tiles x 128 rows x (width + 2).
+__host__ __device__ inline int64_t partial_floats(int tiles, int width) { return int64_t(tiles) * 128 * (width + 2); }
 
 // Launchers; each returns the launch's cudaError_t.
 cudaError_t launch_kv_write(const void* src, void* pool, const int32_t* rows, int64_t n, int n_layers,
@@ -98,6 +123,8 @@ cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st);
 // work items carry the output half (0 or 1) in n_b.
 cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st);
 
+// Merge split-KV partials: items [n_items], tiles_per_item query tiles of 128
+// rows each, `width` output columns per part.
 // Shared-memory bytes the attention kernel needs for head dimension dim.
 int segment_attn_smem_bytes(int dim);
 

@@ -280,6 +280,9 @@ struct akv_ctx {
   akv::DevErr* dev_err = nullptr;
   Uploader up;
   Staging st_k, st_v, st_q, st_o, st_lse;
+  Staging partial;         // split-KV partial results (device only)
+  int n_sm = 148;          // SMs of the device, for split decisions
+  int split_override = 0;  // 0: choose the split factor; n >= 1: use n
   CUtensorMap k_map{}, v_map{};
   bool maps_ok = false;
 
@@ -878,12 +881,13 @@ struct akv_ctx {
         // one query tile per item, one item per half of the 512 output columns (n_b = half)
         for (int qt = 0; qt < n_qt; ++qt) {
           const int32_t nt = tiles_of(qt);
-          for (int half = 0; half < 2; ++half) work.push_back(akv::AttnWork{i, 0, qt, nt, half, {0, 0, 0}});
+          for (int half = 0; half < 2; ++half) work.push_back(akv::AttnWork{i, 0, qt, nt, half, 0, nt, -1, -1});
         }
       } else {
         for (int qt = 0; qt < n_qt; qt += 2) {
           const int32_t na = tiles_of(qt), nb = tiles_of(qt + 1);
-          for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, na, nb, {0, 0, 0}});
+          for (int h = 0; h < cfg.n_kv_heads; ++h)
+            work.push_back(akv::AttnWork{i, h, qt, na, nb, 0, std::max(na, nb), -1, -1});
         }
       }
       runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
@@ -891,10 +895,59 @@ struct akv_ctx {
     }
     if (meta) return;
     const bool mla = cfg.layout == AKV_LAYOUT_MLA;
-    // Longest first (LPT); ties in (segment, head, tile) order.
-    std::stable_sort(work.begin(), work.end(), [mla](const akv::AttnWork& a, const akv::AttnWork& b) {
-      return mla ? a.n_a > b.n_a : a.n_a + a.n_b > b.n_a + b.n_b;
-    });
+    // Split-KV: cut every item's KV-tile range into up to S chunks so the
+    // launch fills whole waves of SMs; split chunks write partials, and the
+    // chunk that finishes last merges them.
+    std::vector<akv::CombineItem> comb;
+    int32_t n_parts = 0;
+    {
+      auto span_of = [mla](const akv::AttnWork& w) { return mla ? w.n_a : std::max(w.n_a, w.n_b); };
+      auto units_for = [&](int S) {
+        int64_t u = 0;
+        for (auto& w : work) u += std::min<int64_t>(S, std::max(1, span_of(w)));
+        return u;
+      };
+      int best_s = 1;
+      double best = -1.0;
+      const int cands[] = {1, 2, 3, 4, 6, 8};
+      for (int S : cands) {
+        if (split_override > 0 && S != split_override) continue;
+        const int64_t u = units_for(S);
+        const int64_t waves = (u + n_sm - 1) / n_sm;
+        const double eff = double(u) / double(waves * n_sm) * (S == 1 ? 1.0 : 0.97);
+        if (eff > best + 1e-9) {
+          best = eff;
+          best_s = S;
+        }
+      }
+      if (split_override > 0) best_s = std::min(split_override, 8);
+      std::vector<akv::AttnWork> units;
+      for (auto& w : work) {
+        const int span = span_of(w);
+        const int chunks = std::min(best_s, std::max(1, span));
+        if (chunks == 1) {
+          units.push_back(w);
+          continue;
+        }
+        comb.push_back(akv::CombineItem{n_parts, chunks, {0, 0}});
+        for (int c = 0; c < chunks; ++c) {
+          akv::AttnWork u = w;
+          u.t0 = int32_t(int64_t(span) * c / chunks);
+          u.t1 = int32_t(int64_t(span) * (c + 1) / chunks);
+          u.part = n_parts++;
+          u.comb = int32_t(comb.size()) - 1;
+          units.push_back(u);
+        }
+      }
+      work.swap(units);
+    }
+    // Longest first (LPT); ties in (segment, head, tile, chunk) order.
+    auto cost = [mla](const akv::AttnWork& w) {
+      auto in = [&](int n) { return std::max(0, std::min(n, w.t1) - w.t0); };
+      return mla ? in(w.n_a) : in(w.n_a) + in(w.n_b);
+    };
+    std::stable_sort(work.begin(), work.end(),
+                     [&](const akv::AttnWork& a, const akv::AttnWork& b) { return cost(a) > cost(b); });
     if (mla) {
       if (cfg.d_v != 512 || cfg.d_rot != 64)
         fail(AKV_ERR_ARG, "MLA segment attention supports a 512-wide latent and a 64-wide K_pe");
@@ -933,9 +986,11 @@ struct akv_ctx {
     void* druns = nullptr;
     void* dsegs = nullptr;
     void* dwork = nullptr;
+    void* dcomb = nullptr;
     up.upload({{runs.data(), runs.size() * sizeof(akv::AttnRun), &druns},
                {tab.data(), tab.size() * sizeof(akv::AttnSeg), &dsegs},
-               {work.data(), work.size() * sizeof(akv::AttnWork), &dwork}},
+               {work.data(), work.size() * sizeof(akv::AttnWork), &dwork},
+               {comb.data(), comb.size() * sizeof(akv::CombineItem), &dcomb}},
               st);
     p.runs = static_cast<akv::AttnRun*>(druns);
     p.segs = static_cast<akv::AttnSeg*>(dsegs);
@@ -951,12 +1006,24 @@ struct akv_ctx {
     p.hq = cfg.n_q_heads;
     p.group = G;
     p.page = cfg.page_size;
+    p.width = mla ? cfg.d_v / 2 : cfg.d_v;
+    p.dv = cfg.d_v;
+    const int tiles_per_item = mla ? 1 : 2;
+    p.comb = static_cast<akv::CombineItem*>(dcomb);
+    p.comb_tiles = tiles_per_item;
+    if (n_parts > 0) {
+      const size_t need = size_t(n_parts) * size_t(akv::partial_floats(tiles_per_item, p.width)) * 4;
+      partial.want_host = false;
+      partial.acquire(need);
+      p.partial = static_cast<float*>(partial.dev);
+    }
     Timed t;
-    begin_timed(kAttn, 0.0, flops, st, t);
+    begin_timed(kAttn, 0.0, flops, st, t, 1);
     cuda_check(mla ? akv::launch_segment_attn_mla(p, st) : akv::launch_segment_attn(p, cfg.d_rot, st),
                "segment_attn launch");
     end_timed(t, st);
     up.done(st);
+    if (n_parts > 0) partial.release(st);
     if (st_q.dev && !is_device_ptr(q)) st_q.release(st);
     if (o_host) {
       cuda_check(cudaMemcpyAsync(o, od, obytes, cudaMemcpyDeviceToHost, st), "O copy to host");
@@ -1003,6 +1070,7 @@ struct akv_ctx {
     kpool = pools->k_pool;
     vpool = pools->v_pool;
     cuda_check(cudaGetDevice(&device), "cudaGetDevice");
+    cuda_check(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, device), "cudaDeviceGetAttribute");
     cuda_check(cudaMalloc(&dev_err, sizeof(akv::DevErr)), "cudaMalloc");
     cuda_check(cudaMemset(dev_err, 0, sizeof(akv::DevErr)), "cudaMemset");
     if (c.d_rot % 64 == 0 && c.d_v % 64 == 0) {
@@ -1029,6 +1097,7 @@ struct akv_ctx {
     st_q.destroy();
     st_o.destroy();
     st_lse.destroy();
+    partial.destroy();
     for (auto& t : timed) {
       cudaEventDestroy(t.a);
       cudaEventDestroy(t.b);
@@ -1224,6 +1293,13 @@ akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code) {
     inner = akv_status(c);
   });
   return s != AKV_OK ? s : inner;
+}
+
+akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split) {
+  return guard(ctx, [&] {
+    if (split < 0 || split > 8) fail(AKV_ERR_ARG, "split must be 0 (automatic) or 1..8");
+    ctx->split_override = split;
+  });
 }
 
 akv_status akv_profile_enable(akv_ctx* ctx, int32_t on) {

@@ -38,6 +38,7 @@
 #include <cstdint>
 
 #include "akv_internal.h"
+#include "attn_merge.cuh"
 #include "sm100_ptx.cuh"
 
 namespace akv {
@@ -98,7 +99,9 @@ __device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& s
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kTileKeys / p.page;
-  const int n_max = max(w.n_a, w.n_b);
+  // KV tiles [t0, t1) of this work item; local tile j is global tile t0 + j
+  const int span = w.t1 - w.t0;
+  const int n_max = max(min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span));
   const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
   ptx::mbar_arrive_expect_tx(bar(kBarQ), (w.n_b > 0 ? 2 : 1) * L::kTile);
   for (int t = 0; t < (w.n_b > 0 ? 2 : 1); ++t)
@@ -119,7 +122,7 @@ __device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& s
     const CUtensorMap* map = is_v ? &p.v_map : &p.k_map;
     ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), L::kTile);
     for (int g = 0; g < rpt; ++g) {
-      const int ri = j * rpt + g;
+      const int ri = (w.t0 + j) * rpt + g;
       const AttnRun run = ri < seg.n_runs ? p.runs[seg.run_off + ri] : first;
       const int pg = layer_base + (is_v ? run.vp : run.kp);
       for (int kb = 0; kb < L::kBlocks; ++kb)
@@ -150,8 +153,9 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kTileKeys, false);
   constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, D, true);
-  const int n_t[2] = {w.n_a, w.n_b};
-  const int n_max = max(w.n_a, w.n_b);
+  const int span = w.t1 - w.t0;  // local tile counts of this KV range
+  const int n_t[2] = {min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span)};
+  const int n_max = max(n_t[0], n_t[1]);
   auto slot_of = [](int ld) { return ld % kSlots; };
   auto full_parity = [](int ld) { return (ld / kSlots) & 1; };
   bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
@@ -202,14 +206,36 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
   ptx::mbar_wait(bar(kBarFin), 0, abort_flag, kDrainLimitNs);
 }
 
+// Split part of query tile t, row r: if this CTA drew the item's last ticket,
+// merge every part's partial into row r's output.
+template <int D>
+__device__ __forceinline__ void merge_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, int r) {
+  const int G = p.group, tpt = kRows / G;
+  const int qi = (w.qt0 + t) * tpt + r / G, g = r % G;
+  const bool valid = qi < seg.q_len;
+  const int64_t row = int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g;
+  merge_if_last<D>(p, w, t, r, 1 + t, valid ? static_cast<__nv_bfloat16*>(p.o) + row * D : nullptr,
+                   valid && p.lse ? p.lse + row : nullptr);
+}
+
 // ----------------------------------------------------------------- softmax
 // One warpgroup per query tile t; thread = row r = TMEM lane r.
 template <int D>
 __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint8_t* smem,
                              uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
   using L = Layout<D>;
-  const int n_t = t == 0 ? w.n_a : w.n_b;
-  if (n_t == 0) return;
+  const int n_glob = t == 0 ? w.n_a : w.n_b;
+  const int n_t = min(max(n_glob - w.t0, 0), w.t1 - w.t0);  // local tiles of this KV range
+  if (n_t == 0) {
+    // A split part in which this query tile sees no key: record an empty partial (l = 0).
+    if (n_glob > 0 && w.part >= 0) {
+      const int r0 = ((threadIdx.x / 32) & 3) * 32 + threadIdx.x % 32;
+      p.partial[w.part * partial_floats(2, D) + (int64_t(t) * (D + 2) + D + 1) * 128 + r0] = 0.f;
+      p.partial[w.part * partial_floats(2, D) + (int64_t(t) * (D + 2) + D) * 128 + r0] = -INFINITY;
+      merge_tile<D>(p, w, seg, t, r0);
+    }
+    return;
+  }
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int wg_warp = (threadIdx.x / 32 - 2) % 4;
@@ -232,8 +258,13 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
   const int sl_own = r & (p.page - 1);
-  bool run_ok = (r >> page_shift) < seg.n_runs;
-  AttnRun run_cur = run_ok ? p.runs[seg.run_off + (r >> page_shift)] : AttnRun{0, 0, 0, 0};
+  bool run_ok;
+  AttnRun run_cur = AttnRun{0, 0, 0, 0};
+  {
+    const int ri0 = w.t0 * rpt + (r >> page_shift);
+    run_ok = ri0 < seg.n_runs;
+    if (run_ok) run_cur = p.runs[seg.run_off + ri0];
+  }
   for (int j = 0; j < n_t; ++j) {
     ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
     if (!ptx::bar_red_and(bar_id, 128, ok)) {
@@ -248,7 +279,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       const int lo = run_cur.lohi & 0xffff, hi = run_cur.lohi >> 16;
       if (run_ok && sl_own >= lo && sl_own < hi) e = run_cur.es + (sl_own - lo);
       colE[r] = e;
-      const int ri = (j + 1) * rpt + (r >> page_shift);
+      const int ri = (w.t0 + j + 1) * rpt + (r >> page_shift);
       run_ok = ri < seg.n_runs;
       if (run_ok) run_cur = p.runs[seg.run_off + ri];
     }
@@ -341,6 +372,22 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     return;
   }
   ptx::tc_fence_after();
+  if (w.part >= 0) {
+    // Split part: unnormalised O, running max and sum for the combine kernel,
+    // column-major per tile so a warp writes consecutive rows.
+    float* base = p.partial + w.part * partial_floats(2, D) + int64_t(t) * (D + 2) * 128 + r;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      ptx::tmem_load32(tO + lane_addr + c * 32, o);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) base[int64_t(c * 32 + k) * 128] = __uint_as_float(o[k]);
+    }
+    base[int64_t(D) * 128] = m_run;
+    base[int64_t(D + 1) * 128] = l_run;
+    merge_tile<D>(p, w, seg, t, r);
+    return;
+  }
   const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
   __nv_bfloat16* orow =
       static_cast<__nv_bfloat16*>(p.o) + (int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g) * D;

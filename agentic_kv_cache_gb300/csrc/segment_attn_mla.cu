@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "akv_internal.h"
+#include "attn_merge.cuh"
 #include "sm100_ptx.cuh"
 
 namespace akv {
@@ -111,9 +112,10 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
   const AttnRun first = p.runs[seg.run_off];
   bool ok = true;
   int issued = 0;
-  for (int ld = 0; ld < w.n_a * kPerTile; ++ld) {
+  const int n_loc = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
+  for (int ld = 0; ld < n_loc * kPerTile; ++ld) {
     int j, c;
-    chunk_at(ld, w.n_a, j, c);
+    chunk_at(ld, n_loc, j, c);
     const int slot = ld % kRing, use = ld / kRing;
     if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
       ok = false;
@@ -126,7 +128,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
     const uint32_t dst = sbase + kSlots + slot * kChunk;
     ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), kChunk);
     for (int g = 0; g < rpt; ++g) {
-      const int ri = j * rpt + g;
+      const int ri = (w.t0 + j) * rpt + g;
       const AttnRun run = ri < seg.n_runs ? p.runs[seg.run_off + ri] : first;
       const int pg = layer_base + (pe ? run.kp : run.vp);
       ptx::tma_load_4d(dst + g * p.page * 128, map, bar(kBarFull0 + slot), col, 0, 0, pg);
@@ -153,7 +155,7 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kKeys, false);
   constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, 64, true);
   const uint32_t tO = tmem + 256;
-  const int n = w.n_a;
+  const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);
   int ld = 0;
   bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
   auto next_chunk = [&]() -> uint32_t {  // wait for the chunk at stream position ld; its slot address
@@ -211,7 +213,7 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
 // ----------------------------------------------------------------- softmax
 __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint8_t* smem,
                                         uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
-  const int n = w.n_a;
+  const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int quad = (threadIdx.x / 32) & 3;  // warps 2..5 -> TMEM lane quadrants 2, 3, 0, 1
@@ -240,7 +242,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     }
     int e = INT_MAX;  // entry index of key column r (INT_MAX: none)
     {
-      const int ri = j * rpt + (r >> page_shift);
+      const int ri = (w.t0 + j) * rpt + (r >> page_shift);
       if (ri < seg.n_runs) {
         const AttnRun ar = p.runs[seg.run_off + ri];
         const int lo = ar.lohi & 0xffff, hi = ar.lohi >> 16;
@@ -329,6 +331,24 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
   }
   ptx::tc_fence_after();
   const int half = w.n_b;
+  if (w.part >= 0) {
+    // Split part: unnormalised O half, running max and sum, [column][row] layout.
+    float* base = p.partial + w.part * partial_floats(1, 256) + r;
+#pragma unroll 1
+    for (int c = 0; c < 256 / 32; ++c) {
+      uint32_t o[32];
+      ptx::tmem_load32(tO + lane_addr + c * 32, o);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) base[int64_t(c * 32 + k) * 128] = __uint_as_float(o[k]);
+    }
+    base[int64_t(256) * 128] = n > 0 ? m_run : -INFINITY;
+    base[int64_t(257) * 128] = n > 0 ? l_run : 0.f;
+    const int64_t row = int64_t(seg.q_row0 + qi) * p.hq + g;
+    merge_if_last<256>(p, w, 0, r, 1,
+                       row_valid ? static_cast<__nv_bfloat16*>(p.o) + row * kLat + 256 * half : nullptr,
+                       row_valid && p.lse && half == 0 ? p.lse + row : nullptr);
+    return;
+  }
   const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
   __nv_bfloat16* orow =
       static_cast<__nv_bfloat16*>(p.o) + (int64_t(seg.q_row0 + qi) * p.hq + g) * kLat + 256 * half;

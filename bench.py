@@ -116,7 +116,7 @@ class ClockSampler:
 class Turn:
     """The engine, the resident 32K-token trajectory and the per-step inputs."""
 
-    def __init__(self, seed=0, host_inputs=False):
+    def __init__(self, seed=0, host_inputs=False, attn_split=0):
         import torch
         from agentic_kv_cache_gb300 import akv, build, runner, synth
         build.build()
@@ -126,6 +126,7 @@ class Turn:
         self.cfg = akv.config_from_shape(s, w.n_pages)
         self.pools = akv.make_pools(self.cfg)
         self.eng = akv.Engine(self.cfg, self.pools)
+        self.eng.set_attention_split(attn_split)
         self.stream = torch.cuda.current_stream()
         fork_at = next(i for i, op in enumerate(w.ops) if op[0] == "fork")
         self.setup_ops, self.step_ops = w.ops[:fork_at], w.ops[fork_at:]
@@ -216,7 +217,7 @@ def gpu_arm(args, rank, world):
     import torch
     dev = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(dev)
-    t = Turn(seed=rank, host_inputs=True)
+    t = Turn(seed=rank, host_inputs=True, attn_split=args.attn_split)
     dist = world > 1
     if dist:
         import torch.distributed as tdist
@@ -296,7 +297,8 @@ def gpu_arm(args, rank, world):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "l2": "flushed between steps (512 MiB write)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "attn_split": args.attn_split or "auto"},
         "repos_rotate": {"rotated_tokens_per_s": rot_tokens / (rep_ms * 1e-3), "rotated_tokens_per_launch": rot_tokens,
                          "GB/s": rep_gbs, "frac_of_hbm": rep_gbs / hbm, "frac_of_8TBs": rep_gbs / 8000.0,
                          "ms_per_launch": rep_ms},
@@ -438,6 +440,8 @@ def main():
     ap.add_argument("--only-sweep", action="store_true", help="run only the repos_rotate sweep (for profiling)")
     ap.add_argument("--sweep-layers", type=int, default=80)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--attn-split", type=int, default=0,
+                    help="KV chunks per attention work item: 0 chooses automatically, 1 never splits")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))

@@ -275,6 +275,12 @@ AKV_API akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_
  * is cleared after reading.  Returns the same status as *code. */
 AKV_API akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code);
 
+/* Split-KV control for akv_attend.  0 (default): the engine cuts long work
+ * items into up to 8 chunks of KV tiles when that fills the GPU's waves of
+ * SMs better, and merges the chunks' partial softmax results in a combine
+ * kernel.  1..8: use exactly that many chunks per item (1 = never split). */
+AKV_API akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split);
+
 /* Enable (1) or disable (0) per-launch CUDA-event timing of the context's
  * kernels; enabling clears the statistics. */
 AKV_API akv_status akv_profile_enable(akv_ctx* ctx, int32_t on);

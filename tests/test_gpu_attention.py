@@ -26,11 +26,12 @@ def sample_rows(q_len, k, rng, tpt):
     return np.array(sorted(r for r in rows if 0 <= r < q_len))
 
 
-def check(w, k_rows=None, seed=0):
+def check(w, k_rows=None, seed=0, split=0):
     from gpu_case import Case
     c = Case(w)
     c.run_ops()
     c.flush_segments()
+    c.eng.set_attention_split(split)
     q32, o, lse = c.attend_gpu()
     rng = np.random.default_rng(seed)
     G = w.shape.n_q_heads // w.shape.n_kv_heads
@@ -103,3 +104,34 @@ def test_mla_spliced_sessions():
 
 def test_mla_small_full_compare():
     check(synth.mla_dsv2lite(n_layers=1, concurrency=1, prompt=3000, span=700, stub=20, n_new=100))
+
+
+# Split-KV: an item's KV tiles cut into S parts whose partial (O, m, l) the
+# combine kernel merges.  Forced factors cover parts that see no key of the
+# shorter query tile (GQA), ragged part boundaries, and both MLA halves.
+@pytest.mark.parametrize("split", [1, 2, 3, 8])
+def test_split_kv_gqa_full_compare(split):
+    check(synth.llama8b_32k(total=4096, n_new=300), split=split)
+
+
+@pytest.mark.parametrize("split", [2, 5])
+def test_split_kv_partial_pages(split):
+    w = synth.tiny()
+    ops = [("alloc", "A"), ("append", "A", 900, "ctx")]
+    for a in range(5, 800, 41):
+        ops.append(("drop", "A", a, a + 13))
+    ops.append(("append", "A", 200, "new"))
+    w.ops = ops
+    w.n_pages = 128
+    w.segments = [dict(seq="A", kv_end=1100, q_len=200, hide=[(300, 333)], q_row0=0)]
+    check(w, split=split)
+
+
+@pytest.mark.parametrize("split", [3, 8])
+def test_split_kv_mla_full_compare(split):
+    check(synth.mla_dsv2lite(n_layers=1, concurrency=1, prompt=3000, span=700, stub=20, n_new=100), split=split)
+
+
+def test_split_kv_many_segments_group_8():
+    w = synth.llama70b_128k(n_layers=1, total=16384, n_branches=4, q_per_branch=200)
+    check(w, k_rows=40, split=4)

@@ -77,6 +77,8 @@ struct AttnParams {
   CUtensorMap q_map;  // Q [n_q_rows][Hq][d_qk], box {64, G, 128/G}
   CUtensorMap k_map;  // rotated pool, [L*P][H][page][d_rot], box {64, page, 1, 1}
   CUtensorMap v_map;  // value pool,  [L*P][H][page][d_v],   box {64, page, 1, 1}
+  CUtensorMap k_tile_map;  // as k_map, box {64, page, 1, 128 / page}: a tile's consecutive pages at once
+  CUtensorMap v_tile_map;  // as v_map, box {64, page, 1, 128 / page}
   const AttnRun* runs;
   const AttnSeg* segs;
   const AttnWork* work;

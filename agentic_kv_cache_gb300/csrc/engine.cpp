@@ -283,7 +283,7 @@ struct akv_ctx {
   Staging partial;         // split-KV partial results (device only)
   int n_sm = 148;          // SMs of the device, for split decisions
   int split_override = 0;  // 0: choose the split factor; n >= 1: use n
-  CUtensorMap k_map{}, v_map{};
+  CUtensorMap k_map{}, v_map{}, k_tile_map{}, v_tile_map{};
   bool maps_ok = false;
 
   // profiling
@@ -914,7 +914,10 @@ struct akv_ctx {
         if (split_override > 0 && S != split_override) continue;
         const int64_t u = units_for(S);
         const int64_t waves = (u + n_sm - 1) / n_sm;
-        const double eff = double(u) / double(waves * n_sm) * (S == 1 ? 1.0 : 0.97);
+        // A split part pays its partial write, a share of the merge and a
+        // slower pipeline start (measured at about 15% on 32K-context items),
+        // so splitting must buy more wave occupancy than that.
+        const double eff = double(u) / double(waves * n_sm) * (S == 1 ? 1.0 : 0.85);
         if (eff > best + 1e-9) {
           best = eff;
           best_s = S;
@@ -983,6 +986,8 @@ struct akv_ctx {
     }
     p.k_map = k_map;
     p.v_map = v_map;
+    p.k_tile_map = k_tile_map;
+    p.v_tile_map = v_tile_map;
     void* druns = nullptr;
     void* dsegs = nullptr;
     void* dwork = nullptr;
@@ -1084,6 +1089,9 @@ struct akv_ctx {
       const uint64_t vs[3] = {uint64_t(c.d_v) * 2, uint64_t(c.page_size) * c.d_v * 2,
                               uint64_t(c.n_kv_heads) * c.page_size * c.d_v * 2};
       encode_map(&v_map, vpool, 4, vd, vs, box);
+      const uint32_t tbox[4] = {64, uint32_t(c.page_size), 1, uint32_t(128 / c.page_size)};
+      encode_map(&k_tile_map, kpool, 4, kd, ks, tbox);
+      encode_map(&v_tile_map, vpool, 4, vd, vs, tbox);
       maps_ok = true;
     }
   }

@@ -53,6 +53,7 @@ constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;  // AKV_ERR_DEVICE_TIMEOUT
 constexpr int32_t kErrDevice = 8;   // AKV_ERR_DEVICE
 constexpr int kSlots = 5;
+constexpr int kMaxRuns = 8;  // runs per 128-key tile: 128 / page, page >= 16
 
 template <int D>
 struct Layout {
@@ -109,11 +110,36 @@ __device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& s
       ptx::tma_load_3d(sbase + L::kQ + t * L::kTile + kb * L::kBlockBytes, &p.q_map, bar(kBarQ), kb * 64,
                        w.kvh * G, q_tok0 + t * tpt);
   const int layer_base = p.layer * p.n_pages;
-  const AttnRun first = p.runs[seg.run_off];
-  int armed[kSlots] = {0, 0, 0};
+  // Pages of a tile's runs (K and V pages of run g).  They are fetched one
+  // tile ahead, so the run-table loads are in flight while the producer waits
+  // for ring slots instead of sitting between TMA issues.  Past the last run
+  // the segment's first page stands in (finite values, masked out).
+  const int2 first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
+  int kpg[kMaxRuns], vpg[kMaxRuns], nkp[kMaxRuns], nvp[kMaxRuns];
+  auto fetch = [&](int j, int (&kk)[kMaxRuns], int (&vv)[kMaxRuns]) {
+#pragma unroll
+    for (int g = 0; g < kMaxRuns; ++g) {
+      const int ri = (w.t0 + j) * rpt + g;
+      int2 kv = first;
+      if (g < rpt && ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
+      kk[g] = layer_base + kv.x;
+      vv[g] = layer_base + kv.y;
+    }
+  };
+  // A tile whose runs sit on consecutive pages loads with one copy per
+  // 64-column block (the tile map's box spans 128 / page pages).
+  auto consecutive = [&](const int (&pg)[kMaxRuns]) {
+    bool c = true;
+#pragma unroll
+    for (int g = 1; g < kMaxRuns; ++g) c = c && (g >= rpt || pg[g] == pg[0] + g);
+    return c;
+  };
+  fetch(0, kpg, vpg);
+  int armed[kSlots] = {0, 0, 0, 0, 0};
   bool ok = true;
   for (int ld = 0; ld < 2 * n_max; ++ld) {
     const int j = ld >> 1, is_v = ld & 1, slot = ld % kSlots, use = ld / kSlots;
+    if (!is_v && j + 1 < n_max) fetch(j + 1, nkp, nvp);
     if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
       ok = false;
       break;
@@ -121,15 +147,31 @@ __device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& s
     const uint32_t dst = sbase + L::kSlot + slot * L::kTile;
     const CUtensorMap* map = is_v ? &p.v_map : &p.k_map;
     ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), L::kTile);
-    for (int g = 0; g < rpt; ++g) {
-      const int ri = (w.t0 + j) * rpt + g;
-      const AttnRun run = ri < seg.n_runs ? p.runs[seg.run_off + ri] : first;
-      const int pg = layer_base + (is_v ? run.vp : run.kp);
+    if (consecutive(is_v ? vpg : kpg)) {
+      const CUtensorMap* tmap = is_v ? &p.v_tile_map : &p.k_tile_map;
+      const int pg = is_v ? vpg[0] : kpg[0];
+#pragma unroll
       for (int kb = 0; kb < L::kBlocks; ++kb)
-        ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, map, bar(kBarFull0 + slot), kb * 64, 0, w.kvh,
-                         pg);
+        ptx::tma_load_4d(dst + kb * L::kBlockBytes, tmap, bar(kBarFull0 + slot), kb * 64, 0, w.kvh, pg);
+    } else {
+#pragma unroll
+      for (int g = 0; g < kMaxRuns; ++g) {
+        if (g >= rpt) break;
+        const int pg = is_v ? vpg[g] : kpg[g];
+#pragma unroll
+        for (int kb = 0; kb < L::kBlocks; ++kb)
+          ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, map, bar(kBarFull0 + slot), kb * 64, 0,
+                           w.kvh, pg);
+      }
     }
     armed[slot] = use + 1;
+    if (is_v) {
+#pragma unroll
+      for (int g = 0; g < kMaxRuns; ++g) {
+        kpg[g] = nkp[g];
+        vpg[g] = nvp[g];
+      }
+    }
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 0, 0);
@@ -444,6 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
     ptx::prefetch_tensormap(&p.q_map);
     ptx::prefetch_tensormap(&p.k_map);
     ptx::prefetch_tensormap(&p.v_map);
+    ptx::prefetch_tensormap(&p.k_tile_map);
+    ptx::prefetch_tensormap(&p.v_tile_map);
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -37,6 +37,7 @@ constexpr int kPe = 64;        // K_pe width
 constexpr int kQChunks = (kLat + kPe) / 64;  // 9 chunks of the QK contraction
 constexpr int kVChunks = 256 / 64;           // 4 chunks of one output half
 constexpr int kRing = 4;
+constexpr int kMaxRuns = 8;  // runs per 128-key tile: 128 / page, page >= 16
 constexpr uint32_t kChunk = 128 * 128;       // 128 rows x 64 bf16
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -109,13 +110,51 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
   for (int c = 0; c < kQChunks; ++c)
     ptx::tma_load_3d(sbase + kQ + c * kChunk, &p.q_map, bar(kBarQ), c * 64, 0, q_tok0);
   const int layer_base = p.layer * p.n_pages;
-  const AttnRun first = p.runs[seg.run_off];
   bool ok = true;
   int issued = 0;
   const int n_loc = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
+  // Pages of the runs of tiles j (cur), j + 1 (nxt) and j + 2 (nn, fetched
+  // at the start of block j so the run-table loads are in flight a whole
+  // block before their first TMA).  Past the last run the segment's first
+  // page stands in (finite values, masked out).
+  const int2 first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
+  int ck[kMaxRuns], cv[kMaxRuns], xk[kMaxRuns], xv[kMaxRuns], nk[kMaxRuns], nv[kMaxRuns];
+  auto fetch = [&](int j, int (&kk)[kMaxRuns], int (&vv)[kMaxRuns]) {
+#pragma unroll
+    for (int g = 0; g < kMaxRuns; ++g) {
+      const int ri = (w.t0 + j) * rpt + g;
+      int2 kv = first;
+      if (g < rpt && ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
+      kk[g] = layer_base + kv.x;
+      vv[g] = layer_base + kv.y;
+    }
+  };
+  // A tile whose runs sit on consecutive pages loads each chunk with one
+  // copy (the tile map's box spans 128 / page pages).
+  auto consecutive = [&](const int (&pg)[kMaxRuns]) {
+    bool c = true;
+#pragma unroll
+    for (int g = 1; g < kMaxRuns; ++g) c = c && (g >= rpt || pg[g] == pg[0] + g);
+    return c;
+  };
+  fetch(0, ck, cv);
+  if (n_loc > 1) fetch(1, xk, xv);
   for (int ld = 0; ld < n_loc * kPerTile; ++ld) {
     int j, c;
     chunk_at(ld, n_loc, j, c);
+    if (ld >= kQChunks && (ld - kQChunks) % kPerTile == 0) {  // start of block b: QK of b + 1, PV of b
+      const int b = (ld - kQChunks) / kPerTile;
+      if (b >= 1) {
+#pragma unroll
+        for (int g = 0; g < kMaxRuns; ++g) {
+          ck[g] = xk[g];
+          cv[g] = xv[g];
+          xk[g] = nk[g];
+          xv[g] = nv[g];
+        }
+      }
+      if (b + 2 < n_loc) fetch(b + 2, nk, nv);
+    }
     const int slot = ld % kRing, use = ld / kRing;
     if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
       ok = false;
@@ -126,12 +165,20 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
     const int col = c < kQChunks ? (pe ? 0 : 64 * c) : 256 * half + 64 * (c - kQChunks);
     const CUtensorMap* map = pe ? &p.k_map : &p.v_map;
     const uint32_t dst = sbase + kSlots + slot * kChunk;
+    // tile j is the current block's tile (cur) or, for QK chunks after the first tile, the next (nxt)
+    const bool use_next = ld >= kQChunks && c < kQChunks;
     ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), kChunk);
-    for (int g = 0; g < rpt; ++g) {
-      const int ri = (w.t0 + j) * rpt + g;
-      const AttnRun run = ri < seg.n_runs ? p.runs[seg.run_off + ri] : first;
-      const int pg = layer_base + (pe ? run.kp : run.vp);
-      ptx::tma_load_4d(dst + g * p.page * 128, map, bar(kBarFull0 + slot), col, 0, 0, pg);
+    int pgs[kMaxRuns];
+#pragma unroll
+    for (int g = 0; g < kMaxRuns; ++g) pgs[g] = use_next ? (pe ? xk[g] : xv[g]) : (pe ? ck[g] : cv[g]);
+    if (consecutive(pgs)) {
+      ptx::tma_load_4d(dst, pe ? &p.k_tile_map : &p.v_tile_map, bar(kBarFull0 + slot), col, 0, 0, pgs[0]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < kMaxRuns; ++g) {
+        if (g >= rpt) break;
+        ptx::tma_load_4d(dst + g * p.page * 128, map, bar(kBarFull0 + slot), col, 0, 0, pgs[g]);
+      }
     }
     issued = ld + 1;
   }

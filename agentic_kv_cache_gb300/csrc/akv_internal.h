@@ -90,6 +90,9 @@ struct AttnParams {
   DevErr* err;
   float scale_log2;   // softmax scale * log2(e)
   int32_t n_work;
+  const int32_t* cta_units;  // persistent schedule: CTA b runs units [cta_units[b], cta_units[b + 1]) of work;
+                             // null: CTA b runs unit b
+  int32_t n_cta;             // CTAs of the persistent schedule (grid size when cta_units is set)
   int32_t layer;
   int32_t n_pages;
   int32_t n_layers;

@@ -830,6 +830,168 @@ struct akv_ctx {
     return sp;
   }
 
+  // Split-KV for the MLA kernel (one CTA per unit): cut every item's KV-tile
+  // range into up to S chunks so the launch fills whole waves of SMs; split
+  // chunks write partials and the chunk that finishes last merges them.
+  // Units run longest first (LPT), ties in (segment, tile, half, chunk) order.
+  void plan_split(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts) {
+    auto units_for = [&](int S) {
+      int64_t u = 0;
+      for (auto& w : work) u += std::min<int64_t>(S, std::max(1, w.n_a));
+      return u;
+    };
+    int best_s = 1;
+    double best = -1.0;
+    const int cands[] = {1, 2, 3, 4, 6, 8};
+    for (int S : cands) {
+      if (split_override > 0 && S != split_override) continue;
+      const int64_t u = units_for(S);
+      const int64_t waves = (u + n_sm - 1) / n_sm;
+      // A split part pays its partial write, a share of the merge and a
+      // slower pipeline start, so splitting must buy more occupancy than that.
+      const double eff = double(u) / double(waves * n_sm) * (S == 1 ? 1.0 : 0.85);
+      if (eff > best + 1e-9) {
+        best = eff;
+        best_s = S;
+      }
+    }
+    if (split_override > 0) best_s = std::min(split_override, 8);
+    std::vector<akv::AttnWork> units;
+    for (auto& w : work) {
+      const int span = w.n_a;
+      const int chunks = std::min(best_s, std::max(1, span));
+      if (chunks == 1) {
+        units.push_back(w);
+        continue;
+      }
+      comb.push_back(akv::CombineItem{n_parts, chunks, {0, 0}});
+      for (int c = 0; c < chunks; ++c) {
+        akv::AttnWork u = w;
+        u.t0 = int32_t(int64_t(span) * c / chunks);
+        u.t1 = int32_t(int64_t(span) * (c + 1) / chunks);
+        u.part = n_parts++;
+        u.comb = int32_t(comb.size()) - 1;
+        units.push_back(u);
+      }
+    }
+    auto cost = [](const akv::AttnWork& w) { return std::max(0, std::min(w.n_a, w.t1) - w.t0); };
+    std::stable_sort(units.begin(), units.end(),
+                     [&](const akv::AttnWork& a, const akv::AttnWork& b) { return cost(a) > cost(b); });
+    work.swap(units);
+  }
+
+  // Persistent stream-K schedule for the GQA kernel: one CTA per SM, each
+  // running an equal share of the work.  Items (query-tile pair x kv head)
+  // are laid end to end as a sequence of KV-tile steps, each step costing
+  // the query tiles it feeds (1 or 2), plus a fixed cost per unit for its
+  // start and epilogue.  The sequence is cut into n_cta contiguous pieces of
+  // equal cost; an item crossing a cut becomes several units (parts) whose
+  // partial results the last one to finish merges.  A cut never leaves a
+  // piece of an item shorter than kMinSteps steps.  akv_set_attention_split
+  // (n >= 1) instead cuts every item into n equal parts, one CTA per unit.
+  void plan_persistent(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts,
+                       std::vector<int32_t>& cta_units) {
+    if (split_override > 0) {
+      std::vector<akv::AttnWork> units;
+      for (auto& w : work) {
+        const int span = w.t1;
+        const int chunks = std::min(split_override, std::max(1, span));
+        if (chunks > 1) comb.push_back(akv::CombineItem{n_parts, chunks, {0, 0}});
+        for (int c = 0; c < chunks; ++c) {
+          akv::AttnWork u = w;
+          u.t0 = int32_t(int64_t(span) * c / chunks);
+          u.t1 = int32_t(int64_t(span) * (c + 1) / chunks);
+          if (chunks > 1) {
+            u.part = n_parts++;
+            u.comb = int32_t(comb.size()) - 1;
+          }
+          units.push_back(u);
+        }
+      }
+      work.swap(units);
+      cta_units.clear();
+      return;
+    }
+    constexpr int64_t kUnitCost = 6;   // start + epilogue of a unit, in query-tile steps
+    constexpr int64_t kMinSteps = 4;   // shortest piece of an item worth a unit
+    constexpr int64_t kMinCtaCost = 48;
+    // cost of the first j steps of item w (O(1): each query tile feeds its first n steps)
+    auto prefix = [](const akv::AttnWork& w, int64_t j) {
+      return std::min<int64_t>(j, w.n_a) + std::min<int64_t>(j, w.n_b);
+    };
+    int64_t total = 0;
+    for (auto& w : work) total += kUnitCost + prefix(w, w.t1);
+    const int64_t n_cta = std::max<int64_t>(1, std::min<int64_t>(n_sm, total / kMinCtaCost));
+    total += (n_cta - 1) * kUnitCost;  // each cut starts one more unit
+    std::vector<akv::AttnWork> units;
+    std::vector<int32_t> item_of;  // unit -> item index
+    units.reserve(work.size() + size_t(n_cta));
+    item_of.reserve(work.size() + size_t(n_cta));
+    cta_units.assign(1, 0);
+    int64_t acc = 0, cta = 0;
+    auto boundary = [&]() { return (cta + 1) * total / n_cta; };
+    auto close_cta = [&]() {
+      cta_units.push_back(int32_t(units.size()));
+      ++cta;
+    };
+    for (size_t it = 0; it < work.size(); ++it) {
+      const akv::AttnWork& w = work[it];
+      const int64_t span = w.t1;
+      int64_t start = 0;
+      acc += kUnitCost;
+      const int64_t base0 = acc;  // acc = base0 + prefix(j) after j steps of this item
+      int64_t base = base0;
+      bool close_at_end = false;
+      while (cta < n_cta - 1 && base + prefix(w, span) >= boundary()) {
+        // first step count j (> start) at which the running cost reaches the boundary
+        const int64_t target = boundary() - base;
+        int64_t lo = start + 1, hi = span;
+        while (lo < hi) {
+          const int64_t mid = (lo + hi) / 2;
+          if (prefix(w, mid) >= target) hi = mid; else lo = mid + 1;
+        }
+        int64_t j = std::max(lo, start + kMinSteps);  // a piece is never shorter than kMinSteps
+        if (span - j < kMinSteps) {
+          close_at_end = true;  // finish the item in this CTA
+          break;
+        }
+        akv::AttnWork u = w;
+        u.t0 = int32_t(start);
+        u.t1 = int32_t(j);
+        units.push_back(u);
+        item_of.push_back(int32_t(it));
+        close_cta();
+        start = j;
+        base += kUnitCost;  // the next piece starts a unit
+      }
+      akv::AttnWork u = w;
+      u.t0 = int32_t(start);
+      u.t1 = int32_t(span);
+      units.push_back(u);
+      item_of.push_back(int32_t(it));
+      acc = base + prefix(w, span);
+      if (close_at_end && cta < n_cta - 1) close_cta();
+    }
+    if (cta_units.back() != int32_t(units.size())) close_cta();
+    // Items cut into several units: partial slots and a ticket counter.
+    std::vector<int32_t> n_of(work.size(), 0), comb_of(work.size(), -1);
+    for (int32_t i : item_of) ++n_of[size_t(i)];
+    for (size_t u = 0; u < units.size(); ++u) {
+      const size_t it = size_t(item_of[u]);
+      if (n_of[it] < 2) continue;
+      if (comb_of[it] < 0) {
+        comb_of[it] = int32_t(comb.size());
+        comb.push_back(akv::CombineItem{0, n_of[it], {0, 0}});
+        comb.back().part0 = -1;
+      }
+      akv::CombineItem& ci = comb[size_t(comb_of[it])];
+      units[u].part = n_parts++;
+      if (ci.part0 < 0) ci.part0 = units[u].part;
+      units[u].comb = comb_of[it];
+    }
+    work.swap(units);
+  }
+
   void attend(int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q, int64_t n_q_rows, void* o,
               float* lse, float scale, cudaStream_t st) {
     if (n_segs < 0 || (n_segs > 0 && !segs)) fail(AKV_ERR_ARG, "bad segment list");
@@ -895,62 +1057,14 @@ struct akv_ctx {
     }
     if (meta) return;
     const bool mla = cfg.layout == AKV_LAYOUT_MLA;
-    // Split-KV: cut every item's KV-tile range into up to S chunks so the
-    // launch fills whole waves of SMs; split chunks write partials, and the
-    // chunk that finishes last merges them.
     std::vector<akv::CombineItem> comb;
+    std::vector<int32_t> cta_units;  // GQA: persistent schedule, CTA b runs units [cta_units[b], cta_units[b+1])
     int32_t n_parts = 0;
-    {
-      auto span_of = [mla](const akv::AttnWork& w) { return mla ? w.n_a : std::max(w.n_a, w.n_b); };
-      auto units_for = [&](int S) {
-        int64_t u = 0;
-        for (auto& w : work) u += std::min<int64_t>(S, std::max(1, span_of(w)));
-        return u;
-      };
-      int best_s = 1;
-      double best = -1.0;
-      const int cands[] = {1, 2, 3, 4, 6, 8};
-      for (int S : cands) {
-        if (split_override > 0 && S != split_override) continue;
-        const int64_t u = units_for(S);
-        const int64_t waves = (u + n_sm - 1) / n_sm;
-        // A split part pays its partial write, a share of the merge and a
-        // slower pipeline start (measured at about 15% on 32K-context items),
-        // so splitting must buy more wave occupancy than that.
-        const double eff = double(u) / double(waves * n_sm) * (S == 1 ? 1.0 : 0.85);
-        if (eff > best + 1e-9) {
-          best = eff;
-          best_s = S;
-        }
-      }
-      if (split_override > 0) best_s = std::min(split_override, 8);
-      std::vector<akv::AttnWork> units;
-      for (auto& w : work) {
-        const int span = span_of(w);
-        const int chunks = std::min(best_s, std::max(1, span));
-        if (chunks == 1) {
-          units.push_back(w);
-          continue;
-        }
-        comb.push_back(akv::CombineItem{n_parts, chunks, {0, 0}});
-        for (int c = 0; c < chunks; ++c) {
-          akv::AttnWork u = w;
-          u.t0 = int32_t(int64_t(span) * c / chunks);
-          u.t1 = int32_t(int64_t(span) * (c + 1) / chunks);
-          u.part = n_parts++;
-          u.comb = int32_t(comb.size()) - 1;
-          units.push_back(u);
-        }
-      }
-      work.swap(units);
+    if (mla) {
+      plan_split(work, comb, n_parts);
+    } else {
+      plan_persistent(work, comb, n_parts, cta_units);
     }
-    // Longest first (LPT); ties in (segment, head, tile, chunk) order.
-    auto cost = [mla](const akv::AttnWork& w) {
-      auto in = [&](int n) { return std::max(0, std::min(n, w.t1) - w.t0); };
-      return mla ? in(w.n_a) : in(w.n_a) + in(w.n_b);
-    };
-    std::stable_sort(work.begin(), work.end(),
-                     [&](const akv::AttnWork& a, const akv::AttnWork& b) { return cost(a) > cost(b); });
     if (mla) {
       if (cfg.d_v != 512 || cfg.d_rot != 64)
         fail(AKV_ERR_ARG, "MLA segment attention supports a 512-wide latent and a 64-wide K_pe");
@@ -992,10 +1106,12 @@ struct akv_ctx {
     void* dsegs = nullptr;
     void* dwork = nullptr;
     void* dcomb = nullptr;
+    void* dcta = nullptr;
     up.upload({{runs.data(), runs.size() * sizeof(akv::AttnRun), &druns},
                {tab.data(), tab.size() * sizeof(akv::AttnSeg), &dsegs},
                {work.data(), work.size() * sizeof(akv::AttnWork), &dwork},
-               {comb.data(), comb.size() * sizeof(akv::CombineItem), &dcomb}},
+               {comb.data(), comb.size() * sizeof(akv::CombineItem), &dcomb},
+               {cta_units.data(), cta_units.size() * sizeof(int32_t), &dcta}},
               st);
     p.runs = static_cast<akv::AttnRun*>(druns);
     p.segs = static_cast<akv::AttnSeg*>(dsegs);
@@ -1005,6 +1121,8 @@ struct akv_ctx {
     p.err = dev_err;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.n_work = int32_t(work.size());
+    p.cta_units = cta_units.empty() ? nullptr : static_cast<const int32_t*>(dcta);
+    p.n_cta = cta_units.empty() ? 0 : int32_t(cta_units.size()) - 1;
     p.layer = layer;
     p.n_pages = cfg.n_pages;
     p.n_layers = cfg.n_layers;

@@ -74,7 +74,8 @@ enum Bar {
   kBarS0 = kBarEmpty0 + kSlots,  // + tile
   kBarP0 = kBarS0 + 2,
   kBarO0 = kBarP0 + 2,
-  kBarFin = kBarO0 + 2,
+  kBarQFree = kBarO0 + 2,  // committed after a unit's last QK MMA: Q buffers may be reloaded
+  kBarFin,
   kNumBars
 };
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
@@ -93,151 +94,182 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // ---------------------------------------------------------------- producer
+// Units run back to back: the K/V stream position ld continues across units
+// (K_j of a unit is ld0 + 2j, V_j is ld0 + 2j + 1), and a unit's Q tiles
+// are loaded once the previous unit's last QK MMA has released the Q buffers.
 template <int D>
-__device__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
-                        volatile int* abort_flag) {
+__device__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, volatile int* abort_flag) {
   using L = Layout<D>;
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kTileKeys / p.page;
-  // KV tiles [t0, t1) of this work item; local tile j is global tile t0 + j
-  const int span = w.t1 - w.t0;
-  const int n_max = max(min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span));
-  const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
-  ptx::mbar_arrive_expect_tx(bar(kBarQ), (w.n_b > 0 ? 2 : 1) * L::kTile);
-  for (int t = 0; t < (w.n_b > 0 ? 2 : 1); ++t)
-    for (int kb = 0; kb < L::kBlocks; ++kb)
-      ptx::tma_load_3d(sbase + L::kQ + t * L::kTile + kb * L::kBlockBytes, &p.q_map, bar(kBarQ), kb * 64,
-                       w.kvh * G, q_tok0 + t * tpt);
   const int layer_base = p.layer * p.n_pages;
-  // Pages of a tile's runs (K and V pages of run g).  They are fetched one
-  // tile ahead, so the run-table loads are in flight while the producer waits
-  // for ring slots instead of sitting between TMA issues.  Past the last run
-  // the segment's first page stands in (finite values, masked out).
-  const int2 first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
-  int kpg[kMaxRuns], vpg[kMaxRuns], nkp[kMaxRuns], nvp[kMaxRuns];
-  auto fetch = [&](int j, int (&kk)[kMaxRuns], int (&vv)[kMaxRuns]) {
-#pragma unroll
-    for (int g = 0; g < kMaxRuns; ++g) {
-      const int ri = (w.t0 + j) * rpt + g;
-      int2 kv = first;
-      if (g < rpt && ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
-      kk[g] = layer_base + kv.x;
-      vv[g] = layer_base + kv.y;
-    }
-  };
-  // A tile whose runs sit on consecutive pages loads with one copy per
-  // 64-column block (the tile map's box spans 128 / page pages).
-  auto consecutive = [&](const int (&pg)[kMaxRuns]) {
-    bool c = true;
-#pragma unroll
-    for (int g = 1; g < kMaxRuns; ++g) c = c && (g >= rpt || pg[g] == pg[0] + g);
-    return c;
-  };
-  fetch(0, kpg, vpg);
   int armed[kSlots] = {0, 0, 0, 0, 0};
+  int ld0 = 0, q_loads = 0;
   bool ok = true;
-  for (int ld = 0; ld < 2 * n_max; ++ld) {
-    const int j = ld >> 1, is_v = ld & 1, slot = ld % kSlots, use = ld / kSlots;
-    if (!is_v && j + 1 < n_max) fetch(j + 1, nkp, nvp);
-    if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
-      ok = false;
-      break;
-    }
-    const uint32_t dst = sbase + L::kSlot + slot * L::kTile;
-    const CUtensorMap* map = is_v ? &p.v_map : &p.k_map;
-    ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), L::kTile);
-    if (consecutive(is_v ? vpg : kpg)) {
-      const CUtensorMap* tmap = is_v ? &p.v_tile_map : &p.k_tile_map;
-      const int pg = is_v ? vpg[0] : kpg[0];
-#pragma unroll
+  for (int u = u0; u < u1 && ok; ++u) {
+    const AttnWork w = p.work[u];
+    const AttnSeg seg = p.segs[w.seg];
+    // KV tiles [t0, t1) of this unit; local tile j is global tile t0 + j
+    const int span = w.t1 - w.t0;
+    const int n_max = max(min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span));
+    const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
+    if (u > u0 && !(ok = ptx::mbar_wait(bar(kBarQFree), (u - u0 - 1) & 1, abort_flag, kWaitLimitNs))) break;
+    ptx::mbar_arrive_expect_tx(bar(kBarQ), (w.n_b > 0 ? 2 : 1) * L::kTile);
+    for (int t = 0; t < (w.n_b > 0 ? 2 : 1); ++t)
       for (int kb = 0; kb < L::kBlocks; ++kb)
-        ptx::tma_load_4d(dst + kb * L::kBlockBytes, tmap, bar(kBarFull0 + slot), kb * 64, 0, w.kvh, pg);
-    } else {
+        ptx::tma_load_3d(sbase + L::kQ + t * L::kTile + kb * L::kBlockBytes, &p.q_map, bar(kBarQ), kb * 64,
+                         w.kvh * G, q_tok0 + t * tpt);
+    ++q_loads;
+    // Pages of a tile's runs (K and V pages of run g).  They are fetched one
+    // tile ahead, so the run-table loads are in flight while the producer
+    // waits for ring slots instead of sitting between TMA issues.  Past the
+    // last run the segment's first page stands in (finite values, masked out).
+    const int2 first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
+    int kpg[kMaxRuns], vpg[kMaxRuns], nkp[kMaxRuns], nvp[kMaxRuns];
+    auto fetch = [&](int j, int (&kk)[kMaxRuns], int (&vv)[kMaxRuns]) {
 #pragma unroll
       for (int g = 0; g < kMaxRuns; ++g) {
-        if (g >= rpt) break;
-        const int pg = is_v ? vpg[g] : kpg[g];
+        const int ri = (w.t0 + j) * rpt + g;
+        int2 kv = first;
+        if (g < rpt && ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
+        kk[g] = layer_base + kv.x;
+        vv[g] = layer_base + kv.y;
+      }
+    };
+    // A tile whose runs sit on consecutive pages loads with one copy per
+    // 64-column block (the tile map's box spans 128 / page pages).
+    auto consecutive = [&](const int (&pg)[kMaxRuns]) {
+      bool c = true;
+#pragma unroll
+      for (int g = 1; g < kMaxRuns; ++g) c = c && (g >= rpt || pg[g] == pg[0] + g);
+      return c;
+    };
+    fetch(0, kpg, vpg);
+    for (int l = 0; l < 2 * n_max; ++l) {
+      const int ld = ld0 + l, j = l >> 1, is_v = l & 1, slot = ld % kSlots, use = ld / kSlots;
+      if (!is_v && j + 1 < n_max) fetch(j + 1, nkp, nvp);
+      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+      const uint32_t dst = sbase + L::kSlot + slot * L::kTile;
+      const CUtensorMap* map = is_v ? &p.v_map : &p.k_map;
+      ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), L::kTile);
+      if (consecutive(is_v ? vpg : kpg)) {
+        const CUtensorMap* tmap = is_v ? &p.v_tile_map : &p.k_tile_map;
+        const int pg = is_v ? vpg[0] : kpg[0];
 #pragma unroll
         for (int kb = 0; kb < L::kBlocks; ++kb)
-          ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, map, bar(kBarFull0 + slot), kb * 64, 0,
-                           w.kvh, pg);
-      }
-    }
-    armed[slot] = use + 1;
-    if (is_v) {
+          ptx::tma_load_4d(dst + kb * L::kBlockBytes, tmap, bar(kBarFull0 + slot), kb * 64, 0, w.kvh, pg);
+      } else {
 #pragma unroll
-      for (int g = 0; g < kMaxRuns; ++g) {
-        kpg[g] = nkp[g];
-        vpg[g] = nvp[g];
+        for (int g = 0; g < kMaxRuns; ++g) {
+          if (g >= rpt) break;
+          const int pg = is_v ? vpg[g] : kpg[g];
+#pragma unroll
+          for (int kb = 0; kb < L::kBlocks; ++kb)
+            ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, map, bar(kBarFull0 + slot), kb * 64, 0,
+                             w.kvh, pg);
+        }
+      }
+      armed[slot] = use + 1;
+      if (is_v) {
+#pragma unroll
+        for (int g = 0; g < kMaxRuns; ++g) {
+          kpg[g] = nkp[g];
+          vpg[g] = nvp[g];
+        }
       }
     }
+    ld0 += 2 * n_max;
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 0, 0);
     *abort_flag = 1;
   }
   // Drain: every copy issued here has landed before the CTA may exit.
-  ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kDrainLimitNs);
+  if (q_loads) ptx::mbar_wait_drain(bar(kBarQ), (q_loads - 1) & 1, kDrainLimitNs);
+#pragma unroll
   for (int s = 0; s < kSlots; ++s)
-    if (armed[s]) ptx::mbar_wait(bar(kBarFull0 + s), (armed[s] - 1) & 1, abort_flag, kDrainLimitNs);
+    if (armed[s]) ptx::mbar_wait_drain(bar(kBarFull0 + s), (armed[s] - 1) & 1, kDrainLimitNs);
 }
 
 // --------------------------------------------------------------------- MMA
 // Per KV tile j and query tile T: O_T += P_T(j-1) V_{j-1} (once P_T(j-1) is
 // written), then S_T(j) = Q_T K_j^T, then one commit to S_T's barrier.  Slots
 // are released (commit to their empty barrier) after their last reader.
+// Across units the S/P phase of tile T continues from the previous units
+// (cs[T] events so far).  The first PV of a unit overwrites O_T; it waits for
+// P_T(0) of that unit, which the softmax threads arrive only after reading
+// out the previous unit's O_T, so O_T is free by then.
 template <int D>
-__device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
+__device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
                           volatile int* abort_flag) {
   using L = Layout<D>;
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kTileKeys, false);
   constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, D, true);
-  const int span = w.t1 - w.t0;  // local tile counts of this KV range
-  const int n_t[2] = {min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span)};
-  const int n_max = max(n_t[0], n_t[1]);
   auto slot_of = [](int ld) { return ld % kSlots; };
   auto full_parity = [](int ld) { return (ld / kSlots) & 1; };
-  bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
-  for (int j = 0; j <= n_max && ok; ++j) {
-    bool k_ready = false, v_ready = false;
-    for (int t = 0; t < 2 && ok; ++t) {
-      const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
-      if (j >= 1 && j - 1 < n_t[t]) {
-        if (!v_ready) {
-          const int ld = 2 * (j - 1) + 1;
-          if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs))) break;
-          v_ready = true;
+  int ld0 = 0, cs0 = 0, cs1 = 0;
+  bool ok = true;
+  for (int u = u0; u < u1 && ok; ++u) {
+    const AttnWork w = p.work[u];
+    const int span = w.t1 - w.t0;  // local tile counts of this KV range
+    const int nt0 = min(max(w.n_a - w.t0, 0), span), nt1 = min(max(w.n_b - w.t0, 0), span);
+    const int n_max = max(nt0, nt1);
+    if (!(ok = ptx::mbar_wait(bar(kBarQ), (u - u0) & 1, abort_flag, kWaitLimitNs))) break;
+    for (int j = 0; j <= n_max && ok; ++j) {
+      bool k_ready = false, v_ready = false;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int nt = t ? nt1 : nt0, cs = t ? cs1 : cs0;
+        const uint32_t tS = tmem + 128u * t, tO = tmem + 256u + 128u * t;
+        if (ok && j >= 1 && j - 1 < nt) {
+          if (!v_ready) {
+            const int ld = ld0 + 2 * (j - 1) + 1;
+            ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs);
+            v_ready = true;
+          }
+          if (ok) ok = ptx::mbar_wait(bar(kBarP0 + t), (cs + j - 1) & 1, abort_flag, kWaitLimitNs);
+          if (ok) {
+            ptx::tc_fence_after();
+            const uint32_t vt = sbase + L::kSlot + slot_of(ld0 + 2 * (j - 1) + 1) * L::kTile;
+            for (int ks = 0; ks < kTileKeys / 16; ++ks)  // P: 16 keys = 8 packed TMEM columns per step
+              ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024),
+                                   idesc_pv, (j > 1 || ks > 0));
+            if (j - 1 == nt - 1) ptx::mma_commit(bar(kBarO0 + t));
+          }
         }
-        if (!(ok = ptx::mbar_wait(bar(kBarP0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
-        ptx::tc_fence_after();
-        const uint32_t vt = sbase + L::kSlot + slot_of(2 * (j - 1) + 1) * L::kTile;
-        for (int ks = 0; ks < kTileKeys / 16; ++ks)  // P: 16 keys = 8 packed TMEM columns per step
-          ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024), idesc_pv,
-                               (j > 1 || ks > 0));
-        if (j - 1 == n_t[t] - 1) ptx::mma_commit(bar(kBarO0 + t));
+        if (ok && j < nt) {
+          if (!k_ready) {
+            const int ld = ld0 + 2 * j;
+            ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs);
+            k_ready = true;
+            ptx::tc_fence_after();
+          }
+          if (ok) {
+            const uint32_t kt = sbase + L::kSlot + slot_of(ld0 + 2 * j) * L::kTile;
+            const uint32_t qt = sbase + L::kQ + t * L::kTile;
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
+              ptx::mma_bf16(tS, ptx::smem_desc(qt + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024), idesc_qk,
+                            ks > 0);
+            }
+            ptx::mma_commit(bar(kBarS0 + t));
+          }
+        }
       }
-      if (j < n_t[t]) {
-        if (!k_ready) {
-          const int ld = 2 * j;
-          if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs))) break;
-          k_ready = true;
-          ptx::tc_fence_after();
-        }
-        const uint32_t kt = sbase + L::kSlot + slot_of(2 * j) * L::kTile;
-        const uint32_t qt = sbase + L::kQ + t * L::kTile;
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
-          ptx::mma_bf16(tS, ptx::smem_desc(qt + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024), idesc_qk, ks > 0);
-        }
-        ptx::mma_commit(bar(kBarS0 + t));
-      }
+      if (!ok) break;
+      if (j >= 1) ptx::mma_commit(bar(kBarEmpty0 + slot_of(ld0 + 2 * (j - 1) + 1)));  // V_{j-1} done
+      if (j < n_max) ptx::mma_commit(bar(kBarEmpty0 + slot_of(ld0 + 2 * j)));        // K_j done
+      if (j == n_max - 1) ptx::mma_commit(bar(kBarQFree));                           // last QK of the unit
     }
-    if (!ok) break;
-    if (j >= 1) ptx::mma_commit(bar(kBarEmpty0 + slot_of(2 * (j - 1) + 1)));  // V_{j-1} done
-    if (j < n_max) ptx::mma_commit(bar(kBarEmpty0 + slot_of(2 * j)));        // K_j done
+    cs0 += nt0;
+    cs1 += nt1;
+    ld0 += 2 * n_max;
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 1, 0);
@@ -245,7 +277,7 @@ __device__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase
   }
   // Every MMA issued above has completed before TMEM is released.
   ptx::mma_commit(bar(kBarFin));
-  ptx::mbar_wait(bar(kBarFin), 0, abort_flag, kDrainLimitNs);
+  ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs);
 }
 
 // Split part of query tile t, row r: if this CTA drew the item's last ticket,
@@ -261,10 +293,13 @@ __device__ __forceinline__ void merge_tile(const AttnParams& p, const AttnWork& 
 }
 
 // ----------------------------------------------------------------- softmax
-// One warpgroup per query tile t; thread = row r = TMEM lane r.
+// One warpgroup per query tile t; thread = row r = TMEM lane r.  One unit:
+// bit 0 of ph is the parity of the S/P phases of tile t consumed by earlier
+// units, bit 1 that of its O phases; both advance here.  Returns false when a
+// wait gave up.
 template <int D>
-__device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint8_t* smem,
-                             uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
+__device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint8_t* smem,
+                             uint32_t sbase, uint32_t tmem, volatile int* abort_flag, int& ph) {
   using L = Layout<D>;
   const int n_glob = t == 0 ? w.n_a : w.n_b;
   const int n_t = min(max(n_glob - w.t0, 0), w.t1 - w.t0);  // local tiles of this KV range
@@ -276,7 +311,7 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       p.partial[w.part * partial_floats(2, D) + (int64_t(t) * (D + 2) + D) * 128 + r0] = -INFINITY;
       merge_tile<D>(p, w, seg, t, r0);
     }
-    return;
+    return true;
   }
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
@@ -300,15 +335,16 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
   const int sl_own = r & (p.page - 1);
-  bool run_ok;
-  AttnRun run_cur = AttnRun{0, 0, 0, 0};
+  // (lohi, es) of the run holding key column r of the current tile; lo = hi = 0
+  // past the segment's last run, so no slot matches
+  int2 run_cur = make_int2(0, 0);
+  const int2* run_le = reinterpret_cast<const int2*>(p.runs + seg.run_off);
   {
     const int ri0 = w.t0 * rpt + (r >> page_shift);
-    run_ok = ri0 < seg.n_runs;
-    if (run_ok) run_cur = p.runs[seg.run_off + ri0];
+    if (ri0 < seg.n_runs) run_cur = run_le[2 * ri0 + 1];
   }
   for (int j = 0; j < n_t; ++j) {
-    ok = ptx::mbar_wait(bar(kBarS0 + t), j & 1, abort_flag, kWaitLimitNs);
+    ok = ptx::mbar_wait(bar(kBarS0 + t), (ph ^ j) & 1, abort_flag, kWaitLimitNs);
     if (!ptx::bar_red_and(bar_id, 128, ok)) {
       ok = false;
       break;
@@ -318,12 +354,11 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // of the next tile is fetched now so its latency hides behind this tile.
     int e = INT_MAX;
     {
-      const int lo = run_cur.lohi & 0xffff, hi = run_cur.lohi >> 16;
-      if (run_ok && sl_own >= lo && sl_own < hi) e = run_cur.es + (sl_own - lo);
+      const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
+      if (sl_own >= lo && sl_own < hi) e = run_cur.y + (sl_own - lo);
       colE[r] = e;
       const int ri = (w.t0 + j + 1) * rpt + (r >> page_shift);
-      run_ok = ri < seg.n_runs;
-      if (run_ok) run_cur = p.runs[seg.run_off + ri];
+      run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
     const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
     ptx::tc_fence_after();
@@ -405,14 +440,15 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     ptx::mbar_arrive(bar(kBarP0 + t));
   }
   if (ok) {
-    ok = ptx::mbar_wait(bar(kBarO0 + t), 0, abort_flag, kWaitLimitNs);
+    ok = ptx::mbar_wait(bar(kBarO0 + t), (ph >> 1) & 1, abort_flag, kWaitLimitNs);
     ok = ptx::bar_red_and(bar_id, 128, ok);
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 2 + t, 0);
     *abort_flag = 1;
-    return;
+    return false;
   }
+  ph ^= (n_t & 1) | 2;
   ptx::tc_fence_after();
   if (w.part >= 0) {
     // Split part: unnormalised O, running max and sum for the combine kernel,
@@ -427,8 +463,9 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     }
     base[int64_t(D) * 128] = m_run;
     base[int64_t(D + 1) * 128] = l_run;
+    ptx::tc_fence_before();
     merge_tile<D>(p, w, seg, t, r);
-    return;
+    return true;
   }
   const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
   __nv_bfloat16* orow =
@@ -453,6 +490,18 @@ __device__ void softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
     p.lse[int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g] = lse;
   }
+  return true;
+}
+
+template <int D>
+__device__ void softmax_units(const AttnParams& p, int u0, int u1, int t, uint8_t* smem, uint32_t sbase,
+                              uint32_t tmem, volatile int* abort_flag) {
+  int ph = 0;
+  for (int u = u0; u < u1; ++u) {
+    const AttnWork w = p.work[u];
+    const AttnSeg seg = p.segs[w.seg];
+    if (!softmax_tile<D>(p, w, seg, t, smem, sbase, tmem, abort_flag, ph)) return;
+  }
 }
 
 template <int D>
@@ -470,8 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const AttnWork w = p.work[blockIdx.x];
-  const AttnSeg seg = p.segs[w.seg];
+  const int u0 = p.cta_units ? p.cta_units[blockIdx.x] : int(blockIdx.x);
+  const int u1 = p.cta_units ? p.cta_units[blockIdx.x + 1] : int(blockIdx.x) + 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, (i == kBarP0 || i == kBarP0 + 1) ? 128 : 1);
@@ -495,11 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) produce<D>(p, w, seg, sbase, abort_flag);
+    if (lane == 0) produce<D>(p, u0, u1, sbase, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) issue_mma<D>(p, w, sbase, tmem, abort_flag);
+    if (lane == 0) issue_mma<D>(p, u0, u1, sbase, tmem, abort_flag);
   } else {
-    softmax_tile<D>(p, w, seg, warp < 6 ? 0 : 1, smem, sbase, tmem, abort_flag);
+    softmax_units<D>(p, u0, u1, warp < 6 ? 0 : 1, smem, sbase, tmem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -521,17 +570,18 @@ int segment_attn_smem_bytes(int dim) {
 
 cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st) {
   if (p.n_work <= 0) return cudaSuccess;
+  const int grid = p.cta_units ? p.n_cta : p.n_work;
   const int smem = segment_attn_smem_bytes(dim);
   if (smem < 0) return cudaErrorInvalidValue;
   cudaError_t e;
   if (dim == 64) {
     e = cudaFuncSetAttribute(segment_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    segment_attn_kernel<64><<<p.n_work, kThreads, smem, st>>>(p, smem);
+    segment_attn_kernel<64><<<grid, kThreads, smem, st>>>(p, smem);
   } else {
     e = cudaFuncSetAttribute(segment_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    segment_attn_kernel<128><<<p.n_work, kThreads, smem, st>>>(p, smem);
+    segment_attn_kernel<128><<<grid, kThreads, smem, st>>>(p, smem);
   }
   return cudaGetLastError();
 }

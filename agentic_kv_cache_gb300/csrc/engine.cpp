@@ -973,20 +973,48 @@ struct akv_ctx {
       if (close_at_end && cta < n_cta - 1) close_cta();
     }
     if (cta_units.back() != int32_t(units.size())) close_cta();
-    // Items cut into several units: partial slots and a ticket counter.
-    std::vector<int32_t> n_of(work.size(), 0), comb_of(work.size(), -1);
+    // Order inside each CTA: the piece that starts an item (at KV step 0)
+    // first, then the piece that ends an item cut by the previous CTA, then
+    // whole items.  With items of similar length every CTA then reads the
+    // same KV step of its item at about the same time (three phases in all),
+    // so the K/V tiles a step needs are fetched from HBM once and served to
+    // the other CTAs from L2.
+    {
+      std::vector<akv::AttnWork> ordered;
+      std::vector<int32_t> ordered_item;
+      ordered.reserve(units.size());
+      ordered_item.reserve(units.size());
+      for (size_t b = 0; b + 1 < cta_units.size(); ++b) {
+        const size_t a0 = size_t(cta_units[b]), a1 = size_t(cta_units[b + 1]);
+        auto is_head = [&](size_t u) { return units[u].t0 == 0 && units[u].t1 < work[size_t(item_of[u])].t1; };
+        auto is_tail = [&](size_t u) { return units[u].t0 > 0; };
+        for (int pass = 0; pass < 3; ++pass)
+          for (size_t u = a0; u < a1; ++u) {
+            const bool h = is_head(u), t = is_tail(u);
+            if ((pass == 0 && h) || (pass == 1 && t && !h) || (pass == 2 && !h && !t)) {
+              ordered.push_back(units[u]);
+              ordered_item.push_back(item_of[u]);
+            }
+          }
+      }
+      units.swap(ordered);
+      item_of.swap(ordered_item);
+    }
+    // Items cut into several units: consecutive partial slots per item and a
+    // ticket counter.
+    std::vector<int32_t> n_of(work.size(), 0), comb_of(work.size(), -1), next_of(work.size(), 0);
     for (int32_t i : item_of) ++n_of[size_t(i)];
+    for (size_t it = 0; it < work.size(); ++it) {
+      if (n_of[it] < 2) continue;
+      comb_of[it] = int32_t(comb.size());
+      comb.push_back(akv::CombineItem{n_parts, n_of[it], {0, 0}});
+      next_of[it] = n_parts;
+      n_parts += n_of[it];
+    }
     for (size_t u = 0; u < units.size(); ++u) {
       const size_t it = size_t(item_of[u]);
-      if (n_of[it] < 2) continue;
-      if (comb_of[it] < 0) {
-        comb_of[it] = int32_t(comb.size());
-        comb.push_back(akv::CombineItem{0, n_of[it], {0, 0}});
-        comb.back().part0 = -1;
-      }
-      akv::CombineItem& ci = comb[size_t(comb_of[it])];
-      units[u].part = n_parts++;
-      if (ci.part0 < 0) ci.part0 = units[u].part;
+      if (comb_of[it] < 0) continue;
+      units[u].part = next_of[it]++;
       units[u].comb = comb_of[it];
     }
     work.swap(units);

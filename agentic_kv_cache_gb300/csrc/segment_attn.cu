@@ -366,10 +366,9 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // holds the tile's largest entry index.
     const bool need_mask = !all_valid || colE[kTileKeys - 1] > lim;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
-    // Pass 1: row max over two 64-column halves read from TMEM.
-    float mx[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+    // Pass 1: row max over two 64-column halves read from TMEM (three-input
+    // max: two scores per instruction).
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t u[64];
@@ -385,9 +384,10 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
         }
       }
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(u[c]));
+      for (int c = 0; c < 32; ++c)
+        mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
     }
-    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+    const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
     const float m_new = fmaxf(m_run, mt);
     const bool resc = m_new > m_run + 8.0f;
     const float m_use = resc ? m_new : m_run;
@@ -406,8 +406,10 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     }
     // Pass 2: P = exp2(s * scale * log2 e - m), packed to bf16 pairs and
     // stored over the S columns already read (keys 2c, 2c+1 -> column c), where
-    // the PV MMA reads it as its A operand.
-    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // the PV MMA reads it as its A operand.  The scale-and-shift and the row
+    // sum run on float pairs (one packed FMA / add per two scores).
+    const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-msub, -msub);
+    float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two pair accumulators: no spills at 168 registers
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t u[64];
@@ -425,15 +427,14 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
-        const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
-        sum[(2 * c) & 7] += p0;
-        sum[(2 * c + 1) & 7] += p1;
-        pk[c] = pack_bf16(p0, p1);
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2v, negm);
+        const float2 pr = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+        sum[c & 1] = __fadd2_rn(sum[c & 1], pr);
+        pk[c] = pack_bf16(pr.x, pr.y);
       }
       ptx::tmem_store32(tS + lane_addr + h * 32, pk);
     }
-    const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) + ((sum[4] + sum[5]) + (sum[6] + sum[7]));
+    const float rowsum = (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
     l_run = l_run * alpha + rowsum;
     m_run = m_use;
     ptx::tc_fence_before();

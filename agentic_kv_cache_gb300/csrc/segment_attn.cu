@@ -215,6 +215,7 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
   auto full_parity = [](int ld) { return (ld / kSlots) & 1; };
   int ld0 = 0, cs0 = 0, cs1 = 0;
   bool ok = true;
+  const uint64_t qd0 = ptx::smem_desc(sbase + L::kQ, 16, 1024), qd1 = ptx::smem_desc(sbase + L::kQ + L::kTile, 16, 1024);
   for (int u = u0; u < u1 && ok; ++u) {
     const AttnWork w = p.work[u];
     const int span = w.t1 - w.t0;  // local tile counts of this KV range
@@ -236,10 +237,13 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
           if (ok) ok = ptx::mbar_wait(bar(kBarP0 + t), (cs + j - 1) & 1, abort_flag, kWaitLimitNs);
           if (ok) {
             ptx::tc_fence_after();
-            const uint32_t vt = sbase + L::kSlot + slot_of(ld0 + 2 * (j - 1) + 1) * L::kTile;
-            for (int ks = 0; ks < kTileKeys / 16; ++ks)  // P: 16 keys = 8 packed TMEM columns per step
-              ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::smem_desc(vt + ks * 16 * 128, L::kBlockBytes, 1024),
-                                   idesc_pv, (j > 1 || ks > 0));
+            const uint64_t vd = ptx::smem_desc(sbase + L::kSlot + slot_of(ld0 + 2 * (j - 1) + 1) * L::kTile,
+                                               L::kBlockBytes, 1024);
+            // P: 16 keys = 8 packed TMEM columns per step; V: 16 key rows = 2 KiB per step
+            ptx::mma_bf16_tmem_a(tO, tS, vd, idesc_pv, j > 1);
+#pragma unroll
+            for (int ks = 1; ks < kTileKeys / 16; ++ks)
+              ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::desc_advance(vd, ks * 16 * 128), idesc_pv, 1);
             if (j - 1 == nt - 1) ptx::mma_commit(bar(kBarO0 + t));
           }
         }
@@ -251,12 +255,13 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
             ptx::tc_fence_after();
           }
           if (ok) {
-            const uint32_t kt = sbase + L::kSlot + slot_of(ld0 + 2 * j) * L::kTile;
-            const uint32_t qt = sbase + L::kQ + t * L::kTile;
+            const uint64_t kd = ptx::smem_desc(sbase + L::kSlot + slot_of(ld0 + 2 * j) * L::kTile, 16, 1024);
+            const uint64_t qd = t ? qd1 : qd0;
+            // 16 head dims per step: 32 bytes inside a 128-byte swizzle row, a new block every 4 steps
+#pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
               const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
-              ptx::mma_bf16(tS, ptx::smem_desc(qt + off, 16, 1024), ptx::smem_desc(kt + off, 16, 1024), idesc_qk,
-                            ks > 0);
+              ptx::mma_bf16(tS, ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), idesc_qk, ks > 0);
             }
             ptx::mma_commit(bar(kBarS0 + t));
           }

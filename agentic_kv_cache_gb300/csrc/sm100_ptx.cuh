@@ -180,6 +180,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
+// Descriptor of the same layout `bytes` further on: only the start-address
+// field (bits 0-13, in 16-byte units) changes, and it cannot carry out while
+// the address stays inside shared memory.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  const uint32_t lo = uint32_t(desc) + (bytes >> 4), hi = uint32_t(desc >> 32);
+  return (uint64_t(hi) << 32) | lo;
+}
+
 // Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B.
 // b_mn_major: B stored MN-major (N contiguous) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool b_mn_major) {

@@ -56,9 +56,12 @@ def measured_traffic(kernel):
         rec = json.load(f).get(kernel)
     if not rec:
         return None
-    with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["source_sha256_16"]:
-            return None
+    h = hashlib.sha256()
+    for src in rec.get("sources", [rec.get("source")]):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
     return rec
 
 
@@ -213,6 +216,110 @@ def repos_sweep(steps, warmup=2, n_layers=80):
             "rotated_tokens_per_s": tokens / n_layers / (ms * 1e-3)}
 
 
+def reprefill_equiv(t, reps=3):
+    """Re-prefill attention-equivalent of the 32K turn: the retained tokens of the post-drop branch
+    re-entered as a fresh, fully visible sequence (what rebuilding the cache from compacted text
+    costs in attention) and attended causally with every token as a query, on the same kernel."""
+    torch = t.torch
+    names = dict(t.names)
+    t.runner.run_ops(t.eng, t.w, kv_source=lambda *_: (t.new_k, t.new_v), ops=t.step_ops, names=names,
+                     stream=t.stream)
+    n = int(t.eng.export_state(names["F"])["visible"].sum())
+    t.eng.seq_free(names["F"])
+    s = t.w.shape
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7)
+    k = torch.randn((s.n_layers, n, s.n_kv_heads, s.d_rot), generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn((s.n_layers, n, s.n_kv_heads, s.d_v), generator=gen, device="cuda").to(torch.bfloat16)
+    sid = t.eng.seq_alloc()
+    t.eng.append(sid, n, k, v, stream=t.stream)
+    q = torch.randn((n, s.n_q_heads, s.d_rot), generator=gen, device="cuda").to(torch.bfloat16)
+    o = torch.empty((n, s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
+    seg = [dict(seq=sid, kv_end=n, q_len=n, hide=np.zeros(0, np.int64), q_row0=0)]
+    t.eng.attend(0, seg, q, n, o, None, s.scale, stream=t.stream)
+    torch.cuda.synchronize()
+    t.eng.profile_enable(True)
+    for _ in range(reps):
+        t.eng.attend(0, seg, q, n, o, None, s.scale, stream=t.stream)
+    stats = t.eng.profile_read()["segment_attn"]
+    t.eng.profile_enable(False)
+    assert t.eng.check_device_error(t.stream) == 0
+    t.eng.seq_free(sid)
+    ms = stats["ms"] / stats["launches"]
+    flops = stats["flops"] / stats["launches"]
+    del q, o, k, v
+    torch.cuda.empty_cache()
+    return {"queries": n, "ms_per_layer": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "flops": flops}
+
+
+def mla_turns(concurrencies=(1, 4, 8, 16), steps=3, warmup=1):
+    """DeepSeek-V2-Lite MLA turn per concurrency C (27 layers, latent 512 + K_pe 64, 16 heads, page 64,
+    17K-token prompts): per session a branch of the prompt, the AMORTIZE splice of 2,016 tokens into a
+    32-token stub, 256 new tokens; then one flush (K_pe of every downstream token, all layers) and
+    segment attention of the 256 queries per session in each of the 27 layers."""
+    import torch
+    from agentic_kv_cache_gb300 import akv, runner, synth
+    out = {}
+    for C in concurrencies:
+        w = synth.mla_dsv2lite(concurrency=C)
+        s = w.shape
+        cfg = akv.config_from_shape(s, w.n_pages + C * (17408 // 64 + 8))  # + copy-on-write K_pe pages of the branches
+        pools = akv.make_pools(cfg)
+        eng = akv.Engine(cfg, pools)
+        st = torch.cuda.current_stream()
+        src = runner.torch_device_kv_source(w)
+        setup = [op for op in w.ops if op[0] == "alloc" or (op[0] == "append" and op[3].startswith("prompt"))]
+        names = runner.run_ops(eng, w, kv_source=src, ops=setup, stream=st)
+        turn = []
+        for op in w.ops:
+            if op[0] == "splice" or (op[0] == "append" and op[3].startswith("new")):
+                turn.append(op)
+        kv = {op[5] if op[0] == "splice" else op[3]: src(op[5] if op[0] == "splice" else op[3],
+                                                          op[4] if op[0] == "splice" else op[2]) for op in turn}
+        q32 = synth.q_array(w)
+        q = torch.from_numpy(q32).cuda().to(torch.bfloat16)
+        o = torch.empty((q.shape[0], s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
+        prompt = next(op for op in w.ops if op[0] == "append")[2]
+
+        def step():
+            br = {}
+            for c in range(C):
+                br[f"C{c}"] = eng.seq_fork(names[f"C{c}"], prompt)
+            runner.run_ops(eng, w, kv_source=lambda key, n: kv[key], ops=turn, names=br, stream=st)
+            for c in range(C):
+                eng.flush(br[f"C{c}"], stream=st)
+            segs = runner.engine_segments(w, br)
+            for layer in range(s.n_layers):
+                eng.attend(layer, segs, q, q.shape[0], o, None, s.scale, stream=st)
+            for c in range(C):
+                eng.seq_free(br[f"C{c}"])
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        eng.profile_enable(True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(steps):
+            step()
+        b.record(st)
+        torch.cuda.synchronize()
+        stats = eng.profile_read()
+        eng.profile_enable(False)
+        assert eng.check_device_error(st) == 0
+        att, rep = stats["segment_attn"], stats["repos_rotate"]
+        out[f"C{C}"] = {
+            "ms_per_turn": a.elapsed_time(b) / steps,
+            "attn_ms_per_layer": att["ms"] / max(att["launches"], 1),
+            "attn_TFLOP/s": att["flops"] / max(att["ms"], 1e-9) / 1e9,
+            "flush_ms": rep["ms"] / max(rep["launches"], 1) * (rep["launches"] / steps),
+            "repos_GB/s": rep["bytes"] / max(rep["ms"], 1e-9) / 1e6,
+        }
+        del eng, pools, q, o, kv
+        torch.cuda.empty_cache()
+    return out
+
+
 def gpu_arm(args, rank, world):
     import torch
     dev = int(os.environ.get("LOCAL_RANK", 0))
@@ -314,8 +421,15 @@ def gpu_arm(args, rank, world):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_total / args.steps},
     }
+    if not args.no_extra:
+        line["reprefill_equiv"] = reprefill_equiv(t)
+        line["reprefill_equiv"]["turn_cache_path_ms"] = total_ms / args.steps
+    del t
+    torch.cuda.empty_cache()
     if not args.no_sweep:
         line["repos_rotate_sweep"] = repos_sweep(steps=4, n_layers=args.sweep_layers)
+    if not args.no_extra:
+        line["mla_dsv2lite_turn"] = mla_turns()
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return line
@@ -440,12 +554,23 @@ def main():
     ap.add_argument("--only-sweep", action="store_true", help="run only the repos_rotate sweep (for profiling)")
     ap.add_argument("--sweep-layers", type=int, default=80)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--only-mla", type=int, default=0, metavar="C",
+                    help="run only the MLA turn at concurrency C (for profiling)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the re-prefill equivalent and the MLA per-concurrency turns")
     ap.add_argument("--attn-split", type=int, default=0,
                     help="KV chunks per attention work item: 0 chooses automatically, 1 never splits")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus if "RANK" in os.environ else 1))
+    if args.only_mla:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        from agentic_kv_cache_gb300 import build
+        build.build()
+        print(json.dumps(mla_turns((args.only_mla,), steps=args.steps, warmup=args.warmup)), flush=True)
+        return
     if args.only_sweep:
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))

@@ -77,6 +77,7 @@ def load(path=LIB_PATH):
         "akv_splice": [P, I32, I64, I64, I64, P, P, P, P],
         "akv_flush": [P, I32, P],
         "akv_attend": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
+        "akv_attend_fused": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
         "akv_debug_rotate_f32": [P, P, I32, P, P],
         "akv_export_state": [P, I32, P, P, P, P, P, P],
         "akv_refcounts": [P, P, P],
@@ -213,10 +214,13 @@ class Engine:
             arr[i].reserved = 0
         return arr, keep
 
-    def attend(self, layer, segs, q, n_q_rows, o, lse=None, scale=1.0, stream=None):
+    def attend(self, layer, segs, q, n_q_rows, o, lse=None, scale=1.0, stream=None, fused=False):
+        """akv_attend (flush, then attention), or with fused=True akv_attend_fused (pending shifts
+        applied to K inside the attention kernel; nothing is written to the pools)."""
         arr, keep = self.make_segments(segs)
-        self._check(self.lib.akv_attend(self.h, layer, arr, len(segs), _ptr(q), n_q_rows, _ptr(o), _ptr(lse),
-                                        float(scale), _stream(stream)))
+        fn = self.lib.akv_attend_fused if fused else self.lib.akv_attend
+        self._check(fn(self.h, layer, arr, len(segs), _ptr(q), n_q_rows, _ptr(o), _ptr(lse), float(scale),
+                       _stream(stream)))
 
     def debug_rotate_f32(self, runs, out, stream=None):
         """runs: int array [n, 4] (K page, lo, hi, delta); out: device float32 tensor

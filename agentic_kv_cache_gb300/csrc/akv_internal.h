@@ -93,6 +93,12 @@ struct AttnParams {
   const int32_t* cta_units;  // persistent schedule: CTA b runs units [cta_units[b], cta_units[b + 1]) of work;
                              // null: CTA b runs unit b
   int32_t n_cta;             // CTAs of the persistent schedule (grid size when cta_units is set)
+  // Fused rotation: the kernel rotates each K row of run r by the shift of
+  // table row run_didx[r] (-1: none) on its way to the tensor core.
+  const int32_t* run_didx;   // per run, or null
+  const float2* cs;          // (cos, sin)(delta * theta_j): [shifts][d_rot / 2], float64-evaluated
+  int32_t rope_half;         // pair layout: 0 interleaved (2j, 2j+1), 1 half-split (j, j + d/2)
+  int32_t fused;             // 1: launch the fused-rotation variant
   int32_t layer;
   int32_t n_pages;
   int32_t n_layers;

@@ -772,6 +772,7 @@ struct akv_ctx {
   // -------------------------------------------------------------- segments
   struct SegPlan {
     std::vector<akv::AttnRun> runs;
+    std::vector<int32_t> shift;  // fused plans: pending shift of each run's tokens
     int64_t kv_len = 0;
   };
 
@@ -791,7 +792,11 @@ struct akv_ctx {
       if (!toks[i].vis) fail(AKV_ERR_ARG, "a query token of the segment is dropped");
   }
 
-  SegPlan plan_segment(const akv_segment& g) {
+  // Runs of the segment's visible entries in logical order: maximal groups of
+  // consecutive slots of one (K page, V page).  With `fused` the tokens may
+  // carry pending shifts; runs then also break where the shift changes, and
+  // each run records it (the attention kernel rotates those keys on the fly).
+  SegPlan plan_segment(const akv_segment& g, bool fused = false) {
     auto& toks = seq(g.seq);
     std::vector<uint8_t> hidden;
     if (g.n_hide > 0) {
@@ -806,14 +811,15 @@ struct akv_ctx {
     for (int64_t i = 0; i < g.kv_end; ++i) {
       const Tok& t = toks[i];
       if (!t.vis || (!hidden.empty() && hidden[i])) continue;
-      if (t.delta != 0) fail(AKV_ERR_ARG, "segment reads token %lld with a pending shift", (long long)i);
-      if (open && cur.kp == t.kp && cur.vp == t.vp && t.slot == hi) {
+      if (!fused && t.delta != 0) fail(AKV_ERR_ARG, "segment reads token %lld with a pending shift", (long long)i);
+      if (open && cur.kp == t.kp && cur.vp == t.vp && t.slot == hi && (!fused || t.delta == sp.shift.back())) {
         ++hi;
       } else {
         if (open) {
           cur.lohi = lo | (hi << 16);
           sp.runs.push_back(cur);
         }
+        if (fused) sp.shift.push_back(t.delta);
         open = true;
         cur.kp = t.kp;
         cur.vp = t.vp;
@@ -1020,8 +1026,10 @@ struct akv_ctx {
     work.swap(units);
   }
 
+  // fused: leave pending shifts pending and rotate those keys inside the
+  // attention kernel (no flush, no copy-on-write, no HBM writes of K).
   void attend(int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q, int64_t n_q_rows, void* o,
-              float* lse, float scale, cudaStream_t st) {
+              float* lse, float scale, cudaStream_t st, bool fused = false) {
     if (n_segs < 0 || (n_segs > 0 && !segs)) fail(AKV_ERR_ARG, "bad segment list");
     if (layer < 0 || layer >= cfg.n_layers) fail(AKV_ERR_RANGE, "layer outside the pools");
     if (n_q_rows < 0 || n_q_rows > kI32Max) fail(AKV_ERR_RANGE, "bad query row count");
@@ -1031,19 +1039,21 @@ struct akv_ctx {
     for (int32_t i = 0; i < n_segs; ++i) ids.push_back(segs[i].seq);
     std::sort(ids.begin(), ids.end());
     ids.erase(std::unique(ids.begin(), ids.end()), ids.end());
-    flush(ids, st);
+    if (!fused) flush(ids, st);
     if (n_segs == 0) return;
 
     const int G = cfg.n_q_heads / cfg.n_kv_heads;
     const int tpt = 128 / G;                   // query tokens per 128-row tile
     const int rpt = 128 / cfg.page_size;       // runs per 128-key tile
     std::vector<akv::AttnRun> runs;
+    std::vector<int32_t> run_shift;  // fused: pending shift per run
     std::vector<akv::AttnSeg> tab;
     std::vector<akv::AttnWork> work;
     double flops = 0.0;
     const int dqk = cfg.layout == AKV_LAYOUT_MLA ? cfg.d_v + cfg.d_rot : cfg.d_rot;
     for (int32_t i = 0; i < n_segs; ++i) {
-      SegPlan sp = plan_segment(segs[i]);
+      SegPlan sp = plan_segment(segs[i], fused);
+      if (fused) run_shift.insert(run_shift.end(), sp.shift.begin(), sp.shift.end());
       if (sp.kv_len > kI32Max) fail(AKV_ERR_RANGE, "segment too long");
       akv::AttnSeg s{};
       s.run_off = int32_t(runs.size());
@@ -1082,6 +1092,26 @@ struct akv_ctx {
       }
       runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
       tab.push_back(s);
+    }
+    // Fused rotation: distinct pending shifts -> angle table rows; runs
+    // without a shift keep -1 (their keys are read as stored).
+    std::vector<int32_t> run_didx, shifts;
+    bool rotate = false;
+    if (fused) {
+      std::unordered_map<int32_t, int32_t> didx;
+      run_didx.resize(run_shift.size(), -1);
+      for (size_t r = 0; r < run_shift.size(); ++r) {
+        if (run_shift[r] == 0) continue;
+        auto it = didx.find(run_shift[r]);
+        if (it == didx.end()) {
+          it = didx.emplace(run_shift[r], int32_t(shifts.size())).first;
+          shifts.push_back(run_shift[r]);
+        }
+        run_didx[r] = it->second;
+      }
+      rotate = !shifts.empty();
+      if (rotate && cfg.layout == AKV_LAYOUT_MLA)
+        fail(AKV_ERR_ARG, "fused rotation is implemented for the GQA layout; flush, then attend");
     }
     if (meta) return;
     const bool mla = cfg.layout == AKV_LAYOUT_MLA;
@@ -1135,11 +1165,17 @@ struct akv_ctx {
     void* dwork = nullptr;
     void* dcomb = nullptr;
     void* dcta = nullptr;
+    void* ddidx = nullptr;
+    void* dcs = nullptr;
+    const std::vector<float2> cs = rotate ? angle_table(shifts) : std::vector<float2>();
+    if (!rotate) run_didx.clear();
     up.upload({{runs.data(), runs.size() * sizeof(akv::AttnRun), &druns},
                {tab.data(), tab.size() * sizeof(akv::AttnSeg), &dsegs},
                {work.data(), work.size() * sizeof(akv::AttnWork), &dwork},
                {comb.data(), comb.size() * sizeof(akv::CombineItem), &dcomb},
-               {cta_units.data(), cta_units.size() * sizeof(int32_t), &dcta}},
+               {cta_units.data(), cta_units.size() * sizeof(int32_t), &dcta},
+               {run_didx.data(), run_didx.size() * sizeof(int32_t), &ddidx},
+               {cs.data(), cs.size() * sizeof(float2), &dcs}},
               st);
     p.runs = static_cast<akv::AttnRun*>(druns);
     p.segs = static_cast<akv::AttnSeg*>(dsegs);
@@ -1159,6 +1195,10 @@ struct akv_ctx {
     p.page = cfg.page_size;
     p.width = mla ? cfg.d_v / 2 : cfg.d_v;
     p.dv = cfg.d_v;
+    p.fused = rotate ? 1 : 0;
+    p.run_didx = rotate ? static_cast<const int32_t*>(ddidx) : nullptr;
+    p.cs = rotate ? static_cast<const float2*>(dcs) : nullptr;
+    p.rope_half = cfg.rope_layout == AKV_ROPE_HALF ? 1 : 0;
     const int tiles_per_item = mla ? 1 : 2;
     p.comb = static_cast<akv::CombineItem*>(dcomb);
     p.comb_tiles = tiles_per_item;
@@ -1373,6 +1413,11 @@ akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream) {
 akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
                       int64_t n_q_rows, void* o, float* lse, float scale, void* stream) {
   return guard(ctx, [&] { ctx->attend(layer, segs, n_segs, q, n_q_rows, o, lse, scale, as_stream(stream)); });
+}
+
+akv_status akv_attend_fused(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
+                            int64_t n_q_rows, void* o, float* lse, float scale, void* stream) {
+  return guard(ctx, [&] { ctx->attend(layer, segs, n_segs, q, n_q_rows, o, lse, scale, as_stream(stream), true); });
 }
 
 akv_status akv_debug_rotate_f32(akv_ctx* ctx, const int32_t* runs, int32_t n_runs, float* out, void* stream) {

@@ -27,31 +27,10 @@
 #include <cuda_bf16.h>
 
 #include "akv_internal.h"
+#include "rope_rot.cuh"
 
 namespace akv {
 namespace {
-
-__device__ __forceinline__ float2 rot2(uint32_t xy, float c, float s) {
-  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&xy);
-  const float2 f = __bfloat1622float2(b);
-  return make_float2(fmaf(c, f.x, -s * f.y), fmaf(s, f.x, c * f.y));
-}
-
-__device__ __forceinline__ uint32_t pack(float2 y) {
-  __nv_bfloat162 r = __floats2bfloat162_rn(y.x, y.y);
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-// Both halves of a (j, j + D/2) pair: a holds first-half elements e, e+1; b
-// the matching second-half elements.
-__device__ __forceinline__ void rot_halves(uint32_t a, uint32_t b, float c0, float s0, float c1, float s1,
-                                           float2& ya, float2& yb) {
-  __nv_bfloat162 ab = *reinterpret_cast<__nv_bfloat162*>(&a);
-  __nv_bfloat162 bb = *reinterpret_cast<__nv_bfloat162*>(&b);
-  const float2 fa = __bfloat1622float2(ab), fb = __bfloat1622float2(bb);
-  ya = make_float2(fmaf(c0, fa.x, -s0 * fb.x), fmaf(c1, fa.y, -s1 * fb.y));
-  yb = make_float2(fmaf(s0, fa.x, c0 * fb.x), fmaf(s1, fa.y, c1 * fb.y));
-}
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
@@ -112,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) repos_interleaved_kernel(uint4* __re
           o[0] = make_float4(y0.x, y0.y, y1.x, y1.y);
           o[1] = make_float4(y2.x, y2.y, y3.x, y3.y);
         } else {
-          __stcs(dst + (h * page + lo) * V + rem, make_uint4(pack(y0), pack(y1), pack(y2), pack(y3)));
+          __stcs(dst + (h * page + lo) * V + rem, make_uint4(pack_rot(y0), pack_rot(y1), pack_rot(y2), pack_rot(y3)));
         }
       }
     }
@@ -162,8 +141,8 @@ __global__ void __launch_bounds__(kThreads) repos_half_kernel(uint4* __restrict_
         ob[0] = make_float4(yb[0].x, yb[0].y, yb[1].x, yb[1].y);
         ob[1] = make_float4(yb[2].x, yb[2].y, yb[3].x, yb[3].y);
       } else {
-        __stcs(dst + off, make_uint4(pack(ya[0]), pack(ya[1]), pack(ya[2]), pack(ya[3])));
-        __stcs(dst + off + HV, make_uint4(pack(yb[0]), pack(yb[1]), pack(yb[2]), pack(yb[3])));
+        __stcs(dst + off, make_uint4(pack_rot(ya[0]), pack_rot(ya[1]), pack_rot(ya[2]), pack_rot(ya[3])));
+        __stcs(dst + off + HV, make_uint4(pack_rot(yb[0]), pack_rot(yb[1]), pack_rot(yb[2]), pack_rot(yb[3])));
       }
     }
   }

@@ -39,12 +39,15 @@
 
 #include "akv_internal.h"
 #include "attn_merge.cuh"
+#include "rope_rot.cuh"
 #include "sm100_ptx.cuh"
 
 namespace akv {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 320;       // producer, MMA, 2 x 4 softmax warps
+constexpr int kThreadsFused = 384;  // + 2 warps rotating K tiles in shared memory
+constexpr int kRotThreads = 64;
 constexpr int kTileKeys = 128;
 constexpr int kRows = 128;
 constexpr uint32_t kTmemCols = 512;
@@ -76,7 +79,8 @@ enum Bar {
   kBarO0 = kBarP0 + 2,
   kBarQFree = kBarO0 + 2,  // committed after a unit's last QK MMA: Q buffers may be reloaded
   kBarFin,
-  kNumBars
+  kBarRdy0,  // + slot, fused rotation only: the slot's tile is ready for the MMA (K rotated)
+  kNumBars = kBarRdy0 + kSlots
 };
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
@@ -203,7 +207,7 @@ __device__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, vol
 // (cs[T] events so far).  The first PV of a unit overwrites O_T; it waits for
 // P_T(0) of that unit, which the softmax threads arrive only after reading
 // out the previous unit's O_T, so O_T is free by then.
-template <int D>
+template <int D, bool kFused>
 __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
                           volatile int* abort_flag) {
   using L = Layout<D>;
@@ -213,6 +217,8 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
   constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, D, true);
   auto slot_of = [](int ld) { return ld % kSlots; };
   auto full_parity = [](int ld) { return (ld / kSlots) & 1; };
+  // a slot's tile may be read once TMA has landed it (and, with fused rotation, once K is rotated)
+  auto ready_bar = [&](int ld) { return bar((kFused ? kBarRdy0 : kBarFull0) + ld % kSlots); };
   int ld0 = 0, cs0 = 0, cs1 = 0;
   bool ok = true;
   const uint64_t qd0 = ptx::smem_desc(sbase + L::kQ, 16, 1024), qd1 = ptx::smem_desc(sbase + L::kQ + L::kTile, 16, 1024);
@@ -231,7 +237,7 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
         if (ok && j >= 1 && j - 1 < nt) {
           if (!v_ready) {
             const int ld = ld0 + 2 * (j - 1) + 1;
-            ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, kWaitLimitNs);
             v_ready = true;
           }
           if (ok) ok = ptx::mbar_wait(bar(kBarP0 + t), (cs + j - 1) & 1, abort_flag, kWaitLimitNs);
@@ -250,7 +256,7 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
         if (ok && j < nt) {
           if (!k_ready) {
             const int ld = ld0 + 2 * j;
-            ok = ptx::mbar_wait(bar(kBarFull0 + slot_of(ld)), full_parity(ld), abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, kWaitLimitNs);
             k_ready = true;
             ptx::tc_fence_after();
           }
@@ -283,6 +289,86 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
   // Every MMA issued above has completed before TMEM is released.
   ptx::mma_commit(bar(kBarFin));
   ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs);
+}
+
+// ------------------------------------------------------------ K rotation
+// Fused rotation ([AKV-blog] section 4: rotate keys on their way to the
+// tensor core instead of writing transient position versions to HBM).  Two
+// warps take every ring slot in stream order after TMA has filled it; for a
+// K tile they rotate each key row whose run carries a pending shift by
+// R(delta * theta_j) in shared memory, with the same arithmetic and angle
+// table as repos_rotate (so the bits equal the materialised key), then make
+// the writes visible to the tensor core and arrive on the slot's ready
+// barrier, which the MMA thread waits on instead of the TMA barrier.
+template <int D>
+__device__ void rotate_k(const AttnParams& p, int u0, int u1, uint32_t sbase, uint8_t* smem,
+                         volatile int* abort_flag) {
+  using L = Layout<D>;
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int i = int(threadIdx.x) - kThreads;  // 0 .. kRotThreads - 1
+  const int rpt = kTileKeys / p.page;
+  int page_shift = 4;
+  while ((1 << page_shift) < p.page) ++page_shift;
+  int ld0 = 0;
+  bool ok = true;
+  for (int u = u0; u < u1 && ok; ++u) {
+    const AttnWork w = p.work[u];
+    const AttnSeg seg = p.segs[w.seg];
+    const int span = w.t1 - w.t0;
+    const int n_max = max(min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span));
+    for (int l = 0; l < 2 * n_max; ++l) {
+      const int ld = ld0 + l, slot = ld % kSlots;
+      if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot), (ld / kSlots) & 1, abort_flag, kWaitLimitNs))) break;
+      if ((l & 1) == 0) {
+        uint8_t* tile = smem + L::kSlot + slot * L::kTile;
+#pragma unroll 1
+        for (int rr = i; rr < kTileKeys; rr += kRotThreads) {
+          const int ri = (w.t0 + (l >> 1)) * rpt + (rr >> page_shift);
+          const int didx = ri < seg.n_runs ? p.run_didx[seg.run_off + ri] : -1;
+          if (didx < 0) continue;
+          const float2* cs = p.cs + int64_t(didx) * (D / 2);
+          auto at = [&](int v) {  // 16-byte vector v of row rr (128-byte swizzle, 64-column blocks)
+            return reinterpret_cast<uint4*>(tile + (v >> 3) * L::kBlockBytes + rr * 128 + (((v & 7) ^ (rr & 7)) << 4));
+          };
+          if (!p.rope_half) {
+#pragma unroll 4
+            for (int v = 0; v < D / 8; ++v) {  // pairs 4v .. 4v + 3
+              uint4* q = at(v);
+              const uint4 x = *q;
+              const float4 a = __ldg(reinterpret_cast<const float4*>(cs + 4 * v));
+              const float4 b = __ldg(reinterpret_cast<const float4*>(cs + 4 * v + 2));
+              *q = make_uint4(pack_rot(rot2(x.x, a.x, a.y)), pack_rot(rot2(x.y, a.z, a.w)),
+                              pack_rot(rot2(x.z, b.x, b.y)), pack_rot(rot2(x.w, b.z, b.w)));
+            }
+          } else {
+#pragma unroll 2
+            for (int v = 0; v < D / 16; ++v) {  // dims 8v .. 8v + 7 pair with dims D/2 + 8v ..
+              uint4* qa = at(v);
+              uint4* qb = at(v + D / 16);
+              const uint4 a = *qa, b = *qb;
+              const float4* c4 = reinterpret_cast<const float4*>(cs + 8 * v);
+              const float4 c01 = __ldg(c4), c23 = __ldg(c4 + 1), c45 = __ldg(c4 + 2), c67 = __ldg(c4 + 3);
+              float2 ya[4], yb[4];
+              rot_halves(a.x, b.x, c01.x, c01.y, c01.z, c01.w, ya[0], yb[0]);
+              rot_halves(a.y, b.y, c23.x, c23.y, c23.z, c23.w, ya[1], yb[1]);
+              rot_halves(a.z, b.z, c45.x, c45.y, c45.z, c45.w, ya[2], yb[2]);
+              rot_halves(a.w, b.w, c67.x, c67.y, c67.z, c67.w, ya[3], yb[3]);
+              *qa = make_uint4(pack_rot(ya[0]), pack_rot(ya[1]), pack_rot(ya[2]), pack_rot(ya[3]));
+              *qb = make_uint4(pack_rot(yb[0]), pack_rot(yb[1]), pack_rot(yb[2]), pack_rot(yb[3]));
+            }
+          }
+        }
+        ptx::fence_proxy_async_smem();  // generic-proxy writes -> tensor-core (async proxy) reads
+      }
+      ptx::mbar_arrive(bar(kBarRdy0 + slot));
+    }
+    ld0 += 2 * n_max;
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 4, 0);
+    *abort_flag = 1;
+  }
 }
 
 // Split part of query tile t, row r: if this CTA drew the item's last ticket,
@@ -510,8 +596,9 @@ __device__ void softmax_units(const AttnParams& p, int u0, int u1, int t, uint8_
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_constant__ AttnParams p, int smem_bytes) {
+template <int D, bool kFused>
+__global__ void __launch_bounds__(kFused ? kThreadsFused : kThreads, 1)
+    segment_attn_kernel(const __grid_constant__ AttnParams p, int smem_bytes) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
@@ -529,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   const int u1 = p.cta_units ? p.cta_units[blockIdx.x + 1] : int(blockIdx.x) + 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, (i == kBarP0 || i == kBarP0 + 1) ? 128 : 1);
+    for (int i = 0; i < kNumBars; ++i)
+      ptx::mbar_init(bars + 8u * i, (i == kBarP0 || i == kBarP0 + 1) ? 128 : i >= kBarRdy0 ? kRotThreads : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -552,9 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_kernel(const __grid_
   if (warp == 0) {
     if (lane == 0) produce<D>(p, u0, u1, sbase, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) issue_mma<D>(p, u0, u1, sbase, tmem, abort_flag);
-  } else {
+    if (lane == 0) issue_mma<D, kFused>(p, u0, u1, sbase, tmem, abort_flag);
+  } else if (warp < 10) {
     softmax_units<D>(p, u0, u1, warp < 6 ? 0 : 1, smem, sbase, tmem, abort_flag);
+  } else if (kFused) {
+    rotate_k<D>(p, u0, u1, sbase, smem, abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -574,22 +664,23 @@ int segment_attn_smem_bytes(int dim) {
   return int(Layout<128>::kBytes) + 1024;
 }
 
+namespace {
+template <int D, bool kFused>
+cudaError_t launch_variant(const AttnParams& p, int grid, int smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(segment_attn_kernel<D, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  segment_attn_kernel<D, kFused><<<grid, kFused ? kThreadsFused : kThreads, smem, st>>>(p, smem);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st) {
   if (p.n_work <= 0) return cudaSuccess;
   const int grid = p.cta_units ? p.n_cta : p.n_work;
   const int smem = segment_attn_smem_bytes(dim);
   if (smem < 0) return cudaErrorInvalidValue;
-  cudaError_t e;
-  if (dim == 64) {
-    e = cudaFuncSetAttribute(segment_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    segment_attn_kernel<64><<<grid, kThreads, smem, st>>>(p, smem);
-  } else {
-    e = cudaFuncSetAttribute(segment_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    segment_attn_kernel<128><<<grid, kThreads, smem, st>>>(p, smem);
-  }
-  return cudaGetLastError();
+  if (dim == 64) return p.fused ? launch_variant<64, true>(p, grid, smem, st) : launch_variant<64, false>(p, grid, smem, st);
+  return p.fused ? launch_variant<128, true>(p, grid, smem, st) : launch_variant<128, false>(p, grid, smem, st);
 }
 
 }  // namespace akv

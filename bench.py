@@ -119,12 +119,12 @@ class ClockSampler:
 class Turn:
     """The engine, the resident 32K-token trajectory and the per-step inputs."""
 
-    def __init__(self, seed=0, host_inputs=False, attn_split=0):
+    def __init__(self, seed=0, host_inputs=False, attn_split=0, n_new=2048):
         import torch
         from agentic_kv_cache_gb300 import akv, build, runner, synth
         build.build()
         self.torch, self.akv, self.runner = torch, akv, runner
-        self.w = w = synth.llama8b_32k(seed=seed, fork=True)
+        self.w = w = synth.llama8b_32k(seed=seed, fork=True, n_new=n_new)
         s = w.shape
         self.cfg = akv.config_from_shape(s, w.n_pages)
         self.pools = akv.make_pools(self.cfg)
@@ -149,14 +149,14 @@ class Turn:
         self.flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
         torch.cuda.synchronize()
 
-    def step(self, host=False):
+    def step(self, host=False, fused=False):
         k, v = (self.h_k, self.h_v) if host else (self.new_k, self.new_v)
         names = dict(self.names)
         self.runner.run_ops(self.eng, self.w, kv_source=lambda *_: (k, v), ops=self.step_ops, names=names,
                             stream=self.stream)
         segs = self.runner.engine_segments(self.w, names)
         q, o = (self.h_q, self.h_o) if host else (self.q, self.o)
-        self.eng.attend(0, segs, q, self.nq, o, None, self.w.shape.scale, stream=self.stream)
+        self.eng.attend(0, segs, q, self.nq, o, None, self.w.shape.scale, stream=self.stream, fused=fused)
         self.eng.seq_free(names["F"])
 
     def flush_l2(self):
@@ -250,6 +250,42 @@ def reprefill_equiv(t, reps=3):
     del q, o, k, v
     torch.cuda.empty_cache()
     return {"queries": n, "ms_per_layer": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "flops": flops}
+
+
+def fused_vs_materialised(t, steps=10, warmup=3):
+    """The same turn two ways: flush (repos_rotate into copy-on-write pages) then attend, or
+    akv_attend_fused (keys rotated in shared memory inside the attention kernel, no HBM writes,
+    no copy-on-write).  GPU time per turn from CUDA events on the stream, plus the attention
+    kernel's own time."""
+    torch = t.torch
+    out = {}
+    for fused in (False, True):
+        for _ in range(warmup):
+            t.step(fused=fused)
+            t.flush_l2()
+        torch.cuda.synchronize()
+        t.eng.profile_enable(True)
+        ms = []
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(t.stream)
+            t.step(fused=fused)
+            b.record(t.stream)
+            t.flush_l2()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        stats = t.eng.profile_read()
+        t.eng.profile_enable(False)
+        assert t.eng.check_device_error(t.stream) == 0
+        att, rep = stats["segment_attn"], stats["repos_rotate"]
+        out["fused" if fused else "materialised"] = {
+            "ms_per_turn": sum(ms) / steps,
+            "attn_ms": att["ms"] / max(att["launches"], 1),
+            "attn_TFLOP/s": att["flops"] / max(att["ms"], 1e-9) / 1e9,
+            "repos_ms": rep["ms"] / steps,
+            "repos_bytes_per_turn": rep["bytes"] / steps,
+        }
+    return out
 
 
 def mla_turns(concurrencies=(1, 4, 8, 16), steps=3, warmup=1):
@@ -424,6 +460,12 @@ def gpu_arm(args, rank, world):
     if not args.no_extra:
         line["reprefill_equiv"] = reprefill_equiv(t)
         line["reprefill_equiv"]["turn_cache_path_ms"] = total_ms / args.steps
+        fz = {"turn_2048_queries": fused_vs_materialised(t)}
+        del t
+        torch.cuda.empty_cache()
+        t = Turn(seed=rank, attn_split=args.attn_split, n_new=16)
+        fz["turn_16_queries"] = fused_vs_materialised(t)
+        line["fused_rotation"] = fz
     del t
     torch.cuda.empty_cache()
     if not args.no_sweep:

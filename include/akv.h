@@ -206,6 +206,22 @@ AKV_API akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* se
                       const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
                       void* stream);
 
+/* Segment-batch attention with the rotation fused in ([AKV-blog] section 4,
+ * "Segment-Batch Attention Kernel Architecture": rotate keys in registers /
+ * shared memory on the way to the tensor core, so transient position versions
+ * cost no HBM writes).  Same arguments and results as akv_attend, but pending
+ * shifts stay pending: no flush, no copy-on-write, the pools are only read.
+ * Each key with a pending shift is rotated in shared memory by the same
+ * float32 arithmetic and (cos, sin) table as akv_flush, so its bf16 bits equal
+ * the materialised key's; runs then also break where the shift changes, so
+ * tile composition (and float rounding order) can differ from akv_attend.
+ * GQA layout only: under MLA with pending shifts it returns AKV_ERR_ARG
+ * (flush, then akv_attend).  Without pending shifts it is akv_attend without
+ * the flush. */
+AKV_API akv_status akv_attend_fused(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs,
+                            const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
+                            void* stream);
+
 /* Float32 debug mode of the repos_rotate kernel: rotate rows of the K pool
  * (K_pe under MLA) by given shifts exactly as akv_flush would, but write the
  * unrounded float32 results to `out` instead of rounding them back into the

@@ -84,13 +84,15 @@ class Case:
         kernels.repos_runs(self.kp, runs, s.rope_base, s.rope_layout, out=self.kp)
         self.flush_runs.extend(runs)
 
-    def flush_segments(self):
-        """The flush attention performs: every segment's sequence, increasing id."""
+    def flush_segments(self, engine=True):
+        """The flush attention performs: every segment's sequence, increasing id.  With
+        engine=False only the oracle materialises (the fused path leaves the GPU pools as they are)."""
         ids = sorted({self.names_o[g["seq"]] for g in self.w.segments})
         runs = self.model.flush(ids)
         self._apply_runs(runs)
-        for i in ids:
-            self.eng.flush(i, stream=self.stream)
+        if engine:
+            for i in ids:
+                self.eng.flush(i, stream=self.stream)
         return runs
 
     # ------------------------------------------------------------ pools
@@ -103,14 +105,14 @@ class Case:
         q32 = synth.q_array(self.w, layer)
         return q32, torch.from_numpy(q32).cuda().to(torch.bfloat16)
 
-    def attend_gpu(self, layer=0, with_lse=True):
+    def attend_gpu(self, layer=0, with_lse=True, fused=False):
         s = self.w.shape
         q32, qd = self.queries(layer)
         nq = q32.shape[0]
         o = torch.full((nq, s.n_q_heads, s.d_v), float("nan"), dtype=torch.bfloat16, device="cuda")
         lse = torch.full((nq, s.n_q_heads), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
         segs = runner.engine_segments(self.w, self.names_e)
-        self.eng.attend(layer, segs, qd, nq, o, lse, s.scale, stream=self.stream)
+        self.eng.attend(layer, segs, qd, nq, o, lse, s.scale, stream=self.stream, fused=fused)
         torch.cuda.synchronize()
         assert self.eng.check_device_error(self.stream) == 0
         return q32, o.float().cpu().numpy(), (lse.cpu().numpy() if with_lse else None)

@@ -50,6 +50,18 @@ Rules where the pages are silent (the engine implements the same rules):
   position of token s (or last + 1), counting up.
 * Positions are int32; an operation that would leave int32 fails.
 * Every failing operation leaves the state unchanged.
+* Compaction ([AKV-blog] "Dilemma 2: Memory Fragmentation in Paged Pools":
+  surviving blocks are copied into contiguous physical spans).  The
+  fragmentation of a sequence is the share of the slots of its K pages that do
+  not hold one of its visible tokens: 1 - n_visible / (n_K_pages * page).
+  compact(seq) writes the visible tokens, in logical order, densely into fresh
+  pages (lowest free ids, one K and one V page per `page` tokens, slot =
+  index mod page), with any pending Delta applied to the copied key (so the
+  copy has Delta 0 and position pos + Delta), the value copied unchanged.
+  Dropped tokens leave the logical sequence (nothing can read them again), so
+  later logical indices move down, as after a splice.  The old pages lose the
+  sequence's reference.  New pages are taken before old ones are released, so
+  the pools must hold ceil(n_visible / page) free pages each.
 """
 import heapq
 
@@ -384,6 +396,38 @@ class CacheModel:
                 cur = [t.kp, t.vp, t.slot, t.slot + 1]
                 runs.append(cur)
         return [tuple(r) for r in runs], n
+
+    # -------------------------------------------------------------- compaction
+    def fragmentation(self, seq):
+        """1 - visible tokens / slots of the sequence's K pages (0.0 for an empty sequence)."""
+        toks = self._seq(seq)
+        kps, _ = self._pages(toks)
+        if not kps:
+            return 0.0
+        return 1.0 - sum(1 for t in toks if t.vis) / (len(kps) * self.page)
+
+    def compact(self, seq):
+        """Copy the visible tokens densely into fresh pages; returns the copy list
+        [(src_k, src_v, src_slot, dst_k, dst_v, dst_slot, delta)], one entry per kept token."""
+        toks = self._seq(seq)
+        keep = [t for t in toks if t.vis]
+        need = -(-len(keep) // self.page)
+        if need > self.K.n_free or need > self.V.n_free:
+            raise CacheError("NO_PAGES", f"compaction needs {need} pages")
+        kps, vps = self._pages(toks)
+        out, new = [], []
+        kp = vp = -1
+        for i, t in enumerate(keep):
+            if i % self.page == 0:
+                kp, vp = self.K.alloc(), self.V.alloc()
+            out.append((t.kp, t.vp, t.slot, kp, vp, i % self.page, t.delta))
+            new.append(Tok(kp, vp, i % self.page, t.pos + t.delta))
+        for p in kps:
+            self.K.dec(p)
+        for p in vps:
+            self.V.dec(p)
+        toks[:] = new
+        return out
 
     # ---------------------------------------------------------------- export
     def state(self, seq):

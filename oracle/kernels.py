@@ -35,6 +35,21 @@ def repos_runs(kpool, runs, base, layout="interleaved", out=None):
     return out
 
 
+def compact_copy(kpool, vpool, copies, base, layout="interleaved"):
+    """Apply a compaction copy list [(src_k, src_v, src_slot, dst_k, dst_v, dst_slot, delta)] to
+    copies of both pools (every layer and head): the key row is rotated by its pending delta in
+    float64 and rounded to bfloat16 (copied as is when delta is 0), the value row copied."""
+    ko = np.array(kpool, dtype=np.float64, copy=True)
+    vo = np.array(vpool, dtype=np.float64, copy=True)
+    for sk, sv, ss, dk, dv, ds, delta in copies:
+        row = kpool[:, sk, :, ss, :]
+        if delta:
+            row = bf16.round_bf16(rope.repos(row, np.full(row.shape[:-1], delta), base, layout))
+        ko[:, dk, :, ds, :] = row
+        vo[:, dv, :, ds, :] = vpool[:, sv, :, ss, :]
+    return ko, vo
+
+
 def repos_rows_f64(kpool, layer, page, head, slot, delta, base, layout="interleaved"):
     """Unrounded float64 rotation of single rows (for the fp32-output check)."""
     rows = kpool[layer, page, head, slot, :]

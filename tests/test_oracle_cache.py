@@ -251,3 +251,101 @@ def test_segment_runs_hide_and_query_rules():
     c.repos(s, 20, 100, -10)
     with pytest.raises(CacheError):
         c.segment_runs(s, 100, 4)                          # pending delta must be flushed first
+
+
+# ------------------------------------------------------------- compaction
+def test_compaction_blog_example_64_blocks_every_second_dropped():
+    # [AKV-blog] "Dilemma 2": 64 blocks with every second block dropped leave 32 live pages
+    # among 32 dead ones; compaction copies the survivors into contiguous pages.
+    P = 16
+    c = CacheModel(200, P)
+    s = c.seq_alloc()
+    c.append(s, 64 * P)
+    for b in range(1, 64, 2):
+        c.drop(s, b * P, (b + 1) * P)
+    assert c.fragmentation(s) == 0.5
+    copies = c.compact(s)
+    st = c.state(s)
+    assert len(st["pos"]) == 32 * P and all(st["visible"])
+    # fresh pages are the lowest free ids at the time of the copy: 64 .. 95, filled densely
+    assert st["k_page"] == [64 + i // P for i in range(32 * P)]
+    assert st["slot"] == [i % P for i in range(32 * P)]
+    # survivors keep their positions and order: blocks 0, 2, 4, ...
+    assert st["pos"] == [b * P + j for b in range(0, 64, 2) for j in range(P)]
+    assert [cp[0] for cp in copies] == [b for b in range(0, 64, 2) for _ in range(P)]
+    assert c.fragmentation(s) == 0.0
+    k_rc, v_rc = c.refcounts()
+    assert sum(k_rc[:64]) == 0 and k_rc[64:96] == [1] * 32 and sum(k_rc) == 32
+    assert sum(v_rc) == 32
+
+
+def test_compaction_fuses_pending_shift():
+    P = 8
+    c = CacheModel(32, P)
+    s = c.seq_alloc()
+    c.append(s, 20)
+    c.drop(s, 3, 6)
+    c.repos(s, 6, 20, -3)
+    c.repos(s, 10, 12, 100)
+    copies = c.compact(s)
+    st = c.state(s)
+    want_pos = [0, 1, 2] + [i - 3 for i in range(6, 20)]
+    want_pos[10 - 3] += 100
+    want_pos[11 - 3] += 100
+    assert st["pos"] == want_pos and st["delta"] == [0] * 17
+    assert [cp[6] for cp in copies] == [0, 0, 0] + [-3] * 4 + [97, 97] + [-3] * 8
+
+
+def test_compaction_of_a_fork_leaves_the_parent_alone():
+    P = 16
+    c = CacheModel(64, P)
+    a = c.seq_alloc()
+    c.append(a, 100)
+    b = c.seq_fork(a, 100)
+    c.drop(b, 0, 40)
+    before = c.state(a)
+    c.compact(b)
+    assert c.state(a) == before
+    k_rc, _ = c.refcounts()
+    assert k_rc[:7] == [1] * 7                     # only the parent references its pages now
+    assert c.state(b)["k_page"] == [7 + i // P for i in range(60)]
+
+
+def test_compaction_without_free_pages_changes_nothing():
+    P = 16
+    c = CacheModel(8, P)
+    s = c.seq_alloc()
+    c.append(s, 100)                                # 7 pages, 1 free
+    c.drop(s, 0, 60)                                # 40 visible -> needs 3 fresh pages
+    st, rc = c.state(s), c.refcounts()
+    with pytest.raises(CacheError) as e:
+        c.compact(s)
+    assert e.value.code == "NO_PAGES"
+    assert c.state(s) == st and c.refcounts() == rc
+
+
+def test_compaction_keeps_the_visible_sequence_random():
+    rng = np.random.default_rng(5)
+    for trial in range(20):
+        P = int(rng.choice([4, 8, 16]))
+        c = CacheModel(400, P)
+        s = c.seq_alloc()
+        n = int(rng.integers(1, 300))
+        c.append(s, n)
+        for _ in range(int(rng.integers(0, 6))):
+            a = int(rng.integers(0, n))
+            b = int(rng.integers(a, n + 1))
+            if rng.random() < 0.5:
+                c.drop(s, a, b)
+            else:
+                c.repos(s, a, b, int(rng.integers(-500, 500)))
+        old = c.state(s)
+        vis = [i for i in range(n) if old["visible"][i]]
+        copies = c.compact(s)
+        new = c.state(s)
+        assert len(new["pos"]) == len(vis) == len(copies)
+        assert new["pos"] == [old["pos"][i] + old["delta"][i] for i in vis]
+        assert [(cp[0], cp[2], cp[6]) for cp in copies] == [(old["k_page"][i], old["slot"][i], old["delta"][i])
+                                                           for i in vis]
+        k_rc, v_rc = c.refcounts()
+        assert sum(k_rc) == sum(v_rc) == -(-len(vis) // P)

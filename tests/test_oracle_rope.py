@@ -92,3 +92,20 @@ def test_relative_position_property():
         a = rope.rope(q, n, base) @ rope.rope(k, m, base)
         b = rope.rope(q, n + c, base) @ rope.rope(k, m + c, base)
         assert abs(a - b) < 1e-9
+
+
+def test_compact_copy_rotates_by_the_pending_shift_and_copies_values():
+    # a key stored unrotated (position 0) and moved by delta must equal RoPE at position delta
+    # (closed form of [AKV-blog] section 2); values are copied bit for bit
+    from oracle import bf16, kernels, rope
+    rng = np.random.default_rng(3)
+    for layout in ("interleaved", "half"):
+        k = bf16.round_bf16(rng.standard_normal((1, 4, 2, 8, 64)))
+        v = bf16.round_bf16(rng.standard_normal((1, 4, 2, 8, 32)))
+        copies = [(0, 1, 3, 2, 3, 0, 777), (0, 1, 5, 2, 3, 1, 0)]
+        ko, vo = kernels.compact_copy(k, v, copies, 1.0e4, layout)
+        want = bf16.round_bf16(rope.rope(k[:, 0, :, 3, :], np.full((1, 2), 777.0), 1.0e4, layout))
+        assert np.array_equal(ko[:, 2, :, 0, :], want)
+        assert np.array_equal(ko[:, 2, :, 1, :], k[:, 0, :, 5, :])
+        assert np.array_equal(vo[:, 3, :, 0, :], v[:, 1, :, 3, :])
+        assert np.array_equal(vo[:, 3, :, 1, :], v[:, 1, :, 5, :])

@@ -49,7 +49,7 @@ class KernelStats(ctypes.Structure):
                 ("flops", ctypes.c_double * 4)]
 
 
-KERNEL_NAMES = ("kv_write", "repos_rotate", "segment_attn")
+KERNEL_NAMES = ("kv_write", "repos_rotate", "segment_attn", "compact_copy")
 
 _lib = None
 
@@ -78,6 +78,8 @@ def load(path=LIB_PATH):
         "akv_flush": [P, I32, P],
         "akv_attend": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
         "akv_attend_fused": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
+        "akv_fragmentation": [P, I32, ctypes.POINTER(ctypes.c_double)],
+        "akv_compact": [P, I32, P],
         "akv_debug_rotate_f32": [P, P, I32, P, P],
         "akv_export_state": [P, I32, P, P, P, P, P, P],
         "akv_refcounts": [P, P, P],
@@ -213,6 +215,14 @@ class Engine:
             arr[i].n_hide = hide.size // 2
             arr[i].reserved = 0
         return arr, keep
+
+    def fragmentation(self, seq):
+        out = ctypes.c_double()
+        self._check(self.lib.akv_fragmentation(self.h, seq, ctypes.byref(out)))
+        return out.value
+
+    def compact(self, seq, stream=None):
+        self._check(self.lib.akv_compact(self.h, seq, _stream(stream)))
 
     def attend(self, layer, segs, q, n_q_rows, o, lse=None, scale=1.0, stream=None, fused=False):
         """akv_attend (flush, then attention), or with fused=True akv_attend_fused (pending shifts

@@ -26,6 +26,20 @@ struct RunDesc {
   int32_t didx;
 };
 
+// One compaction copy run: n consecutive slots from (src_k, src_v) at src_lo
+// to (dst_k, dst_v) at dst_lo; the key rows are rotated by shift table row
+// didx (-1: copied as they are).
+struct CopyRun {
+  int32_t src_k;
+  int32_t src_v;
+  int32_t dst_k;
+  int32_t dst_v;
+  int32_t src_lo;
+  int32_t dst_lo;
+  int32_t n;
+  int32_t didx;
+};
+
 // One attention run: rows [lo, hi) of K page kp / V page vp hold the
 // segment's entries es .. es + (hi - lo) - 1.
 struct AttnRun {
@@ -115,6 +129,10 @@ __host__ __device__ inline int64_t partial_floats(int tiles, int width) { return
 // Launchers; each returns the launch's cudaError_t.
 cudaError_t launch_kv_write(const void* src, void* pool, const int32_t* rows, int64_t n, int n_layers,
                             int heads, int dim, int page, int64_t n_pages, cudaStream_t st);
+
+cudaError_t launch_compact_copy(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs,
+                                int n_layers, int heads, int d_rot, int d_v, int page, int64_t n_pages, bool half,
+                                int n_sm, cudaStream_t st);
 
 cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int page, int64_t n_pages,

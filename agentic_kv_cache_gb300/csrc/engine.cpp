@@ -253,7 +253,7 @@ void encode_map(CUtensorMap* m, void* base, int rank, const uint64_t* dims, cons
   if (r != CUDA_SUCCESS) fail(AKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
 }
 
-enum KernelId { kKvWrite = 0, kRepos = 1, kAttn = 2 };
+enum KernelId { kKvWrite = 0, kRepos = 1, kAttn = 2, kCompact = 3 };
 
 }  // namespace
 
@@ -585,6 +585,85 @@ struct akv_ctx {
     std::vector<Tok>().swap(toks);
     live[sid] = 0;
     free_ids.push(sid);
+  }
+
+  // ------------------------------------------------------------ compaction
+  // [AKV-blog] "Dilemma 2: Memory Fragmentation in Paged Pools".  The share
+  // of the slots of the sequence's K pages that hold none of its visible tokens.
+  double fragmentation(int32_t sid) {
+    auto& toks = seq(sid);
+    std::vector<int32_t> kps, vps;
+    pages_of(toks, 0, toks.size(), kps, vps);
+    if (kps.empty()) return 0.0;
+    int64_t vis = 0;
+    for (const Tok& t : toks) vis += t.vis;
+    return 1.0 - double(vis) / (double(kps.size()) * cfg.page_size);
+  }
+
+  // Visible tokens, in logical order, copied densely into fresh pages (any
+  // pending shift applied to the copied key); dropped tokens leave the
+  // sequence; the old pages lose its reference.
+  void compact(int32_t sid, cudaStream_t st) {
+    auto& toks = seq(sid);
+    int64_t n_vis = 0;
+    for (const Tok& t : toks) n_vis += t.vis;
+    const int64_t need = (n_vis + cfg.page_size - 1) / cfg.page_size;
+    if (need > K.n_free() || need > V.n_free()) fail(AKV_ERR_NO_PAGES, "compaction needs %lld pages", (long long)need);
+    std::vector<int32_t> kps, vps;
+    pages_of(toks, 0, toks.size(), kps, vps);
+    std::vector<Tok> out;
+    out.reserve(size_t(n_vis));
+    std::vector<akv::CopyRun> runs;
+    std::vector<int32_t> shifts;
+    std::unordered_map<int32_t, int32_t> didx;
+    int32_t dk = -1, dv = -1;
+    int64_t b = 0;
+    for (const Tok& t : toks) {
+      if (!t.vis) continue;
+      const int32_t ds = int32_t(out.size() % size_t(cfg.page_size));
+      if (ds == 0) {
+        dk = K.alloc();
+        dv = V.alloc();
+      }
+      int32_t di = -1;
+      if (t.delta != 0) {
+        auto it = didx.find(t.delta);
+        if (it == didx.end()) {
+          it = didx.emplace(t.delta, int32_t(shifts.size())).first;
+          shifts.push_back(t.delta);
+        }
+        di = it->second;
+      }
+      akv::CopyRun* last = runs.empty() ? nullptr : &runs.back();
+      if (last && last->src_k == t.kp && last->src_v == t.vp && last->src_lo + last->n == t.slot && last->didx == di &&
+          last->dst_k == dk && last->dst_lo + last->n == ds) {
+        ++last->n;
+      } else {
+        runs.push_back(akv::CopyRun{t.kp, t.vp, dk, dv, t.slot, ds, 1, di});
+      }
+      const int32_t pos = int32_t(t.eff());
+      out.push_back(Tok{dk, dv, ds, pos, 0, 1});
+      b = std::max<int64_t>(b, std::abs(int64_t(pos)));
+    }
+    for (int32_t q : kps) K.dec(q);
+    for (int32_t q : vps) V.dec(q);
+    toks.swap(out);
+    bound[sid] = b;
+    if (meta || runs.empty()) return;
+    const std::vector<float2> cs = angle_table(shifts);
+    void* druns = nullptr;
+    void* dcs = nullptr;
+    up.upload({{runs.data(), runs.size() * sizeof(akv::CopyRun), &druns}, {cs.data(), cs.size() * sizeof(float2), &dcs}},
+              st);
+    Timed tm;
+    const double bytes = 2.0 * double(n_vis) * cfg.n_layers * cfg.n_kv_heads * (cfg.d_rot + cfg.d_v) * 2.0;
+    begin_timed(kCompact, bytes, 0.0, st, tm);
+    cuda_check(akv::launch_compact_copy(kpool, vpool, static_cast<akv::CopyRun*>(druns), static_cast<float2*>(dcs),
+                                        int(runs.size()), cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.d_v,
+                                        cfg.page_size, cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, n_sm, st),
+               "compact_copy launch");
+    end_timed(tm, st);
+    up.done(st);
   }
 
   // ----------------------------------------------------------------- flush
@@ -1413,6 +1492,17 @@ akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream) {
 akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
                       int64_t n_q_rows, void* o, float* lse, float scale, void* stream) {
   return guard(ctx, [&] { ctx->attend(layer, segs, n_segs, q, n_q_rows, o, lse, scale, as_stream(stream)); });
+}
+
+akv_status akv_fragmentation(akv_ctx* ctx, int32_t seq, double* frac_out) {
+  return guard(ctx, [&] {
+    if (!frac_out) fail(AKV_ERR_ARG, "null output");
+    *frac_out = ctx->fragmentation(seq);
+  });
+}
+
+akv_status akv_compact(akv_ctx* ctx, int32_t seq, void* stream) {
+  return guard(ctx, [&] { ctx->compact(seq, as_stream(stream)); });
 }
 
 akv_status akv_attend_fused(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,

@@ -57,6 +57,8 @@ def run_ops(engine, w, kv_source=None, stream=None, ops=None, names=None):
             engine.splice(names[op[1]], op[2], op[3], op[4], k, v, stream=stream)
         elif kind == "flush":
             engine.flush(names[op[1]], stream=stream)
+        elif kind == "compact":
+            engine.compact(names[op[1]], stream=stream)
         else:
             raise ValueError(f"unknown op {kind}")
     return names

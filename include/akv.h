@@ -121,9 +121,9 @@ typedef struct akv_segment {
 
 /* Per-kernel launch statistics collected while profiling is enabled. */
 typedef struct akv_kernel_stats {
-  int64_t launches[4];   /* [0] kv_write  [1] repos_rotate  [2] segment_attn  [3] reserved */
+  int64_t launches[4];   /* [0] kv_write  [1] repos_rotate  [2] segment_attn  [3] compact_copy */
   double ms[4];          /* summed CUDA-event time of those launches, milliseconds */
-  double bytes[4];       /* algorithmic bytes moved (kv_write, repos_rotate) */
+  double bytes[4];       /* algorithmic bytes moved (kv_write, repos_rotate, compact_copy) */
   double flops[4];       /* algorithmic FLOPs (segment_attn) */
 } akv_kernel_stats;
 
@@ -205,6 +205,24 @@ AKV_API akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream);
 AKV_API akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs,
                       const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
                       void* stream);
+
+/* Fragmentation of a sequence's pages ([AKV-blog] "Dilemma 2: Memory
+ * Fragmentation in Paged Pools"): 1 - visible tokens / (K pages * page_size),
+ * the share of the slots of its K pages holding none of its visible tokens
+ * (0 for an empty sequence).  The page's policy (compact above 40 %) is the
+ * caller's. */
+AKV_API akv_status akv_fragmentation(akv_ctx* ctx, int32_t seq, double* frac_out);
+
+/* Compaction (same passage: surviving blocks copied into contiguous physical
+ * spans; the compact_copy kernel).  The visible tokens of `seq`, in logical
+ * order, are copied densely into fresh pages (lowest free ids, one K and one
+ * V page per page_size tokens); a pending shift is applied to the copied key
+ * in the same pass (position += shift, shift 0), the value is copied as is.
+ * Dropped tokens leave the logical sequence, so later logical indices move
+ * down as after a splice.  The old pages lose the sequence's reference (pages
+ * shared with other sequences stay with them).  Needs ceil(visible /
+ * page_size) free pages in each pool (AKV_ERR_NO_PAGES, state unchanged). */
+AKV_API akv_status akv_compact(akv_ctx* ctx, int32_t seq, void* stream);
 
 /* Segment-batch attention with the rotation fused in ([AKV-blog] section 4,
  * "Segment-Batch Attention Kernel Architecture": rotate keys in registers /

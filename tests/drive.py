@@ -20,6 +20,8 @@ def oracle_run_ops(model, w, ops=None, names=None):
             model.splice(names[op[1]], op[2], op[3], op[4])
         elif kind == "flush":
             model.flush([names[op[1]]])
+        elif kind == "compact":
+            model.compact(names[op[1]])
         else:
             raise ValueError(kind)
     return names

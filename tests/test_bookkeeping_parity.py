@@ -107,7 +107,8 @@ def test_random_operations_match_oracle(seed):
         live = sorted(model.seqs)
         s = live[int(rng.integers(len(live)))]
         n = len(model.seqs[s])
-        op = rng.choice(["append", "fork", "drop", "repos", "splice", "flush", "flush_all", "free", "seg", "bad"])
+        op = rng.choice(["append", "fork", "drop", "repos", "splice", "flush", "flush_all", "free", "seg", "bad",
+                         "compact"])
         if op == "append":
             apply_both(eng, model, "append", (s, int(rng.integers(0, 3 * P))))
         elif op == "fork" and len(live) < 8:
@@ -173,6 +174,10 @@ def test_random_operations_match_oracle(seed):
         elif op == "bad":
             apply_both(eng, model, "drop", (s, -1, 2))
             apply_both(eng, model, "repos", (s, 0, n + 1, 1))
+        elif op == "compact":
+            assert eng.fragmentation(s) == model.fragmentation(s)
+            apply_both(eng, model, "compact", (s,))
+            assert eng.fragmentation(s) == model.fragmentation(s)
         # full comparison after every step
         for sid in model.seqs:
             a, b = eng.export_state(sid), model.state(sid)
@@ -181,3 +186,22 @@ def test_random_operations_match_oracle(seed):
         ke, ve = eng.refcounts()
         ko, vo = model.refcounts()
         assert np.array_equal(ke, ko) and np.array_equal(ve, vo), (step, op)
+
+
+@pytest.mark.parametrize("name,make", WORKLOADS, ids=[n for n, _ in WORKLOADS])
+def test_compaction_matches_oracle(name, make):
+    # every live sequence compacted in turn after the workload's operations (pending shifts
+    # included); each step must agree, NO_PAGES included
+    w = make()
+    w.n_pages = int(w.n_pages * 1.6) + 64
+    eng, model = engine_for(w), oracle_model(w)
+    ne = runner.run_ops(eng, w)
+    no = oracle_run_ops(model, w)
+    for name_ in sorted(no):
+        sid = no[name_]
+        if sid not in model.seqs:
+            continue
+        assert eng.fragmentation(sid) == model.fragmentation(sid)
+        apply_both(eng, model, "compact", (sid,))
+        assert_same_state(eng, model, ne, no)
+        assert eng.fragmentation(sid) == model.fragmentation(sid)

@@ -28,87 +28,78 @@ template <int D, bool kHalf>
 __global__ void __launch_bounds__(kThreads) compact_copy_kernel(uint4* __restrict__ kpool, uint4* __restrict__ vpool,
                                                                const CopyRun* __restrict__ runs,
                                                                const float2* __restrict__ cs, int n_runs, int n_layers,
-                                                               int heads, int page, int64_t n_pages, int dv) {
-  constexpr int VK = D / 8;  // 16-byte vectors per K row
-  const int VV = dv / 8;     // ... per V row
+                                                               int heads, int page, int64_t n_pages, int vv_shift) {
+  constexpr int VK = D / 8;                  // 16-byte vectors per K row
+  constexpr int W = kHalf ? VK / 2 : VK;     // K work items per row: vectors, or (v, v + VK/2) pairs
+  const int VV = 1 << vv_shift;              // vectors per V row
   const int64_t kpage = int64_t(heads) * page * VK, vpage = int64_t(heads) * page * VV;
   const int64_t units = int64_t(n_layers) * n_runs;
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int r = int(u % n_runs);
     const int64_t layer = u / n_runs;
     const CopyRun cr = runs[r];
-    // ---- K rows: rotated when the run carries a shift, else copied
+    // ---- K rows: rotated when the run carries a shift, else copied.  A head's
+    // rows are contiguous in a page; threads walk (row, vector) of one head and
+    // kUnroll heads are in flight at once.
     {
-      const uint4* src = kpool + (layer * n_pages + cr.src_k) * kpage;
-      uint4* dst = kpool + (layer * n_pages + cr.dst_k) * kpage;
+      const uint4* src = kpool + (layer * n_pages + cr.src_k) * kpage + cr.src_lo * VK;
+      uint4* dst = kpool + (layer * n_pages + cr.dst_k) * kpage + cr.dst_lo * VK;
       const float2* cs_row = cr.didx >= 0 ? cs + int64_t(cr.didx) * (D / 2) : nullptr;
-      constexpr int W = kHalf ? VK / 2 : VK;  // work items per row: vectors, or (v, v + VK/2) pairs
-      const int per_head = cr.n * W, total = heads * per_head;
-      for (int base = 0; base < total; base += kThreads * kUnroll) {
-        uint4 x[kUnroll], y[kUnroll];
-        int soff[kUnroll], doff[kUnroll];
+      const int per_head = cr.n * W;
+      for (int t = int(threadIdx.x); t < per_head; t += kThreads) {
+        const int row = t / W, v = t % W, off = row * VK + v;
+        for (int h0 = 0; h0 < heads; h0 += kUnroll) {
+          uint4 x[kUnroll], y[kUnroll];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          const int idx = base + k * kThreads + int(threadIdx.x);
-          soff[k] = -1;
-          if (idx < total) {
-            const int h = idx / per_head, rem = idx - h * per_head, row = rem / W, v = rem % W;
-            soff[k] = (h * page + cr.src_lo + row) * VK + v;
-            doff[k] = (h * page + cr.dst_lo + row) * VK + v;
-            x[k] = __ldcs(src + soff[k]);
-            if (kHalf) y[k] = __ldcs(src + soff[k] + VK / 2);
+          for (int k = 0; k < kUnroll; ++k) {
+            if (h0 + k < heads) {
+              x[k] = __ldcs(src + int64_t(h0 + k) * page * VK + off);
+              if (kHalf) y[k] = __ldcs(src + int64_t(h0 + k) * page * VK + off + VK / 2);
+            }
           }
-        }
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          if (soff[k] < 0) continue;
-          if (!cs_row) {
-            __stcs(dst + doff[k], x[k]);
-            if (kHalf) __stcs(dst + doff[k] + VK / 2, y[k]);
-            continue;
-          }
-          const int v = soff[k] % VK;
-          if constexpr (!kHalf) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v));
-            const float4 b = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v + 2));
-            __stcs(dst + doff[k], make_uint4(pack_rot(rot2(x[k].x, a.x, a.y)), pack_rot(rot2(x[k].y, a.z, a.w)),
-                                             pack_rot(rot2(x[k].z, b.x, b.y)), pack_rot(rot2(x[k].w, b.z, b.w))));
-          } else {
-            const float4* c4 = reinterpret_cast<const float4*>(cs_row + 8 * v);
-            const float4 c01 = __ldg(c4), c23 = __ldg(c4 + 1), c45 = __ldg(c4 + 2), c67 = __ldg(c4 + 3);
-            float2 ya[4], yb[4];
-            rot_halves(x[k].x, y[k].x, c01.x, c01.y, c01.z, c01.w, ya[0], yb[0]);
-            rot_halves(x[k].y, y[k].y, c23.x, c23.y, c23.z, c23.w, ya[1], yb[1]);
-            rot_halves(x[k].z, y[k].z, c45.x, c45.y, c45.z, c45.w, ya[2], yb[2]);
-            rot_halves(x[k].w, y[k].w, c67.x, c67.y, c67.z, c67.w, ya[3], yb[3]);
-            __stcs(dst + doff[k], make_uint4(pack_rot(ya[0]), pack_rot(ya[1]), pack_rot(ya[2]), pack_rot(ya[3])));
-            __stcs(dst + doff[k] + VK / 2,
-                   make_uint4(pack_rot(yb[0]), pack_rot(yb[1]), pack_rot(yb[2]), pack_rot(yb[3])));
+          for (int k = 0; k < kUnroll; ++k) {
+            if (h0 + k >= heads) continue;
+            uint4* d = dst + int64_t(h0 + k) * page * VK + off;
+            if (!cs_row) {
+              __stcs(d, x[k]);
+              if (kHalf) __stcs(d + VK / 2, y[k]);
+            } else if constexpr (!kHalf) {
+              const float4 a = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v));
+              const float4 b = __ldg(reinterpret_cast<const float4*>(cs_row + 4 * v + 2));
+              __stcs(d, make_uint4(pack_rot(rot2(x[k].x, a.x, a.y)), pack_rot(rot2(x[k].y, a.z, a.w)),
+                                   pack_rot(rot2(x[k].z, b.x, b.y)), pack_rot(rot2(x[k].w, b.z, b.w))));
+            } else {
+              const float4* c4 = reinterpret_cast<const float4*>(cs_row + 8 * v);
+              const float4 c01 = __ldg(c4), c23 = __ldg(c4 + 1), c45 = __ldg(c4 + 2), c67 = __ldg(c4 + 3);
+              float2 ya[4], yb[4];
+              rot_halves(x[k].x, y[k].x, c01.x, c01.y, c01.z, c01.w, ya[0], yb[0]);
+              rot_halves(x[k].y, y[k].y, c23.x, c23.y, c23.z, c23.w, ya[1], yb[1]);
+              rot_halves(x[k].z, y[k].z, c45.x, c45.y, c45.z, c45.w, ya[2], yb[2]);
+              rot_halves(x[k].w, y[k].w, c67.x, c67.y, c67.z, c67.w, ya[3], yb[3]);
+              __stcs(d, make_uint4(pack_rot(ya[0]), pack_rot(ya[1]), pack_rot(ya[2]), pack_rot(ya[3])));
+              __stcs(d + VK / 2, make_uint4(pack_rot(yb[0]), pack_rot(yb[1]), pack_rot(yb[2]), pack_rot(yb[3])));
+            }
           }
         }
       }
     }
-    // ---- V rows: copied
+    // ---- V rows: copied, the same walk
     {
-      const uint4* src = vpool + (layer * n_pages + cr.src_v) * vpage;
-      uint4* dst = vpool + (layer * n_pages + cr.dst_v) * vpage;
-      const int per_head = cr.n * VV, total = heads * per_head;
-      for (int base = 0; base < total; base += kThreads * kUnroll) {
-        uint4 x[kUnroll];
-        int doff[kUnroll];
+      const uint4* src = vpool + (layer * n_pages + cr.src_v) * vpage + int64_t(cr.src_lo) * VV;
+      uint4* dst = vpool + (layer * n_pages + cr.dst_v) * vpage + int64_t(cr.dst_lo) * VV;
+      const int per_head = cr.n << vv_shift;
+      constexpr int kU = 2 * kUnroll;  // a plain copy holds twice as many vectors in flight
+      for (int t = int(threadIdx.x); t < per_head; t += kThreads) {
+        for (int h0 = 0; h0 < heads; h0 += kU) {
+          uint4 x[kU];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          const int idx = base + k * kThreads + int(threadIdx.x);
-          doff[k] = -1;
-          if (idx < total) {
-            const int h = idx / per_head, rem = idx - h * per_head, row = rem / VV, v = rem % VV;
-            x[k] = __ldcs(src + (h * page + cr.src_lo + row) * VV + v);
-            doff[k] = (h * page + cr.dst_lo + row) * VV + v;
-          }
+          for (int k = 0; k < kU; ++k)
+            if (h0 + k < heads) x[k] = __ldcs(src + int64_t(h0 + k) * page * VV + t);
+#pragma unroll
+          for (int k = 0; k < kU; ++k)
+            if (h0 + k < heads) __stcs(dst + int64_t(h0 + k) * page * VV + t, x[k]);
         }
-#pragma unroll
-        for (int k = 0; k < kUnroll; ++k)
-          if (doff[k] >= 0) __stcs(dst + doff[k], x[k]);
       }
     }
   }
@@ -117,10 +108,13 @@ __global__ void __launch_bounds__(kThreads) compact_copy_kernel(uint4* __restric
 template <int D, bool kHalf>
 cudaError_t launch_variant(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs, int n_layers,
                            int heads, int page, int64_t n_pages, int dv, int n_sm, cudaStream_t st) {
+  int vv_shift = 0;
+  while ((8 << vv_shift) < dv) ++vv_shift;
+  if ((8 << vv_shift) != dv) return cudaErrorInvalidValue;  // d_v must be 8 x a power of two
   const int64_t units = int64_t(n_layers) * n_runs;
   const int grid = int(units < int64_t(n_sm) * 8 ? units : int64_t(n_sm) * 8);
   compact_copy_kernel<D, kHalf><<<grid, kThreads, 0, st>>>(static_cast<uint4*>(kpool), static_cast<uint4*>(vpool), runs,
-                                                           cs, n_runs, n_layers, heads, page, n_pages, dv);
+                                                           cs, n_runs, n_layers, heads, page, n_pages, vv_shift);
   return cudaGetLastError();
 }
 

@@ -288,6 +288,45 @@ def fused_vs_materialised(t, steps=10, warmup=3):
     return out
 
 
+def compaction(steps=4, warmup=1, n_layers=32):
+    """akv_compact on the post-drop branch of the 32K trajectory with every layer of a
+    Llama-3.1-8B-shaped model (32 layers): ~24.5K visible tokens copied into dense pages, the
+    pending suffix shift applied to the keys on the way.  HBM-bound copy: algorithmic bytes =
+    read + write of every kept K and V row."""
+    import torch
+    from agentic_kv_cache_gb300 import akv, runner, synth
+    w = synth.llama8b_32k(fork=True, n_layers=n_layers)
+    w.n_pages += 2 * (32768 // 16)
+    cfg = akv.config_from_shape(w.shape, w.n_pages)
+    pools = akv.make_pools(cfg)
+    eng = akv.Engine(cfg, pools)
+    st = torch.cuda.current_stream()
+    src = runner.torch_device_kv_source(w)
+    fork_at = next(i for i, op in enumerate(w.ops) if op[0] == "fork")
+    names = runner.run_ops(eng, w, kv_source=src, ops=w.ops[:fork_at], stream=st)
+    new_op = next(op for op in w.ops[fork_at:] if op[0] == "append")
+    kv = src(new_op[3], new_op[2])
+    frag = None
+    for i in range(warmup + steps):
+        if i == warmup:
+            torch.cuda.synchronize()
+            eng.profile_enable(True)
+        nm = runner.run_ops(eng, w, kv_source=lambda *_: kv, ops=w.ops[fork_at:], names=dict(names), stream=st)
+        frag = eng.fragmentation(nm["F"])
+        eng.compact(nm["F"], stream=st)
+        eng.seq_free(nm["F"])
+    stats = eng.profile_read()["compact_copy"]
+    eng.profile_enable(False)
+    assert eng.check_device_error(st) == 0
+    del eng, pools, kv
+    torch.cuda.empty_cache()
+    ms = stats["ms"] / stats["launches"]
+    gbs = stats["bytes"] / stats["launches"] / (ms * 1e-3) / 1e9
+    return {"workload": f"llama8b_32k post-drop branch, {n_layers} layers", "fragmentation_before": frag,
+            "ms_per_launch": ms, "bytes_per_launch": stats["bytes"] / stats["launches"], "GB/s": gbs,
+            "frac_of_hbm": gbs / load_peaks()[0]}
+
+
 def mla_turns(concurrencies=(1, 4, 8, 16), steps=3, warmup=1):
     """DeepSeek-V2-Lite MLA turn per concurrency C (27 layers, latent 512 + K_pe 64, 16 heads, page 64,
     17K-token prompts): per session a branch of the prompt, the AMORTIZE splice of 2,016 tokens into a
@@ -472,6 +511,7 @@ def gpu_arm(args, rank, world):
         line["repos_rotate_sweep"] = repos_sweep(steps=4, n_layers=args.sweep_layers)
     if not args.no_extra:
         line["mla_dsv2lite_turn"] = mla_turns()
+        line["compact_copy"] = compaction()
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
     return line

@@ -50,8 +50,9 @@ def compact_case(w, check_attention=True):
             if d:
                 x = np.abs(c.kp[:, sk, :, ss, :].astype(np.float64))
                 t = 2.0 ** -20 * (x[..., a] + x[..., b])
-                c.kterm[:, dk, :, ds, a] = t
-                c.kterm[:, dk, :, ds, b] = t
+                view = c.kterm[:, dk, :, ds, :]        # basic indexing: a view [L][H][d]
+                view[..., a] = t
+                view[..., b] = t
                 rot[:, dk, :, ds] = True
                 n_rot += 1
             else:  # a plain copy carries the source row's state (rotated earlier or not)

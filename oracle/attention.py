@@ -65,3 +65,24 @@ def segment_attention(q, k, v, scale, rows=None):
     for h in range(hq):
         o[:, h], lse[:, h] = masked_attention(q[rows, h], k[:, h // group], v[:, h // group], vis, scale)
     return o, lse
+
+
+def attention_mass(q, k, scale):
+    """Attention mass of one segment's entries: the softmax probability each visible entry
+    receives, summed over every query row and query head of the segment (the cumulative
+    attention weight a serving engine watches to pick droppable blocks, [AKV-blog] "Dilemma 1:
+    Client-Side vs Server-Side Drop Policy").  Causal rule and head grouping as
+    segment_attention.  q [q_len, Hq, d], k [kv_len, Hkv, d] -> mass [kv_len] (float64).
+    """
+    q_len, hq, _ = q.shape
+    kv_len, hkv, _ = k.shape
+    group = hq // hkv
+    vis = causal_visibility(q_len, kv_len)
+    mass = np.zeros(kv_len)
+    for h in range(hq):
+        s = scale * (np.asarray(q[:, h], np.float64) @ np.asarray(k[:, h // group], np.float64).T)
+        s = np.where(vis, s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        mass += (p / p.sum(axis=1, keepdims=True)).sum(axis=0)
+    return mass

@@ -74,3 +74,9 @@ def attend_segment(q_seg, kpool, vpool, layer, runs, scale, mla=False, rows=None
     if mla:
         k = np.concatenate([v, k], axis=-1)
     return attention.segment_attention(np.asarray(q_seg, np.float64), k, v, scale, rows=rows)
+
+
+def mass_segment(q_seg, kpool, vpool, layer, runs, scale):
+    """Attention mass of a segment's entries over paged pools (GQA): see attention.attention_mass."""
+    k = gather(kpool, layer, runs, 0)
+    return attention.attention_mass(np.asarray(q_seg, np.float64), k, scale)

@@ -184,3 +184,40 @@ def test_repos_runs_copy_on_write_and_identity():
     out = kernels.repos_runs(kpool, runs, 1.0e4)
     assert np.array_equal(out[:, 2, :, 0:4], kpool[:, 0, :, 0:4])
     assert np.array_equal(out[:, :2], kpool[:, :2])   # the shared source pages are not written
+
+
+# ------------------------------------------------------------ attention mass
+def test_attention_mass_totals_rows_times_heads():
+    # every query row's probabilities sum to one, for every head
+    rng = np.random.default_rng(11)
+    for q_len, kv_len, hq, hkv in ((1, 1, 4, 1), (5, 37, 8, 2), (16, 16, 4, 4)):
+        q = rng.standard_normal((q_len, hq, 16))
+        k = rng.standard_normal((kv_len, hkv, 16))
+        m = attention.attention_mass(q, k, 0.25)
+        assert abs(m.sum() - q_len * hq) < 1e-9 * q_len * hq
+        assert np.all(m >= 0)
+
+
+def test_attention_mass_identical_keys_closed_form():
+    # identical keys: row i spreads its weight evenly over the kv_len - q_len + i + 1 entries it sees
+    q_len, kv_len, hq = 6, 20, 3
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((q_len, hq, 8))
+    k = np.tile(rng.standard_normal((1, 1, 8)), (kv_len, 1, 1))
+    m = attention.attention_mass(q, k, 0.3)
+    want = np.zeros(kv_len)
+    for i in range(q_len):
+        seen = kv_len - q_len + i + 1
+        want[:seen] += hq / seen
+    assert np.allclose(m, want, rtol=0, atol=1e-12)
+
+
+def test_attention_mass_one_dominant_key():
+    # a key far more aligned with every query than the others takes (almost) all the weight of
+    # the rows that see it; rows that do not see it spread theirs over the rest
+    q = np.ones((2, 2, 4))
+    k = np.zeros((5, 1, 4))
+    k[4] = 50.0                       # entry 4 is only visible to the last row (bottom-right)
+    m = attention.attention_mass(q, k, 1.0)
+    assert abs(m[4] - 2.0) < 1e-9     # last row, both heads
+    assert np.allclose(m[:4], 2.0 / 4)  # first row (sees entries 0..3) spread evenly, both heads

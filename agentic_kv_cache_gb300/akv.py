@@ -79,6 +79,7 @@ def load(path=LIB_PATH):
         "akv_attend": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
         "akv_attend_fused": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
         "akv_fragmentation": [P, I32, ctypes.POINTER(ctypes.c_double)],
+        "akv_attention_mass": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, F32, P, P],
         "akv_compact": [P, I32, P],
         "akv_debug_rotate_f32": [P, P, I32, P, P],
         "akv_export_state": [P, I32, P, P, P, P, P, P],
@@ -215,6 +216,12 @@ class Engine:
             arr[i].n_hide = hide.size // 2
             arr[i].reserved = 0
         return arr, keep
+
+    def attention_mass(self, layer, segs, q, n_q_rows, lse, mass, scale=1.0, stream=None):
+        """akv_attention_mass: mass [sum of kv_end] per segment and logical token (see include/akv.h)."""
+        arr, keep = self.make_segments(segs)
+        self._check(self.lib.akv_attention_mass(self.h, layer, arr, len(segs), _ptr(q), n_q_rows, _ptr(lse),
+                                                float(scale), _ptr(mass), _stream(stream)))
 
     def fragmentation(self, seq):
         out = ctypes.c_double()

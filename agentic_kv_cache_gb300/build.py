@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libakv.so")
 
-SOURCES = ["engine.cpp", "kv_write.cu", "repos_rotate.cu", "segment_attn.cu", "segment_attn_mla.cu", "repos_noalloc.cu", "compact_copy.cu"]
+SOURCES = ["engine.cpp", "kv_write.cu", "repos_rotate.cu", "segment_attn.cu", "segment_attn_mla.cu", "repos_noalloc.cu", "compact_copy.cu", "attn_mass.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

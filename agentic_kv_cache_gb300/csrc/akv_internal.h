@@ -55,7 +55,9 @@ struct AttnSeg {
   int32_t kv_len;
   int32_t q_len;
   int32_t q_row0;
-  int32_t pad[3];
+  int32_t ent_off;   // attention mass: first entry of this segment in the entry -> token table
+  int32_t mass_off;  // attention mass: first output element of this segment
+  int32_t pad;
 };
 
 // One CTA's work: two consecutive 128-row query tiles (A = qt0, B = qt0 + 1)
@@ -123,6 +125,28 @@ struct AttnParams {
   int32_t dv;         // output row width (d_v)
 };
 
+// Attention-mass pass (GQA): one CTA per (segment, kv head, query tile);
+// work[i].n_a = the KV tiles that query tile reads.
+struct MassParams {
+  CUtensorMap q_map;       // as AttnParams
+  CUtensorMap k_map;
+  CUtensorMap k_tile_map;
+  const AttnRun* runs;
+  const AttnSeg* segs;
+  const AttnWork* work;
+  const float* lse;        // natural-log softmax normaliser [n_q_rows][Hq] from the attention pass
+  const int32_t* ent_tok;  // per segment entry: its logical token index
+  float* mass;             // [sum of segments' kv_end], zeroed by the host, accumulated with atomics
+  DevErr* err;
+  float scale_log2;
+  int32_t n_work;
+  int32_t layer;
+  int32_t n_pages;
+  int32_t hq;
+  int32_t group;
+  int32_t page;
+};
+
 // Floats of one partial slot: tiles x 128 rows x (width + 2).
 __host__ __device__ inline int64_t partial_floats(int tiles, int width) { return int64_t(tiles) * 128 * (width + 2); }
 
@@ -133,6 +157,8 @@ cudaError_t launch_kv_write(const void* src, void* pool, const int32_t* rows, in
 cudaError_t launch_compact_copy(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int d_v, int page, int64_t n_pages, bool half,
                                 int n_sm, cudaStream_t st);
+
+cudaError_t launch_attn_mass(const MassParams& p, int dim, cudaStream_t st);
 
 cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int page, int64_t n_pages,

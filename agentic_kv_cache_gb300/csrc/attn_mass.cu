@@ -1,0 +1,377 @@
+// attn_mass: per-token attention mass of a segment-batch attention launch.
+//
+// [AKV-blog] "Dilemma 1: Client-Side vs Server-Side Drop Policy": a serving
+// engine can pick droppable blocks itself by watching the cumulative
+// attention weight historical blocks receive.  This pass measures it: for
+// every visible entry of a segment, the softmax probability it receives,
+// summed over the segment's query rows and query heads,
+//     mass[e] = sum_rows sum_heads exp(scale * q . k_e - lse_row),
+// with lse the natural-log normaliser the attention pass returned (so the
+// probabilities are the final ones).  The policy on top (an epsilon over
+// three decode turns) is the caller's.
+//
+// GB300 design (one CTA per (segment, kv head, 128-row query tile)):
+//   * warp 0 loads Q once and streams K tiles (128 keys) through a 4-slot
+//     ring by TMA, whole-tile copies when the runs sit on consecutive pages;
+//   * warp 1 issues S(j) = Q K_j^T into one of two TMEM score buffers, then
+//     the column sums of the probability tile of j - 1 as a second MMA,
+//     D = ones(128 x 128) P(j-1), whose every row is the vector of column sums
+//     (the P tile is bf16 in shared memory as the B operand);
+//   * warps 2-5 (one row per thread) turn scores into probabilities with the
+//     final lse, write them to shared memory, and read back the column sums of
+//     the previous tile (lane l of quadrant q takes column 32q + l) to add
+//     them into the output of the entry's token with one atomic each.
+// Every wait is bounded; on time-out the CTA records AKV_ERR_DEVICE_TIMEOUT.
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "akv_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace akv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kKeys = 128;
+constexpr int kRows = 128;
+constexpr int kRing = 4;
+constexpr int kMaxRuns = 8;
+constexpr uint32_t kTmemCols = 512;  // S0, S1, D (128 columns each)
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kDrainLimitNs = 100000000ull;
+constexpr int32_t kErrTimeout = 7;
+constexpr int32_t kErrDevice = 8;
+
+template <int D>
+struct MLayout {
+  static constexpr int kBlocks = D / 64;
+  static constexpr uint32_t kBlockBytes = 128 * 128;
+  static constexpr uint32_t kTile = kBlocks * kBlockBytes;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kSlot = kQ + kTile;
+  static constexpr uint32_t kP = kSlot + kRing * kTile;  // probability tile, 2 x 64-key blocks
+  static constexpr uint32_t kOnes = kP + 2 * kBlockBytes;  // one 128 x 64 block of bf16 ones
+  static constexpr uint32_t kColE = kOnes + kBlockBytes;
+  static constexpr uint32_t kBars = kColE + 128 * 4;
+  static constexpr uint32_t kBytes = kBars + 256;
+};
+
+enum MBar {
+  kMQ = 0,
+  kMFull0,
+  kMEmpty0 = kMFull0 + kRing,
+  kMS0 = kMEmpty0 + kRing,  // + buffer
+  kMSFree0 = kMS0 + 2,      // + buffer, 128 arrivals
+  kMPFull = kMSFree0 + 2,   // 128 arrivals
+  kMD,
+  kMFin,
+  kMNumBars
+};
+static_assert(kMNumBars * 8 + 8 <= 256, "barrier area");
+
+__device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
+  if (atomicCAS(&err->code, 0, code) == 0) {
+    err->info[0] = a;
+    err->info[1] = b;
+    err->info[2] = c;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- producer
+template <int D>
+__device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
+                          volatile int* abort_flag) {
+  using L = MLayout<D>;
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
+  const int n = w.n_a;
+  ptx::mbar_arrive_expect_tx(bar(kMQ), L::kTile);
+  for (int kb = 0; kb < L::kBlocks; ++kb)
+    ptx::tma_load_3d(sbase + L::kQ + kb * L::kBlockBytes, &p.q_map, bar(kMQ), kb * 64, w.kvh * G,
+                     seg.q_row0 + w.qt0 * tpt);
+  const int layer_base = p.layer * p.n_pages;
+  const int first = p.runs[seg.run_off].kp;
+  int kpg[kMaxRuns], nkp[kMaxRuns];
+  auto fetch = [&](int j, int (&kk)[kMaxRuns]) {  // K pages of tile j's runs, one tile ahead
+#pragma unroll
+    for (int g = 0; g < kMaxRuns; ++g) {
+      const int ri = j * rpt + g;
+      kk[g] = layer_base + ((g < rpt && ri < seg.n_runs) ? p.runs[seg.run_off + ri].kp : first);
+    }
+  };
+  fetch(0, kpg);
+  int armed[kRing] = {0, 0, 0, 0};
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const int slot = j % kRing, use = j / kRing;
+    if (j + 1 < n) fetch(j + 1, nkp);
+    if (use >= 1 && !(ok = ptx::mbar_wait(bar(kMEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs))) break;
+    const uint32_t dst = sbase + L::kSlot + slot * L::kTile;
+    ptx::mbar_arrive_expect_tx(bar(kMFull0 + slot), L::kTile);
+    bool cons = true;
+#pragma unroll
+    for (int g = 1; g < kMaxRuns; ++g) cons = cons && (g >= rpt || kpg[g] == kpg[0] + g);
+    if (cons) {
+#pragma unroll
+      for (int kb = 0; kb < L::kBlocks; ++kb)
+        ptx::tma_load_4d(dst + kb * L::kBlockBytes, &p.k_tile_map, bar(kMFull0 + slot), kb * 64, 0, w.kvh, kpg[0]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < kMaxRuns; ++g) {
+        if (g >= rpt) break;
+#pragma unroll
+        for (int kb = 0; kb < L::kBlocks; ++kb)
+          ptx::tma_load_4d(dst + kb * L::kBlockBytes + g * p.page * 128, &p.k_map, bar(kMFull0 + slot), kb * 64, 0,
+                           w.kvh, kpg[g]);
+      }
+    }
+    armed[slot] = use + 1;
+#pragma unroll
+    for (int g = 0; g < kMaxRuns; ++g) kpg[g] = nkp[g];
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 0, 0);
+    *abort_flag = 1;
+  }
+  ptx::mbar_wait_drain(bar(kMQ), 0, kDrainLimitNs);
+#pragma unroll
+  for (int s = 0; s < kRing; ++s)
+    if (armed[s]) ptx::mbar_wait_drain(bar(kMFull0 + s), (armed[s] - 1) & 1, kDrainLimitNs);
+}
+
+// --------------------------------------------------------------------- MMA
+// Per tile j: S(j & 1) = Q K_j^T; then, once the probabilities of tile j - 1
+// are in shared memory, D = ones P(j - 1) (column sums in every row of D).
+template <int D>
+__device__ void m_mma(const MassParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
+  using L = MLayout<D>;
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kKeys, false);
+  constexpr uint32_t idesc_sum = ptx::idesc_bf16(kRows, kKeys, true);  // B = P, keys (N) contiguous
+  const int n = w.n_a;
+  const uint64_t qd = ptx::smem_desc(sbase + L::kQ, 16, 1024);
+  const uint64_t ones = ptx::smem_desc(sbase + L::kOnes, 16, 1024);
+  const uint64_t pd = ptx::smem_desc(sbase + L::kP, L::kBlockBytes, 1024);
+  bool ok = ptx::mbar_wait(bar(kMQ), 0, abort_flag, kWaitLimitNs);
+  for (int j = 0; j <= n && ok; ++j) {
+    if (j < n) {
+      const int slot = j % kRing;
+      if (!(ok = ptx::mbar_wait(bar(kMFull0 + slot), (j / kRing) & 1, abort_flag, kWaitLimitNs))) break;
+      if (j >= 2 && !(ok = ptx::mbar_wait(bar(kMSFree0 + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, kWaitLimitNs)))
+        break;
+      ptx::tc_fence_after();
+      const uint64_t kd = ptx::smem_desc(sbase + L::kSlot + slot * L::kTile, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
+        ptx::mma_bf16(tmem + 128u * (j & 1), ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), idesc_qk, ks > 0);
+      }
+      ptx::mma_commit(bar(kMS0 + (j & 1)));
+      ptx::mma_commit(bar(kMEmpty0 + slot));
+    }
+    if (j >= 1) {
+      if (!(ok = ptx::mbar_wait(bar(kMPFull), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kRows / 16; ++ks)  // 16 probability rows per step; every A element is 1
+        ptx::mma_bf16(tmem + 256u, ptx::desc_advance(ones, (ks & 3) * 32), ptx::desc_advance(pd, ks * 16 * 128),
+                      idesc_sum, ks > 0);
+      ptx::mma_commit(bar(kMD));
+    }
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 1, 0);
+    *abort_flag = 1;
+  }
+  ptx::mma_commit(bar(kMFin));
+  ptx::mbar_wait_drain(bar(kMFin), 0, kDrainLimitNs);
+}
+
+// ----------------------------------------------------------------- softmax
+// Thread = row r = TMEM lane r: probabilities of its row with the final lse,
+// bf16 into the shared P tile (128-byte swizzle, keys contiguous); thread r
+// also owns key column r when the column sums come back.
+template <int D>
+__device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg& seg, uint8_t* smem, uint32_t sbase,
+                          uint32_t tmem, volatile int* abort_flag) {
+  using L = MLayout<D>;
+  const uint32_t bars = sbase + L::kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int n = w.n_a;
+  const int quad = (threadIdx.x / 32) & 3, lane = threadIdx.x % 32;
+  const int r = quad * 32 + lane;
+  const uint32_t lane_addr = uint32_t(quad * 32) << 16;
+  const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
+  const int qi = w.qt0 * tpt + r / G, g = r % G;
+  const bool row_valid = qi < seg.q_len;
+  const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
+  // log2-domain normaliser of this row; rows past the segment's queries contribute nothing
+  const float lse2 = row_valid ? p.lse[int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g] * 1.4426950408889634f
+                               : INFINITY;
+  const float2 sl2v = make_float2(p.scale_log2, p.scale_log2), neg = make_float2(-lse2, -lse2);
+  int* colE = reinterpret_cast<int*>(smem + L::kColE);
+  uint8_t* P = smem + L::kP;
+  int page_shift = 4;
+  while ((1 << page_shift) < p.page) ++page_shift;
+  const int sl_own = r & (p.page - 1);
+  const int2* run_le = reinterpret_cast<const int2*>(p.runs + seg.run_off);
+  int2 run_cur = make_int2(0, 0);
+  if ((r >> page_shift) < seg.n_runs) run_cur = run_le[2 * (r >> page_shift) + 1];
+  bool ok = true;
+  int e_prev = INT_MAX;
+  // column sums of tile jj come back in D: lane l of quadrant q reads column 32q + l
+  auto take_sums = [&](int jj) {
+    ok = ptx::mbar_wait(bar(kMD), jj & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(1, 128, ok)) return false;
+    ptx::tc_fence_after();
+    uint32_t v[32];
+    ptx::tmem_load32(tmem + 256u + lane_addr + quad * 32, v);
+    float mine = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) mine = lane == k ? __uint_as_float(v[k]) : mine;
+    if (e_prev != INT_MAX) atomicAdd(p.mass + seg.mass_off + p.ent_tok[seg.ent_off + e_prev], mine);
+    return true;
+  };
+  for (int j = 0; j < n && ok; ++j) {
+    ok = ptx::mbar_wait(bar(kMS0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(1, 128, ok)) {
+      ok = false;
+      break;
+    }
+    int e = INT_MAX;  // entry index of key column r of tile j
+    {
+      const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
+      if (sl_own >= lo && sl_own < hi) e = run_cur.y + (sl_own - lo);
+      colE[r] = e;
+      const int ri = (j + 1) * rpt + (r >> page_shift);
+      run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
+    }
+    const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
+    ptx::tc_fence_after();
+    const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
+    // the sums of tile j - 1 are read before its P buffer is overwritten
+    if (j >= 1 && !(ok = take_sums(j - 1))) break;
+    const int4* ce4 = reinterpret_cast<const int4*>(colE);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
+      ptx::tmem_load64(tmem + 128u * (j & 1) + lane_addr + h * 64, u);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const int4 e4 = ce4[h * 16 + c];
+          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
+          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2v, neg);
+        pk[c] = pack_bf16(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+      }
+      uint8_t* rowp = P + h * L::kBlockBytes + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8)
+        *reinterpret_cast<uint4*>(rowp + ((c8 ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(bar(kMSFree0 + (j & 1)));
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive(bar(kMPFull));
+    e_prev = e;
+  }
+  if (ok && n >= 1) ok = take_sums(n - 1);
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 2, 0);
+    *abort_flag = 1;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_mass_kernel(const __grid_constant__ MassParams p, int smem_bytes) {
+  using L = MLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  uint8_t* smem = reinterpret_cast<uint8_t*>((raw + 1023) & ~uintptr_t(1023));
+  if (smem + L::kBytes > smem_raw + smem_bytes) {
+    if (threadIdx.x == 0) raise_error(p.err, kErrDevice, blockIdx.x, int(raw & 1023), 1);
+    return;
+  }
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const uint32_t bars = sbase + L::kBars;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kMNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kMNumBars + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const AttnWork w = p.work[blockIdx.x];
+  const AttnSeg seg = p.segs[w.seg];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMNumBars; ++i)
+      ptx::mbar_init(bars + 8u * i, (i == kMSFree0 || i == kMSFree0 + 1 || i == kMPFull) ? 128 : 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  // the all-ones A operand of the column-sum MMA (bf16 1.0 = 0x3f80)
+  for (uint32_t i = threadIdx.x; i < L::kBlockBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(smem + L::kOnes)[i] = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+  ptx::fence_proxy_async_smem();
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&p.q_map);
+    ptx::prefetch_tensormap(&p.k_map);
+    ptx::prefetch_tensormap(&p.k_tile_map);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp == 0) {
+    if (lane == 0) m_produce<D>(p, w, seg, sbase, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) m_mma<D>(p, w, sbase, tmem, abort_flag);
+  } else {
+    m_softmax<D>(p, w, seg, smem, sbase, tmem, abort_flag);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_variant(const MassParams& p, cudaStream_t st) {
+  const int smem = int(MLayout<D>::kBytes) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_mass_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_mass_kernel<D><<<p.n_work, kThreads, smem, st>>>(p, smem);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_mass(const MassParams& p, int dim, cudaStream_t st) {
+  if (p.n_work <= 0) return cudaSuccess;
+  if (dim == 64) return launch_variant<64>(p, st);
+  if (dim == 128) return launch_variant<128>(p, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace akv

@@ -852,6 +852,7 @@ struct akv_ctx {
   struct SegPlan {
     std::vector<akv::AttnRun> runs;
     std::vector<int32_t> shift;  // fused plans: pending shift of each run's tokens
+    std::vector<int32_t> tok;    // with want_tok: logical token index of each entry
     int64_t kv_len = 0;
   };
 
@@ -875,7 +876,7 @@ struct akv_ctx {
   // consecutive slots of one (K page, V page).  With `fused` the tokens may
   // carry pending shifts; runs then also break where the shift changes, and
   // each run records it (the attention kernel rotates those keys on the fly).
-  SegPlan plan_segment(const akv_segment& g, bool fused = false) {
+  SegPlan plan_segment(const akv_segment& g, bool fused = false, bool want_tok = false) {
     auto& toks = seq(g.seq);
     std::vector<uint8_t> hidden;
     if (g.n_hide > 0) {
@@ -906,6 +907,7 @@ struct akv_ctx {
         lo = t.slot;
         hi = t.slot + 1;
       }
+      if (want_tok) sp.tok.push_back(int32_t(i));
       ++sp.kv_len;
     }
     if (open) {
@@ -1306,7 +1308,115 @@ struct akv_ctx {
     }
   }
 
-  // ------------------------------------------------------------ lifecycle
+  // ------------------------------------------------------- attention mass
+  // Per segment and logical token: the softmax probability the token's entry
+  // receives, summed over the segment's query rows and heads, from the Q and
+  // the lse of a finished attention pass ([AKV-blog] "Dilemma 1").
+  void attention_mass(int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q, int64_t n_q_rows,
+                      const float* lse, float scale, float* mass, cudaStream_t st) {
+    if (n_segs < 0 || (n_segs > 0 && !segs)) fail(AKV_ERR_ARG, "bad segment list");
+    if (layer < 0 || layer >= cfg.n_layers) fail(AKV_ERR_RANGE, "layer outside the pools");
+    if (n_q_rows < 0 || n_q_rows > kI32Max) fail(AKV_ERR_RANGE, "bad query row count");
+    if (cfg.layout != AKV_LAYOUT_GQA) fail(AKV_ERR_ARG, "attention mass is implemented for the GQA layout");
+    if (!meta && n_segs > 0 && (!q || !lse || !mass)) fail(AKV_ERR_ARG, "null Q, lse or mass pointer");
+    for (int32_t i = 0; i < n_segs; ++i) validate_segment(segs[i], n_q_rows);
+    std::vector<int32_t> ids;
+    for (int32_t i = 0; i < n_segs; ++i) ids.push_back(segs[i].seq);
+    std::sort(ids.begin(), ids.end());
+    ids.erase(std::unique(ids.begin(), ids.end()), ids.end());
+    flush(ids, st);
+    if (n_segs == 0) return;
+    const int G = cfg.n_q_heads / cfg.n_kv_heads, tpt = 128 / G, rpt = 128 / cfg.page_size;
+    std::vector<akv::AttnRun> runs;
+    std::vector<akv::AttnSeg> tab;
+    std::vector<akv::AttnWork> work;
+    std::vector<int32_t> ent_tok;
+    int64_t mass_len = 0;
+    for (int32_t i = 0; i < n_segs; ++i) {
+      SegPlan sp = plan_segment(segs[i], false, true);
+      akv::AttnSeg sg{};
+      sg.run_off = int32_t(runs.size());
+      sg.n_runs = int32_t(sp.runs.size());
+      sg.kv_len = int32_t(sp.kv_len);
+      sg.q_len = segs[i].q_len;
+      sg.q_row0 = int32_t(segs[i].q_row0);
+      sg.ent_off = int32_t(ent_tok.size());
+      sg.mass_off = int32_t(mass_len);
+      if (mass_len + segs[i].kv_end > kI32Max) fail(AKV_ERR_RANGE, "mass output too long");
+      mass_len += segs[i].kv_end;
+      const int64_t ql = sg.q_len, kl = sg.kv_len;
+      const int n_qt = int((ql + tpt - 1) / tpt);
+      for (int qt = 0; qt < n_qt; ++qt) {
+        // KV tiles the query tile reads: runs whose first entry is <= its last row's limit
+        const int64_t limit = kl - ql + std::min<int64_t>(ql, int64_t(qt + 1) * tpt) - 1;
+        int64_t lo_r = 0, hi_r = int64_t(sp.runs.size());
+        while (lo_r < hi_r) {
+          const int64_t mid = (lo_r + hi_r) / 2;
+          if (sp.runs[mid].es <= limit) lo_r = mid + 1; else hi_r = mid;
+        }
+        const int32_t nt = int32_t((lo_r + rpt - 1) / rpt);
+        for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, nt, 0, 0, nt, -1, -1});
+      }
+      runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
+      ent_tok.insert(ent_tok.end(), sp.tok.begin(), sp.tok.end());
+      tab.push_back(sg);
+    }
+    if (meta) return;
+    if (!(cfg.d_rot == 64 || cfg.d_rot == 128)) fail(AKV_ERR_ARG, "attention mass supports head_dim 64 or 128");
+    std::stable_sort(work.begin(), work.end(),
+                     [](const akv::AttnWork& a, const akv::AttnWork& b) { return a.n_a > b.n_a; });
+    const size_t qbytes = size_t(n_q_rows) * cfg.n_q_heads * cfg.d_rot * 2;
+    const void* qd = device_input(q, qbytes, st_q, st);
+    const float* lsed = static_cast<const float*>(device_input(lse, size_t(n_q_rows) * cfg.n_q_heads * 4, st_lse, st));
+    if (reinterpret_cast<uintptr_t>(qd) % 16) fail(AKV_ERR_ARG, "Q must be 16-byte aligned");
+    const bool m_host = !is_device_ptr(mass);
+    float* md = mass;
+    if (m_host) {
+      st_o.want_host = false;
+      st_o.acquire(size_t(mass_len) * 4);
+      md = static_cast<float*>(st_o.dev);
+    }
+    cuda_check(cudaMemsetAsync(md, 0, size_t(mass_len) * 4, st), "mass zeroing");
+    akv::MassParams p{};
+    {
+      const uint64_t dims[3] = {uint64_t(cfg.d_rot), uint64_t(cfg.n_q_heads), uint64_t(std::max<int64_t>(n_q_rows, 1))};
+      const uint64_t strides[2] = {uint64_t(cfg.d_rot) * 2, uint64_t(cfg.n_q_heads) * cfg.d_rot * 2};
+      const uint32_t box[3] = {64, uint32_t(G), uint32_t(tpt)};
+      encode_map(&p.q_map, const_cast<void*>(qd), 3, dims, strides, box);
+    }
+    p.k_map = k_map;
+    p.k_tile_map = k_tile_map;
+    void *druns = nullptr, *dsegs = nullptr, *dwork = nullptr, *dtok = nullptr;
+    up.upload({{runs.data(), runs.size() * sizeof(akv::AttnRun), &druns},
+               {tab.data(), tab.size() * sizeof(akv::AttnSeg), &dsegs},
+               {work.data(), work.size() * sizeof(akv::AttnWork), &dwork},
+               {ent_tok.data(), ent_tok.size() * sizeof(int32_t), &dtok}},
+              st);
+    p.runs = static_cast<akv::AttnRun*>(druns);
+    p.segs = static_cast<akv::AttnSeg*>(dsegs);
+    p.work = static_cast<akv::AttnWork*>(dwork);
+    p.ent_tok = static_cast<const int32_t*>(dtok);
+    p.lse = lsed;
+    p.mass = md;
+    p.err = dev_err;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.n_work = int32_t(work.size());
+    p.layer = layer;
+    p.n_pages = cfg.n_pages;
+    p.hq = cfg.n_q_heads;
+    p.group = G;
+    p.page = cfg.page_size;
+    cuda_check(akv::launch_attn_mass(p, cfg.d_rot, st), "attn_mass launch");
+    up.done(st);
+    if (st_q.dev && !is_device_ptr(q)) st_q.release(st);
+    if (st_lse.dev && !is_device_ptr(lse)) st_lse.release(st);
+    if (m_host) {
+      cuda_check(cudaMemcpyAsync(mass, md, size_t(mass_len) * 4, cudaMemcpyDeviceToHost, st), "mass copy to host");
+      st_o.release(st);
+    }
+  }
+
+  // ------------------------------------------------------------ lifecycle  // ------------------------------------------------------------ lifecycle
   void create(const akv_config& c, const akv_pools* pools) {
     cfg = c;
     if (c.n_layers <= 0 || c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.n_pages <= 0 || c.reserved != 0)
@@ -1503,6 +1613,11 @@ akv_status akv_fragmentation(akv_ctx* ctx, int32_t seq, double* frac_out) {
 
 akv_status akv_compact(akv_ctx* ctx, int32_t seq, void* stream) {
   return guard(ctx, [&] { ctx->compact(seq, as_stream(stream)); });
+}
+
+akv_status akv_attention_mass(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
+                              int64_t n_q_rows, const float* lse, float scale, float* mass, void* stream) {
+  return guard(ctx, [&] { ctx->attention_mass(layer, segs, n_segs, q, n_q_rows, lse, scale, mass, as_stream(stream)); });
 }
 
 akv_status akv_attend_fused(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,

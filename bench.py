@@ -327,6 +327,36 @@ def compaction(steps=4, warmup=1, n_layers=32):
             "frac_of_hbm": gbs / load_peaks()[0]}
 
 
+def mass_pass(t, reps=5):
+    """Per-token attention mass (the attn_mass kernel) of the 32K turn's 2,048 queries, after the
+    attention pass that produced the lse; CUDA events around the call on the stream."""
+    torch = t.torch
+    names = dict(t.names)
+    t.runner.run_ops(t.eng, t.w, kv_source=lambda *_: (t.new_k, t.new_v), ops=t.step_ops, names=names,
+                     stream=t.stream)
+    segs = t.runner.engine_segments(t.w, names)
+    s = t.w.shape
+    lse = torch.empty((t.nq, s.n_q_heads), dtype=torch.float32, device="cuda")
+    t.eng.attend(0, segs, t.q, t.nq, t.o, lse, s.scale, stream=t.stream)
+    total = sum(g["kv_end"] for g in t.w.segments)
+    mass = torch.empty((total,), dtype=torch.float32, device="cuda")
+    t.eng.attention_mass(0, segs, t.q, t.nq, lse, mass, s.scale, stream=t.stream)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        t.flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(t.stream)
+        t.eng.attention_mass(0, segs, t.q, t.nq, lse, mass, s.scale, stream=t.stream)
+        b.record(t.stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert t.eng.check_device_error(t.stream) == 0
+    total_mass = float(mass.sum())
+    t.eng.seq_free(names["F"])
+    return {"ms": sorted(ms)[len(ms) // 2], "mass_sum": total_mass, "expected_sum": t.nq * s.n_q_heads}
+
+
 def mla_turns(concurrencies=(1, 4, 8, 16), steps=3, warmup=1):
     """DeepSeek-V2-Lite MLA turn per concurrency C (27 layers, latent 512 + K_pe 64, 16 heads, page 64,
     17K-token prompts): per session a branch of the prompt, the AMORTIZE splice of 2,016 tokens into a
@@ -499,6 +529,7 @@ def gpu_arm(args, rank, world):
     if not args.no_extra:
         line["reprefill_equiv"] = reprefill_equiv(t)
         line["reprefill_equiv"]["turn_cache_path_ms"] = total_ms / args.steps
+        line["attention_mass"] = mass_pass(t)
         fz = {"turn_2048_queries": fused_vs_materialised(t)}
         del t
         torch.cuda.empty_cache()

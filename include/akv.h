@@ -224,6 +224,24 @@ AKV_API akv_status akv_fragmentation(akv_ctx* ctx, int32_t seq, double* frac_out
  * page_size) free pages in each pool (AKV_ERR_NO_PAGES, state unchanged). */
 AKV_API akv_status akv_compact(akv_ctx* ctx, int32_t seq, void* stream);
 
+/* Attention mass (the attn_mass kernel, a second light pass after
+ * akv_attend): for every segment and every logical token t < kv_end of its
+ * sequence, the softmax probability the token's entry receives summed over
+ * the segment's q_len query rows and all query heads,
+ *   mass[off_s + t] = sum_rows sum_heads exp(scale * q . k_t - lse_row),
+ * and 0 for tokens the segment does not see.  This is the cumulative attention
+ * weight a serving engine watches to pick droppable blocks ([AKV-blog]
+ * "Dilemma 1: Client-Side vs Server-Side Drop Policy"); the policy on top is
+ * the caller's.  q, scale and the segments must be those of the attention
+ * pass, lse its natural-log output [n_q_rows][n_q_heads].  mass: float
+ * [sum over segments of kv_end], segment s at off_s = kv_end of segments
+ * before it; host or device memory.  Values are sums of bf16-rounded
+ * probabilities accumulated in float32 (atomics: the summation order varies
+ * between runs).  GQA layout only. */
+AKV_API akv_status akv_attention_mass(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs,
+                              const void* q, int64_t n_q_rows, const float* lse, float scale, float* mass,
+                              void* stream);
+
 /* Segment-batch attention with the rotation fused in ([AKV-blog] section 4,
  * "Segment-Batch Attention Kernel Architecture": rotate keys in registers /
  * shared memory on the way to the tensor core, so transient position versions

@@ -438,7 +438,8 @@ struct akv_ctx {
     if (need > K.n_free() || need > V.n_free()) fail(AKV_ERR_NO_PAGES, "append needs %lld pages", (long long)need);
     if (int64_t(toks.size()) + n > kI32Max) fail(AKV_ERR_RANGE, "sequence too long");
     std::vector<int32_t> krow(n), vrow(n);
-    toks.reserve(toks.size() + n);
+    if (toks.capacity() < toks.size() + size_t(n))  // geometric growth: repeated appends stay amortised O(n)
+      toks.reserve(std::max(toks.size() + size_t(n), toks.capacity() + toks.capacity() / 2));
     for (int64_t i = 0; i < n; ++i) {
       if (room > 0) {
         ++slot;
@@ -564,7 +565,10 @@ struct akv_ctx {
   void fork(int32_t src, int64_t n_prefix, int32_t* out) {
     auto& toks = seq(src);
     if (n_prefix < 0 || n_prefix > int64_t(toks.size())) fail(AKV_ERR_RANGE, "fork prefix outside the sequence");
-    std::vector<Tok> child(toks.begin(), toks.begin() + n_prefix);
+    // headroom, so the branch's first appends do not reallocate (and copy) every token record
+    std::vector<Tok> child;
+    child.reserve(size_t(n_prefix) + size_t(n_prefix) / 4 + 4096);
+    child.assign(toks.begin(), toks.begin() + n_prefix);
     std::vector<int32_t> kps, vps;
     pages_of(child, 0, child.size(), kps, vps);
     for (int32_t q : kps) K.inc(q);

@@ -215,17 +215,20 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
     ptx::mma_commit(bar(kBarEmpty0 + ld % kRing));
     ++ld;
   };
+  // Descriptors are built once and advanced by constants (only the start
+  // address changes); the MMA thread shares its sub-partition with softmax.
+  const uint64_t qd0 = ptx::smem_desc(sbase + kQ, 16, 1024);
   auto qk = [&](int j) {
     const uint32_t tS = tmem + 128u * (j & 1);
 #pragma unroll 1
     for (int c = 0; c < kQChunks && ok; ++c) {
       const uint32_t kt = next_chunk();
       if (!ok) break;
-      const uint32_t qt = sbase + kQ + c * kChunk;
-#pragma unroll 1
-      for (int ks = 0; ks < 4; ++ks)
-        ptx::mma_bf16(tS, ptx::smem_desc(qt + ks * 32, 16, 1024), ptx::smem_desc(kt + ks * 32, 16, 1024), idesc_qk,
-                      (c > 0 || ks > 0));
+      const uint64_t kd = ptx::smem_desc(kt, 16, 1024), qd = ptx::desc_advance(qd0, c * kChunk);
+      ptx::mma_bf16(tS, qd, kd, idesc_qk, c > 0);
+#pragma unroll
+      for (int ks = 1; ks < 4; ++ks)
+        ptx::mma_bf16(tS, ptx::desc_advance(qd, ks * 32), ptx::desc_advance(kd, ks * 32), idesc_qk, 1);
       release();
     }
     if (ok) ptx::mma_commit(bar(kBarS0 + (j & 1)));
@@ -241,10 +244,11 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
     for (int i = 0; i < kVChunks && ok; ++i) {
       const uint32_t vt = next_chunk();
       if (!ok) break;
-#pragma unroll 1
-      for (int ks = 0; ks < kKeys / 16; ++ks)
-        ptx::mma_bf16_tmem_a(tO + 64u * i, tP + 8u * ks, ptx::smem_desc(vt + ks * 2048, kChunk, 1024), idesc_pv,
-                             (j > 0 || ks > 0));
+      const uint64_t vd = ptx::smem_desc(vt, kChunk, 1024);
+      ptx::mma_bf16_tmem_a(tO + 64u * i, tP, vd, idesc_pv, j > 0);
+#pragma unroll
+      for (int ks = 1; ks < kKeys / 16; ++ks)
+        ptx::mma_bf16_tmem_a(tO + 64u * i, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
       release();
     }
     if (ok) ptx::mma_commit(bar(kBarO));
@@ -320,9 +324,10 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
       uint32_t u[64];
       masked(h, u);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(u[c]));
+      for (int c = 0; c < 32; ++c)  // three-input max: two scores per instruction
+        mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
     }
-    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+    const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
     const float m_new = fmaxf(m_run, mt);
     const bool resc = m_new > m_run + 8.0f;
     const float m_use = resc ? m_new : m_run;
@@ -353,9 +358,10 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
       masked(h, u);
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c]), sl2, -msub));
-        const float p1 = ptx::ex2_approx(fmaf(__uint_as_float(u[2 * c + 1]), sl2, -msub));
+      for (int c = 0; c < 32; ++c) {  // scale-and-shift as one packed FMA per score pair
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])),
+                                    make_float2(sl2, sl2), make_float2(-msub, -msub));
+        const float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
         sum[(2 * c) & 3] += p0;
         sum[(2 * c + 1) & 3] += p1;
         pk[c] = pack_bf16(p0, p1);

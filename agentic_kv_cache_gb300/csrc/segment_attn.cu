@@ -457,9 +457,18 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // holds the tile's largest entry index.
     const bool need_mask = !all_valid || colE[kTileKeys - 1] > lim;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
-    // Pass 1: row max over two 64-column halves read from TMEM (three-input
-    // max: two scores per instruction).
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    // One pass over the two 64-column halves of S: each half is read from TMEM
+    // once, its max taken (three-input max, two scores per instruction), and
+    // P = exp2(s * scale * log2 e - m) formed with the running max m, packed to
+    // bf16 pairs and stored over the S columns already read (keys 2c, 2c+1 ->
+    // column c), where the PV MMA reads it as its A operand.  m is raised only
+    // when a half's max exceeds it by more than 2^8 (lazy rescale); if the
+    // second half raises it, the first half's P and sum are scaled down.  The
+    // scale-and-shift and the row sum run on float pairs.
+    const float2 sl2v = make_float2(sl2, sl2);
+    float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two pair accumulators: no spills at 168 registers
+    float m_use = m_run, alpha = 1.0f, a_first = 1.0f;
+    bool resc = false;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t u[64];
@@ -474,47 +483,27 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
           if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
         }
       }
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
-    }
-    const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
-    const float m_new = fmaxf(m_run, mt);
-    const bool resc = m_new > m_run + 8.0f;
-    const float m_use = resc ? m_new : m_run;
-    const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
-    const float msub = m_use == -INFINITY ? 0.f : m_use;
-    // O_T is stable here: S_T(j) completes after PV_T(j-1).
-    if (j > 0 && __any_sync(0xffffffffu, resc)) {
+      for (int c = 0; c < 16; ++c)
+        mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]));
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        ptx::tmem_load32(tO + lane_addr + c * 32, o);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-        ptx::tmem_store32(tO + lane_addr + c * 32, o);
-      }
-    }
-    // Pass 2: P = exp2(s * scale * log2 e - m), packed to bf16 pairs and
-    // stored over the S columns already read (keys 2c, 2c+1 -> column c), where
-    // the PV MMA reads it as its A operand.  The scale-and-shift and the row
-    // sum run on float pairs (one packed FMA / add per two scores).
-    const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-msub, -msub);
-    float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two pair accumulators: no spills at 168 registers
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t u[64];
-      ptx::tmem_load64(tS + lane_addr + h * 64, u);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int4 e4 = ce4[h * 16 + c];
-          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
-          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
-          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
-          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+      for (int c = 0; c < 16; ++c)
+        mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
+      const float mh = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
+      if (mh > m_use + 8.0f) {
+        const float a = m_use == -INFINITY ? 0.f : ptx::ex2_approx(m_use - mh);
+        if (h == 1) {  // rare: the first half was formed with the smaller max
+          sum[0] = make_float2(sum[0].x * a, sum[0].y * a);
+          sum[1] = make_float2(sum[1].x * a, sum[1].y * a);
+          a_first = a;  // its P is scaled once this half is stored (fewer live registers)
         }
+        alpha *= a;
+        m_use = mh;
+        resc = true;
       }
+      const float msub = m_use == -INFINITY ? 0.f : m_use;
+      const float2 negm = make_float2(-msub, -msub);
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
@@ -524,6 +513,29 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
         pk[c] = pack_bf16(pr.x, pr.y);
       }
       ptx::tmem_store32(tS + lane_addr + h * 32, pk);
+    }
+    // P of the first half, scaled to the raised max.  TMEM loads and stores are
+    // warp-collective: the whole warp takes this branch (other lanes scale by 1).
+    if (__any_sync(0xffffffffu, a_first != 1.0f)) {
+      uint32_t q[32];
+      ptx::tmem_load32(tS + lane_addr, q);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q[c]));
+        q[c] = pack_bf16(f.x * a_first, f.y * a_first);
+      }
+      ptx::tmem_store32(tS + lane_addr, q);
+    }
+    // O_T is stable here (S_T(j) completes after PV_T(j-1)); PV_T(j) waits for P below.
+    if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_load32(tO + lane_addr + c * 32, o);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+        ptx::tmem_store32(tO + lane_addr + c * 32, o);
+      }
     }
     const float rowsum = (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
     l_run = l_run * alpha + rowsum;

@@ -135,3 +135,29 @@ def test_split_kv_mla_full_compare(split):
 def test_split_kv_many_segments_group_8():
     w = synth.llama70b_128k(n_layers=1, total=16384, n_branches=4, q_per_branch=200)
     check(w, k_rows=40, split=4)
+
+
+def test_outlier_keys_exercise_lazy_rescale():
+    # Keys scaled up by 12-30x give score jumps far beyond the 2^8 lazy-rescale threshold:
+    # inside a tile (the second 64-key half raises the running max after the first half's P
+    # was formed) and across tiles (O rescaled in TMEM).  Same values on both sides.
+    from gpu_case import Case
+
+    class Outliers(Case):
+        def _values(self, key, n):
+            k32, v32 = super()._values(key, n)
+            k32 = k32.copy()
+            k32[:, 37::97] *= 12.0
+            k32[:, 101::251] *= 30.0
+            return k32, v32
+
+    w = synth.llama8b_32k(total=2048, n_new=200)
+    c = Outliers(w)
+    c.run_ops()
+    c.flush_segments()
+    q32, o, lse = c.attend_gpu()
+    for i, g in enumerate(w.segments):
+        rows = np.arange(g["q_len"])
+        want_o, want_lse = c.attend_oracle(q32, i, rows)
+        assert np.abs(o[g["q_row0"] + rows] - want_o).max() <= ATOL
+        assert np.abs(lse[g["q_row0"] + rows] - want_lse).max() <= ATOL

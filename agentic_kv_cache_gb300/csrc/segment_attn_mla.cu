@@ -284,6 +284,14 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
   const int sl_own = r & (p.page - 1);
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
+  // (lohi, es) of the run holding key column r of the current tile, fetched one tile ahead;
+  // lo = hi = 0 past the segment's last run, so no slot matches
+  const int2* run_le = reinterpret_cast<const int2*>(p.runs + seg.run_off);
+  int2 run_cur = make_int2(0, 0);
+  {
+    const int ri0 = w.t0 * rpt + (r >> page_shift);
+    if (ri0 < seg.n_runs) run_cur = run_le[2 * ri0 + 1];
+  }
   for (int j = 0; j < n; ++j) {
     const uint32_t tS = tmem + 128u * (j & 1);
     ok = ptx::mbar_wait(bar(kBarS0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs);
@@ -293,19 +301,25 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     }
     int e = INT_MAX;  // entry index of key column r (INT_MAX: none)
     {
-      const int ri = (w.t0 + j) * rpt + (r >> page_shift);
-      if (ri < seg.n_runs) {
-        const AttnRun ar = p.runs[seg.run_off + ri];
-        const int lo = ar.lohi & 0xffff, hi = ar.lohi >> 16;
-        if (sl_own >= lo && sl_own < hi) e = ar.es + (sl_own - lo);
-      }
+      const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
+      if (sl_own >= lo && sl_own < hi) e = run_cur.y + (sl_own - lo);
       colE[r] = e;
+      const int ri = (w.t0 + j + 1) * rpt + (r >> page_shift);
+      run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
     const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
     ptx::tc_fence_after();
     const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
-    auto masked = [&](int h, uint32_t (&u)[64]) {
+    // One TMEM pass per 64-column half: max in registers, P with the running
+    // max (raised lazily, beyond 2^8), stored packed over consumed S columns;
+    // the first half's P is rescaled afterwards if the second half raised it.
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    float m_use = m_run, alpha = 1.0f, a_first = 1.0f;
+    bool resc = false;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t u[64];
       ptx::tmem_load64(tS + lane_addr + h * 64, u);
       if (need_mask) {
 #pragma unroll
@@ -317,22 +331,46 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
           if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
         }
       }
-    };
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t u[64];
-      masked(h, u);
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 32; ++c)  // three-input max: two scores per instruction
         mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1]));
+      const float mh = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
+      if (mh > m_use + 8.0f) {
+        const float a = m_use == -INFINITY ? 0.f : ptx::ex2_approx(m_use - mh);
+        if (h == 1) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sum[k] *= a;
+          a_first = a;
+        }
+        alpha *= a;
+        m_use = mh;
+        resc = true;
+      }
+      const float msub = m_use == -INFINITY ? 0.f : m_use;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {  // scale-and-shift as one packed FMA per score pair
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])),
+                                    make_float2(sl2, sl2), make_float2(-msub, -msub));
+        const float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
+        sum[(2 * c) & 3] += p0;
+        sum[(2 * c + 1) & 3] += p1;
+        pk[c] = pack_bf16(p0, p1);
+      }
+      ptx::tmem_store32(tS + lane_addr + h * 32, pk);  // over S columns already read
     }
-    const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
-    const float m_new = fmaxf(m_run, mt);
-    const bool resc = m_new > m_run + 8.0f;
-    const float m_use = resc ? m_new : m_run;
-    const float alpha = resc ? ptx::ex2_approx(m_run - m_new) : 1.0f;
-    const float msub = m_use == -INFINITY ? 0.f : m_use;
+    // TMEM loads / stores are warp-collective: the whole warp takes these branches.
+    if (__any_sync(0xffffffffu, a_first != 1.0f)) {
+      uint32_t q[32];
+      ptx::tmem_load32(tS + lane_addr, q);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q[c]));
+        q[c] = pack_bf16(f.x * a_first, f.y * a_first);
+      }
+      ptx::tmem_store32(tS + lane_addr, q);
+    }
     if (j > 0) {  // O stable (PV of tile j-1 done) before any rescale
       ok = ptx::mbar_wait(bar(kBarO), (j - 1) & 1, abort_flag, kWaitLimitNs);
       if (!ptx::bar_red_and(1, 128, ok)) {
@@ -350,23 +388,6 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
           ptx::tmem_store32(tO + lane_addr + c * 32, o);
         }
       }
-    }
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t u[64];
-      masked(h, u);
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {  // scale-and-shift as one packed FMA per score pair
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])),
-                                    make_float2(sl2, sl2), make_float2(-msub, -msub));
-        const float p0 = ptx::ex2_approx(x.x), p1 = ptx::ex2_approx(x.y);
-        sum[(2 * c) & 3] += p0;
-        sum[(2 * c + 1) & 3] += p1;
-        pk[c] = pack_bf16(p0, p1);
-      }
-      ptx::tmem_store32(tS + lane_addr + h * 32, pk);  // over S columns already read
     }
     l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
     m_run = m_use;

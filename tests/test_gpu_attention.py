@@ -161,3 +161,29 @@ def test_outlier_keys_exercise_lazy_rescale():
         want_o, want_lse = c.attend_oracle(q32, i, rows)
         assert np.abs(o[g["q_row0"] + rows] - want_o).max() <= ATOL
         assert np.abs(lse[g["q_row0"] + rows] - want_lse).max() <= ATOL
+
+
+def test_mla_outlier_keys_exercise_lazy_rescale():
+    # MLA keys are [latent | K_pe]: scale both parts (and so the latent value) of some tokens
+    from gpu_case import Case
+
+    class Outliers(Case):
+        def _values(self, key, n):
+            k32, v32 = super()._values(key, n)
+            k32, v32 = k32.copy(), v32.copy()
+            for a, step, f in ((37, 97, 6.0), (101, 251, 12.0)):
+                k32[:, a::step] *= f
+                v32[:, a::step] *= f
+            return k32, v32
+
+    w = synth.mla_dsv2lite(n_layers=1, concurrency=1, prompt=3000, span=700, stub=20, n_new=100)
+    c = Outliers(w)
+    c.run_ops()
+    c.flush_segments()
+    q32, o, lse = c.attend_gpu()
+    for i, g in enumerate(w.segments):
+        rows = np.arange(g["q_len"])
+        want_o, want_lse = c.attend_oracle(q32, i, rows)
+        scale = max(1.0, float(np.abs(want_o).max()))
+        assert np.abs(o[g["q_row0"] + rows] - want_o).max() <= ATOL * scale
+        assert np.abs(lse[g["q_row0"] + rows] - want_lse).max() <= ATOL

@@ -23,9 +23,11 @@ cache      the paged KV bookkeeping model: pages, sequences, fork/CoW,
            append / drop / repos / splice, flush run lists, segment run lists.
 attention  masked softmax attention and segment-batch attention (bottom-right
            causal over a segment's visible KV list), with LSE.
-kernels    what the two GPU kernels compute, written as plain loops over the
+kernels    what the GPU kernels compute, written as plain loops over the
            run lists the bookkeeping model produces (repos over paged pools,
-           paged segment attention).
+           paged segment attention, compaction copies, attention mass).
+radix      extended radix-tree matching (exact vs retrigger) by brute force
+           over the inserted paths.
 
 Every function here is pinned by a ``-m "not gpu"`` test against something
 other than itself (closed forms, the pages' worked examples, library routines,

@@ -44,6 +44,26 @@ class Segment(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class Match(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("seq", ctypes.c_int32), ("n_items", ctypes.c_int64),
+                ("n_tokens", ctypes.c_int64)]
+
+
+MATCH_KINDS = {0: "none", 1: "exact", 2: "retrigger"}
+
+
+def items_array(items):
+    """Path items as int32 [n, 4] (kind, a, b, c): ("tok", x, p) -> (0, x, p, 0); ("op", code, a, b, c)
+    -> (code, a, b, c)."""
+    rows = []
+    for it in items:
+        if it[0] == "tok":
+            rows.append((0, it[1], it[2], 0))
+        else:
+            rows.append((it[1], it[2], it[3], it[4]))
+    return np.ascontiguousarray(np.asarray(rows, np.int32).reshape(-1, 4))
+
+
 class KernelStats(ctypes.Structure):
     _fields_ = [("launches", ctypes.c_int64 * 4), ("ms", ctypes.c_double * 4), ("bytes", ctypes.c_double * 4),
                 ("flops", ctypes.c_double * 4)]
@@ -79,6 +99,10 @@ def load(path=LIB_PATH):
         "akv_attend": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
         "akv_attend_fused": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
         "akv_fragmentation": [P, I32, ctypes.POINTER(ctypes.c_double)],
+        "akv_tree_insert": [P, P, I64, I32, pi32],
+        "akv_tree_match": [P, P, I64, ctypes.POINTER(Match)],
+        "akv_tree_reuse": [P, P, I64, ctypes.POINTER(Match), pi32, P],
+        "akv_tree_clear": [P],
         "akv_attention_mass": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, F32, P, P],
         "akv_compact": [P, I32, P],
         "akv_debug_rotate_f32": [P, P, I32, P, P],
@@ -222,6 +246,34 @@ class Engine:
         arr, keep = self.make_segments(segs)
         self._check(self.lib.akv_attention_mass(self.h, layer, arr, len(segs), _ptr(q), n_q_rows, _ptr(lse),
                                                 float(scale), _ptr(mass), _stream(stream)))
+
+    # --------------------------------------------------------- radix tree
+    def tree_insert(self, items, seq):
+        a = items_array(items)
+        out = ctypes.c_int32()
+        self._check(self.lib.akv_tree_insert(self.h, a.ctypes.data, a.shape[0], seq, ctypes.byref(out)))
+        return out.value
+
+    @staticmethod
+    def _match(m):
+        return dict(kind=MATCH_KINDS[m.kind], seq=m.seq, n_items=m.n_items, n_tokens=m.n_tokens)
+
+    def tree_match(self, items):
+        a = items_array(items)
+        m = Match()
+        self._check(self.lib.akv_tree_match(self.h, a.ctypes.data, a.shape[0], ctypes.byref(m)))
+        return self._match(m)
+
+    def tree_reuse(self, items, stream=None):
+        a = items_array(items)
+        m = Match()
+        sid = ctypes.c_int32()
+        self._check(self.lib.akv_tree_reuse(self.h, a.ctypes.data, a.shape[0], ctypes.byref(m), ctypes.byref(sid),
+                                            _stream(stream)))
+        return self._match(m), sid.value
+
+    def tree_clear(self):
+        self._check(self.lib.akv_tree_clear(self.h))
 
     def fragmentation(self, seq):
         out = ctypes.c_double()

@@ -272,6 +272,19 @@ struct akv_ctx {
   std::vector<int32_t> page_dst;  // flush scratch: destination of each moving K page
   std::vector<int32_t> sim_rc;    // flush scratch: simulated reference-count changes
   std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ids;
+
+  // extended radix tree: node 0 is the root
+  struct TreeNode {
+    akv_item item{};       // the item on the edge into this node
+    int32_t parent = -1;
+    int32_t owner = -1;    // tree-held sequence with this prefix
+    int64_t order = -1;    // insertion number of the owner (ties: earliest)
+    int64_t n_tok = 0;     // tokens on the path root .. this node
+    std::vector<int32_t> kids;
+  };
+  std::vector<TreeNode> tree = std::vector<TreeNode>(1);
+  std::vector<int32_t> tree_seqs;
+  int64_t tree_inserts = 0;
   std::string err;
   std::vector<int32_t> last_runs;  // 5 per run
 
@@ -1312,6 +1325,160 @@ struct akv_ctx {
     }
   }
 
+  // ---------------------------------------------------------- radix tree
+  static bool same_item(const akv_item& x, const akv_item& y) {
+    return x.kind == y.kind && x.a == y.a && x.b == y.b && x.c == y.c;
+  }
+  // what a retrigger match compares: a token without its position
+  static bool same_key(const akv_item& x, const akv_item& y) {
+    if (x.kind != y.kind) return false;
+    if (x.kind == AKV_ITEM_TOKEN) return x.a == y.a;
+    return x.a == y.a && x.b == y.b && x.c == y.c;
+  }
+  static void check_items(const akv_item* items, int64_t n) {
+    if (n < 0 || (n > 0 && !items)) fail(AKV_ERR_ARG, "bad item list");
+    for (int64_t i = 0; i < n; ++i)
+      if (items[i].kind < 0) fail(AKV_ERR_ARG, "item %lld has a negative kind", (long long)i);
+  }
+
+  int32_t tree_insert(const akv_item* items, int64_t n, int32_t sid) {
+    check_items(items, n);
+    auto& toks = seq(sid);
+    int64_t n_tok = 0;
+    for (int64_t i = 0; i < n; ++i) n_tok += items[i].kind == AKV_ITEM_TOKEN;
+    if (n_tok > int64_t(toks.size())) fail(AKV_ERR_RANGE, "path has more tokens than the sequence");
+    int32_t at = 0;
+    int64_t i = 0;
+    for (; i < n; ++i) {  // existing prefix
+      int32_t next = -1;
+      for (int32_t k : tree[at].kids)
+        if (same_item(tree[k].item, items[i])) {
+          next = k;
+          break;
+        }
+      if (next < 0) break;
+      at = next;
+    }
+    if (i == n) return -1;  // already present
+    int32_t holder = -1;
+    fork(sid, n_tok, &holder);
+    tree_seqs.push_back(holder);
+    const int64_t order = tree_inserts++;
+    for (; i < n; ++i) {
+      TreeNode nd;
+      nd.item = items[i];
+      nd.parent = at;
+      nd.owner = holder;
+      nd.order = order;
+      nd.n_tok = tree[at].n_tok + (items[i].kind == AKV_ITEM_TOKEN);
+      tree.push_back(nd);
+      const int32_t id = int32_t(tree.size()) - 1;
+      tree[at].kids.push_back(id);
+      at = id;
+    }
+    return holder;
+  }
+
+  // Deepest node (and its depth) reachable under the exact rule, and under the
+  // compatible rule (a depth-first walk over every branch whose key matches).
+  void tree_walk(const akv_item* items, int64_t n, int32_t& exact_node, int64_t& exact_len, int32_t& comp_node,
+                 int64_t& comp_len) {
+    exact_node = 0;
+    exact_len = 0;
+    for (int64_t i = 0; i < n; ++i) {
+      int32_t next = -1;
+      for (int32_t k : tree[exact_node].kids)
+        if (same_item(tree[k].item, items[i])) {
+          next = k;
+          break;
+        }
+      if (next < 0) break;
+      exact_node = next;
+      exact_len = i + 1;
+    }
+    comp_node = 0;
+    comp_len = 0;
+    std::vector<std::pair<int32_t, int64_t>> stack{{0, 0}};
+    while (!stack.empty()) {
+      auto [nd, d] = stack.back();
+      stack.pop_back();
+      if (d > comp_len || (d == comp_len && d > 0 && tree[nd].order < tree[comp_node].order)) {
+        comp_node = nd;
+        comp_len = d;
+      }
+      if (d == n) continue;
+      for (int32_t k : tree[nd].kids)
+        if (same_key(tree[k].item, items[d])) stack.push_back({k, d + 1});
+    }
+  }
+
+  akv_match tree_match(const akv_item* items, int64_t n, int32_t* node_out = nullptr) {
+    check_items(items, n);
+    int32_t en, cn;
+    int64_t el, cl;
+    tree_walk(items, n, en, el, cn, cl);
+    akv_match m{AKV_MATCH_NONE, -1, 0, 0};
+    int32_t node = 0;
+    if (cl > el) {
+      m.kind = AKV_MATCH_RETRIGGER;
+      node = cn;
+      m.n_items = cl;
+    } else if (el > 0) {
+      m.kind = AKV_MATCH_EXACT;
+      node = en;
+      m.n_items = el;
+    }
+    if (node > 0) {
+      m.seq = tree[node].owner;
+      m.n_tokens = tree[node].n_tok;
+    }
+    if (node_out) *node_out = node;
+    return m;
+  }
+
+  int32_t tree_reuse(const akv_item* items, int64_t n, akv_match* out, cudaStream_t st) {
+    int32_t node = 0;
+    const akv_match m = tree_match(items, n, &node);
+    if (out) *out = m;
+    if (m.kind == AKV_MATCH_NONE) return -1;
+    // shifts: request position - cached position, per token of the matched path
+    std::vector<int32_t> shift;
+    if (m.kind == AKV_MATCH_RETRIGGER) {
+      std::vector<const akv_item*> path;
+      for (int32_t k = node; k > 0; k = tree[k].parent) path.push_back(&tree[k].item);
+      std::reverse(path.begin(), path.end());
+      for (size_t i = 0; i < path.size(); ++i)
+        if (path[i]->kind == AKV_ITEM_TOKEN) {
+          const int64_t d = int64_t(items[i].b) - path[i]->b;
+          if (d < kI32Min || d > kI32Max) fail(AKV_ERR_OVERFLOW, "position shift of token %zu leaves int32", i);
+          shift.push_back(int32_t(d));
+        }
+    }
+    int32_t sid = -1;
+    fork(m.seq, m.n_tokens, &sid);
+    try {
+      for (size_t a = 0; a < shift.size();) {
+        size_t b = a + 1;
+        while (b < shift.size() && shift[b] == shift[a]) ++b;
+        if (shift[a] != 0) repos(sid, int64_t(a), int64_t(b), shift[a]);
+        a = b;
+      }
+      if (!shift.empty()) flush(std::vector<int32_t>{sid}, st);
+    } catch (...) {
+      free_seq(sid);  // leave nothing behind on failure
+      throw;
+    }
+    return sid;
+  }
+
+  void tree_clear() {
+    for (int32_t q : tree_seqs)
+      if (q >= 0 && q < int32_t(seqs.size()) && live[q]) free_seq(q);
+    tree_seqs.clear();
+    tree.assign(1, TreeNode{});
+    tree_inserts = 0;
+  }
+
   // ------------------------------------------------------- attention mass
   // Per segment and logical token: the softmax probability the token's entry
   // receives, summed over the segment's query rows and heads, from the Q and
@@ -1606,6 +1773,32 @@ akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream) {
 akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs, const void* q,
                       int64_t n_q_rows, void* o, float* lse, float scale, void* stream) {
   return guard(ctx, [&] { ctx->attend(layer, segs, n_segs, q, n_q_rows, o, lse, scale, as_stream(stream)); });
+}
+
+akv_status akv_tree_insert(akv_ctx* ctx, const akv_item* items, int64_t n, int32_t seq, int32_t* tree_seq_out) {
+  return guard(ctx, [&] {
+    const int32_t t = ctx->tree_insert(items, n, seq);
+    if (tree_seq_out) *tree_seq_out = t;
+  });
+}
+
+akv_status akv_tree_match(akv_ctx* ctx, const akv_item* items, int64_t n, akv_match* out) {
+  return guard(ctx, [&] {
+    if (!out) fail(AKV_ERR_ARG, "null output");
+    *out = ctx->tree_match(items, n);
+  });
+}
+
+akv_status akv_tree_reuse(akv_ctx* ctx, const akv_item* items, int64_t n, akv_match* out, int32_t* seq_out,
+                          void* stream) {
+  return guard(ctx, [&] {
+    if (!seq_out) fail(AKV_ERR_ARG, "null output");
+    *seq_out = ctx->tree_reuse(items, n, out, as_stream(stream));
+  });
+}
+
+akv_status akv_tree_clear(akv_ctx* ctx) {
+  return guard(ctx, [&] { ctx->tree_clear(); });
 }
 
 akv_status akv_fragmentation(akv_ctx* ctx, int32_t seq, double* frac_out) {

@@ -119,6 +119,31 @@ typedef struct akv_segment {
   int32_t reserved;   /* must be 0 */
 } akv_segment;
 
+/* Extended radix tree ([AKV-blog] section 3 "Resolving History Dependence via
+ * Extended Radix Trees"; [AKV-notes] "Cache Reuse Matching Rules").  A path is
+ * a list of items: a cached token (kind AKV_ITEM_TOKEN, a = token id, b = the
+ * position its cached key encodes) or a cache-operation marker (kind >= 1 is
+ * the caller's operation code, a, b, c its arguments), in the order they were
+ * applied.  Tokens of a path are the logical tokens of the sequence that holds
+ * it, in order. */
+#define AKV_ITEM_TOKEN 0
+typedef struct akv_item {
+  int32_t kind;
+  int32_t a;
+  int32_t b;
+  int32_t c;
+} akv_item;
+
+#define AKV_MATCH_NONE 0
+#define AKV_MATCH_EXACT 1      /* same tokens, positions and operations: reuse as is */
+#define AKV_MATCH_RETRIGGER 2  /* same tokens and operations, other positions: reuse after rotating keys */
+typedef struct akv_match {
+  int32_t kind;       /* AKV_MATCH_* */
+  int32_t seq;        /* tree-held sequence with the matched prefix (-1: none) */
+  int64_t n_items;    /* request items matched */
+  int64_t n_tokens;   /* tokens among them */
+} akv_match;
+
 /* Per-kernel launch statistics collected while profiling is enabled. */
 typedef struct akv_kernel_stats {
   int64_t launches[4];   /* [0] kv_write  [1] repos_rotate  [2] segment_attn  [3] compact_copy */
@@ -205,6 +230,32 @@ AKV_API akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream);
 AKV_API akv_status akv_attend(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs,
                       const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
                       void* stream);
+
+/* Insert the path `items[0 .. n)` held by live sequence `seq` (its first
+ * n_tokens(items) logical tokens).  When the path adds tree nodes the tree
+ * forks `seq` (shared pages, reference-counted) and keeps that fork as the
+ * holder of the new nodes; *tree_seq_out (nullable) receives it, or -1 when
+ * the path was already present.  Items are compared exactly. */
+AKV_API akv_status akv_tree_insert(akv_ctx* ctx, const akv_item* items, int64_t n, int32_t seq,
+                           int32_t* tree_seq_out);
+
+/* Match a request path: the longest exact-match prefix, replaced by the
+ * longest history-compatible branch (same tokens and operations, positions
+ * free) only if that is strictly longer; a walk stops at the first item that
+ * differs.  Ties between equally long branches go to the earliest inserted
+ * holder. */
+AKV_API akv_status akv_tree_match(akv_ctx* ctx, const akv_item* items, int64_t n, akv_match* out);
+
+/* Match, then give the request a new sequence holding the matched prefix:
+ * a fork of the holder (copy-on-write page references); on a retrigger match
+ * every token is also repositioned by (request position - cached position)
+ * and flushed, i.e. the repos_rotate kernel rotates the keys into
+ * copy-on-write pages.  *seq_out = -1 when nothing matches. */
+AKV_API akv_status akv_tree_reuse(akv_ctx* ctx, const akv_item* items, int64_t n, akv_match* out, int32_t* seq_out,
+                          void* stream);
+
+/* Forget every path and free the tree's sequences. */
+AKV_API akv_status akv_tree_clear(akv_ctx* ctx);
 
 /* Fragmentation of a sequence's pages ([AKV-blog] "Dilemma 2: Memory
  * Fragmentation in Paged Pools"): 1 - visible tokens / (K pages * page_size),

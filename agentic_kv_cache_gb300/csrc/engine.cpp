@@ -266,6 +266,11 @@ struct akv_ctx {
   Marks mk, mv;
   std::vector<std::vector<Tok>> seqs;
   std::vector<uint8_t> live;
+  struct Pend {  // a recorded reposition not yet folded into the tokens
+    int64_t s, e;
+    int32_t d;
+  };
+  std::vector<std::vector<Pend>> pend;  // per sequence
   // Per sequence: an upper bound on |position| and |pending shift| of its
   // tokens; while bound + |delta| fits in int32 no per-token overflow check is needed.
   std::vector<int64_t> bound;
@@ -313,9 +318,42 @@ struct akv_ctx {
 
   int64_t row_elems_k() const { return int64_t(cfg.n_kv_heads) * cfg.page_size * cfg.d_rot; }
 
-  std::vector<Tok>& seq(int32_t id) {
+  // Token records of a live sequence as they are; repositions recorded since
+  // the last settle are still in pend[id].
+  std::vector<Tok>& seq_raw(int32_t id) {
     if (id < 0 || id >= int32_t(seqs.size()) || !live[id]) fail(AKV_ERR_ARG, "sequence %d is not live", id);
     return seqs[id];
+  }
+
+  // Token records with every recorded reposition folded into the per-token
+  // pending shift (what every reader of shifts, positions or order sees).
+  std::vector<Tok>& seq(int32_t id) {
+    auto& toks = seq_raw(id);
+    settle(id);
+    return toks;
+  }
+
+  // repos records a shift for a span in O(1); the spans are folded into the
+  // tokens here, all at once, with a difference array (O(tokens + spans)).
+  void settle(int32_t id) {
+    auto& p = pend[id];
+    if (p.empty()) return;
+    auto& toks = seqs[id];
+    if (p.size() == 1) {
+      for (int64_t i = p[0].s; i < p[0].e; ++i) toks[i].delta += p[0].d;
+    } else {
+      std::vector<int64_t> diff(toks.size() + 1, 0);
+      for (const Pend& r : p) {
+        diff[size_t(r.s)] += r.d;
+        diff[size_t(r.e)] -= r.d;
+      }
+      int64_t acc = 0;
+      for (size_t i = 0; i < toks.size(); ++i) {
+        acc += diff[i];
+        if (acc) toks[i].delta += int32_t(acc);
+      }
+    }
+    p.clear();
   }
 
   int32_t new_id() {
@@ -327,6 +365,7 @@ struct akv_ctx {
       return id;
     }
     seqs.emplace_back();
+    pend.emplace_back();
     live.push_back(1);
     bound.push_back(0);
     return int32_t(seqs.size() - 1);
@@ -476,7 +515,7 @@ struct akv_ctx {
   }
 
   void drop(int32_t sid, int64_t s, int64_t e) {
-    auto& toks = seq(sid);
+    auto& toks = seq_raw(sid);  // visibility only
     check_span(toks, s, e, "drop");
     for (int64_t i = s; i < e; ++i) toks[i].vis = 0;
   }
@@ -501,14 +540,20 @@ struct akv_ctx {
 
   void grow_bound(int32_t sid, int64_t by) {
     bound[sid] += by;
-    if (bound[sid] > kI32Max) bound[sid] = exact_bound(seqs[sid]);
+    if (bound[sid] > kI32Max) bound[sid] = exact_bound(seq(sid));
   }
 
   void repos(int32_t sid, int64_t s, int64_t e, int32_t delta) {
-    auto& toks = seq(sid);
+    auto& toks = seq_raw(sid);
     check_span(toks, s, e, "repos");
-    check_shift(toks, s, e, delta, bound[sid]);
-    for (int64_t i = s; i < e; ++i) toks[i].delta += delta;
+    if (bound[sid] + std::abs(int64_t(delta)) <= kI32Max) {
+      // no token can leave int32: record the span, fold it in when read
+      if (s < e && delta != 0) pend[sid].push_back(Pend{s, e, delta});
+    } else {
+      settle(sid);
+      check_shift(toks, s, e, delta, bound[sid]);
+      for (int64_t i = s; i < e; ++i) toks[i].delta += delta;
+    }
     grow_bound(sid, std::abs(int64_t(delta)));
   }
 
@@ -594,7 +639,8 @@ struct akv_ctx {
   }
 
   void free_seq(int32_t sid) {
-    auto& toks = seq(sid);
+    auto& toks = seq_raw(sid);
+    pend[sid].clear();
     std::vector<int32_t> kps, vps;
     pages_of(toks, 0, toks.size(), kps, vps);
     for (int32_t q : kps) K.dec(q);
@@ -608,7 +654,7 @@ struct akv_ctx {
   // [AKV-blog] "Dilemma 2: Memory Fragmentation in Paged Pools".  The share
   // of the slots of the sequence's K pages that hold none of its visible tokens.
   double fragmentation(int32_t sid) {
-    auto& toks = seq(sid);
+    auto& toks = seq_raw(sid);  // visibility only
     std::vector<int32_t> kps, vps;
     pages_of(toks, 0, toks.size(), kps, vps);
     if (kps.empty()) return 0.0;
@@ -693,6 +739,7 @@ struct akv_ctx {
   }
 
   void flush(const std::vector<int32_t>& ids, cudaStream_t st) {
+    for (int32_t sid : ids) settle(sid);
     // Budget check on simulated reference counts, so a failure changes nothing.
     std::vector<int32_t> touched;  // pages with a simulated change
     int64_t need = 0;
@@ -1734,7 +1781,7 @@ akv_status akv_seq_free(akv_ctx* ctx, int32_t seq) {
 akv_status akv_seq_len(akv_ctx* ctx, int32_t seq, int64_t* n_out) {
   return guard(ctx, [&] {
     if (!n_out) fail(AKV_ERR_ARG, "null output");
-    *n_out = int64_t(ctx->seq(seq).size());
+    *n_out = int64_t(ctx->seq_raw(seq).size());
   });
 }
 

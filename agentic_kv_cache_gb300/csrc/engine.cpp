@@ -741,34 +741,40 @@ struct akv_ctx {
   void flush(const std::vector<int32_t>& ids, cudaStream_t st) {
     for (int32_t sid : ids) settle(sid);
     // Budget check on simulated reference counts, so a failure changes nothing.
-    std::vector<int32_t> touched;  // pages with a simulated change
+    // Each sequence's moving pages are computed once and reused by flush_seq.
+    std::vector<std::vector<int32_t>> orders(ids.size());
     int64_t need = 0;
-    std::vector<int32_t> order;
-    for (int32_t sid : ids) {
-      auto& toks = seqs[sid];
-      moving_pages(toks, order);
-      std::vector<int32_t> cow;
-      for (int32_t q : order)
-        if (K.rc(q) + sim_rc[q] > 1) cow.push_back(q);
-      need += int64_t(cow.size());
-      if (cow.empty()) continue;
-      mk.next();
-      for (const Tok& t : toks)
-        if (!t.vis) mk.test_set(t.kp);  // marked: a dropped token of this sequence sits in the page
-      for (int32_t q : cow)
-        if (!mk.test(q)) {
-          if (sim_rc[q] == 0) touched.push_back(q);
-          sim_rc[q] -= 1;
-        }
+    if (ids.size() == 1) {  // one sequence: its copies are its shared moving pages
+      moving_pages(seqs[ids[0]], orders[0]);
+      for (int32_t q : orders[0]) need += K.rc(q) > 1;
+    } else {
+      std::vector<int32_t> touched;  // pages with a simulated change
+      for (size_t k = 0; k < ids.size(); ++k) {
+        auto& toks = seqs[ids[k]];
+        moving_pages(toks, orders[k]);
+        std::vector<int32_t> cow;
+        for (int32_t q : orders[k])
+          if (K.rc(q) + sim_rc[q] > 1) cow.push_back(q);
+        need += int64_t(cow.size());
+        if (cow.empty()) continue;
+        mk.next();
+        for (const Tok& t : toks)
+          if (!t.vis) mk.test_set(t.kp);  // marked: a dropped token of this sequence sits in the page
+        for (int32_t q : cow)
+          if (!mk.test(q)) {
+            if (sim_rc[q] == 0) touched.push_back(q);
+            sim_rc[q] -= 1;
+          }
+      }
+      for (int32_t q : touched) sim_rc[q] = 0;
     }
-    for (int32_t q : touched) sim_rc[q] = 0;
     if (need > K.n_free()) fail(AKV_ERR_NO_PAGES, "flush needs %lld copy-on-write pages", (long long)need);
 
     std::vector<akv::RunDesc> runs;
     std::vector<int32_t> deltas;          // distinct shifts, first-appearance order
     std::unordered_map<int32_t, int32_t> didx;
     std::vector<int32_t> flat;
-    for (int32_t sid : ids) flush_seq(seqs[sid], runs, deltas, didx, flat);
+    for (size_t k = 0; k < ids.size(); ++k) flush_seq(seqs[ids[k]], orders[k], runs, deltas, didx, flat);
     if (!runs.empty()) last_runs.swap(flat);
     if (meta || runs.empty()) return;
 
@@ -841,10 +847,9 @@ struct akv_ctx {
     up.done(st);
   }
 
-  void flush_seq(std::vector<Tok>& toks, std::vector<akv::RunDesc>& runs, std::vector<int32_t>& deltas,
-                 std::unordered_map<int32_t, int32_t>& didx, std::vector<int32_t>& flat) {
-    std::vector<int32_t> order;
-    moving_pages(toks, order);
+  // order: the sequence's moving pages in first-appearance order (moving_pages).
+  void flush_seq(std::vector<Tok>& toks, const std::vector<int32_t>& order, std::vector<akv::RunDesc>& runs,
+                 std::vector<int32_t>& deltas, std::unordered_map<int32_t, int32_t>& didx, std::vector<int32_t>& flat) {
     if (order.empty()) return;
     std::vector<int32_t> cow;
     for (int32_t q : order) {  // page_dst: source page -> destination page
@@ -857,8 +862,10 @@ struct akv_ctx {
     }
     mk.next();
     for (int32_t q : cow) mk.test_set(q);  // marked = copied page
-    // Runs: maximal groups of consecutive emitted tokens with equal
-    // (source, destination, shift) and consecutive slots.
+    mv.next();                             // marked = a copied page that keeps a token of this sequence
+    // One pass: runs (maximal groups of consecutive emitted tokens with equal
+    // source, destination and shift, consecutive slots), and each emitted
+    // token moved to its destination with its shift folded into its position.
     bool open = false;
     int32_t c_src = 0, c_dst = 0, c_delta = 0, c_lo = 0, c_hi = 0;
     auto close = [&]() {
@@ -880,6 +887,7 @@ struct akv_ctx {
       const bool copied = mk.test(t.kp);
       const bool emit = t.vis && (t.delta != 0 || copied);
       if (!emit) {
+        if (copied) mv.test_set(t.kp);  // a dropped token stays behind in the copied page
         close();
         continue;
       }
@@ -895,21 +903,14 @@ struct akv_ctx {
         c_lo = t.slot;
         c_hi = t.slot + 1;
       }
+      t.kp = d;
+      t.pos += t.delta;
+      t.delta = 0;
     }
     close();
-    for (Tok& t : toks) {
-      const bool copied = mk.test(t.kp);
-      if (t.vis && (t.delta != 0 || copied)) {
-        if (copied) t.kp = page_dst[t.kp];
-        t.pos += t.delta;
-        t.delta = 0;
-      }
-    }
     // A copied page loses this sequence's reference unless a dropped token stays in it.
-    mk.next();
-    for (const Tok& t : toks) mk.test_set(t.kp);
     for (int32_t q : cow)
-      if (!mk.test(q)) K.dec(q);
+      if (!mv.test(q)) K.dec(q);
   }
 
   // -------------------------------------------------------------- segments

@@ -12,7 +12,8 @@
 // Work: the copy-run list (source K / V page and first slot, destination K /
 // V page and first slot, row count, shift index or -1) times every layer and
 // kv head.  HBM-bound streaming: a CTA takes one (layer, run) unit and moves
-// 16-byte vectors with several independent loads in flight before stores.
+// 16-byte vectors with several independent loads in flight before stores;
+// keys and values go in two launches so each keeps its register count low.
 #include <cuda_bf16.h>
 
 #include "akv_internal.h"
@@ -24,8 +25,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
-template <int D, bool kHalf>
-__global__ void __launch_bounds__(kThreads) compact_copy_kernel(uint4* __restrict__ kpool, uint4* __restrict__ vpool,
+// kPart 0: the key rows (rotated or copied); 1: the value rows (copied).  Two
+// launches keep each one's registers low, so more warps keep loads in flight.
+template <int D, bool kHalf, int kPart>
+__global__ void __launch_bounds__(kThreads, kPart == 1 ? 2 : 3) compact_copy_kernel(uint4* __restrict__ kpool, uint4* __restrict__ vpool,
                                                                const CopyRun* __restrict__ runs,
                                                                const float2* __restrict__ cs, int n_runs, int n_layers,
                                                                int heads, int page, int64_t n_pages, int vv_shift) {
@@ -41,13 +44,15 @@ __global__ void __launch_bounds__(kThreads) compact_copy_kernel(uint4* __restric
     // ---- K rows: rotated when the run carries a shift, else copied.  A head's
     // rows are contiguous in a page; threads walk (row, vector) of one head and
     // kUnroll heads are in flight at once.
-    {
+    if constexpr (kPart == 0) {
       const uint4* src = kpool + (layer * n_pages + cr.src_k) * kpage + cr.src_lo * VK;
       uint4* dst = kpool + (layer * n_pages + cr.dst_k) * kpage + cr.dst_lo * VK;
       const float2* cs_row = cr.didx >= 0 ? cs + int64_t(cr.didx) * (D / 2) : nullptr;
       const int per_head = cr.n * W;
+#pragma unroll 1
       for (int t = int(threadIdx.x); t < per_head; t += kThreads) {
         const int row = t / W, v = t % W, off = row * VK + v;
+#pragma unroll 1
         for (int h0 = 0; h0 < heads; h0 += kUnroll) {
           uint4 x[kUnroll], y[kUnroll];
 #pragma unroll
@@ -85,12 +90,14 @@ __global__ void __launch_bounds__(kThreads) compact_copy_kernel(uint4* __restric
       }
     }
     // ---- V rows: copied, the same walk
-    {
+    if constexpr (kPart == 1) {
       const uint4* src = vpool + (layer * n_pages + cr.src_v) * vpage + int64_t(cr.src_lo) * VV;
       uint4* dst = vpool + (layer * n_pages + cr.dst_v) * vpage + int64_t(cr.dst_lo) * VV;
       const int per_head = cr.n << vv_shift;
       constexpr int kU = 2 * kUnroll;  // a plain copy holds twice as many vectors in flight
+#pragma unroll 1
       for (int t = int(threadIdx.x); t < per_head; t += kThreads) {
+#pragma unroll 1
         for (int h0 = 0; h0 < heads; h0 += kU) {
           uint4 x[kU];
 #pragma unroll
@@ -113,8 +120,10 @@ cudaError_t launch_variant(void* kpool, void* vpool, const CopyRun* runs, const 
   if ((8 << vv_shift) != dv) return cudaErrorInvalidValue;  // d_v must be 8 x a power of two
   const int64_t units = int64_t(n_layers) * n_runs;
   const int grid = int(units < int64_t(n_sm) * 8 ? units : int64_t(n_sm) * 8);
-  compact_copy_kernel<D, kHalf><<<grid, kThreads, 0, st>>>(static_cast<uint4*>(kpool), static_cast<uint4*>(vpool), runs,
-                                                           cs, n_runs, n_layers, heads, page, n_pages, vv_shift);
+  compact_copy_kernel<D, kHalf, 0><<<grid, kThreads, 0, st>>>(static_cast<uint4*>(kpool), static_cast<uint4*>(vpool),
+                                                              runs, cs, n_runs, n_layers, heads, page, n_pages, vv_shift);
+  compact_copy_kernel<D, kHalf, 1><<<grid, kThreads, 0, st>>>(static_cast<uint4*>(kpool), static_cast<uint4*>(vpool),
+                                                              runs, cs, n_runs, n_layers, heads, page, n_pages, vv_shift);
   return cudaGetLastError();
 }
 

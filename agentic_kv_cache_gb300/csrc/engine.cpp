@@ -720,7 +720,7 @@ struct akv_ctx {
               st);
     Timed tm;
     const double bytes = 2.0 * double(n_vis) * cfg.n_layers * cfg.n_kv_heads * (cfg.d_rot + cfg.d_v) * 2.0;
-    begin_timed(kCompact, bytes, 0.0, st, tm);
+    begin_timed(kCompact, bytes, 0.0, st, tm, 2);  // key launch + value launch
     cuda_check(akv::launch_compact_copy(kpool, vpool, static_cast<akv::CopyRun*>(druns), static_cast<float2*>(dcs),
                                         int(runs.size()), cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.d_v,
                                         cfg.page_size, cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, n_sm, st),

@@ -320,10 +320,11 @@ def compaction(steps=4, warmup=1, n_layers=32):
     assert eng.check_device_error(st) == 0
     del eng, pools, kv
     torch.cuda.empty_cache()
-    ms = stats["ms"] / stats["launches"]
-    gbs = stats["bytes"] / stats["launches"] / (ms * 1e-3) / 1e9
+    calls = stats["launches"] // 2  # one compaction = a key launch and a value launch
+    ms = stats["ms"] / calls
+    gbs = stats["bytes"] / calls / (ms * 1e-3) / 1e9
     return {"workload": f"llama8b_32k post-drop branch, {n_layers} layers", "fragmentation_before": frag,
-            "ms_per_launch": ms, "bytes_per_launch": stats["bytes"] / stats["launches"], "GB/s": gbs,
+            "ms_per_compaction": ms, "bytes_per_compaction": stats["bytes"] / calls, "GB/s": gbs,
             "frac_of_hbm": gbs / load_peaks()[0]}
 
 

@@ -55,7 +55,7 @@ constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitim
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;  // AKV_ERR_DEVICE_TIMEOUT
 constexpr int32_t kErrDevice = 8;   // AKV_ERR_DEVICE
-constexpr int kSlots = 5;
+constexpr int kSlots = 4;
 constexpr int kMaxRuns = 8;  // runs per 128-key tile: 128 / page, page >= 16
 
 template <int D>
@@ -65,8 +65,8 @@ struct Layout {
   static constexpr uint32_t kTile = kBlocks * kBlockBytes;
   static constexpr uint32_t kQ = 0;                          // Q_A, Q_B
   static constexpr uint32_t kSlot = kQ + 2 * kTile;          // K/V slots
-  static constexpr uint32_t kColE = kSlot + kSlots * kTile;  // int32 [2][128]: entry per key column
-  static constexpr uint32_t kBars = kColE + 2 * 128 * 4;
+  static constexpr uint32_t kColE = kSlot + kSlots * kTile;  // int32 [2 tiles][2 buffers][128]: entry per key column
+  static constexpr uint32_t kBars = kColE + 2 * 2 * 128 * 4;
   static constexpr uint32_t kBytes = kBars + 256;
 };
 
@@ -108,7 +108,7 @@ __device__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, vol
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kTileKeys / p.page;
   const int layer_base = p.layer * p.n_pages;
-  int armed[kSlots] = {0, 0, 0, 0, 0};
+  int armed[kSlots] = {0, 0, 0, 0};
   int ld0 = 0, q_loads = 0;
   bool ok = true;
   for (int u = u0; u < u1 && ok; ++u) {
@@ -420,7 +420,7 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
   const float sl2 = p.scale_log2;
   const int bar_id = 1 + t;  // named barrier of this warpgroup
-  int* colE = reinterpret_cast<int*>(smem + L::kColE) + t * 128;
+  int* colE_base = reinterpret_cast<int*>(smem + L::kColE) + t * 256;  // two buffers, by tile parity
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
   float m_run = -INFINITY, l_run = 0.f;
@@ -436,13 +436,12 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
   }
   for (int j = 0; j < n_t; ++j) {
     ok = ptx::mbar_wait(bar(kBarS0 + t), (ph ^ j) & 1, abort_flag, kWaitLimitNs);
-    if (!ptx::bar_red_and(bar_id, 128, ok)) {
-      ok = false;
-      break;
-    }
     // Entry index of key column r of tile j (INT_MAX: no entry there);
     // columns are (run c / page, slot c % page) of the tile's runs.  The run
     // of the next tile is fetched now so its latency hides behind this tile.
+    // The entries go to the buffer of this tile's parity: the other buffer may
+    // still be read by a thread finishing tile j - 1.
+    int* colE = colE_base + (j & 1) * 128;
     int e = INT_MAX;
     {
       const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
@@ -451,7 +450,13 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       const int ri = (w.t0 + j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
-    const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
+    // One barrier per tile: every thread's S arrived and every column has an
+    // entry; only when that fails does a second one tell a time-out from masking.
+    const bool all_valid = ptx::bar_red_and(bar_id, 128, ok && e != INT_MAX);
+    if (!all_valid && !ptx::bar_red_and(bar_id, 128, ok)) {
+      ok = false;
+      break;
+    }
     ptx::tc_fence_after();
     // With every column valid the entries are consecutive, so the last column
     // holds the tile's largest entry index.

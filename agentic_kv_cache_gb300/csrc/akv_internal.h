@@ -69,7 +69,7 @@ struct AttnSeg {
 // to partial slot `part`; the part that finishes last merges them all.
 struct AttnWork {
   int32_t seg;
-  int32_t kvh;
+  int32_t kvh;   // GQA: kv head; MLA: flags (kShadow)
   int32_t qt0;
   int32_t n_a;
   int32_t n_b;
@@ -78,6 +78,12 @@ struct AttnWork {
   int32_t part;  // partial slot of this split part, -1 when the item is not split
   int32_t comb;  // its CombineItem
 };
+
+// MLA work runs as CTA pairs (entries 2i, 2i + 1: two query tiles, one KV
+// range, one output half).  A segment with an odd number of query tiles
+// fills its last pair with a shadow: it repeats its partner's tile so the
+// pair's MMAs have both row halves, and writes nothing.
+constexpr int32_t kShadow = 1;
 
 // One split work item: its parts own partial slots [part0, part0 + n_parts);
 // count[t] is the ticket counter of query tile t, zero at launch (the host
@@ -93,8 +99,9 @@ struct AttnParams {
   CUtensorMap q_map;  // Q [n_q_rows][Hq][d_qk], box {64, G, 128/G}
   CUtensorMap k_map;  // rotated pool, [L*P][H][page][d_rot], box {64, page, 1, 1}
   CUtensorMap v_map;  // value pool,  [L*P][H][page][d_v],   box {64, page, 1, 1}
-  CUtensorMap k_tile_map;  // as k_map, box {64, page, 1, 128 / page}: a tile's consecutive pages at once
-  CUtensorMap v_tile_map;  // as v_map, box {64, page, 1, 128 / page}
+  CUtensorMap k_tile_map;  // GQA: as k_map, box {64, page, 1, 128 / page}: a tile's consecutive pages at once;
+                           // MLA: box {64, min(page, 64), 1, max(64 / page, 1)}: the pages of 64 keys
+  CUtensorMap v_tile_map;  // as v_map, with k_tile_map's box
   const AttnRun* runs;
   const AttnSeg* segs;
   const AttnWork* work;
@@ -177,6 +184,7 @@ cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st);
 // MLA variant: 16 query heads over one latent (d_v 512) + K_pe (64) per token;
 // work items carry the output half (0 or 1) in n_b.
 cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st);
+int segment_attn_mla_slots();
 
 // Merge split-KV partials: items [n_items], tiles_per_item query tiles of 128
 // rows each, `width` output columns per part.

@@ -26,6 +26,7 @@
 //     and shifts later tokens by n_stub - (e - s) ([Leyline] "Method").
 
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -300,6 +301,7 @@ struct akv_ctx {
   Staging st_k, st_v, st_q, st_o, st_lse;
   Staging partial;         // split-KV partial results (device only)
   int n_sm = 148;          // SMs of the device, for split decisions
+  int mla_slots = 148;     // MLA kernel CTAs resident at once (CTA pairs x 2)
   int split_override = 0;  // 0: choose the split factor; n >= 1: use n
   CUtensorMap k_map{}, v_map{}, k_tile_map{}, v_tile_map{};
   bool maps_ok = false;
@@ -982,14 +984,18 @@ struct akv_ctx {
     return sp;
   }
 
-  // Split-KV for the MLA kernel (one CTA per unit): cut every item's KV-tile
-  // range into up to S chunks so the launch fills whole waves of SMs; split
-  // chunks write partials and the chunk that finishes last merges them.
-  // Units run longest first (LPT), ties in (segment, tile, half, chunk) order.
+  // Split-KV for the MLA kernel (one CTA pair per pair of units): cut every
+  // pair's KV-tile range into up to S chunks so the launch fills whole waves
+  // of the SM pairs; split chunks write partials and the chunk that finishes
+  // last merges them.  Pairs run longest first (LPT), ties in (segment, tile,
+  // half, chunk) order.
   void plan_split(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts) {
+    // work holds CTA pairs (2i, 2i + 1) sharing one KV range; a pair is cut
+    // and scheduled as one.
+    const int64_t slots = std::max(2, mla_slots);
     auto units_for = [&](int S) {
       int64_t u = 0;
-      for (auto& w : work) u += std::min<int64_t>(S, std::max(1, w.n_a));
+      for (size_t k = 0; k < work.size(); k += 2) u += 2 * std::min<int64_t>(S, std::max(1, work[k].n_a));
       return u;
     };
     int best_s = 1;
@@ -998,38 +1004,53 @@ struct akv_ctx {
     for (int S : cands) {
       if (split_override > 0 && S != split_override) continue;
       const int64_t u = units_for(S);
-      const int64_t waves = (u + n_sm - 1) / n_sm;
+      const int64_t waves = (u + slots - 1) / slots;
       // A split part pays its partial write, a share of the merge and a
       // slower pipeline start, so splitting must buy more occupancy than that.
-      const double eff = double(u) / double(waves * n_sm) * (S == 1 ? 1.0 : 0.85);
+      const double eff = double(u) / double(waves * slots) * (S == 1 ? 1.0 : 0.85);
       if (eff > best + 1e-9) {
         best = eff;
         best_s = S;
       }
     }
     if (split_override > 0) best_s = std::min(split_override, 8);
-    std::vector<akv::AttnWork> units;
-    for (auto& w : work) {
-      const int span = w.n_a;
+    std::vector<std::array<akv::AttnWork, 2>> pairs;
+    for (size_t k = 0; k < work.size(); k += 2) {
+      const int span = work[k].n_a;
       const int chunks = std::min(best_s, std::max(1, span));
-      if (chunks == 1) {
-        units.push_back(w);
-        continue;
+      int32_t base[2] = {-1, -1}, ci[2] = {-1, -1};
+      if (chunks > 1) {
+        for (int m = 0; m < 2; ++m) {
+          if (work[k + m].kvh & akv::kShadow) continue;  // a shadow writes nothing, so owns no parts
+          comb.push_back(akv::CombineItem{n_parts, chunks, {0, 0}});
+          base[m] = n_parts;
+          ci[m] = int32_t(comb.size()) - 1;
+          n_parts += chunks;
+        }
       }
-      comb.push_back(akv::CombineItem{n_parts, chunks, {0, 0}});
       for (int c = 0; c < chunks; ++c) {
-        akv::AttnWork u = w;
-        u.t0 = int32_t(int64_t(span) * c / chunks);
-        u.t1 = int32_t(int64_t(span) * (c + 1) / chunks);
-        u.part = n_parts++;
-        u.comb = int32_t(comb.size()) - 1;
-        units.push_back(u);
+        std::array<akv::AttnWork, 2> pr = {work[k], work[k + 1]};
+        for (int m = 0; m < 2; ++m) {
+          pr[m].t0 = int32_t(int64_t(span) * c / chunks);
+          pr[m].t1 = int32_t(int64_t(span) * (c + 1) / chunks);
+          pr[m].part = base[m] >= 0 ? base[m] + c : -1;
+          pr[m].comb = ci[m];
+        }
+        pairs.push_back(pr);
       }
     }
-    auto cost = [](const akv::AttnWork& w) { return std::max(0, std::min(w.n_a, w.t1) - w.t0); };
-    std::stable_sort(units.begin(), units.end(),
-                     [&](const akv::AttnWork& a, const akv::AttnWork& b) { return cost(a) > cost(b); });
-    work.swap(units);
+    auto cost = [](const std::array<akv::AttnWork, 2>& pr) {
+      return std::max(0, std::min(pr[0].n_a, pr[0].t1) - pr[0].t0);
+    };
+    std::stable_sort(pairs.begin(), pairs.end(),
+                     [&](const std::array<akv::AttnWork, 2>& a, const std::array<akv::AttnWork, 2>& b) {
+                       return cost(a) > cost(b);
+                     });
+    work.clear();
+    for (auto& pr : pairs) {
+      work.push_back(pr[0]);
+      work.push_back(pr[1]);
+    }
   }
 
   // Persistent stream-K schedule for the GQA kernel: one CTA per SM, each
@@ -1224,10 +1245,16 @@ struct akv_ctx {
         return int32_t((lo_r + rpt - 1) / rpt);
       };
       if (cfg.layout == AKV_LAYOUT_MLA) {
-        // one query tile per item, one item per half of the 512 output columns (n_b = half)
-        for (int qt = 0; qt < n_qt; ++qt) {
-          const int32_t nt = tiles_of(qt);
-          for (int half = 0; half < 2; ++half) work.push_back(akv::AttnWork{i, 0, qt, nt, half, 0, nt, -1, -1});
+        // CTA pairs: query tiles qt and qt + 1 over the KV tiles either reads,
+        // one pair per half of the 512 output columns (n_b = half); a missing
+        // second tile becomes a shadow of the first
+        for (int qt = 0; qt < n_qt; qt += 2) {
+          const int32_t nt = std::max(tiles_of(qt), tiles_of(qt + 1));
+          const bool shadow = qt + 1 >= n_qt;
+          for (int half = 0; half < 2; ++half) {
+            work.push_back(akv::AttnWork{i, 0, qt, nt, half, 0, nt, -1, -1});
+            work.push_back(akv::AttnWork{i, shadow ? akv::kShadow : 0, shadow ? qt : qt + 1, nt, half, 0, nt, -1, -1});
+          }
         }
       } else {
         for (int qt = 0; qt < n_qt; qt += 2) {
@@ -1683,10 +1710,18 @@ struct akv_ctx {
       const uint64_t vs[3] = {uint64_t(c.d_v) * 2, uint64_t(c.page_size) * c.d_v * 2,
                               uint64_t(c.n_kv_heads) * c.page_size * c.d_v * 2};
       encode_map(&v_map, vpool, 4, vd, vs, box);
-      const uint32_t tbox[4] = {64, uint32_t(c.page_size), 1, uint32_t(128 / c.page_size)};
+      // GQA loads a 128-key tile's consecutive pages at once, MLA a 64-key unit
+      // (a 128-slot page is then two units).
+      const bool mla_units = c.layout == AKV_LAYOUT_MLA;
+      const uint32_t tbox[4] = {64, uint32_t(mla_units ? std::min(c.page_size, 64) : c.page_size), 1,
+                                uint32_t(mla_units ? std::max(1, 64 / c.page_size) : 128 / c.page_size)};
       encode_map(&k_tile_map, kpool, 4, kd, ks, tbox);
       encode_map(&v_tile_map, vpool, 4, vd, vs, tbox);
       maps_ok = true;
+    }
+    if (c.layout == AKV_LAYOUT_MLA) {
+      mla_slots = akv::segment_attn_mla_slots();
+      if (mla_slots <= 0) mla_slots = n_sm & ~1;
     }
   }
 

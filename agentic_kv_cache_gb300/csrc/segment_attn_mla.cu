@@ -7,16 +7,21 @@
 //   score = q_latent . c + q_pe . k_pe   (d_qk = 512 + 64)
 //   out   = sum_j p_j c_j                (d_v = 512).
 //
-// GB300 design.  One CTA = one 128-row query tile (8 tokens x 16 heads) and
-// one half of the 512 output columns: O for all 512 columns would fill TMEM
-// by itself, so each half recomputes S (+53% MMA over the algorithmic count;
-// the two halves run as separate CTAs).  TMEM: S0, S1 (double-buffered, P
-// written back over the consumed S columns as bf16 pairs) and the 256-column O
-// half.  The Q tile (144 KiB) stays in shared memory; keys stream through a
-// 4-slot ring of 16 KiB chunks: per 128-key tile, the 8 latent chunks and the
-// K_pe chunk for QK^T, then the 4 latent chunks of this half for PV.
-// Warp 0: TMA producer; warp 1: TMEM owner and single-thread MMA issuer;
-// warps 2-5: softmax (one row per thread).  Every wait is bounded.
+// GB300 design: a CTA pair (cluster of 2, tcgen05 cta_group::2).  Each CTA
+// holds one 128-row query tile (8 tokens x 16 heads) and the pair shares one
+// half of the 512 output columns: O for all 512 columns would fill TMEM by
+// itself, so each half recomputes S (+53% MMA over the algorithmic count; the
+// two halves run as separate pairs).  Every MMA covers the pair's 256 rows
+// (M = 256, N = 128) and each CTA supplies half of its B operand: for QK^T the
+// 64 keys of its half of the 128-key tile, for PV 64 of the 128 output columns
+// of each quarter.  Per SM that halves the key bytes streamed per MMA clock;
+// a 5-slot ring of 16 KiB rounds (80 KiB) sits beside the resident 144 KiB Q
+// tile.  TMEM (allocated for the pair): S0, S1 (double-buffered, P written
+// back over the consumed S columns as bf16 pairs) and the 256-column O half.
+// Warps 0, 6, 7: TMA producers taking rounds of the key stream in turn (their
+// copies count on the even CTA's barriers); warp 1: TMEM allocation and, in
+// the even CTA, the single-thread MMA issuer; warps 2-5: softmax of the CTA's
+// own rows.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -29,28 +34,41 @@
 namespace akv {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kKeys = 128;     // keys per KV tile
-constexpr int kRows = 128;     // rows per query tile
+constexpr int kThreads = 256;
+constexpr int kProducers = 3;  // warps 0, 6 and 7 issue the copies, taking rounds in turn
+constexpr int kKeys = 128;     // keys per KV tile (the pair MMA's N for QK^T)
+constexpr int kRows = 128;     // rows per CTA; the pair covers 256
 constexpr int kLat = 512;      // latent width
 constexpr int kPe = 64;        // K_pe width
 constexpr int kQChunks = (kLat + kPe) / 64;  // 9 chunks of the QK contraction
-constexpr int kVChunks = 256 / 64;           // 4 chunks of one output half
-constexpr int kRing = 4;
+constexpr int kQKRounds = 5;                 // latent chunks in pairs, then K_pe
+constexpr int kPVRounds = 2;                 // one per O quarter
+constexpr int kPerTile = kQKRounds + kPVRounds;
+constexpr int kRing = 5;
 constexpr int kMaxRuns = 8;  // runs per 128-key tile: 128 / page, page >= 16
-constexpr uint32_t kChunk = 128 * 128;       // 128 rows x 64 bf16
+constexpr uint32_t kQChunk = 128 * 128;      // 128 rows x 64 bf16
+constexpr uint32_t kUnit = 64 * 128;         // 64 keys x 64 bf16: one copy
+constexpr uint32_t kSlot = 2 * kUnit;        // one round: two copies
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;
+constexpr uint16_t kBoth = 0x3;  // CTA mask of the pair
 
 // shared memory layout (bytes)
-constexpr uint32_t kQ = 0;                          // 9 chunks of Q
-constexpr uint32_t kSlots = kQ + kQChunks * kChunk;  // ring
-constexpr uint32_t kColE = kSlots + kRing * kChunk;  // int32[128]
+constexpr uint32_t kQ = 0;                           // 9 chunks of Q
+constexpr uint32_t kSlots = kQ + kQChunks * kQChunk;  // ring of 16 KiB slots
+constexpr uint32_t kColE = kSlots + kRing * kSlot;    // int32[128]
 constexpr uint32_t kBars = kColE + 128 * 4;
 constexpr uint32_t kBytes = kBars + 256;
+static_assert(kBytes + 1024 <= 232448, "shared memory");
 
+// Full and Q count both CTAs' bytes and live in the even CTA; Empty, S and O
+// are signalled to both CTAs by multicast commits; P (even CTA) collects the
+// 256 softmax threads of the pair.  Only the wait on P acquires at cluster
+// scope (thread arrivals from the peer); the others are completed by copies
+// and commits, whose CTA-scope waits are much cheaper on the producer's and
+// the MMA thread's per-unit path.
 enum Bar { kBarQ = 0, kBarFull0, kBarEmpty0 = kBarFull0 + kRing, kBarS0 = kBarEmpty0 + kRing, kBarP = kBarS0 + 2,
            kBarO, kBarFin, kNumBars };
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
@@ -68,202 +86,260 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Chunks are loaded in the order the MMA thread consumes them:
-//   QK chunks of tile 0, then for each tile j: QK chunks of tile j+1 (if
-//   any), PV chunks of tile j.
-// Stream position ld goes to ring slot ld % kRing.  chunk_at() maps a stream
-// position to (tile, chunk), chunk < 9: QK (latent 0..7, K_pe 8), 9..12: PV.
-constexpr int kPerTile = kQChunks + kVChunks;
+// The key stream is cut into rounds, each one ring slot filled by one or two
+// copies counted on one barrier (a copy and its barrier cost a producer thread
+// far more than the bytes, so rounds are large and three threads issue them).
+// Order = the MMA thread's: QK rounds of tile 0, then for each tile j: QK
+// rounds of tile j+1 (if any), PV rounds of tile j.  QK round m < 4: latent
+// chunks 2m and 2m+1 of the CTA's own 64 keys; m = 4: its K_pe chunk.  PV
+// round q: latent columns 256 half + 128 q + 64 rank of all 128 keys (two
+// copies, one per key half).  Round rd uses slot rd % kRing.
 
-__device__ __forceinline__ void chunk_at(int ld, int n_tiles, int& tile, int& chunk) {
-  if (ld < kQChunks) {
-    tile = 0;
-    chunk = ld;
-    return;
-  }
-  int rest = ld - kQChunks;
-  // blocks of (QK of j+1, PV of j) for j = 0 .. n-2 (13 chunks each), then PV of n-1
-  const int j = rest / kPerTile;
-  if (j < n_tiles - 1) {
-    const int c = rest % kPerTile;
-    if (c < kQChunks) {
-      tile = j + 1;
-      chunk = c;
-    } else {
-      tile = j;
-      chunk = c;
-    }
-  } else {
-    tile = n_tiles - 1;
-    chunk = kQChunks + (rest - (n_tiles - 1) * kPerTile);
+// Pages of one KV tile per 64-key half h: the K_pe and latent pages of the
+// half's first run and whether the half's pages are consecutive (then one
+// copy loads the unit).
+struct TilePages {
+  int k0, k1, v0, v1;
+  uint32_t cons;  // bit h: K_pe pages of half h consecutive; bit 2 + h: latent pages
+};
+
+__device__ __forceinline__ void load_runs(const AttnParams& p, const AttnSeg& seg, int tile, int rpt, int2 first,
+                                          int2 (&kv)[kMaxRuns]) {
+#pragma unroll
+  for (int g = 0; g < kMaxRuns; ++g) {
+    const int ri = tile * rpt + g;
+    kv[g] = first;  // past the last run the segment's first page stands in (finite values, masked out)
+    if (g < rpt && ri < seg.n_runs) kv[g] = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
   }
 }
 
+__device__ __forceinline__ TilePages tile_pages(const int2 (&kv)[kMaxRuns], int page, int rpu, int layer_base) {
+  TilePages t;
+  t.cons = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int g0 = page > 64 ? 0 : h * rpu;  // a 128-slot page holds both halves
+    int kf = kv[0].x, vf = kv[0].y;
+#pragma unroll
+    for (int g = 1; g < kMaxRuns; ++g)
+      if (g == g0) {
+        kf = kv[g].x;
+        vf = kv[g].y;
+      }
+    bool kc = true, vc = true;
+#pragma unroll
+    for (int g = 1; g < kMaxRuns; ++g) {
+      const int rel = g - g0;
+      if (rel > 0 && rel < rpu) {
+        kc = kc && kv[g].x == kf + rel;
+        vc = vc && kv[g].y == vf + rel;
+      }
+    }
+    if (h == 0) {
+      t.k0 = layer_base + kf;
+      t.v0 = layer_base + vf;
+    } else {
+      t.k1 = layer_base + kf;
+      t.v1 = layer_base + vf;
+    }
+    t.cons |= (kc ? 1u << h : 0u) | (vc ? 4u << h : 0u);
+  }
+  return t;
+}
+
 __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
-                                        volatile int* abort_flag) {
+                                        uint32_t rank, int who, volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
-  const int half = w.n_b;  // which 256 output columns
-  const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
-  ptx::mbar_arrive_expect_tx(bar(kBarQ), kQChunks * kChunk);
-  for (int c = 0; c < kQChunks; ++c)
-    ptx::tma_load_3d(sbase + kQ + c * kChunk, &p.q_map, bar(kBarQ), c * 64, 0, q_tok0);
+  const int rpu = p.page >= 64 ? 1 : 64 / p.page;  // runs per 64-key half
+  const int half = w.n_b;                           // which 256 output columns
+  const uint32_t lead_full0 = ptx::mapa(bar(kBarFull0), 0);
+  if (who == 0) {
+    ptx::prefetch_tensormap(&p.q_map);
+    ptx::prefetch_tensormap(&p.k_map);
+    ptx::prefetch_tensormap(&p.v_map);
+    ptx::prefetch_tensormap(&p.k_tile_map);
+    ptx::prefetch_tensormap(&p.v_tile_map);
+    const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
+    const uint32_t lead_q = ptx::mapa(bar(kBarQ), 0);
+    if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * kQChunks * kQChunk);
+    for (int c = 0; c < kQChunks; ++c)
+      ptx::tma_load_3d_pair(sbase + kQ + c * kQChunk, &p.q_map, lead_q, c * 64, 0, q_tok0);
+  }
   const int layer_base = p.layer * p.n_pages;
-  bool ok = true;
-  int issued = 0;
   const int n_loc = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
-  // Pages of the runs of tiles j (cur), j + 1 (nxt) and j + 2 (nn, fetched
-  // at the start of block j so the run-table loads are in flight a whole
-  // block before their first TMA).  Past the last run the segment's first
-  // page stands in (finite values, masked out).
   const int2 first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
-  int ck[kMaxRuns], cv[kMaxRuns], xk[kMaxRuns], xv[kMaxRuns], nk[kMaxRuns], nv[kMaxRuns];
-  auto fetch = [&](int j, int (&kk)[kMaxRuns], int (&vv)[kMaxRuns]) {
-#pragma unroll
-    for (int g = 0; g < kMaxRuns; ++g) {
-      const int ri = (w.t0 + j) * rpt + g;
-      int2 kv = first;
-      if (g < rpt && ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
-      kk[g] = layer_base + kv.x;
-      vv[g] = layer_base + kv.y;
+  bool ok = true;
+  // One 64-key x 64-column block: keys of half kh of local tile j (pages tp),
+  // columns col of K_pe (pe) or of the latent.
+  auto copy = [&](uint32_t dst, uint32_t fb, bool pe, int kh, int col, int j, const TilePages& tp) {
+    const int pg = pe ? (kh ? tp.k1 : tp.k0) : (kh ? tp.v1 : tp.v0);
+    const bool cons = (tp.cons >> ((pe ? 0 : 2) + kh)) & 1u;
+    if (p.page > 64) {  // one page per tile, the block is its half kh
+      ptx::tma_load_4d_pair(dst, pe ? &p.k_tile_map : &p.v_tile_map, fb, col, 64 * kh, 0, pg);
+    } else if (cons) {
+      ptx::tma_load_4d_pair(dst, pe ? &p.k_tile_map : &p.v_tile_map, fb, col, 0, 0, pg);
+    } else {  // pages of the half one by one (copied pages of a fork)
+      const CUtensorMap* map = pe ? &p.k_map : &p.v_map;
+      for (int g = 0; g < rpu; ++g) {
+        const int ri = (w.t0 + j) * rpt + kh * rpu + g;
+        int2 kv = first;
+        if (ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
+        ptx::tma_load_4d_pair(dst + g * p.page * 128, map, fb, col, 0, 0, layer_base + (pe ? kv.x : kv.y));
+      }
     }
   };
-  // A tile whose runs sit on consecutive pages loads each chunk with one
-  // copy (the tile map's box spans 128 / page pages).
-  auto consecutive = [&](const int (&pg)[kMaxRuns]) {
-    bool c = true;
-#pragma unroll
-    for (int g = 1; g < kMaxRuns; ++g) c = c && (g >= rpt || pg[g] == pg[0] + g);
-    return c;
-  };
-  fetch(0, ck, cv);
-  if (n_loc > 1) fetch(1, xk, xv);
-  for (int ld = 0; ld < n_loc * kPerTile; ++ld) {
-    int j, c;
-    chunk_at(ld, n_loc, j, c);
-    if (ld >= kQChunks && (ld - kQChunks) % kPerTile == 0) {  // start of block b: QK of b + 1, PV of b
-      const int b = (ld - kQChunks) / kPerTile;
-      if (b >= 1) {
-#pragma unroll
-        for (int g = 0; g < kMaxRuns; ++g) {
-          ck[g] = xk[g];
-          cv[g] = xv[g];
-          xk[g] = nk[g];
-          xv[g] = nv[g];
+  int rd = 0;
+  // Round `kind` (< kQKRounds: QK round, else PV round kind - kQKRounds) of local tile j.
+  auto round = [&](int kind, int j, const TilePages& tp) {
+    if (ok && rd % kProducers == who) {
+      const int slot = rd % kRing, use = rd / kRing;
+      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+        ok = false;
+      } else {
+        const uint32_t dst = sbase + kSlots + slot * kSlot;
+        const uint32_t fb = lead_full0 + 8u * uint32_t(slot);
+        const int kr = int(rank);
+        if (kind < kQKRounds - 1) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), 2 * kSlot);
+          copy(dst, fb, false, kr, 128 * kind, j, tp);
+          copy(dst + kUnit, fb, false, kr, 128 * kind + 64, j, tp);
+        } else if (kind == kQKRounds - 1) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), 2 * kUnit);
+          copy(dst, fb, true, kr, 0, j, tp);
+        } else {
+          const int col = 256 * half + 128 * (kind - kQKRounds) + 64 * kr;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), 2 * kSlot);
+          copy(dst, fb, false, 0, col, j, tp);
+          copy(dst + kUnit, fb, false, 1, col, j, tp);
         }
       }
-      if (b + 2 < n_loc) fetch(b + 2, nk, nv);
     }
-    const int slot = ld % kRing, use = ld / kRing;
-    if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
-      ok = false;
-      break;
-    }
-    // chunk c < 8: latent columns 64c (QK); c == 8: K_pe; c > 8: latent columns of this half (PV)
-    const bool pe = c == kLat / 64;
-    const int col = c < kQChunks ? (pe ? 0 : 64 * c) : 256 * half + 64 * (c - kQChunks);
-    const CUtensorMap* map = pe ? &p.k_map : &p.v_map;
-    const uint32_t dst = sbase + kSlots + slot * kChunk;
-    // tile j is the current block's tile (cur) or, for QK chunks after the first tile, the next (nxt)
-    const bool use_next = ld >= kQChunks && c < kQChunks;
-    ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), kChunk);
-    int pgs[kMaxRuns];
-#pragma unroll
-    for (int g = 0; g < kMaxRuns; ++g) pgs[g] = use_next ? (pe ? xk[g] : xv[g]) : (pe ? ck[g] : cv[g]);
-    if (consecutive(pgs)) {
-      ptx::tma_load_4d(dst, pe ? &p.k_tile_map : &p.v_tile_map, bar(kBarFull0 + slot), col, 0, 0, pgs[0]);
-    } else {
-#pragma unroll
-      for (int g = 0; g < kMaxRuns; ++g) {
-        if (g >= rpt) break;
-        ptx::tma_load_4d(dst + g * p.page * 128, map, bar(kBarFull0 + slot), col, 0, 0, pgs[g]);
-      }
-    }
-    issued = ld + 1;
+    ++rd;
+  };
+  int2 raw[kMaxRuns];
+  load_runs(p, seg, w.t0, rpt, first, raw);
+  TilePages cur = tile_pages(raw, p.page, rpu, layer_base), nxt = cur;
+  if (n_loc > 1) {
+    load_runs(p, seg, w.t0 + 1, rpt, first, raw);
+    nxt = tile_pages(raw, p.page, rpu, layer_base);
+  }
+  for (int m = 0; m < kQKRounds; ++m) round(m, 0, cur);
+  for (int b = 0; b < n_loc && ok; ++b) {
+    // runs of tile b + 2 are loaded here and used a block later
+    if (b + 2 < n_loc) load_runs(p, seg, w.t0 + b + 2, rpt, first, raw);
+    if (b + 1 < n_loc)
+      for (int m = 0; m < kQKRounds; ++m) round(m, b + 1, nxt);
+    for (int q = 0; q < kPVRounds; ++q) round(kQKRounds + q, b, cur);
+    cur = nxt;
+    if (b + 2 < n_loc) nxt = tile_pages(raw, p.page, rpu, layer_base);
   }
   if (!ok) {
-    raise_error(p.err, kErrTimeout, blockIdx.x, 10, 0);
+    raise_error(p.err, kErrTimeout, blockIdx.x, 10, who);
     *abort_flag = 1;
   }
-  ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kDrainLimitNs);
-#pragma unroll
+  if (who != 0) return;
+  // Drain (one thread): every round consumed (so every copy into this CTA has
+  // landed) and every multicast commit to this CTA's ring barriers arrived.
+  const int total = kPerTile * n_loc;
+  if (rank == 0) ptx::mbar_wait_drain(bar(kBarQ), 0, kDrainLimitNs);
+#pragma unroll 1
   for (int s = 0; s < kRing; ++s) {
-    const int uses = issued > s ? (issued - s + kRing - 1) / kRing : 0;
-    if (uses) ptx::mbar_wait(bar(kBarFull0 + s), (uses - 1) & 1, abort_flag, kDrainLimitNs);
+    const int uses = total > s ? (total - s + kRing - 1) / kRing : 0;
+    if (!uses) continue;
+    if (rank == 0) ptx::mbar_wait_drain(bar(kBarFull0 + s), (uses - 1) & 1, kDrainLimitNs);
+    ptx::mbar_wait_drain(bar(kBarEmpty0 + s), (uses - 1) & 1, kDrainLimitNs);
   }
 }
 
 // --------------------------------------------------------------------- MMA
+// Even CTA only.  QK^T: D (S, 128 columns per CTA) = Q (256 rows) x K (128
+// keys, 64 from each CTA).  PV: O quarter q (128 columns) += P (256 rows x
+// 128 keys, from each CTA's TMEM) x V (128 keys x 128 columns, 64 from each
+// CTA).
 __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
                                           volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
-  constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kKeys, false);
-  constexpr uint32_t idesc_pv = ptx::idesc_bf16(kRows, 64, true);
+  constexpr uint32_t idesc_qk = ptx::idesc_bf16(2 * kRows, kKeys, false);
+  constexpr uint32_t idesc_pv = ptx::idesc_bf16(2 * kRows, 128, true);
   const uint32_t tO = tmem + 256;
   const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);
-  int ld = 0;
+  int rd = 0;
+  bool issued = false;  // a commit is only issued after this thread's first MMA
   bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
-  auto next_chunk = [&]() -> uint32_t {  // wait for the chunk at stream position ld; its slot address
-    const int slot = ld % kRing;
-    ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (ld / kRing) & 1, abort_flag, kWaitLimitNs);
+  ptx::tc_fence_after();
+  auto next_round = [&]() -> uint32_t {  // wait for round rd; its slot address
+    const int slot = rd % kRing;
+    ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kRing) & 1, abort_flag, kWaitLimitNs);
     ptx::tc_fence_after();
-    return sbase + kSlots + slot * kChunk;
+    return sbase + kSlots + slot * kSlot;
   };
   auto release = [&]() {
-    ptx::mma_commit(bar(kBarEmpty0 + ld % kRing));
-    ++ld;
+    ptx::mma_commit_pair_mc(bar(kBarEmpty0 + rd % kRing), kBoth);
+    ++rd;
   };
   // Descriptors are built once and advanced by constants (only the start
-  // address changes); the MMA thread shares its sub-partition with softmax.
+  // address changes).
   const uint64_t qd0 = ptx::smem_desc(sbase + kQ, 16, 1024);
+  auto chunk = [&](uint32_t tS, int c, uint32_t kt) {  // S (+)= Q chunk c x K chunk at kt
+    const uint64_t kd = ptx::smem_desc(kt, 16, 1024), qd = ptx::desc_advance(qd0, c * kQChunk);
+    ptx::mma_bf16_pair(tS, qd, kd, idesc_qk, c > 0);
+#pragma unroll
+    for (int ks = 1; ks < 4; ++ks)
+      ptx::mma_bf16_pair(tS, ptx::desc_advance(qd, ks * 32), ptx::desc_advance(kd, ks * 32), idesc_qk, 1);
+  };
   auto qk = [&](int j) {
     const uint32_t tS = tmem + 128u * (j & 1);
 #pragma unroll 1
-    for (int c = 0; c < kQChunks && ok; ++c) {
-      const uint32_t kt = next_chunk();
+    for (int m = 0; m < kQKRounds && ok; ++m) {
+      const uint32_t kt = next_round();
       if (!ok) break;
-      const uint64_t kd = ptx::smem_desc(kt, 16, 1024), qd = ptx::desc_advance(qd0, c * kChunk);
-      ptx::mma_bf16(tS, qd, kd, idesc_qk, c > 0);
-#pragma unroll
-      for (int ks = 1; ks < 4; ++ks)
-        ptx::mma_bf16(tS, ptx::desc_advance(qd, ks * 32), ptx::desc_advance(kd, ks * 32), idesc_qk, 1);
+      if (m < kQKRounds - 1) {
+        chunk(tS, 2 * m, kt);
+        chunk(tS, 2 * m + 1, kt + kUnit);
+      } else {
+        chunk(tS, kQChunks - 1, kt);
+      }
+      issued = true;
       release();
     }
-    if (ok) ptx::mma_commit(bar(kBarS0 + (j & 1)));
+    if (ok) ptx::mma_commit_pair_mc(bar(kBarS0 + (j & 1)), kBoth);
   };
   if (ok && n > 0) qk(0);
   for (int j = 0; j < n && ok; ++j) {
     if (j + 1 < n) qk(j + 1);
     if (!ok) break;
-    if (!(ok = ptx::mbar_wait(bar(kBarP), j & 1, abort_flag, kWaitLimitNs))) break;
+    if (!(ok = ptx::mbar_wait_cl(bar(kBarP), j & 1, abort_flag, kWaitLimitNs))) break;
     ptx::tc_fence_after();
     const uint32_t tP = tmem + 128u * (j & 1);  // P of tile j, packed over S
 #pragma unroll 1
-    for (int i = 0; i < kVChunks && ok; ++i) {
-      const uint32_t vt = next_chunk();
+    for (int q = 0; q < kPVRounds && ok; ++q) {
+      const uint32_t vt = next_round();
       if (!ok) break;
-      const uint64_t vd = ptx::smem_desc(vt, kChunk, 1024);
-      ptx::mma_bf16_tmem_a(tO + 64u * i, tP, vd, idesc_pv, j > 0);
+      const uint64_t vd = ptx::smem_desc(vt, kSlot, 1024);
+      ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP, vd, idesc_pv, j > 0);
 #pragma unroll
       for (int ks = 1; ks < kKeys / 16; ++ks)
-        ptx::mma_bf16_tmem_a(tO + 64u * i, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
+        ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
       release();
     }
-    if (ok) ptx::mma_commit(bar(kBarO));
+    if (ok) ptx::mma_commit_pair_mc(bar(kBarO), kBoth);
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 11, 0);
     *abort_flag = 1;
   }
-  ptx::mma_commit(bar(kBarFin));
-  ptx::mbar_wait(bar(kBarFin), 0, abort_flag, kDrainLimitNs);
+  if (issued) {
+    ptx::mma_commit_pair(bar(kBarFin));
+    ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs);
+  }
 }
 
 // ----------------------------------------------------------------- softmax
 __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint8_t* smem,
-                                        uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
+                                        uint32_t sbase, uint32_t tmem, uint32_t rank, volatile int* abort_flag) {
   const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
@@ -282,6 +358,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
   const int sl_own = r & (p.page - 1);
+  const uint32_t lead_p = ptx::mapa(bar(kBarP), 0);  // P barrier of the even CTA
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
   // (lohi, es) of the run holding key column r of the current tile, fetched one tile ahead;
@@ -392,7 +469,10 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
     m_run = m_use;
     ptx::tc_fence_before();
-    ptx::mbar_arrive(bar(kBarP));
+    if (rank == 0)
+      ptx::mbar_arrive(bar(kBarP));
+    else
+      ptx::mbar_arrive_cluster(lead_p);
   }
   if (ok && n > 0) {
     ok = ptx::mbar_wait(bar(kBarO), (n - 1) & 1, abort_flag, kWaitLimitNs);
@@ -404,6 +484,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     return;
   }
   ptx::tc_fence_after();
+  if (w.kvh & kShadow) return;  // stand-in for a missing query tile: computes, writes nothing
   const int half = w.n_b;
   if (w.part >= 0) {
     // Split part: unnormalised O half, running max and sum, [column][row] layout.
@@ -448,7 +529,8 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) segment_attn_mla_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    segment_attn_mla_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
@@ -456,40 +538,63 @@ __global__ void __launch_bounds__(kThreads, 1) segment_attn_mla_kernel(const __g
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBars + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = ptx::cluster_ctarank();
   const AttnWork w = p.work[blockIdx.x];
   const AttnSeg seg = p.segs[w.seg];
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, i == kBarP ? 128 : 1);
+    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, i == kBarP ? 2 * 128 : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
+  ptx::cluster_sync();  // both CTAs' barriers initialised before any remote arrive or copy
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  ptx::cluster_sync();  // the pair's TMEM is allocated in both CTAs before the first MMA
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp == 0) {
-    if (lane == 0) produce(p, w, seg, sbase, abort_flag);
+  if (warp == 0 || warp >= 6) {
+    if (lane == 0) produce(p, w, seg, sbase, rank, warp == 0 ? 0 : warp - 5, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) issue_mma(p, w, sbase, tmem, abort_flag);
+    if (lane == 0 && rank == 0) issue_mma(p, w, sbase, tmem, abort_flag);
   } else {
-    softmax(p, w, seg, smem, sbase, tmem, abort_flag);
+    softmax(p, w, seg, smem, sbase, tmem, rank, abort_flag);
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  ptx::cluster_sync();  // every MMA of the pair done and every remote signal delivered
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc_pair(tmem, kTmemCols);
   }
+  ptx::cluster_sync();
 }
 
 }  // namespace
 
+// CTAs of this kernel that can be resident at once (pairs x 2): the planner's
+// wave size.  0 if the occupancy query fails.
+int segment_attn_mla_slots() {
+  const int smem = int(kBytes) + 1024;
+  if (cudaFuncSetAttribute(segment_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, segment_attn_mla_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return 2 * clusters;
+}
+
 cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st) {
   if (p.n_work <= 0) return cudaSuccess;
+  if (p.n_work % 2) return cudaErrorInvalidValue;  // CTA pairs
   const int smem = int(kBytes) + 1024;
   cudaError_t e = cudaFuncSetAttribute(segment_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -106,6 +106,28 @@ def test_mla_small_full_compare():
     check(synth.mla_dsv2lite(n_layers=1, concurrency=1, prompt=3000, span=700, stub=20, n_new=100))
 
 
+@pytest.mark.parametrize("page,split", [(16, 0), (32, 0), (128, 0), (16, 4)])
+def test_mla_page_sizes_forks_and_drops(page, split):
+    # MLA at other page sizes: a 64-key unit spans several pages (16, 32) or
+    # half a page (128).  Branch B is a fork whose repositioned K_pe pages are
+    # copies, so key and latent page ids differ and a unit's pages are not
+    # always consecutive; dropped and hidden spans leave partial pages; 100
+    # and 36 queries give odd query-tile counts (the pair's second tile is a
+    # stand-in that writes nothing).
+    import dataclasses
+    w = synth.mla_dsv2lite(n_layers=1, concurrency=1)
+    w.shape = dataclasses.replace(w.shape, page_size=page)
+    w.ops = [("alloc", "A"), ("append", "A", 1500, "ctx"),
+             ("fork", "B", "A", 1500),
+             ("drop", "B", 100, 333), ("repos", "B", 333, 1500, -233),
+             ("drop", "A", 700, 717), ("drop", "A", 901, 950),
+             ("append", "A", 100, "newA"), ("append", "B", 36, "newB")]
+    w.segments = [dict(seq="A", kv_end=1600, q_len=100, hide=[(40, 77)], q_row0=0),
+                  dict(seq="B", kv_end=1536, q_len=36, hide=[], q_row0=100)]
+    w.n_pages = 3 * (1600 // page + 4) + 16
+    check(w, split=split)
+
+
 # Split-KV: an item's KV tiles cut into S parts whose partial (O, m, l) the
 # combine kernel merges.  Forced factors cover parts that see no key of the
 # shorter query tile (GQA), ragged part boundaries, and both MLA halves.

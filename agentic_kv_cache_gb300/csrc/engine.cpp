@@ -985,39 +985,73 @@ struct akv_ctx {
   }
 
   // Split-KV for the MLA kernel (one CTA pair per pair of units): cut every
-  // pair's KV-tile range into up to S chunks so the launch fills whole waves
-  // of the SM pairs; split chunks write partials and the chunk that finishes
-  // last merges them.  Pairs run longest first (LPT), ties in (segment, tile,
-  // half, chunk) order.
+  // pair's KV-tile range into chunks so the launch ends as early as an
+  // estimate of its schedule says; split chunks write partials and the chunk
+  // that finishes last merges them.  Pairs run longest first (LPT), ties in
+  // (segment, tile, half, chunk) order.
+  static constexpr double kMlaUnitCost = 1.5;  // start + epilogue of a unit, in KV tiles
+  static constexpr double kMlaPartCost = 2.5;  // the same for a split part (partial write, merge share)
   void plan_split(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts) {
     // work holds CTA pairs (2i, 2i + 1) sharing one KV range; a pair is cut
     // and scheduled as one.
-    const int64_t slots = std::max(2, mla_slots);
-    auto units_for = [&](int S) {
-      int64_t u = 0;
-      for (size_t k = 0; k < work.size(); k += 2) u += 2 * std::min<int64_t>(S, std::max(1, work[k].n_a));
-      return u;
+    const int64_t pair_slots = std::max(1, mla_slots / 2);
+    const size_t n_items = work.size() / 2;
+    // Estimated makespan of a cut (chunks per item), in KV tiles: units run
+    // longest first, each on the pair that frees first; a unit costs its
+    // tiles plus a start and epilogue (more for a split part: its partial
+    // write and a share of the merge).
+    auto makespan = [&](const std::vector<int>& chunks) {
+      std::vector<double> cost;
+      for (size_t k = 0; k < n_items; ++k) {
+        const int span = std::max(1, work[2 * k].n_a);
+        for (int c = 0; c < chunks[k]; ++c)
+          cost.push_back(double(span) / chunks[k] + (chunks[k] > 1 ? kMlaPartCost : kMlaUnitCost));
+      }
+      std::sort(cost.begin(), cost.end(), std::greater<double>());
+      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+      for (int64_t i = 0; i < pair_slots; ++i) free_at.push(0.0);
+      double end = 0.0;
+      for (double c : cost) {
+        const double t = free_at.top() + c;
+        free_at.pop();
+        free_at.push(t);
+        end = std::max(end, t);
+      }
+      return end;
     };
-    int best_s = 1;
+    // Candidates: every item in S chunks, or in S chunks with the smallest
+    // number of items in S + 1 that fills the last wave of pairs.
+    std::vector<int> best_chunks(n_items, 1);
     double best = -1.0;
     const int cands[] = {1, 2, 3, 4, 6, 8};
     for (int S : cands) {
       if (split_override > 0 && S != split_override) continue;
-      const int64_t u = units_for(S);
-      const int64_t waves = (u + slots - 1) / slots;
-      // A split part pays its partial write, a share of the merge and a
-      // slower pipeline start, so splitting must buy more occupancy than that.
-      const double eff = double(u) / double(waves * slots) * (S == 1 ? 1.0 : 0.85);
-      if (eff > best + 1e-9) {
-        best = eff;
-        best_s = S;
+      for (int top = 0; top < 2; ++top) {
+        std::vector<int> ch(n_items);
+        int64_t units = 0;
+        for (size_t k = 0; k < n_items; ++k) units += ch[k] = std::min(S, std::max(1, work[2 * k].n_a));
+        if (top) {
+          if (split_override > 0 || units % pair_slots == 0) continue;
+          int64_t need = pair_slots - units % pair_slots;
+          for (size_t k = n_items; k-- > 0 && need > 0;)
+            if (ch[k] < 8 && ch[k] < work[2 * k].n_a) {
+              ++ch[k];
+              --need;
+            }
+        }
+        const double m = makespan(ch);
+        if (best < 0.0 || m < best - 1e-9) {
+          best = m;
+          best_chunks = ch;
+        }
       }
     }
-    if (split_override > 0) best_s = std::min(split_override, 8);
+    if (split_override > 0)
+      for (size_t k = 0; k < n_items; ++k) best_chunks[k] = std::min(std::min(split_override, 8), std::max(1, work[2 * k].n_a));
     std::vector<std::array<akv::AttnWork, 2>> pairs;
     for (size_t k = 0; k < work.size(); k += 2) {
       const int span = work[k].n_a;
-      const int chunks = std::min(best_s, std::max(1, span));
+      const int chunks = best_chunks[k / 2];
       int32_t base[2] = {-1, -1}, ci[2] = {-1, -1};
       if (chunks > 1) {
         for (int m = 0; m < 2; ++m) {

@@ -989,8 +989,8 @@ struct akv_ctx {
   // estimate of its schedule says; split chunks write partials and the chunk
   // that finishes last merges them.  Pairs run longest first (LPT), ties in
   // (segment, tile, half, chunk) order.
-  static constexpr double kMlaUnitCost = 1.5;  // start + epilogue of a unit, in KV tiles
-  static constexpr double kMlaPartCost = 2.5;  // the same for a split part (partial write, merge share)
+  static constexpr double kMlaUnitCost = 6.0;  // start + epilogue of a unit, in KV tiles (fitted to measured launches)
+  static constexpr double kMlaPartCost = 8.0;  // the same for a split part (partial write, merge share)
   void plan_split(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts) {
     // work holds CTA pairs (2i, 2i + 1) sharing one KV range; a pair is cut
     // and scheduled as one.

@@ -129,44 +129,58 @@ class Marks {
 // A pinned-host + device buffer pair reused across calls.  acquire() waits
 // for the event recorded by the previous user, so a buffer is never
 // overwritten while a copy or kernel that reads it is still queued.
+// Staging for host inputs / outputs (and device scratch): two buffers used in
+// turn, so the host can stage the next call while the GPU still reads the
+// previous one; acquire waits only for the use before last of its buffer.
 struct Staging {
-  void* host = nullptr;
+  void* host = nullptr;  // the current buffer (valid after acquire)
   void* dev = nullptr;
-  size_t cap = 0;
-  cudaEvent_t ev = nullptr;
-  bool pending = false;
   bool want_host = true;
+  struct Buf {
+    void* host = nullptr;
+    void* dev = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    bool pending = false;
+  } buf[2];
+  int cur = 1;
 
   void acquire(size_t bytes) {
-    if (!ev) cuda_check(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming), "cudaEventCreate");
-    if (pending) {
-      cuda_check(cudaEventSynchronize(ev), "cudaEventSynchronize");
-      pending = false;
+    cur ^= 1;
+    Buf& b = buf[cur];
+    if (!b.ev) cuda_check(cudaEventCreateWithFlags(&b.ev, cudaEventDisableTiming), "cudaEventCreate");
+    if (b.pending) {
+      cuda_check(cudaEventSynchronize(b.ev), "cudaEventSynchronize");
+      b.pending = false;
     }
-    if (bytes <= cap) return;
-    size_t want = std::max<size_t>(bytes + bytes / 2, 4096);
-    if (host) cudaFreeHost(host);
-    if (dev) cudaFree(dev);
-    host = dev = nullptr;
-    cap = 0;
-    if (want_host) cuda_check(cudaMallocHost(&host, want), "cudaMallocHost");
-    cuda_check(cudaMalloc(&dev, want), "cudaMalloc");
-    cap = want;
+    if (bytes > b.cap || (want_host && !b.host)) {
+      const size_t want = std::max<size_t>(bytes + bytes / 2, 4096);
+      if (b.host) cudaFreeHost(b.host);
+      if (b.dev) cudaFree(b.dev);
+      b.host = b.dev = nullptr;
+      b.cap = 0;
+      if (want_host) cuda_check(cudaMallocHost(&b.host, want), "cudaMallocHost");
+      cuda_check(cudaMalloc(&b.dev, want), "cudaMalloc");
+      b.cap = want;
+    }
+    host = b.host;
+    dev = b.dev;
   }
   void release(cudaStream_t st) {
-    cuda_check(cudaEventRecord(ev, st), "cudaEventRecord");
-    pending = true;
+    cuda_check(cudaEventRecord(buf[cur].ev, st), "cudaEventRecord");
+    buf[cur].pending = true;
   }
   void destroy() {
-    if (ev) {
-      cudaEventSynchronize(ev);
-      cudaEventDestroy(ev);
+    for (Buf& b : buf) {
+      if (b.ev) {
+        cudaEventSynchronize(b.ev);
+        cudaEventDestroy(b.ev);
+      }
+      if (b.host) cudaFreeHost(b.host);
+      if (b.dev) cudaFree(b.dev);
+      b = Buf{};
     }
-    if (host) cudaFreeHost(host);
-    if (dev) cudaFree(dev);
     host = dev = nullptr;
-    ev = nullptr;
-    cap = 0;
   }
 };
 

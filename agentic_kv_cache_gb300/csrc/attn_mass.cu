@@ -11,16 +11,19 @@
 // three decode turns) is the caller's.
 //
 // GB300 design (one CTA per (segment, kv head, 128-row query tile)):
-//   * warp 0 loads Q once and streams K tiles (128 keys) through a 4-slot
+//   * warp 0 loads Q once and streams K tiles (128 keys) through a 3-slot
 //     ring by TMA, whole-tile copies when the runs sit on consecutive pages;
 //   * warp 1 issues S(j) = Q K_j^T into one of two TMEM score buffers, then
 //     the column sums of the probability tile of j - 1 as a second MMA,
 //     D = ones(128 x 128) P(j-1), whose every row is the vector of column sums
-//     (the P tile is bf16 in shared memory as the B operand);
+//     (P tiles are bf16 in shared memory as the B operand, two buffers; D has
+//     two TMEM buffers);
 //   * warps 2-5 (one row per thread) turn scores into probabilities with the
 //     final lse, write them to shared memory, and read back the column sums of
-//     the previous tile (lane l of quadrant q takes column 32q + l) to add
-//     them into the output of the entry's token with one atomic each.
+//     tile j - 2 (lane l of quadrant q takes column 32q + l) before reusing its
+//     P buffer, adding them into the output of the entry's token with one
+//     atomic each.  Reading two tiles back keeps the sum MMA of one tile off
+//     the critical path of the next.
 // Every wait is bounded; on time-out the CTA records AKV_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 
@@ -37,9 +40,9 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kKeys = 128;
 constexpr int kRows = 128;
-constexpr int kRing = 4;
+constexpr int kRing = 3;
 constexpr int kMaxRuns = 8;
-constexpr uint32_t kTmemCols = 512;  // S0, S1, D (128 columns each)
+constexpr uint32_t kTmemCols = 512;  // S0, S1, D0, D1 (128 columns each)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;
@@ -52,8 +55,9 @@ struct MLayout {
   static constexpr uint32_t kTile = kBlocks * kBlockBytes;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kSlot = kQ + kTile;
-  static constexpr uint32_t kP = kSlot + kRing * kTile;  // probability tile, 2 x 64-key blocks
-  static constexpr uint32_t kOnes = kP + 2 * kBlockBytes;  // one 128 x 64 block of bf16 ones
+  static constexpr uint32_t kP = kSlot + kRing * kTile;  // two probability tiles, each 2 x 64-key blocks
+  static constexpr uint32_t kPTile = 2 * kBlockBytes;
+  static constexpr uint32_t kOnes = kP + 2 * kPTile;     // one 128 x 64 block of bf16 ones
   static constexpr uint32_t kColE = kOnes + kBlockBytes;
   static constexpr uint32_t kBars = kColE + 128 * 4;
   static constexpr uint32_t kBytes = kBars + 256;
@@ -65,9 +69,9 @@ enum MBar {
   kMEmpty0 = kMFull0 + kRing,
   kMS0 = kMEmpty0 + kRing,  // + buffer
   kMSFree0 = kMS0 + 2,      // + buffer, 128 arrivals
-  kMPFull = kMSFree0 + 2,   // 128 arrivals
-  kMD,
-  kMFin,
+  kMPFull0 = kMSFree0 + 2,  // + tile parity, 128 arrivals
+  kMD0 = kMPFull0 + 2,      // + tile parity
+  kMFin = kMD0 + 2,
   kMNumBars
 };
 static_assert(kMNumBars * 8 + 8 <= 256, "barrier area");
@@ -109,7 +113,7 @@ __device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg&
     }
   };
   fetch(0, kpg);
-  int armed[kRing] = {0, 0, 0, 0};
+  int armed[kRing] = {};
   bool ok = true;
   for (int j = 0; j < n; ++j) {
     const int slot = j % kRing, use = j / kRing;
@@ -180,13 +184,15 @@ __device__ void m_mma(const MassParams& p, const AttnWork& w, uint32_t sbase, ui
       ptx::mma_commit(bar(kMEmpty0 + slot));
     }
     if (j >= 1) {
-      if (!(ok = ptx::mbar_wait(bar(kMPFull), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
+      const int b = (j - 1) & 1;  // buffers of tile j - 1
+      if (!(ok = ptx::mbar_wait(bar(kMPFull0 + b), ((j - 1) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
       ptx::tc_fence_after();
+      const uint64_t pdb = ptx::desc_advance(pd, b * L::kPTile);
 #pragma unroll
       for (int ks = 0; ks < kRows / 16; ++ks)  // 16 probability rows per step; every A element is 1
-        ptx::mma_bf16(tmem + 256u, ptx::desc_advance(ones, (ks & 3) * 32), ptx::desc_advance(pd, ks * 16 * 128),
-                      idesc_sum, ks > 0);
-      ptx::mma_commit(bar(kMD));
+        ptx::mma_bf16(tmem + 256u + 128u * b, ptx::desc_advance(ones, (ks & 3) * 32),
+                      ptx::desc_advance(pdb, ks * 16 * 128), idesc_sum, ks > 0);
+      ptx::mma_commit(bar(kMD0 + b));
     }
   }
   if (!ok) {
@@ -228,18 +234,20 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
   int2 run_cur = make_int2(0, 0);
   if ((r >> page_shift) < seg.n_runs) run_cur = run_le[2 * (r >> page_shift) + 1];
   bool ok = true;
-  int e_prev = INT_MAX;
+  int e_even = INT_MAX, e_odd = INT_MAX;  // entry of key column r in the last even / odd tile
   // column sums of tile jj come back in D: lane l of quadrant q reads column 32q + l
   auto take_sums = [&](int jj) {
-    ok = ptx::mbar_wait(bar(kMD), jj & 1, abort_flag, kWaitLimitNs);
+    const int b = jj & 1;
+    ok = ptx::mbar_wait(bar(kMD0 + b), (jj >> 1) & 1, abort_flag, kWaitLimitNs);
     if (!ptx::bar_red_and(1, 128, ok)) return false;
     ptx::tc_fence_after();
     uint32_t v[32];
-    ptx::tmem_load32(tmem + 256u + lane_addr + quad * 32, v);
+    ptx::tmem_load32(tmem + 256u + 128u * b + lane_addr + quad * 32, v);
     float mine = 0.f;
 #pragma unroll
     for (int k = 0; k < 32; ++k) mine = lane == k ? __uint_as_float(v[k]) : mine;
-    if (e_prev != INT_MAX) atomicAdd(p.mass + seg.mass_off + p.ent_tok[seg.ent_off + e_prev], mine);
+    const int e_jj = b ? e_odd : e_even;
+    if (e_jj != INT_MAX) atomicAdd(p.mass + seg.mass_off + p.ent_tok[seg.ent_off + e_jj], mine);
     return true;
   };
   for (int j = 0; j < n && ok; ++j) {
@@ -259,8 +267,8 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
     const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
     ptx::tc_fence_after();
     const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
-    // the sums of tile j - 1 are read before its P buffer is overwritten
-    if (j >= 1 && !(ok = take_sums(j - 1))) break;
+    // the sums of tile j - 2 are read before its P buffer is overwritten
+    if (j >= 2 && !(ok = take_sums(j - 2))) break;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -282,7 +290,7 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
         const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2v, neg);
         pk[c] = pack_bf16(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
       }
-      uint8_t* rowp = P + h * L::kBlockBytes + r * 128;
+      uint8_t* rowp = P + (j & 1) * L::kPTile + h * L::kBlockBytes + r * 128;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8)
         *reinterpret_cast<uint4*>(rowp + ((c8 ^ (r & 7)) << 4)) =
@@ -291,9 +299,13 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
     ptx::tc_fence_before();
     ptx::mbar_arrive(bar(kMSFree0 + (j & 1)));
     ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(bar(kMPFull));
-    e_prev = e;
+    ptx::mbar_arrive(bar(kMPFull0 + (j & 1)));
+    if (j & 1)
+      e_odd = e;
+    else
+      e_even = e;
   }
+  if (ok && n >= 2) ok = take_sums(n - 2);
   if (ok && n >= 1) ok = take_sums(n - 1);
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 2, 0);
@@ -320,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mass_kernel(const __grid_con
   const AttnSeg seg = p.segs[w.seg];
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMNumBars; ++i)
-      ptx::mbar_init(bars + 8u * i, (i == kMSFree0 || i == kMSFree0 + 1 || i == kMPFull) ? 128 : 1);
+      ptx::mbar_init(bars + 8u * i, (i == kMSFree0 || i == kMSFree0 + 1 || i == kMPFull0 || i == kMPFull0 + 1) ? 128 : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }

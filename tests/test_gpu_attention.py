@@ -128,6 +128,22 @@ def test_mla_page_sizes_forks_and_drops(page, split):
     check(w, split=split)
 
 
+@pytest.mark.parametrize("split", [0, 2])
+def test_mla_tiny_sessions(split):
+    # Degenerate MLA launches: a single query (one 8-token tile, 16 rows of 128
+    # valid, its pair partner a shadow), key lists shorter than one tile, a
+    # tile boundary exactly at the last key, several sessions in one launch.
+    w = synth.mla_dsv2lite(n_layers=1, concurrency=1)
+    w.ops, w.segments, row = [], [], 0
+    for i, (prompt, q) in enumerate([(10, 1), (70, 3), (119, 9), (247, 17), (600, 1)]):
+        name = f"S{i}"
+        w.ops += [("alloc", name), ("append", name, prompt, f"p{i}"), ("append", name, q, f"n{i}")]
+        w.segments.append(dict(seq=name, kv_end=prompt + q, q_len=q, hide=[], q_row0=row))
+        row += q
+    w.n_pages = 64
+    check(w, split=split)
+
+
 # Split-KV: an item's KV tiles cut into S parts whose partial (O, m, l) the
 # combine kernel merges.  Forced factors cover parts that see no key of the
 # shorter query tile (GQA), ragged part boundaries, and both MLA halves.

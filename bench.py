@@ -338,7 +338,13 @@ def mass_pass(t, reps=5):
     segs = t.runner.engine_segments(t.w, names)
     s = t.w.shape
     lse = torch.empty((t.nq, s.n_q_heads), dtype=torch.float32, device="cuda")
+    t.eng.profile_enable(True)
     t.eng.attend(0, segs, t.q, t.nq, t.o, lse, s.scale, stream=t.stream)
+    att = t.eng.profile_read()["segment_attn"]
+    t.eng.profile_enable(False)
+    # Same contraction sizes as the attention launch: QK^T over the visible pairs, then the
+    # column-sum product ones(128 x 128) P, as many FLOPs as PV for d_v = d.
+    flops = att["flops"] / max(att["launches"], 1)
     total = sum(g["kv_end"] for g in t.w.segments)
     mass = torch.empty((total,), dtype=torch.float32, device="cuda")
     t.eng.attention_mass(0, segs, t.q, t.nq, lse, mass, s.scale, stream=t.stream)
@@ -355,7 +361,11 @@ def mass_pass(t, reps=5):
     assert t.eng.check_device_error(t.stream) == 0
     total_mass = float(mass.sum())
     t.eng.seq_free(names["F"])
-    return {"ms": sorted(ms)[len(ms) // 2], "mass_sum": total_mass, "expected_sum": t.nq * s.n_q_heads}
+    med = sorted(ms)[len(ms) // 2]
+    _, bf16_peak, _, _ = load_peaks()
+    tf = flops / (med * 1e-3) / 1e12
+    return {"ms": med, "mass_sum": total_mass, "expected_sum": t.nq * s.n_q_heads, "TFLOP/s": tf,
+            "frac_of_bf16_dense": tf / bf16_peak}
 
 
 def mla_turns(concurrencies=(1, 4, 8, 16), steps=3, warmup=1):

@@ -10,20 +10,22 @@
 // probabilities are the final ones).  The policy on top (an epsilon over
 // three decode turns) is the caller's.
 //
-// GB300 design (one CTA per (segment, kv head, 128-row query tile)):
-//   * warp 0 loads Q once and streams K tiles (128 keys) through a 3-slot
-//     ring by TMA, whole-tile copies when the runs sit on consecutive pages;
-//   * warp 1 issues S(j) = Q K_j^T into one of two TMEM score buffers, then
-//     the column sums of the probability tile of j - 1 as a second MMA,
-//     D = ones(128 x 128) P(j-1), whose every row is the vector of column sums
-//     (P tiles are bf16 in shared memory as the B operand, two buffers; D has
-//     two TMEM buffers);
-//   * warps 2-5 (one row per thread) turn scores into probabilities with the
-//     final lse, write them to shared memory, and read back the column sums of
-//     tile j - 2 (lane l of quadrant q takes column 32q + l) before reusing its
-//     P buffer, adding them into the output of the entry's token with one
-//     atomic each.  Reading two tiles back keeps the sum MMA of one tile off
-//     the critical path of the next.
+// GB300 design (one CTA per (segment, kv head, pair of 128-row query tiles)):
+//   * warp 0 loads both Q tiles once and streams K tiles (128 keys) through a
+//     2-slot ring by TMA, whole-tile copies when the runs sit on consecutive
+//     pages; each K tile feeds both query tiles;
+//   * warp 1 issues, per K tile j and query tile t, S_t(j) = Q_t K_j^T into
+//     the TMEM score buffer of t, then the column sums of t's probability tile
+//     of j - 1 as a second MMA, D_t = ones(128 x 128) P_t(j-1), whose every
+//     row is the vector of column sums (P_t is bf16 in shared memory as the B
+//     operand);
+//   * warps 2-5 (query tile 0) and 6-9 (query tile 1), one row per thread,
+//     turn scores into probabilities with the final lse; a warpgroup frees its
+//     score buffer as soon as it has read it (so the next QK runs under its
+//     exponentials), reads back the column sums of its previous tile (lane l
+//     of quadrant q takes column 32q + l) just before overwriting its P tile,
+//     and adds them into the output of the entry's token with one atomic each.
+//     The two warpgroups keep the tensor pipe fed while either one waits.
 // Every wait is bounded; on time-out the CTA records AKV_ERR_DEVICE_TIMEOUT.
 #include <cuda_bf16.h>
 
@@ -37,12 +39,12 @@
 namespace akv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 2 x 4 softmax warps
 constexpr int kKeys = 128;
 constexpr int kRows = 128;
-constexpr int kRing = 3;
+constexpr int kRing = 2;
 constexpr int kMaxRuns = 8;
-constexpr uint32_t kTmemCols = 512;  // S0, S1, D0, D1 (128 columns each)
+constexpr uint32_t kTmemCols = 512;  // S_0, S_1, D_0, D_1 (128 columns each)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;
@@ -53,13 +55,13 @@ struct MLayout {
   static constexpr int kBlocks = D / 64;
   static constexpr uint32_t kBlockBytes = 128 * 128;
   static constexpr uint32_t kTile = kBlocks * kBlockBytes;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kSlot = kQ + kTile;
-  static constexpr uint32_t kP = kSlot + kRing * kTile;  // two probability tiles, each 2 x 64-key blocks
-  static constexpr uint32_t kPTile = 2 * kBlockBytes;
-  static constexpr uint32_t kOnes = kP + 2 * kPTile;     // one 128 x 64 block of bf16 ones
-  static constexpr uint32_t kColE = kOnes + kBlockBytes;
-  static constexpr uint32_t kBars = kColE + 128 * 4;
+  static constexpr uint32_t kQ = 0;                        // two Q tiles
+  static constexpr uint32_t kSlot = kQ + 2 * kTile;        // K ring
+  static constexpr uint32_t kP = kSlot + kRing * kTile;    // one probability tile per query tile
+  static constexpr uint32_t kPTile = 2 * kBlockBytes;      // 2 x 64-key blocks
+  static constexpr uint32_t kOnes = kP + 2 * kPTile;       // one 128 x 64 block of bf16 ones
+  static constexpr uint32_t kColE = kOnes + kBlockBytes;   // int32 [2 query tiles][128]
+  static constexpr uint32_t kBars = kColE + 2 * 128 * 4;
   static constexpr uint32_t kBytes = kBars + 256;
 };
 
@@ -67,10 +69,10 @@ enum MBar {
   kMQ = 0,
   kMFull0,
   kMEmpty0 = kMFull0 + kRing,
-  kMS0 = kMEmpty0 + kRing,  // + buffer
-  kMSFree0 = kMS0 + 2,      // + buffer, 128 arrivals
-  kMPFull0 = kMSFree0 + 2,  // + tile parity, 128 arrivals
-  kMD0 = kMPFull0 + 2,      // + tile parity
+  kMS0 = kMEmpty0 + kRing,  // + query tile
+  kMSFree0 = kMS0 + 2,      // + query tile, 128 arrivals
+  kMPFull0 = kMSFree0 + 2,  // + query tile, 128 arrivals
+  kMD0 = kMPFull0 + 2,      // + query tile
   kMFin = kMD0 + 2,
   kMNumBars
 };
@@ -97,11 +99,13 @@ __device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg&
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
-  const int n = w.n_a;
-  ptx::mbar_arrive_expect_tx(bar(kMQ), L::kTile);
-  for (int kb = 0; kb < L::kBlocks; ++kb)
-    ptx::tma_load_3d(sbase + L::kQ + kb * L::kBlockBytes, &p.q_map, bar(kMQ), kb * 64, w.kvh * G,
-                     seg.q_row0 + w.qt0 * tpt);
+  const int n = max(w.n_a, w.n_b);
+  const int n_q = w.n_b > 0 ? 2 : 1;
+  ptx::mbar_arrive_expect_tx(bar(kMQ), n_q * L::kTile);
+  for (int t = 0; t < n_q; ++t)
+    for (int kb = 0; kb < L::kBlocks; ++kb)
+      ptx::tma_load_3d(sbase + L::kQ + t * L::kTile + kb * L::kBlockBytes, &p.q_map, bar(kMQ), kb * 64, w.kvh * G,
+                       seg.q_row0 + (w.qt0 + t) * tpt);
   const int layer_base = p.layer * p.n_pages;
   const int first = p.runs[seg.run_off].kp;
   int kpg[kMaxRuns], nkp[kMaxRuns];
@@ -153,8 +157,11 @@ __device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg&
 }
 
 // --------------------------------------------------------------------- MMA
-// Per tile j: S(j & 1) = Q K_j^T; then, once the probabilities of tile j - 1
-// are in shared memory, D = ones P(j - 1) (column sums in every row of D).
+// Per K tile j, for each query tile t that reads it: S_t(j) = Q_t K_j^T once
+// t's softmax has read S_t(j-1); then, for each t whose probabilities of tile
+// j - 1 are in shared memory, D_t = ones P_t(j-1).  D_t and P_t have one
+// buffer each: P_t(j-1) is written only after t's softmax has read D_t(j-2),
+// so the sum MMA of j - 1 never overwrites unread sums.
 template <int D>
 __device__ void m_mma(const MassParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
   using L = MLayout<D>;
@@ -162,37 +169,44 @@ __device__ void m_mma(const MassParams& p, const AttnWork& w, uint32_t sbase, ui
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kKeys, false);
   constexpr uint32_t idesc_sum = ptx::idesc_bf16(kRows, kKeys, true);  // B = P, keys (N) contiguous
-  const int n = w.n_a;
-  const uint64_t qd = ptx::smem_desc(sbase + L::kQ, 16, 1024);
+  const int nt[2] = {w.n_a, w.n_b};
+  const int n = max(w.n_a, w.n_b);
   const uint64_t ones = ptx::smem_desc(sbase + L::kOnes, 16, 1024);
-  const uint64_t pd = ptx::smem_desc(sbase + L::kP, L::kBlockBytes, 1024);
   bool ok = ptx::mbar_wait(bar(kMQ), 0, abort_flag, kWaitLimitNs);
   for (int j = 0; j <= n && ok; ++j) {
     if (j < n) {
       const int slot = j % kRing;
       if (!(ok = ptx::mbar_wait(bar(kMFull0 + slot), (j / kRing) & 1, abort_flag, kWaitLimitNs))) break;
-      if (j >= 2 && !(ok = ptx::mbar_wait(bar(kMSFree0 + (j & 1)), ((j >> 1) - 1) & 1, abort_flag, kWaitLimitNs)))
-        break;
-      ptx::tc_fence_after();
       const uint64_t kd = ptx::smem_desc(sbase + L::kSlot + slot * L::kTile, 16, 1024);
+#pragma unroll 1
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j >= nt[t]) continue;
+        if (j >= 1 && !(ok = ptx::mbar_wait(bar(kMSFree0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        ptx::tc_fence_after();
+        const uint64_t qd = ptx::smem_desc(sbase + L::kQ + t * L::kTile, 16, 1024);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
-        ptx::mma_bf16(tmem + 128u * (j & 1), ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), idesc_qk, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
+          ptx::mma_bf16(tmem + 128u * t, ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), idesc_qk, ks > 0);
+        }
+        ptx::mma_commit(bar(kMS0 + t));
       }
-      ptx::mma_commit(bar(kMS0 + (j & 1)));
+      if (!ok) break;
       ptx::mma_commit(bar(kMEmpty0 + slot));
     }
     if (j >= 1) {
-      const int b = (j - 1) & 1;  // buffers of tile j - 1
-      if (!(ok = ptx::mbar_wait(bar(kMPFull0 + b), ((j - 1) >> 1) & 1, abort_flag, kWaitLimitNs))) break;
-      ptx::tc_fence_after();
-      const uint64_t pdb = ptx::desc_advance(pd, b * L::kPTile);
+#pragma unroll 1
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j - 1 >= nt[t]) continue;
+        if (!(ok = ptx::mbar_wait(bar(kMPFull0 + t), (j - 1) & 1, abort_flag, kWaitLimitNs))) break;
+        ptx::tc_fence_after();
+        const uint64_t pd = ptx::smem_desc(sbase + L::kP + t * L::kPTile, L::kBlockBytes, 1024);
 #pragma unroll
-      for (int ks = 0; ks < kRows / 16; ++ks)  // 16 probability rows per step; every A element is 1
-        ptx::mma_bf16(tmem + 256u + 128u * b, ptx::desc_advance(ones, (ks & 3) * 32),
-                      ptx::desc_advance(pdb, ks * 16 * 128), idesc_sum, ks > 0);
-      ptx::mma_commit(bar(kMD0 + b));
+        for (int ks = 0; ks < kRows / 16; ++ks)  // 16 probability rows per step; every A element is 1
+          ptx::mma_bf16(tmem + 256u + 128u * t, ptx::desc_advance(ones, (ks & 3) * 32),
+                        ptx::desc_advance(pd, ks * 16 * 128), idesc_sum, ks > 0);
+        ptx::mma_commit(bar(kMD0 + t));
+      }
     }
   }
   if (!ok) {
@@ -204,29 +218,31 @@ __device__ void m_mma(const MassParams& p, const AttnWork& w, uint32_t sbase, ui
 }
 
 // ----------------------------------------------------------------- softmax
-// Thread = row r = TMEM lane r: probabilities of its row with the final lse,
-// bf16 into the shared P tile (128-byte swizzle, keys contiguous); thread r
-// also owns key column r when the column sums come back.
+// Warpgroup t, thread = row r = TMEM lane r: probabilities of its row with the
+// final lse, bf16 into t's shared P tile (128-byte swizzle, keys contiguous);
+// thread r also owns key column r when the column sums come back.
 template <int D>
-__device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg& seg, uint8_t* smem, uint32_t sbase,
-                          uint32_t tmem, volatile int* abort_flag) {
+__device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg& seg, int t, uint8_t* smem,
+                          uint32_t sbase, uint32_t tmem, volatile int* abort_flag) {
   using L = MLayout<D>;
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
-  const int n = w.n_a;
+  const int n = t == 0 ? w.n_a : w.n_b;
+  const int bar_id = 1 + t;  // named barrier of this warpgroup
   const int quad = (threadIdx.x / 32) & 3, lane = threadIdx.x % 32;
   const int r = quad * 32 + lane;
   const uint32_t lane_addr = uint32_t(quad * 32) << 16;
+  const uint32_t tS = tmem + 128u * t, tD = tmem + 256u + 128u * t;
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
-  const int qi = w.qt0 * tpt + r / G, g = r % G;
+  const int qi = (w.qt0 + t) * tpt + r / G, g = r % G;
   const bool row_valid = qi < seg.q_len;
   const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
   // log2-domain normaliser of this row; rows past the segment's queries contribute nothing
   const float lse2 = row_valid ? p.lse[int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g] * 1.4426950408889634f
                                : INFINITY;
   const float2 sl2v = make_float2(p.scale_log2, p.scale_log2), neg = make_float2(-lse2, -lse2);
-  int* colE = reinterpret_cast<int*>(smem + L::kColE);
-  uint8_t* P = smem + L::kP;
+  int* colE = reinterpret_cast<int*>(smem + L::kColE) + 128 * t;
+  uint8_t* P = smem + L::kP + t * L::kPTile;
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
   const int sl_own = r & (p.page - 1);
@@ -234,25 +250,49 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
   int2 run_cur = make_int2(0, 0);
   if ((r >> page_shift) < seg.n_runs) run_cur = run_le[2 * (r >> page_shift) + 1];
   bool ok = true;
-  int e_even = INT_MAX, e_odd = INT_MAX;  // entry of key column r in the last even / odd tile
-  // column sums of tile jj come back in D: lane l of quadrant q reads column 32q + l
+  int e_prev = INT_MAX;
+  // column sums of tile jj come back in D_t: lane l of quadrant q reads column 32q + l
   auto take_sums = [&](int jj) {
-    const int b = jj & 1;
-    ok = ptx::mbar_wait(bar(kMD0 + b), (jj >> 1) & 1, abort_flag, kWaitLimitNs);
-    if (!ptx::bar_red_and(1, 128, ok)) return false;
+    ok = ptx::mbar_wait(bar(kMD0 + t), jj & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(bar_id, 128, ok)) return false;
     ptx::tc_fence_after();
     uint32_t v[32];
-    ptx::tmem_load32(tmem + 256u + 128u * b + lane_addr + quad * 32, v);
+    ptx::tmem_load32(tD + lane_addr + quad * 32, v);
     float mine = 0.f;
 #pragma unroll
     for (int k = 0; k < 32; ++k) mine = lane == k ? __uint_as_float(v[k]) : mine;
-    const int e_jj = b ? e_odd : e_even;
-    if (e_jj != INT_MAX) atomicAdd(p.mass + seg.mass_off + p.ent_tok[seg.ent_off + e_jj], mine);
+    if (e_prev != INT_MAX) atomicAdd(p.mass + seg.mass_off + p.ent_tok[seg.ent_off + e_prev], mine);
     return true;
   };
+  // probabilities of 64 scores, packed as bf16 pairs
+  auto probs = [&](uint32_t (&u)[64], bool need_mask, int h, uint32_t (&pk)[32]) {
+    const int4* ce4 = reinterpret_cast<const int4*>(colE);
+    if (need_mask) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int4 e4 = ce4[h * 16 + c];
+        if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
+        if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
+        if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
+        if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2v, neg);
+      pk[c] = pack_bf16(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
+    }
+  };
+  auto store = [&](int h, const uint32_t (&pk)[32]) {
+    uint8_t* rowp = P + h * L::kBlockBytes + r * 128;
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4*>(rowp + ((c8 ^ (r & 7)) << 4)) =
+          make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+  };
   for (int j = 0; j < n && ok; ++j) {
-    ok = ptx::mbar_wait(bar(kMS0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs);
-    if (!ptx::bar_red_and(1, 128, ok)) {
+    ok = ptx::mbar_wait(bar(kMS0 + t), j & 1, abort_flag, kWaitLimitNs);
+    if (!ptx::bar_red_and(bar_id, 128, ok)) {
       ok = false;
       break;
     }
@@ -264,51 +304,34 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
       const int ri = (j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
-    const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
+    const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
     ptx::tc_fence_after();
     const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
-    // the sums of tile j - 2 are read before its P buffer is overwritten
-    if (j >= 2 && !(ok = take_sums(j - 2))) break;
-    const int4* ce4 = reinterpret_cast<const int4*>(colE);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    uint32_t pk0[32], pk1[32];
+    {
       uint32_t u[64];
-      ptx::tmem_load64(tmem + 128u * (j & 1) + lane_addr + h * 64, u);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int4 e4 = ce4[h * 16 + c];
-          if (e4.x > lim) u[4 * c + 0] = 0xff800000u;
-          if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
-          if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
-          if (e4.w > lim) u[4 * c + 3] = 0xff800000u;
-        }
-      }
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2v, neg);
-        pk[c] = pack_bf16(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
-      }
-      uint8_t* rowp = P + (j & 1) * L::kPTile + h * L::kBlockBytes + r * 128;
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8)
-        *reinterpret_cast<uint4*>(rowp + ((c8 ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+      ptx::tmem_load64(tS + lane_addr, u);
+      probs(u, need_mask, 0, pk0);
     }
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(bar(kMSFree0 + (j & 1)));
+    {
+      uint32_t u[64];
+      ptx::tmem_load64(tS + lane_addr + 64, u);
+      // S_t is read: the next QK of this query tile may overwrite it
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kMSFree0 + t));
+      probs(u, need_mask, 1, pk1);
+    }
+    // the sums of tile j - 1 are read before its P tile is overwritten
+    if (j >= 1 && !(ok = take_sums(j - 1))) break;
+    store(0, pk0);
+    store(1, pk1);
     ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(bar(kMPFull0 + (j & 1)));
-    if (j & 1)
-      e_odd = e;
-    else
-      e_even = e;
+    ptx::mbar_arrive(bar(kMPFull0 + t));
+    e_prev = e;
   }
-  if (ok && n >= 2) ok = take_sums(n - 2);
   if (ok && n >= 1) ok = take_sums(n - 1);
   if (!ok) {
-    raise_error(p.err, kErrTimeout, blockIdx.x, 2, 0);
+    raise_error(p.err, kErrTimeout, blockIdx.x, 2 + t, 0);
     *abort_flag = 1;
   }
 }
@@ -331,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mass_kernel(const __grid_con
   const AttnWork w = p.work[blockIdx.x];
   const AttnSeg seg = p.segs[w.seg];
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kMNumBars; ++i)
-      ptx::mbar_init(bars + 8u * i, (i == kMSFree0 || i == kMSFree0 + 1 || i == kMPFull0 || i == kMPFull0 + 1) ? 128 : 1);
+    for (int i = 0; i < kMNumBars; ++i) {
+      const bool many = (i >= kMSFree0 && i < kMSFree0 + 2) || (i >= kMPFull0 && i < kMPFull0 + 2);
+      ptx::mbar_init(bars + 8u * i, many ? 128 : 1);
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -358,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mass_kernel(const __grid_con
   } else if (warp == 1) {
     if (lane == 0) m_mma<D>(p, w, sbase, tmem, abort_flag);
   } else {
-    m_softmax<D>(p, w, seg, smem, sbase, tmem, abort_flag);
+    m_softmax<D>(p, w, seg, warp < 6 ? 0 : 1, smem, sbase, tmem, abort_flag);
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -1640,16 +1640,22 @@ struct akv_ctx {
       mass_len += segs[i].kv_end;
       const int64_t ql = sg.q_len, kl = sg.kv_len;
       const int n_qt = int((ql + tpt - 1) / tpt);
-      for (int qt = 0; qt < n_qt; ++qt) {
-        // KV tiles the query tile reads: runs whose first entry is <= its last row's limit
+      // KV tiles query tile qt reads: runs whose first entry is <= its last row's limit
+      auto tiles_of = [&](int qt) -> int32_t {
+        if (qt >= n_qt) return 0;
         const int64_t limit = kl - ql + std::min<int64_t>(ql, int64_t(qt + 1) * tpt) - 1;
         int64_t lo_r = 0, hi_r = int64_t(sp.runs.size());
         while (lo_r < hi_r) {
           const int64_t mid = (lo_r + hi_r) / 2;
           if (sp.runs[mid].es <= limit) lo_r = mid + 1; else hi_r = mid;
         }
-        const int32_t nt = int32_t((lo_r + rpt - 1) / rpt);
-        for (int h = 0; h < cfg.n_kv_heads; ++h) work.push_back(akv::AttnWork{i, h, qt, nt, 0, 0, nt, -1, -1});
+        return int32_t((lo_r + rpt - 1) / rpt);
+      };
+      // one item per pair of query tiles (the second absent: n_b = 0) and kv head
+      for (int qt = 0; qt < n_qt; qt += 2) {
+        const int32_t na = tiles_of(qt), nb = tiles_of(qt + 1);
+        for (int h = 0; h < cfg.n_kv_heads; ++h)
+          work.push_back(akv::AttnWork{i, h, qt, na, nb, 0, std::max(na, nb), -1, -1});
       }
       runs.insert(runs.end(), sp.runs.begin(), sp.runs.end());
       ent_tok.insert(ent_tok.end(), sp.tok.begin(), sp.tok.end());
@@ -1657,8 +1663,9 @@ struct akv_ctx {
     }
     if (meta) return;
     if (!(cfg.d_rot == 64 || cfg.d_rot == 128)) fail(AKV_ERR_ARG, "attention mass supports head_dim 64 or 128");
-    std::stable_sort(work.begin(), work.end(),
-                     [](const akv::AttnWork& a, const akv::AttnWork& b) { return a.n_a > b.n_a; });
+    std::stable_sort(work.begin(), work.end(), [](const akv::AttnWork& a, const akv::AttnWork& b) {
+      return std::max(a.n_a, a.n_b) > std::max(b.n_a, b.n_b);
+    });
     const size_t qbytes = size_t(n_q_rows) * cfg.n_q_heads * cfg.d_rot * 2;
     const void* qd = device_input(q, qbytes, st_q, st);
     const float* lsed = static_cast<const float*>(device_input(lse, size_t(n_q_rows) * cfg.n_q_heads * 4, st_lse, st));

@@ -158,8 +158,9 @@ struct MassParams {
 __host__ __device__ inline int64_t partial_floats(int tiles, int width) { return int64_t(tiles) * 128 * (width + 2); }
 
 // Launchers; each returns the launch's cudaError_t.
-cudaError_t launch_kv_write(const void* src, void* pool, const int32_t* rows, int64_t n, int n_layers,
-                            int heads, int dim, int page, int64_t n_pages, cudaStream_t st);
+cudaError_t launch_kv_write(const void* src_k, void* pool_k, const int32_t* rows_k, int dim_k, const void* src_v,
+                            void* pool_v, const int32_t* rows_v, int dim_v, int64_t n, int n_layers, int heads,
+                            int page, int64_t n_pages, int n_sm, cudaStream_t st);
 
 cudaError_t launch_compact_copy(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int d_v, int page, int64_t n_pages, bool half,

@@ -465,12 +465,10 @@ struct akv_ctx {
     void* dv = nullptr;
     up.upload({{krow.data(), krow.size() * 4, &dk}, {vrow.data(), vrow.size() * 4, &dv}}, st);
     Timed t;
-    begin_timed(kKvWrite, double(kbytes + vbytes) * 2.0, 0.0, st, t, 2);
-    cuda_check(akv::launch_kv_write(kd, kpool, static_cast<int32_t*>(dk), n, cfg.n_layers, cfg.n_kv_heads,
-                                    cfg.d_rot, cfg.page_size, cfg.n_pages, st),
-               "kv_write launch");
-    cuda_check(akv::launch_kv_write(vd, vpool, static_cast<int32_t*>(dv), n, cfg.n_layers, cfg.n_kv_heads,
-                                    cfg.d_v, cfg.page_size, cfg.n_pages, st),
+    begin_timed(kKvWrite, double(kbytes + vbytes) * 2.0, 0.0, st, t, 1);
+    cuda_check(akv::launch_kv_write(kd, kpool, static_cast<int32_t*>(dk), cfg.d_rot, vd, vpool,
+                                    static_cast<int32_t*>(dv), cfg.d_v, n, cfg.n_layers, cfg.n_kv_heads,
+                                    cfg.page_size, cfg.n_pages, n_sm, st),
                "kv_write launch");
     end_timed(t, st);
     up.done(st);

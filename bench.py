@@ -569,7 +569,92 @@ def gpu_arm(args, rank, world):
         line["compact_copy"] = compaction()
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        if not args.no_extra:
+            line["oracle_beside"] = oracle_beside(line)
     return line
+
+
+def oracle_beside(line):
+    """The float64 oracle timed on host cores beside the GPU numbers of the next rows (attention
+    mass, compaction, one MLA layer), each on a bounded sample scaled to the GPU's workload."""
+    from agentic_kv_cache_gb300 import synth
+    from oracle import attention, bf16, kernels
+    from oracle.cache import CacheModel
+    out = {"cores": os.cpu_count(), "kind": "oracle"}
+    ot = OracleTurn(extra_pages=2048)  # room for the compacted copy of the branch
+    m, w, sh = ot.model, ot.w, ot.w.shape
+    names = dict(ot.names)
+    for op in ot.step_ops:
+        if op[0] == "fork":
+            names[op[1]] = m.seq_fork(names[op[2]], op[3])
+        elif op[0] == "drop":
+            m.drop(names[op[1]], op[2], op[3])
+        elif op[0] == "repos":
+            m.repos(names[op[1]], op[2], op[3], op[4])
+        elif op[0] == "append":
+            ot._write(m.append(names[op[1]], op[2]), op[3], op[2])
+    g = w.segments[0]
+    kernels.repos_runs(ot.kp, m.flush([names[g["seq"]]]), sh.rope_base, sh.rope_layout, out=ot.kp)
+    seg_runs, _ = m.segment_runs(names[g["seq"]], g["kv_end"], g["q_len"], g["hide"])
+    k = kernels.gather(ot.kp, 0, seg_runs, 0).astype(np.float64)
+    # attention mass: the first `rows` queries against the entries they see (same cost per row)
+    rows, q_len, q0 = 32, g["q_len"], g["q_row0"]
+    t0 = time.perf_counter()
+    attention.attention_mass(ot.qb[q0:q0 + rows], k[:k.shape[0] - q_len + rows], sh.scale)
+    t_mass = (time.perf_counter() - t0) * q_len / rows
+    gm = line.get("attention_mass", {}).get("ms")
+    out["attention_mass"] = {"oracle_s": t_mass, "gpu_ms": gm, "gpu_speedup": t_mass / (gm * 1e-3) if gm else None,
+                             "sample": f"{rows} of {q_len} query rows (all heads) over their visible entries, "
+                                       "scaled to all rows"}
+    # compaction: bookkeeping plus the copy of one layer (rotating the pending shifts), scaled to 32
+    t0 = time.perf_counter()
+    copies = m.compact(names["F"])
+    t_book = time.perf_counter() - t0
+    part = copies[:2048]
+    t0 = time.perf_counter()
+    kernels.compact_copy(ot.kp, ot.vp, [], sh.rope_base, sh.rope_layout)  # the pools' copy alone
+    t_fixed = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    kernels.compact_copy(ot.kp, ot.vp, part, sh.rope_base, sh.rope_layout)
+    t_copy = t_fixed + max(time.perf_counter() - t0 - t_fixed, 0.0) * len(copies) / max(len(part), 1)
+    gc = line.get("compact_copy", {}).get("ms_per_compaction")
+    t_comp = t_book + 32 * t_copy
+    out["compaction"] = {"oracle_s": t_comp, "gpu_ms": gc, "gpu_speedup": t_comp / (gc * 1e-3) if gc else None,
+                         "sample": f"bookkeeping of the whole branch ({len(copies)} kept tokens) and the copy of "
+                                   f"{len(part)} of them in one layer, the per-token part scaled to all tokens, "
+                                   "the one-layer copy scaled linearly to 32 layers"}
+    m.seq_free(names["F"])
+    # one MLA layer of a one-session turn: the spliced 17K session, attention on sampled rows
+    wm = synth.mla_dsv2lite(n_layers=1, concurrency=1)
+    ms_ = wm.shape
+    cm = CacheModel(wm.n_pages, ms_.page_size)
+    kp = np.zeros((1, wm.n_pages, 1, ms_.page_size, ms_.d_rot), np.float32)
+    vp = np.zeros((1, wm.n_pages, 1, ms_.page_size, ms_.d_v), np.float32)
+    mn = {}
+    for op in wm.ops:
+        if op[0] == "alloc":
+            mn[op[1]] = cm.seq_alloc()
+            continue
+        n, key = (op[2], op[3]) if op[0] == "append" else (op[4], op[5])
+        slots = cm.append(mn[op[1]], n) if op[0] == "append" else cm.splice(mn[op[1]], op[2], op[3], op[4])
+        k32, v32 = synth.kv_arrays(wm, key, n)
+        idx = np.array(slots)
+        kp[:, idx[:, 0], :, idx[:, 2]] = bf16.round_bf16(k32.astype(np.float64)).astype(np.float32).transpose(1, 0, 2, 3)
+        vp[:, idx[:, 1], :, idx[:, 2]] = bf16.round_bf16(v32.astype(np.float64)).astype(np.float32).transpose(1, 0, 2, 3)
+    gs = wm.segments[0]
+    kernels.repos_runs(kp, cm.flush([mn[gs["seq"]]]), ms_.rope_base, ms_.rope_layout, out=kp)
+    runs_m, _ = cm.segment_runs(mn[gs["seq"]], gs["kv_end"], gs["q_len"], gs["hide"])
+    qm = bf16.round_bf16(synth.q_array(wm).astype(np.float64))[gs["q_row0"]:gs["q_row0"] + gs["q_len"]]
+    rows_m = 8
+    t0 = time.perf_counter()
+    kernels.attend_segment(qm, kp, vp, 0, runs_m, ms_.scale, mla=True,
+                           rows=np.linspace(0, gs["q_len"] - 1, rows_m).astype(np.int64))
+    t_mla = (time.perf_counter() - t0) * gs["q_len"] / rows_m
+    c1 = line.get("mla_dsv2lite_turn", {}).get("C1", {}).get("attn_ms_per_layer")
+    out["mla_attention_one_layer_c1"] = {
+        "oracle_s": t_mla, "gpu_ms": c1, "gpu_speedup": t_mla / (c1 * 1e-3) if c1 else None,
+        "sample": f"{rows_m} of {gs['q_len']} query rows (16 heads, d_qk 576) over the spliced session, scaled"}
+    return out
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
@@ -577,7 +662,7 @@ class OracleTurn:
     """The float64 oracle on the same turn: resident trajectory built once, then per step
     the turn's bookkeeping, the full repos and attention on a sample of query rows."""
 
-    def __init__(self, seed=0):
+    def __init__(self, seed=0, extra_pages=0):
         from agentic_kv_cache_gb300 import synth
         from oracle import attention, bf16, kernels
         from oracle.cache import CacheModel
@@ -586,8 +671,8 @@ class OracleTurn:
         s = w.shape
         fork_at = next(i for i, op in enumerate(w.ops) if op[0] == "fork")
         self.step_ops = w.ops[fork_at:]
-        self.model = CacheModel(w.n_pages, s.page_size)
-        self.kp = np.zeros((1, w.n_pages, s.n_kv_heads, s.page_size, s.d_rot), np.float32)
+        self.model = CacheModel(w.n_pages + extra_pages, s.page_size)
+        self.kp = np.zeros((1, w.n_pages + extra_pages, s.n_kv_heads, s.page_size, s.d_rot), np.float32)
         self.vp = np.zeros_like(self.kp)
         self.names = {}
         self.values = {}

@@ -1,4 +1,5 @@
-"""Randomised segment_batch_attn workloads against the float64 oracle.
+"""Randomised segment_batch_attn workloads against the float64 oracle (and,
+for GQA, the fused-rotation path on histories with pending shifts).
 
 Each case draws a small cache history (prompt, drops, repositions, a splice, a
 fork with its own edits, new tokens on both branches, hidden spans) for GQA
@@ -19,7 +20,7 @@ pytestmark = pytest.mark.gpu
 ATOL = 2e-2
 
 
-def random_workload(seed, mla):
+def random_workload(seed, mla, force_repos=False):
     rng = np.random.default_rng(9100 + seed)
     if mla:
         w = synth.mla_dsv2lite(n_layers=1, concurrency=1)
@@ -55,6 +56,10 @@ def random_workload(seed, mla):
                 length[seq] = n - (e - s) + stub
 
     edits("A", int(rng.integers(0, 6)))
+    if force_repos:  # at least one pending shift on A
+        a = int(rng.integers(0, length["A"]))
+        ops.append(("repos", "A", a, int(rng.integers(a + 1, length["A"] + 1)), int(rng.choice([-1, 1])) *
+                    int(rng.integers(1, 3000))))
     fork_at = int(rng.integers(1, length["A"] + 1))
     ops.append(("fork", "B", "A", fork_at))
     length["B"] = fork_at
@@ -100,3 +105,9 @@ def test_random_workloads_match_oracle(seed, mla):
     w = random_workload(seed, mla)
     split = 0 if seed % 2 == 0 else int(np.random.default_rng(seed).integers(2, 6))
     check_all_rows(w, split)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_fused_histories_match_oracle(seed):
+    from test_gpu_fused import fused_case
+    fused_case(random_workload(100 + seed, False, force_repos=True))

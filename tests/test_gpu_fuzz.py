@@ -1,5 +1,6 @@
 """Randomised segment_batch_attn workloads against the float64 oracle (and,
-for GQA, the fused-rotation path on histories with pending shifts).
+for GQA, the fused-rotation path on histories with pending shifts and the
+attention-mass pass).
 
 Each case draws a small cache history (prompt, drops, repositions, a splice, a
 fork with its own edits, new tokens on both branches, hidden spans) for GQA
@@ -111,3 +112,9 @@ def test_random_workloads_match_oracle(seed, mla):
 def test_random_fused_histories_match_oracle(seed):
     from test_gpu_fused import fused_case
     fused_case(random_workload(100 + seed, False, force_repos=True))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_histories_attention_mass(seed):
+    from test_gpu_mass import mass_case
+    mass_case(random_workload(200 + seed, False))

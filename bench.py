@@ -65,6 +65,18 @@ def measured_traffic(kernel):
     return rec
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over the process group (the slowest rank sets
+    the whole job's time); the values unchanged when no group is initialised."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()):
+        return list(values)
+    x = torch.tensor(list(values), dtype=torch.float64, device=device)
+    tdist.all_reduce(x, op=tdist.ReduceOp.MAX)
+    return x.tolist()
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples during the timed region."""
 
@@ -497,9 +509,7 @@ def gpu_arm(args, rank, world):
     lat_ms.sort()
 
     if dist:
-        x = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device="cuda")
-        tdist.all_reduce(x, op=tdist.ReduceOp.MAX)
-        total_ms, e2e_total = x.tolist()
+        total_ms, e2e_total = max_over_ranks([total_ms, e2e_total], "cuda")
     if rank != 0:
         return None
 

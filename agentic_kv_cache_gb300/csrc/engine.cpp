@@ -73,16 +73,21 @@ struct Tok {
 // Reference counts of one pool with lowest-free-id-first allocation.
 class Pool {
  public:
+  // Free pages are the set bits of a bitmap; the lowest set bit at or after
+  // hint_ (no free page lies below it) is the lowest free id, so allocation
+  // follows the lowest-free-id-first rule and a free is O(1).
   void init(int32_t n) {
     rc_.assign(n, 0);
-    std::vector<int32_t> ids(n);
-    for (int32_t i = 0; i < n; ++i) ids[i] = i;
-    free_ = decltype(free_)(std::greater<int32_t>(), std::move(ids));
+    free_.assign((size_t(n) + 63) / 64, ~uint64_t(0));
+    if (n % 64) free_.back() = (uint64_t(1) << (n % 64)) - 1;
+    hint_ = 0;
     n_free_ = n;
   }
-  int32_t alloc() {
-    int32_t p = free_.top();
-    free_.pop();
+  int32_t alloc() {  // callers check n_free() first
+    while (free_[hint_] == 0) ++hint_;
+    const int b = __builtin_ctzll(free_[hint_]);
+    free_[hint_] &= free_[hint_] - 1;
+    const int32_t p = int32_t(hint_ * 64 + size_t(b));
     rc_[p] = 1;
     --n_free_;
     return p;
@@ -90,7 +95,8 @@ class Pool {
   void inc(int32_t p) { ++rc_[p]; }
   void dec(int32_t p) {
     if (--rc_[p] == 0) {
-      free_.push(p);
+      free_[size_t(p) / 64] |= uint64_t(1) << (p % 64);
+      hint_ = std::min(hint_, size_t(p) / 64);
       ++n_free_;
     }
   }
@@ -100,7 +106,8 @@ class Pool {
 
  private:
   std::vector<int32_t> rc_;
-  std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_;
+  std::vector<uint64_t> free_;
+  size_t hint_ = 0;
   int32_t n_free_ = 0;
 };
 
@@ -814,11 +821,12 @@ struct akv_ctx {
   // and stored as float32: [deltas][d_rot / 2].
   std::vector<float2> angle_table(const std::vector<int32_t>& deltas) const {
     const int half = cfg.d_rot / 2;
+    std::vector<double> th(half);  // theta_j, the same for every shift
+    for (int j = 0; j < half; ++j) th[j] = std::pow(cfg.rope_base, -2.0 * j / cfg.d_rot);
     std::vector<float2> cs(deltas.size() * half);
     for (size_t d = 0; d < deltas.size(); ++d)
       for (int j = 0; j < half; ++j) {
-        const double th = std::pow(cfg.rope_base, -2.0 * j / cfg.d_rot);
-        const double a = double(deltas[d]) * th;
+        const double a = double(deltas[d]) * th[j];
         cs[d * half + j] = make_float2(float(std::cos(a)), float(std::sin(a)));
       }
     return cs;

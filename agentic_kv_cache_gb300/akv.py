@@ -65,11 +65,11 @@ def items_array(items):
 
 
 class KernelStats(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_int64 * 4), ("ms", ctypes.c_double * 4), ("bytes", ctypes.c_double * 4),
-                ("flops", ctypes.c_double * 4)]
+    _fields_ = [("launches", ctypes.c_int64 * 5), ("ms", ctypes.c_double * 5), ("bytes", ctypes.c_double * 5),
+                ("flops", ctypes.c_double * 5)]
 
 
-KERNEL_NAMES = ("kv_write", "repos_rotate", "segment_attn", "compact_copy")
+KERNEL_NAMES = ("kv_write", "repos_rotate", "segment_attn", "compact_copy", "attn_mass")
 
 _lib = None
 
@@ -339,7 +339,8 @@ class Engine:
         return code.value
 
     def set_attention_split(self, split):
-        """0: automatic split-KV; n >= 1: exactly n KV chunks per work item (1 = never split)."""
+        """0: automatic split-KV; n >= 1: exactly n KV chunks per work item (1 = never split).
+        Applies to attend and attention_mass."""
         self._check(self.lib.akv_set_attention_split(self.h, int(split)))
 
     def profile_enable(self, on=True):

@@ -10,7 +10,10 @@
 // probabilities are the final ones).  The policy on top (an epsilon over
 // three decode turns) is the caller's.
 //
-// GB300 design (one CTA per (segment, kv head, pair of 128-row query tiles)):
+// GB300 design (one CTA per (segment, kv head, pair of 128-row query tiles,
+// range of K tiles); the mass needs no online rescaling, since the lse is
+// final, so the host may cut a pair's K tiles into ranges that run as
+// separate CTAs and add into the same outputs):
 //   * warp 0 loads both Q tiles once and streams K tiles (128 keys) through a
 //     2-slot ring by TMA, whole-tile copies when the runs sit on consecutive
 //     pages; each K tile feeds both query tiles;
@@ -91,6 +94,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// K tiles [t0, t0 + n) of this CTA; na / nb of them are read by query tile 0 / 1.
+struct MassRange {
+  int t0, na, nb, n;
+};
+__device__ __forceinline__ MassRange mass_range(const AttnWork& w) {
+  const int na = max(0, min(w.n_a, w.t1) - w.t0), nb = max(0, min(w.n_b, w.t1) - w.t0);
+  return MassRange{w.t0, na, nb, max(na, nb)};
+}
+
 // ---------------------------------------------------------------- producer
 template <int D>
 __device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
@@ -99,8 +111,9 @@ __device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg&
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
-  const int n = max(w.n_a, w.n_b);
-  const int n_q = w.n_b > 0 ? 2 : 1;
+  const MassRange rg = mass_range(w);
+  const int n = rg.n;
+  const int n_q = rg.nb > 0 ? 2 : 1;
   ptx::mbar_arrive_expect_tx(bar(kMQ), n_q * L::kTile);
   for (int t = 0; t < n_q; ++t)
     for (int kb = 0; kb < L::kBlocks; ++kb)
@@ -109,10 +122,10 @@ __device__ void m_produce(const MassParams& p, const AttnWork& w, const AttnSeg&
   const int layer_base = p.layer * p.n_pages;
   const int first = p.runs[seg.run_off].kp;
   int kpg[kMaxRuns], nkp[kMaxRuns];
-  auto fetch = [&](int j, int (&kk)[kMaxRuns]) {  // K pages of tile j's runs, one tile ahead
+  auto fetch = [&](int j, int (&kk)[kMaxRuns]) {  // K pages of local tile j's runs, one tile ahead
 #pragma unroll
     for (int g = 0; g < kMaxRuns; ++g) {
-      const int ri = j * rpt + g;
+      const int ri = (rg.t0 + j) * rpt + g;
       kk[g] = layer_base + ((g < rpt && ri < seg.n_runs) ? p.runs[seg.run_off + ri].kp : first);
     }
   };
@@ -169,8 +182,9 @@ __device__ void m_mma(const MassParams& p, const AttnWork& w, uint32_t sbase, ui
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(kRows, kKeys, false);
   constexpr uint32_t idesc_sum = ptx::idesc_bf16(kRows, kKeys, true);  // B = P, keys (N) contiguous
-  const int nt[2] = {w.n_a, w.n_b};
-  const int n = max(w.n_a, w.n_b);
+  const MassRange rg = mass_range(w);
+  const int nt[2] = {rg.na, rg.nb};
+  const int n = rg.n;
   const uint64_t ones = ptx::smem_desc(sbase + L::kOnes, 16, 1024);
   bool ok = ptx::mbar_wait(bar(kMQ), 0, abort_flag, kWaitLimitNs);
   for (int j = 0; j <= n && ok; ++j) {
@@ -227,7 +241,8 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
   using L = MLayout<D>;
   const uint32_t bars = sbase + L::kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
-  const int n = t == 0 ? w.n_a : w.n_b;
+  const MassRange rg = mass_range(w);
+  const int n = t == 0 ? rg.na : rg.nb;
   const int bar_id = 1 + t;  // named barrier of this warpgroup
   const int quad = (threadIdx.x / 32) & 3, lane = threadIdx.x % 32;
   const int r = quad * 32 + lane;
@@ -248,7 +263,7 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
   const int sl_own = r & (p.page - 1);
   const int2* run_le = reinterpret_cast<const int2*>(p.runs + seg.run_off);
   int2 run_cur = make_int2(0, 0);
-  if ((r >> page_shift) < seg.n_runs) run_cur = run_le[2 * (r >> page_shift) + 1];
+  if (rg.t0 * rpt + (r >> page_shift) < seg.n_runs) run_cur = run_le[2 * (rg.t0 * rpt + (r >> page_shift)) + 1];
   bool ok = true;
   int e_prev = INT_MAX;
   // column sums of tile jj come back in D_t: lane l of quadrant q reads column 32q + l
@@ -301,7 +316,7 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
       const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
       if (sl_own >= lo && sl_own < hi) e = run_cur.y + (sl_own - lo);
       colE[r] = e;
-      const int ri = (j + 1) * rpt + (r >> page_shift);
+      const int ri = (rg.t0 + j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
     const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);

@@ -275,7 +275,43 @@ void encode_map(CUtensorMap* m, void* base, int rank, const uint64_t* dims, cons
   if (r != CUDA_SUCCESS) fail(AKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
 }
 
-enum KernelId { kKvWrite = 0, kRepos = 1, kAttn = 2, kCompact = 3 };
+enum KernelId { kKvWrite = 0, kRepos = 1, kAttn = 2, kCompact = 3, kMass = 4 };
+
+// End of a launch whose CTAs (or CTA pairs) cost `cost` each, run longest
+// first, each on the slot that frees first (the hardware hands out CTAs in
+// launch order as slots free up).
+double lpt_makespan(std::vector<double> cost, int64_t slots) {
+  std::sort(cost.begin(), cost.end(), std::greater<double>());
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int64_t i = 0; i < std::max<int64_t>(1, slots); ++i) free_at.push(0.0);
+  double end = 0.0;
+  for (double c : cost) {
+    const double t = free_at.top() + c;
+    free_at.pop();
+    free_at.push(t);
+    end = std::max(end, t);
+  }
+  return end;
+}
+
+// The same estimate in linear time for integer costs, given as a histogram
+// (count[c] = CTAs of cost c): the CTAs taken longest first in waves of
+// `slots`, each wave as long as its longest CTA (within a wave of LPT on
+// near-equal costs; an upper bound when costs are skewed).
+int64_t wave_makespan(const std::vector<int64_t>& count, int64_t slots) {
+  slots = std::max<int64_t>(1, slots);
+  int64_t end = 0, in_wave = 0;
+  for (size_t c = count.size(); c-- > 0;) {
+    int64_t m = count[c];
+    while (m > 0) {
+      if (in_wave == 0) end += int64_t(c);  // a new wave starts with its longest CTA
+      const int64_t take = std::min(m, slots - in_wave);
+      m -= take;
+      in_wave = (in_wave + take) % slots;
+    }
+  }
+  return end;
+}
 
 }  // namespace
 
@@ -1027,17 +1063,7 @@ struct akv_ctx {
         for (int c = 0; c < chunks[k]; ++c)
           cost.push_back(double(span) / chunks[k] + (chunks[k] > 1 ? kMlaPartCost : kMlaUnitCost));
       }
-      std::sort(cost.begin(), cost.end(), std::greater<double>());
-      std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-      for (int64_t i = 0; i < pair_slots; ++i) free_at.push(0.0);
-      double end = 0.0;
-      for (double c : cost) {
-        const double t = free_at.top() + c;
-        free_at.pop();
-        free_at.push(t);
-        end = std::max(end, t);
-      }
-      return end;
+      return lpt_makespan(std::move(cost), pair_slots);
     };
     // Candidates: every item in S chunks, or in S chunks with the smallest
     // number of items in S + 1 that fills the last wave of pairs.
@@ -1105,6 +1131,84 @@ struct akv_ctx {
       work.push_back(pr[0]);
       work.push_back(pr[1]);
     }
+  }
+
+  // K-tile ranges of the attention-mass pass.  The lse is final, so a pair
+  // item's K tiles can be cut into ranges that run as separate CTAs and add
+  // into the same outputs, with no merge.  Every item is cut into S equal
+  // ranges (or S + 1 for the fewest items that fill the last wave), S taken
+  // from the estimated makespan over one CTA per SM; a range costs its
+  // (K tile, query tile) steps plus a start (Q tiles, pipeline fill, drain).
+  // CTAs run longest first.
+  static constexpr int32_t kMassPartCost = 4;  // a CTA's start and drain, in (K tile, query tile) steps
+  void plan_mass_split(std::vector<akv::AttnWork>& work) {
+    const size_t n_items = work.size();
+    auto tiles = [](const akv::AttnWork& w) { return std::max(w.n_a, w.n_b); };
+    auto range = [&](const akv::AttnWork& w, int S, int c) {
+      return std::make_pair(int32_t(int64_t(tiles(w)) * c / S), int32_t(int64_t(tiles(w)) * (c + 1) / S));
+    };
+    auto cost = [](const akv::AttnWork& w, int32_t t0, int32_t t1) {
+      return std::max(0, std::min(w.n_a, t1) - t0) + std::max(0, std::min(w.n_b, t1) - t0) + kMassPartCost;
+    };
+    // largest items first: the extra range of a top-up goes to them
+    std::stable_sort(work.begin(), work.end(),
+                     [&](const akv::AttnWork& a, const akv::AttnWork& b) { return cost(a, 0, tiles(a)) > cost(b, 0, tiles(b)); });
+    // costs as a histogram; items alike (the kv heads of one query-tile
+    // pair, adjacent after the sort) are costed once
+    int32_t max_cost = 0;
+    for (const auto& w : work) max_cost = std::max(max_cost, cost(w, 0, tiles(w)));
+    std::vector<int64_t> hist;
+    auto makespan = [&](const std::vector<int>& ch) {
+      hist.assign(size_t(max_cost) + 1, 0);
+      for (size_t k = 0; k < n_items;) {
+        size_t e = k + 1;
+        while (e < n_items && ch[e] == ch[k] && work[e].n_a == work[k].n_a && work[e].n_b == work[k].n_b) ++e;
+        for (int i = 0; i < ch[k]; ++i) {
+          const auto r = range(work[k], ch[k], i);
+          hist[size_t(cost(work[k], r.first, r.second))] += int64_t(e - k);
+        }
+        k = e;
+      }
+      return wave_makespan(hist, n_sm);
+    };
+    std::vector<int> best_ch(n_items, 1);
+    int64_t best = -1;
+    const int cands[] = {1, 2, 3, 4, 5, 6, 8};
+    for (int S : cands) {
+      if (split_override > 0 && S != std::min(split_override, 8)) continue;
+      for (int top = 0; top < 2; ++top) {
+        std::vector<int> ch(n_items);
+        int64_t units = 0;
+        for (size_t k = 0; k < n_items; ++k) units += ch[k] = std::min(S, std::max(1, tiles(work[k])));
+        if (top) {
+          if (split_override > 0 || units % n_sm == 0) continue;
+          int64_t need = n_sm - units % n_sm;
+          for (size_t k = 0; k < n_items && need > 0; ++k)
+            if (ch[k] < 8 && ch[k] < tiles(work[k])) {
+              ++ch[k];
+              --need;
+            }
+        }
+        const int64_t m = makespan(ch);
+        if (best < 0 || m < best) {
+          best = m;
+          best_ch = ch;
+        }
+      }
+    }
+    std::vector<std::pair<int32_t, akv::AttnWork>> parts;
+    for (size_t k = 0; k < n_items; ++k)
+      for (int i = 0; i < best_ch[k]; ++i) {
+        akv::AttnWork w = work[k];
+        const auto r = range(w, best_ch[k], i);
+        w.t0 = r.first;
+        w.t1 = r.second;
+        parts.emplace_back(cost(w, w.t0, w.t1), w);
+      }
+    std::stable_sort(parts.begin(), parts.end(),
+                     [](const auto& a, const auto& b) { return a.first > b.first; });
+    work.clear();
+    for (const auto& pr : parts) work.push_back(pr.second);
   }
 
   // Persistent stream-K schedule for the GQA kernel: one CTA per SM, each
@@ -1632,6 +1736,7 @@ struct akv_ctx {
     std::vector<akv::AttnWork> work;
     std::vector<int32_t> ent_tok;
     int64_t mass_len = 0;
+    double flops = 0.0;  // QK^T and the column-sum product (ones(128 x 128) P) over the visible pairs
     for (int32_t i = 0; i < n_segs; ++i) {
       SegPlan sp = plan_segment(segs[i], false, true);
       akv::AttnSeg sg{};
@@ -1645,6 +1750,7 @@ struct akv_ctx {
       if (mass_len + segs[i].kv_end > kI32Max) fail(AKV_ERR_RANGE, "mass output too long");
       mass_len += segs[i].kv_end;
       const int64_t ql = sg.q_len, kl = sg.kv_len;
+      flops += double(cfg.n_q_heads) * 2.0 * (cfg.d_rot + 128) * double(ql * (kl - ql) + ql * (ql + 1) / 2);
       const int n_qt = int((ql + tpt - 1) / tpt);
       // KV tiles query tile qt reads: runs whose first entry is <= its last row's limit
       auto tiles_of = [&](int qt) -> int32_t {
@@ -1667,11 +1773,9 @@ struct akv_ctx {
       ent_tok.insert(ent_tok.end(), sp.tok.begin(), sp.tok.end());
       tab.push_back(sg);
     }
+    plan_mass_split(work);
     if (meta) return;
     if (!(cfg.d_rot == 64 || cfg.d_rot == 128)) fail(AKV_ERR_ARG, "attention mass supports head_dim 64 or 128");
-    std::stable_sort(work.begin(), work.end(), [](const akv::AttnWork& a, const akv::AttnWork& b) {
-      return std::max(a.n_a, a.n_b) > std::max(b.n_a, b.n_b);
-    });
     const size_t qbytes = size_t(n_q_rows) * cfg.n_q_heads * cfg.d_rot * 2;
     const void* qd = device_input(q, qbytes, st_q, st);
     const float* lsed = static_cast<const float*>(device_input(lse, size_t(n_q_rows) * cfg.n_q_heads * 4, st_lse, st));
@@ -1713,7 +1817,10 @@ struct akv_ctx {
     p.hq = cfg.n_q_heads;
     p.group = G;
     p.page = cfg.page_size;
+    Timed t;
+    begin_timed(kMass, 0.0, flops, st, t, 1);
     cuda_check(akv::launch_attn_mass(p, cfg.d_rot, st), "attn_mass launch");
+    end_timed(t, st);
     up.done(st);
     if (st_q.dev && !is_device_ptr(q)) st_q.release(st);
     if (st_lse.dev && !is_device_ptr(lse)) st_lse.release(st);

@@ -146,10 +146,11 @@ typedef struct akv_match {
 
 /* Per-kernel launch statistics collected while profiling is enabled. */
 typedef struct akv_kernel_stats {
-  int64_t launches[4];   /* [0] kv_write  [1] repos_rotate  [2] segment_attn  [3] compact_copy */
-  double ms[4];          /* summed CUDA-event time of those launches, milliseconds */
-  double bytes[4];       /* algorithmic bytes moved (kv_write, repos_rotate, compact_copy) */
-  double flops[4];       /* algorithmic FLOPs (segment_attn) */
+  int64_t launches[5];   /* [0] kv_write  [1] repos_rotate  [2] segment_attn  [3] compact_copy  [4] attn_mass */
+  double ms[5];          /* summed CUDA-event time of those launches (events around each launch), milliseconds */
+  double bytes[5];       /* algorithmic bytes moved (kv_write, repos_rotate, compact_copy) */
+  double flops[5];       /* algorithmic FLOPs (segment_attn: QK^T and PV over the visible pairs; attn_mass:
+                          * QK^T and the column-sum product, 2 x 128 FLOPs per visible pair and head) */
 } akv_kernel_stats;
 
 typedef struct akv_ctx akv_ctx;
@@ -378,10 +379,12 @@ AKV_API akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_
  * is cleared after reading.  Returns the same status as *code. */
 AKV_API akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code);
 
-/* Split-KV control for akv_attend.  0 (default): the engine cuts long work
- * items into up to 8 chunks of KV tiles when that fills the GPU's waves of
- * SMs better, and merges the chunks' partial softmax results in a combine
- * kernel.  1..8: use exactly that many chunks per item (1 = never split). */
+/* Split-KV control for akv_attend and akv_attention_mass.  0 (default): the
+ * engine cuts long work items into up to 8 chunks of KV tiles when that
+ * fills the GPU's waves of SMs better; akv_attend merges the chunks' partial
+ * softmax results in a combine kernel, akv_attention_mass needs no merge (its
+ * lse is final; chunks add into the same outputs).  1..8: use exactly that
+ * many chunks per item (1 = never split). */
 AKV_API akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split);
 
 /* Enable (1) or disable (0) per-launch CUDA-event timing of the context's

@@ -17,7 +17,7 @@ from agentic_kv_cache_gb300 import runner, synth
 pytestmark = pytest.mark.gpu
 
 
-def mass_case(w, seg_rows_only=False):
+def mass_case(w, split=0):
     from gpu_case import Case, bf16_of
     from oracle import attention, kernels
     c = Case(w)
@@ -32,6 +32,7 @@ def mass_case(w, seg_rows_only=False):
     c.eng.attend(0, segs, qd, nq, o, lse, s.scale, stream=c.stream)
     total = sum(g["kv_end"] for g in w.segments)
     mass = torch.full((total,), float("nan"), dtype=torch.float32, device="cuda")
+    c.eng.set_attention_split(split)
     c.eng.attention_mass(0, segs, qd, nq, lse, mass, s.scale, stream=c.stream)
     torch.cuda.synchronize()
     assert c.eng.check_device_error(c.stream) == 0
@@ -84,3 +85,8 @@ def test_mass_partial_pages_and_hidden_span():
 def test_mass_sessions_many_segments_group_8():
     w = synth.llama70b_128k(n_layers=1, total=8192, n_branches=3, q_per_branch=130)
     mass_case(w)
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 8])
+def test_mass_forced_k_ranges(split):
+    mass_case(synth.llama8b_32k(total=4096, n_new=300), split=split)

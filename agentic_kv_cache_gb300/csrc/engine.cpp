@@ -148,6 +148,7 @@ struct Staging {
     void* dev = nullptr;
     size_t cap = 0;
     cudaEvent_t ev = nullptr;
+    cudaEvent_t copied = nullptr;
     bool pending = false;
   } buf[2];
   int cur = 1;
@@ -177,11 +178,36 @@ struct Staging {
     cuda_check(cudaEventRecord(buf[cur].ev, st), "cudaEventRecord");
     buf[cur].pending = true;
   }
+  // Copy `bytes` of host `src` into the current device buffer.  With a copy
+  // stream `cp` the copy runs there, ahead of `st`'s earlier work, and `st`
+  // waits for it; acquire() has already waited until `st` no longer reads
+  // this buffer's previous contents.  Without one (or while `st` is being
+  // captured into a graph) the copy is ordered on `st` itself.
+  void copy_in(const void* src, size_t bytes, cudaStream_t st, cudaStream_t cp, const char* what) {
+    if (cp) {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cuda_check(cudaStreamIsCapturing(st, &cs), "cudaStreamIsCapturing");
+      if (cs != cudaStreamCaptureStatusNone) cp = nullptr;
+    }
+    if (!cp) {
+      cuda_check(cudaMemcpyAsync(dev, src, bytes, cudaMemcpyHostToDevice, st), what);
+      return;
+    }
+    Buf& b = buf[cur];
+    if (!b.copied) cuda_check(cudaEventCreateWithFlags(&b.copied, cudaEventDisableTiming), "cudaEventCreate");
+    cuda_check(cudaMemcpyAsync(dev, src, bytes, cudaMemcpyHostToDevice, cp), what);
+    cuda_check(cudaEventRecord(b.copied, cp), "cudaEventRecord");
+    cuda_check(cudaStreamWaitEvent(st, b.copied, 0), "cudaStreamWaitEvent");
+  }
   void destroy() {
     for (Buf& b : buf) {
       if (b.ev) {
         cudaEventSynchronize(b.ev);
         cudaEventDestroy(b.ev);
+      }
+      if (b.copied) {
+        cudaEventSynchronize(b.copied);
+        cudaEventDestroy(b.copied);
       }
       if (b.host) cudaFreeHost(b.host);
       if (b.dev) cudaFree(b.dev);
@@ -202,6 +228,7 @@ class Uploader {
     void** dst_dev;
   };
   void upload(std::initializer_list<Piece> pieces, cudaStream_t st) {
+    // the tables are the library's own and final here, so they may go ahead on the copy stream
     size_t total = 0;
     for (auto& p : pieces) total += (p.bytes + 15) & ~size_t(15);
     Staging& s = ring_[next_];
@@ -213,10 +240,10 @@ class Uploader {
       *p.dst_dev = static_cast<char*>(s.dev) + off;
       off += (p.bytes + 15) & ~size_t(15);
     }
-    cuda_check(cudaMemcpyAsync(s.dev, s.host, std::max<size_t>(off, 16), cudaMemcpyHostToDevice, st),
-               "descriptor upload");
+    s.copy_in(s.host, std::max<size_t>(off, 16), st, copy_stream, "descriptor upload");
     last_ = &s;
   }
+  cudaStream_t copy_stream = nullptr;
   // Record the event after the kernel that reads the last upload.
   void done(cudaStream_t st) {
     if (last_) last_->release(st);
@@ -356,6 +383,7 @@ struct akv_ctx {
   akv::DevErr* dev_err = nullptr;
   Uploader up;
   Staging st_k, st_v, st_q, st_o, st_lse;
+  cudaStream_t copy_st = nullptr;  // host-to-device copies of inputs and descriptor tables
   Staging partial;         // split-KV partial results (device only)
   int n_sm = 148;          // SMs of the device, for split decisions
   int mla_slots = 148;     // MLA kernel CTAs resident at once (CTA pairs x 2)
@@ -487,11 +515,13 @@ struct akv_ctx {
 
   // ------------------------------------------------------------- device IO
   // Returns a device pointer holding `bytes` of `src` (device: as is; host: staged).
+  // Host inputs are read on the context's copy stream when the call is made
+  // (so they overlap the kernels of earlier calls still running on `st`).
   const void* device_input(const void* src, size_t bytes, Staging& s, cudaStream_t st) {
     if (is_device_ptr(src)) return src;
     s.want_host = false;
     s.acquire(bytes);
-    cuda_check(cudaMemcpyAsync(s.dev, src, bytes, cudaMemcpyHostToDevice, st), "host input copy");
+    s.copy_in(src, bytes, st, copy_st, "host input copy");
     return s.dev;
   }
 
@@ -1867,6 +1897,8 @@ struct akv_ctx {
     cuda_check(cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, device), "cudaDeviceGetAttribute");
     cuda_check(cudaMalloc(&dev_err, sizeof(akv::DevErr)), "cudaMalloc");
     cuda_check(cudaMemset(dev_err, 0, sizeof(akv::DevErr)), "cudaMemset");
+    cuda_check(cudaStreamCreateWithFlags(&copy_st, cudaStreamNonBlocking), "cudaStreamCreate");
+    up.copy_stream = copy_st;
     if (c.d_rot % 64 == 0 && c.d_v % 64 == 0) {
       const uint64_t lp = uint64_t(c.n_layers) * c.n_pages;
       const uint32_t box[4] = {64, uint32_t(c.page_size), 1, 1};
@@ -1908,6 +1940,7 @@ struct akv_ctx {
       cudaEventDestroy(t.b);
     }
     for (auto e : ev_pool) cudaEventDestroy(e);
+    if (copy_st) cudaStreamDestroy(copy_st);
     if (dev_err) cudaFree(dev_err);
   }
 };

@@ -32,9 +32,14 @@
  *     slots it does not need, and a NaN there would leak through 0 * NaN.
  *   - Data pointers passed to append / splice / attend may be device memory
  *     or host memory (pinned for asynchronous copies).  Host inputs are copied
- *     into library-owned device staging memory on the given stream; a host
- *     output is copied back on the stream, so synchronise the stream before
- *     reading it.
+ *     into library-owned device staging memory on the context's own copy
+ *     stream, which does not wait for earlier work on the given stream (the
+ *     copy overlaps the kernels of earlier calls); the given stream waits for
+ *     the copy before the kernel that reads it.  So a host input must hold its
+ *     final contents when the call is made, and stay unchanged until the given
+ *     stream has passed the call.  A host output is copied back on the given
+ *     stream, so synchronise it before reading the output.  (While the given
+ *     stream is being captured into a graph, inputs are copied on it.)
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  All device work of a call is enqueued on it asynchronously;
  *     host bookkeeping changes at call time.  Use one stream per context, or

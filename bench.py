@@ -377,9 +377,10 @@ def mass_pass(t, reps=5):
     med = sorted(kern_ms)[len(kern_ms) // 2]
     _, bf16_peak, _, _ = load_peaks()
     tf = flops / (med * 1e-3) / 1e12
+    tr = measured_traffic("attn_mass")
     return {"ms": med, "call_ms": sorted(call_ms)[len(call_ms) // 2], "mass_sum": total_mass,
             "expected_sum": t.nq * s.n_q_heads, "TFLOP/s": tf, "flops_per_launch": flops,
-            "frac_of_bf16_dense": tf / bf16_peak}
+            "frac_of_bf16_dense": tf / bf16_peak, "traffic": tr["dram_bytes_per_launch"] if tr else None}
 
 
 def mla_turns(concurrencies=(1, 4, 8, 16), steps=3, warmup=1):

@@ -265,7 +265,9 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
   int2 run_cur = make_int2(0, 0);
   if (rg.t0 * rpt + (r >> page_shift) < seg.n_runs) run_cur = run_le[2 * (rg.t0 * rpt + (r >> page_shift)) + 1];
   bool ok = true;
-  int e_prev = INT_MAX;
+  // token of key column r of the previous tile (-1: no entry); its index is loaded a tile
+  // before the column sums need it, off the path that releases the next P tile
+  int tok_prev = -1;
   // column sums of tile jj come back in D_t: lane l of quadrant q reads column 32q + l
   auto take_sums = [&](int jj) {
     ok = ptx::mbar_wait(bar(kMD0 + t), jj & 1, abort_flag, kWaitLimitNs);
@@ -276,7 +278,7 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
     float mine = 0.f;
 #pragma unroll
     for (int k = 0; k < 32; ++k) mine = lane == k ? __uint_as_float(v[k]) : mine;
-    if (e_prev != INT_MAX) atomicAdd(p.mass + seg.mass_off + p.ent_tok[seg.ent_off + e_prev], mine);
+    if (tok_prev >= 0) atomicAdd(p.mass + seg.mass_off + tok_prev, mine);
     return true;
   };
   // probabilities of 64 scores, packed as bf16 pairs
@@ -312,9 +314,11 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
       break;
     }
     int e = INT_MAX;  // entry index of key column r of tile j
+    int tok = -1;     // its logical token
     {
       const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
       if (sl_own >= lo && sl_own < hi) e = run_cur.y + (sl_own - lo);
+      if (e != INT_MAX) tok = __ldg(p.ent_tok + seg.ent_off + e);
       colE[r] = e;
       const int ri = (rg.t0 + j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
@@ -342,7 +346,7 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
     store(1, pk1);
     ptx::fence_proxy_async_smem();
     ptx::mbar_arrive(bar(kMPFull0 + t));
-    e_prev = e;
+    tok_prev = tok;
   }
   if (ok && n >= 1) ok = take_sums(n - 1);
   if (!ok) {

@@ -6,7 +6,10 @@
 * the Llama-3.1-70B-shaped 128K cache, 80 layers (~54 GB of pools): the
   in-place full-cache sweep with shifts up to +-64K, sampled rows; attention
   of four of the 32 branch segments on layers 0 and 79;
-* 16 DeepSeek-V2-Lite MLA sessions, 27 layers: the splice's K_pe rotation.
+* 16 DeepSeek-V2-Lite MLA sessions, 27 layers: the splice's K_pe rotation;
+* the post-drop 32K turn's attention-mass launch as the benchmark runs it
+  (2,048 queries x 32 heads over 24,479 visible entries, automatic K-tile
+  ranges): every token against the float64 oracle.
 Bars as in the other GPU tests (rotated keys: one bf16 ulp plus the float32
 rotation allowance, >= 99.9% bit-identical; attention: 2e-2 max-abs)."""
 import gc
@@ -80,3 +83,8 @@ def test_mla_16_sessions_full_size_sampled():
     for layer in (0, w.shape.n_layers - 1):
         c.check_attention(layer, 16, rng, segments=[0, 7, 15])
     release(c)
+
+
+def test_mass_32k_turn_full_size():
+    from test_gpu_mass import mass_case
+    mass_case(synth.llama8b_32k(seed=0, fork=True))

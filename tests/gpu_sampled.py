@@ -32,7 +32,9 @@ class SampledCase:
         self.names = {}
         self.origin = {}  # name -> list of (key, row, position at append)
 
-    def run(self):
+    def run(self, flush=True):
+        """Replay the workload on the engine and the oracle; with `flush` the segments' sequences
+        are flushed at the end (else their shifts stay pending)."""
         w, m = self.w, self.model
         for op in w.ops:
             runner.run_ops(self.eng, w, kv_source=self.src, ops=[op], names=self.names, stream=self.stream)
@@ -60,12 +62,27 @@ class SampledCase:
                                      + self.origin[name][op[3]:])
             elif kind == "flush":
                 m.flush([self.names[name]])
-        ids = sorted({self.names[g["seq"]] for g in w.segments})
-        m.flush(ids)
-        for i in ids:
-            self.eng.flush(i, stream=self.stream)
+        if flush:
+            ids = sorted({self.names[g["seq"]] for g in w.segments})
+            m.flush(ids)
+            for i in ids:
+                self.eng.flush(i, stream=self.stream)
         torch.cuda.synchronize()
         assert self.eng.check_device_error(self.stream) == 0
+
+    def compact(self, name):
+        """Compact `name` on the engine and in the oracle (pending shifts fused into the copy); the
+        dropped tokens leave the logical sequence, so the sample origins follow.  Returns the
+        oracle's copy list."""
+        sid = self.names[name]
+        vis = [t.vis for t in self.model.seqs[sid]]
+        copies = self.model.compact(sid)
+        self.eng.compact(sid, stream=self.stream)
+        torch.cuda.synchronize()
+        assert self.eng.check_device_error(self.stream) == 0
+        assert self.eng.fragmentation(sid) == self.model.fragmentation(sid)
+        self.origin[name] = [o for o, v in zip(self.origin[name], vis) if v]
+        return copies
 
     # ------------------------------------------------------------- inputs
     def inputs(self, refs, layer=None):
@@ -143,6 +160,22 @@ class SampledCase:
         if n_all:
             assert n_eq / n_all >= 0.999, n_eq / n_all
         return n_rot, worst
+
+    def check_values(self, n_samples, rng):
+        """Sampled tokens of every live sequence: GPU V rows (all layers, heads) bit-identical to
+        the appended values."""
+        names = [n for n in self.origin if self.names[n] in self.model.seqs]
+        n_checked = 0
+        for name in names:
+            toks = self.model.seqs[self.names[name]]
+            idxs = sorted(set(int(x) for x in rng.integers(0, len(toks), size=max(1, n_samples // len(names)))))
+            _, _, want, _ = self.expected(name, idxs)
+            vp = torch.tensor([toks[i].vp for i in idxs], device="cuda")
+            sl = torch.tensor([toks[i].slot for i in idxs], device="cuda")
+            got = self.pools[1][:, vp, :, sl, :].double().cpu().numpy()  # [n][L][H][d]
+            assert np.array_equal(got, want), name
+            n_checked += len(idxs)
+        return n_checked
 
     def check_attention(self, layer, rows_per_segment, rng, segments=None):
         """Sampled query rows of the given segments: GPU output vs float64 oracle over the full visible list."""

@@ -7,6 +7,10 @@
   in-place full-cache sweep with shifts up to +-64K, sampled rows; attention
   of four of the 32 branch segments on layers 0 and 79;
 * 16 DeepSeek-V2-Lite MLA sessions, 27 layers: the splice's K_pe rotation;
+* the benchmark's compaction: the post-drop branch of the 32K trajectory over
+  32 layers, shifts still pending (fused into the copy): sampled K rows
+  against the oracle's rotation, sampled V rows bit-identical, attention over
+  the compacted branch on layers 0 and 31;
 * the post-drop 32K turn's attention-mass launch as the benchmark runs it
   (2,048 queries x 32 heads over 24,479 visible entries, automatic K-tile
   ranges): every token against the float64 oracle.
@@ -88,3 +92,25 @@ def test_mla_16_sessions_full_size_sampled():
 def test_mass_32k_turn_full_size():
     from test_gpu_mass import mass_case
     mass_case(synth.llama8b_32k(seed=0, fork=True))
+
+
+def test_compaction_32k_branch_full_size_sampled():
+    from gpu_sampled import SampledCase
+    from test_gpu_compact import remap_segments
+    w = synth.llama8b_32k(fork=True, n_layers=32)
+    w.n_pages += 2 * (32768 // 16)
+    c = SampledCase(w)
+    c.run(flush=False)
+    sid = c.names["F"]
+    assert c.model.fragmentation(sid) > 0.2
+    states = {sid: c.model.state(sid)}
+    copies = c.compact("F")
+    assert sum(1 for cp in copies if cp[6]) > 1000, "no pending shift fused into the copy"
+    rng = np.random.default_rng(5)
+    n_rot, _ = c.check_repos(4096, rng)
+    assert n_rot > 500
+    assert c.check_values(2048, rng) > 1000
+    w.segments = remap_segments(w, states, c.names)
+    for layer in (0, w.shape.n_layers - 1):
+        c.check_attention(layer, 12, rng)
+    release(c)

@@ -78,7 +78,10 @@ def max_over_ranks(values, device):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """nvidia-smi clock / throttle samples (every 20 ms) over the loaded stretch that holds the timed
+    region.  A reader thread collects the lines as they come; start() waits until nvidia-smi is up,
+    mark() is called just before the warm-up and stop() after the end-to-end loop, and the summary
+    keeps the samples taken in between (the device-timed steps alone last only milliseconds)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -87,31 +90,49 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.thread = None
+        self.lines = []
+        self.first = 0
 
-    def __enter__(self):
+    def start(self, wait_s=3.0):
+        import threading
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t_end = time.time() + wait_s
+        while not self.lines and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
-    def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+    def _read(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.lines.append(line)
+
+    def mark(self):
+        self.first = len(self.lines)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.thread.join(timeout=5)
 
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in self.lines[self.first:]:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -124,7 +145,7 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "warm-up through the end-to-end loop, every 20 ms"}
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -465,6 +486,8 @@ def gpu_arm(args, rank, world):
             tdist.barrier()
         torch.cuda.synchronize()
 
+    clk = ClockSampler(dev).start()
+    clk.mark()
     for _ in range(args.warmup):
         t.step()
         t.flush_l2()
@@ -472,13 +495,12 @@ def gpu_arm(args, rank, world):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     t.eng.profile_enable(True)
-    with ClockSampler(dev) as clk:
-        for i in range(args.steps):
-            ev[i][0].record(t.stream)
-            t.step()
-            ev[i][1].record(t.stream)
-            t.flush_l2()
-        barrier()
+    for i in range(args.steps):
+        ev[i][0].record(t.stream)
+        t.step()
+        ev[i][1].record(t.stream)
+        t.flush_l2()
+    barrier()
     stats = t.eng.profile_read()
     t.eng.profile_enable(False)
     assert t.eng.check_device_error(t.stream) == 0
@@ -510,6 +532,7 @@ def gpu_arm(args, rank, world):
         torch.cuda.synchronize()
         lat_ms.append((time.perf_counter() - t1) * 1e3)
     lat_ms.sort()
+    clk.stop()
 
     if dist:
         total_ms, e2e_total = max_over_ranks([total_ms, e2e_total], "cuda")

@@ -865,6 +865,20 @@ struct akv_ctx {
     if (!runs.empty()) last_runs.swap(flat);
     if (meta || runs.empty()) return;
 
+    // A page shared by two flushed sequences is copied out by the first
+    // (copy-on-write) and, its reference gone, rotated in place by the second.
+    // Runs execute concurrently within a launch, so when some page is both a
+    // copy source and an in-place target the copies go in a first launch and
+    // the in-place runs in a second (the bookkeeping applies them in order).
+    std::stable_partition(runs.begin(), runs.end(), [](const akv::RunDesc& r) { return r.src != r.dst; });
+    int n_copy = 0;
+    while (n_copy < int(runs.size()) && runs[n_copy].src != runs[n_copy].dst) ++n_copy;
+    bool conflict = false;
+    if (n_copy > 0 && n_copy < int(runs.size())) {
+      mk.next();
+      for (int i = 0; i < n_copy; ++i) mk.test_set(runs[i].src);
+      for (size_t i = n_copy; i < runs.size() && !conflict; ++i) conflict = mk.test(runs[i].dst);
+    }
     std::vector<float2> cs = angle_table(deltas);
     void* druns = nullptr;
     void* dcs = nullptr;
@@ -874,11 +888,19 @@ struct akv_ctx {
     for (auto& r : runs) rows += (r.lohi >> 16) - (r.lohi & 0xffff);
     Timed t;
     const double bytes = 2.0 * double(rows) * cfg.n_layers * cfg.n_kv_heads * cfg.d_rot * 2.0;
-    begin_timed(kRepos, bytes, 0.0, st, t);
-    cuda_check(akv::launch_repos_rotate(kpool, static_cast<akv::RunDesc*>(druns), static_cast<float2*>(dcs),
-                                        int(runs.size()), cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.page_size,
-                                        cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, st),
-               "repos_rotate launch");
+    begin_timed(kRepos, bytes, 0.0, st, t, conflict ? 2 : 1);
+    auto launch = [&](int first, int n) {
+      cuda_check(akv::launch_repos_rotate(kpool, static_cast<akv::RunDesc*>(druns) + first, static_cast<float2*>(dcs),
+                                          n, cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.page_size, cfg.n_pages,
+                                          cfg.rope_layout == AKV_ROPE_HALF, st),
+                 "repos_rotate launch");
+    };
+    if (conflict) {
+      launch(0, n_copy);
+      launch(n_copy, int(runs.size()) - n_copy);
+    } else {
+      launch(0, int(runs.size()));
+    }
     end_timed(t, st);
     up.done(st);
   }

@@ -21,6 +21,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <algorithm>
 #include <vector>
 
 #include "../../include/akv.h"
@@ -89,6 +90,20 @@ extern "C" AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_l
     }
     desc[size_t(r)] = akv::RunDesc{src, dst, lo | (hi << 16), di};
   }
+  // Runs of one launch execute concurrently: when a page is both the source
+  // of a copy (src != dst) and rotated in place by another run (as a flush of
+  // two sequences sharing it lists them), the copies run in a first launch.
+  std::stable_partition(desc.begin(), desc.end(), [](const akv::RunDesc& r) { return r.src != r.dst; });
+  int32_t n_copy = 0;
+  while (n_copy < n_runs && desc[size_t(n_copy)].src != desc[size_t(n_copy)].dst) ++n_copy;
+  bool conflict = false;
+  if (n_copy > 0 && n_copy < n_runs) {
+    std::vector<int32_t> srcs;
+    for (int32_t r = 0; r < n_copy; ++r) srcs.push_back(desc[size_t(r)].src);
+    std::sort(srcs.begin(), srcs.end());
+    for (int32_t r = n_copy; r < n_runs && !conflict; ++r)
+      conflict = std::binary_search(srcs.begin(), srcs.end(), desc[size_t(r)].dst);
+  }
   const int half = d_rot / 2;
   const size_t runs_bytes = (desc.size() * sizeof(akv::RunDesc) + 255) & ~size_t(255);
   const size_t cs_bytes = deltas.size() * half * sizeof(float2);
@@ -113,8 +128,12 @@ extern "C" AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_l
     cudaGetLastError();
     return AKV_ERR_CUDA;
   }
-  if (akv::launch_repos_rotate(k_pool, dev_runs, dev_cs, n_runs, n_layers, n_kv_heads, d_rot, page_size, n_pages,
+  const int32_t first_n = conflict ? n_copy : n_runs;
+  if (akv::launch_repos_rotate(k_pool, dev_runs, dev_cs, first_n, n_layers, n_kv_heads, d_rot, page_size, n_pages,
                                rope_layout == AKV_ROPE_HALF, st) != cudaSuccess)
+    return AKV_ERR_CUDA;
+  if (conflict && akv::launch_repos_rotate(k_pool, dev_runs + n_copy, dev_cs, n_runs - n_copy, n_layers, n_kv_heads,
+                                           d_rot, page_size, n_pages, rope_layout == AKV_ROPE_HALF, st) != cudaSuccess)
     return AKV_ERR_CUDA;
   return AKV_OK;
 }

@@ -205,3 +205,37 @@ def test_compaction_matches_oracle(name, make):
         apply_both(eng, model, "compact", (sid,))
         assert_same_state(eng, model, ne, no)
         assert eng.fragmentation(sid) == model.fragmentation(sid)
+
+
+def shared_prefix_both_shifted(n=4096, q=16):
+    """Two branches sharing an n-token prefix, every prefix token shifted on both (by different
+    amounts), one segment each: attend flushes both in one call."""
+    import dataclasses
+    w = synth.tiny()
+    w.shape = dataclasses.replace(w.shape, n_q_heads=8, n_kv_heads=2)
+    w.ops = [("alloc", "A"), ("append", "A", n, "ctx"), ("fork", "B", "A", n),
+             ("repos", "A", 0, n, 1000), ("repos", "B", 0, n, -2000),
+             ("append", "A", q, "newA"), ("append", "B", q, "newB")]
+    w.segments = [dict(seq="A", kv_end=n + q, q_len=q, hide=[], q_row0=0),
+                  dict(seq="B", kv_end=n + q, q_len=q, hide=[], q_row0=q)]
+    w.n_pages = 3 * (n // w.shape.page_size) + 16
+    return w
+
+
+def test_one_flush_copies_a_page_out_and_rotates_it_in_place():
+    # The first sharer copies each shared page out (copy-on-write); the second, then its only
+    # holder, rotates it in place.  The two kinds of run must not share a launch (the GPU runs a
+    # launch's runs concurrently), which the engine orders; here: the run list holds both kinds.
+    w = shared_prefix_both_shifted()
+    eng = engine_for(w)
+    names = runner.run_ops(eng, w)
+    nq = sum(g["q_len"] for g in w.segments)
+    eng.attend(0, runner.engine_segments(w, names), None, nq, None)
+    runs = eng.last_flush_runs()
+    model, names_o = oracle_model(w), {}
+    oracle_run_ops(model, w, names=names_o)
+    want = model.flush(sorted({names_o[g["seq"]] for g in w.segments}))
+    assert np.array_equal(np.asarray(runs), np.asarray(want, np.int32).reshape(-1, 5))
+    copied = {int(r[0]) for r in runs if r[0] != r[1]}
+    in_place = {int(r[1]) for r in runs if r[0] == r[1]}
+    assert len(copied & in_place) == w.ops[1][2] // w.shape.page_size

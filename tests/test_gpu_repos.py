@@ -146,3 +146,26 @@ def test_f32_debug_mode_meets_rotated_key_tolerance(layout):
     assert err.max() < 1e-5          # float32 rotation: far inside the tolerance
     kg, _ = c.gpu_pools()
     assert np.array_equal(kg, c.kp)  # the debug mode only reads the pool
+
+
+def test_one_flush_of_two_sharers_copies_before_rotating_in_place():
+    # attend flushes both branches in one call: each shared page is copied out (copy-on-write,
+    # rotated for A) and then rotated in place for B, its last holder; the copies must read the
+    # page before the in-place rotation writes it
+    from gpu_case import Case
+    from test_bookkeeping_parity import shared_prefix_both_shifted
+    from test_gpu_attention import ATOL
+    w = shared_prefix_both_shifted()
+    c = Case(w)
+    c.run_ops()
+    runs = c.flush_segments(engine=False)  # the oracle's flush; the engine's runs inside attend
+    assert {r[0] for r in runs if r[0] != r[1]} & {r[1] for r in runs if r[0] == r[1]}
+    q32, o, lse = c.attend_gpu()
+    kg, vg = c.gpu_pools()
+    compare_rotated(kg, c.kp, rotated_mask(c, c.flush_runs), c.kterm)
+    assert np.array_equal(vg, c.vp)
+    for i, g in enumerate(w.segments):
+        rows = np.arange(g["q_len"])
+        want_o, want_lse = c.attend_oracle(q32, i, rows)
+        assert np.abs(o[g["q_row0"] + rows] - want_o).max() <= ATOL
+        assert np.abs(lse[g["q_row0"] + rows] - want_lse).max() <= ATOL

@@ -21,6 +21,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <unordered_map>
 #include <algorithm>
 #include <vector>
 
@@ -70,44 +71,86 @@ extern "C" AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_l
   if (reinterpret_cast<uintptr_t>(k_pool) % 16) return AKV_ERR_ARG;
   if (n_runs == 0) return AKV_OK;
 
-  // Run descriptors and the distinct shifts, checked against the pool.
+  const int half = d_rot / 2;
+  // A list whose descriptors alone exceed the array is refused before any work.
+  const size_t runs_bytes = (size_t(n_runs) * sizeof(akv::RunDesc) + 255) & ~size_t(255);
+  if (runs_bytes > kScratchBytes) return AKV_ERR_RANGE;
+
+  // The run list and the table are copied from temporary host memory, which a
+  // graph node would read only at replay, after this call has freed it.
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return AKV_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return AKV_ERR_ARG;
+
+  // Run descriptors and the distinct shifts, checked against the pool.  The
+  // table grows with the shifts; a list that cannot fit stops at the shift
+  // that overflows the array.
   std::vector<akv::RunDesc> desc(static_cast<size_t>(n_runs));
   std::vector<int32_t> deltas;
+  std::unordered_map<int32_t, int32_t> delta_index;
   for (int32_t r = 0; r < n_runs; ++r) {
     const int32_t src = runs[5 * r], dst = runs[5 * r + 1], lo = runs[5 * r + 2], hi = runs[5 * r + 3];
     const int32_t d = runs[5 * r + 4];
     if (src < 0 || src >= n_pages || dst < 0 || dst >= n_pages || lo < 0 || lo >= hi || hi > page_size)
       return AKV_ERR_RANGE;
-    int32_t di = -1;
-    for (size_t k = 0; k < deltas.size(); ++k)
-      if (deltas[k] == d) {
-        di = int32_t(k);
-        break;
-      }
-    if (di < 0) {
-      di = int32_t(deltas.size());
+    auto it = delta_index.find(d);
+    if (it == delta_index.end()) {
+      if (runs_bytes + (deltas.size() + 1) * half * sizeof(float2) > kScratchBytes) return AKV_ERR_RANGE;
+      it = delta_index.emplace(d, int32_t(deltas.size())).first;
       deltas.push_back(d);
     }
-    desc[size_t(r)] = akv::RunDesc{src, dst, lo | (hi << 16), di};
+    desc[size_t(r)] = akv::RunDesc{src, dst, lo | (hi << 16), it->second};
   }
-  // Runs of one launch execute concurrently: when a page is both the source
-  // of a copy (src != dst) and rotated in place by another run (as a flush of
-  // two sequences sharing it lists them), the copies run in a first launch.
+
+  // Runs of one launch execute concurrently, so the rows they write must be
+  // disjoint: no two runs may write the same (page, row), and a copy (src !=
+  // dst) may not read rows another copy writes.  The one overlap allowed is
+  // the one a flush of two sequences sharing a page produces: a copy reading
+  // rows that an in-place run (src == dst) rotates.  Such copies run in a
+  // first launch, the in-place runs in a second.  Rows of a page are at most
+  // 128, so each page keeps two 64-bit row masks.
+  struct Rows {
+    uint64_t w[2] = {0, 0};    // rows written by any run
+    uint64_t cw[2] = {0, 0};   // rows written by copies
+    uint64_t ip[2] = {0, 0};   // rows rotated in place
+  };
+  auto mask_of = [](int lo, int hi, uint64_t m[2]) {
+    for (int k = 0; k < 2; ++k) {
+      const int a = std::max(lo, 64 * k), b = std::min(hi, 64 * k + 64);
+      m[k] = a < b ? ((b - a == 64 ? ~uint64_t(0) : ((uint64_t(1) << (b - a)) - 1)) << (a - 64 * k)) : 0;
+    }
+  };
+  std::unordered_map<int32_t, Rows> pages;
+  pages.reserve(size_t(n_runs) * 2);
+  for (const akv::RunDesc& r : desc) {
+    uint64_t m[2];
+    mask_of(r.lohi & 0xffff, r.lohi >> 16, m);
+    Rows& p = pages[r.dst];
+    if ((p.w[0] & m[0]) | (p.w[1] & m[1])) return AKV_ERR_ARG;  // two runs write one row
+    p.w[0] |= m[0];
+    p.w[1] |= m[1];
+    uint64_t* kind = r.src != r.dst ? p.cw : p.ip;
+    kind[0] |= m[0];
+    kind[1] |= m[1];
+  }
+  bool conflict = false;
+  for (const akv::RunDesc& r : desc) {
+    if (r.src == r.dst) continue;
+    auto it = pages.find(r.src);
+    if (it == pages.end()) continue;
+    uint64_t m[2];
+    mask_of(r.lohi & 0xffff, r.lohi >> 16, m);
+    if ((it->second.cw[0] & m[0]) | (it->second.cw[1] & m[1])) return AKV_ERR_ARG;  // reads another copy's rows
+    if ((it->second.ip[0] & m[0]) | (it->second.ip[1] & m[1])) conflict = true;
+  }
   std::stable_partition(desc.begin(), desc.end(), [](const akv::RunDesc& r) { return r.src != r.dst; });
   int32_t n_copy = 0;
   while (n_copy < n_runs && desc[size_t(n_copy)].src != desc[size_t(n_copy)].dst) ++n_copy;
-  bool conflict = false;
-  if (n_copy > 0 && n_copy < n_runs) {
-    std::vector<int32_t> srcs;
-    for (int32_t r = 0; r < n_copy; ++r) srcs.push_back(desc[size_t(r)].src);
-    std::sort(srcs.begin(), srcs.end());
-    for (int32_t r = n_copy; r < n_runs && !conflict; ++r)
-      conflict = std::binary_search(srcs.begin(), srcs.end(), desc[size_t(r)].dst);
-  }
-  const int half = d_rot / 2;
-  const size_t runs_bytes = (desc.size() * sizeof(akv::RunDesc) + 255) & ~size_t(255);
   const size_t cs_bytes = deltas.size() * half * sizeof(float2);
-  if (runs_bytes + cs_bytes > kScratchBytes) return AKV_ERR_RANGE;  // beyond the fixed scratch size
 
   // (cos, sin)(delta * theta_j), evaluated in float64, stored as float32.
   std::vector<float2> cs(deltas.size() * half);
@@ -119,7 +162,6 @@ extern "C" AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_l
 
   void* base = nullptr;
   if (akv_status s = scratch_address(&base); s != AKV_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto* dev_runs = static_cast<akv::RunDesc*>(base);
   auto* dev_cs = reinterpret_cast<float2*>(static_cast<unsigned char*>(base) + runs_bytes);
   if (cudaMemcpyAsync(dev_runs, desc.data(), desc.size() * sizeof(akv::RunDesc), cudaMemcpyHostToDevice, st) !=

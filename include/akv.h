@@ -217,16 +217,25 @@ AKV_API akv_status akv_repos(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, in
 AKV_API akv_status akv_splice(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int64_t n_stub,
                       const void* k_stub, const void* v_stub, const int32_t* pos, void* stream);
 
-/* Materialise pending shifts (the repos_rotate kernel): every visible token
- * with a pending shift is rotated once, K'[i] = R(delta_i) K[i], in fp32 with
- * one rounding to bf16.  A K page referenced by this sequence only is rotated
- * in place; a shared one is first copied (copy-on-write of the K page only,
- * [AKV-notes] section 3 "Cache Management").  seq = -1 flushes every live
- * sequence in increasing id order. */
+/* Materialise pending shifts (the repos_rotate kernel; [AKV-blog] section 2
+ * "The Repos Primitive and Rotary Position Embeddings": a retained key moves
+ * from position m to m + delta by one more rotation, K' = R(delta) K, since
+ * R(a) R(b) = R(a + b); [Leyline] "Method": several directives collapse into
+ * one composed shift per token, and under MLA only K_pe rotates).  Every
+ * visible token with a pending shift is rotated once, K'[i] = R(delta_i) K[i],
+ * in fp32 with one rounding to bf16.  A K page referenced by this sequence
+ * only is rotated in place; a shared one is first copied (copy-on-write of
+ * the K page only, [AKV-notes] section 3 "Cache Management").  seq = -1
+ * flushes every live sequence in increasing id order. */
 AKV_API akv_status akv_flush(akv_ctx* ctx, int32_t seq, void* stream);
 
-/* Segment-batch attention for one layer (the segment_batch_attn kernel):
- * flushes the segments' sequences first, then one launch covers every segment.
+/* Segment-batch attention for one layer (the segment_batch_attn kernel;
+ * [AKV-notes] section 3 "Segment-Batch Attention": the incoming queries are
+ * split into segments by the history they see, and each segment runs
+ * ordinary causal attention over the KV pages it selects, with no dense
+ * custom mask; [AKV-blog] section 4 "Segment-Batch Attention Kernel
+ * Architecture": heterogeneous segments share one launch).  Flushes the
+ * segments' sequences first, then one launch covers every segment.
  *   q:   bf16 [n_q_rows][n_q_heads][d_qk]  (d_qk = d_rot under GQA; d_v + d_rot
  *        under MLA, laid out [latent part | rope part]); already RoPE'd.
  *   o:   bf16 [n_q_rows][n_q_heads][d_v]; rows outside the segments are not written.
@@ -342,14 +351,23 @@ AKV_API akv_status akv_debug_rotate_f32(akv_ctx* ctx, const int32_t* runs, int32
  *           head, rotated by delta and stored to the same rows of page dst
  *           (the run format of akv_last_flush_runs).
  *   d_rot: 16, 32, 64, 128 or 256; page_size: 16, 32, 64 or 128.
+ * Runs of one call execute concurrently, so they must write disjoint rows:
+ * two runs writing the same (page, row), or a copy (src != dst) reading rows
+ * that another copy writes, give AKV_ERR_ARG.  A copy may read rows that an
+ * in-place run (src == dst) rotates, as a flush of two sequences sharing a
+ * page lists them: those copies are made in a first launch, before the
+ * in-place rotations.  Run lists from akv_last_flush_runs always qualify.
  * Returns AKV_ERR_RANGE when a run is outside the pool or when the runs plus
  * the table (16 B per run, rounded up to 256 B, plus 4 * d_rot B per distinct
- * delta) exceed 256 KiB, AKV_ERR_ARG for a bad shape.  Every call overwrites
- * the part of the array it uses, so nothing needs clearing between calls, but
- * calls that overlap on the GPU (e.g. unordered streams) race on the array;
- * calls on one stream are ordered.  The first call on a device, with that
- * device current, looks up the array's device address (cudaGetSymbolAddress)
- * and caches it: make that first call before any stream capture. */
+ * delta) exceed 256 KiB, checked before any device work; AKV_ERR_ARG for a bad
+ * shape, for overlapping runs, and while `stream` is being captured into a
+ * graph (the run list and the table are copied from temporary host memory
+ * during the call).  Every call overwrites the part of the array it uses, so
+ * nothing needs clearing between calls, but calls that overlap on the GPU
+ * (e.g. unordered streams) race on the array; calls on one stream are
+ * ordered.  The first call on a device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it: make that
+ * first call before any stream capture. */
 AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_layers, int32_t n_kv_heads,
                                             int32_t page_size, int32_t n_pages, int32_t d_rot,
                                             int32_t rope_layout, double rope_base, const int32_t* runs,
@@ -385,9 +403,10 @@ AKV_API akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_
 AKV_API akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code);
 
 /* Split-KV control for akv_attend and akv_attention_mass.  0 (default): the
- * engine cuts long work items into up to 8 chunks of KV tiles when that
- * fills the GPU's waves of SMs better; akv_attend merges the chunks' partial
- * softmax results in a combine kernel, akv_attention_mass needs no merge (its
+ * engine cuts long work items into chunks of KV tiles when that fills the
+ * GPU's waves of SMs better; in akv_attend the CTA that finishes an item's
+ * last chunk merges the chunks' partial softmax results (running maximum and
+ * sum rescaled to a common maximum), akv_attention_mass needs no merge (its
  * lse is final; chunks add into the same outputs).  1..8: use exactly that
  * many chunks per item (1 = never split). */
 AKV_API akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split);

@@ -23,12 +23,16 @@ def masked_attention(q, k, v, visible, scale):
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
-    s = scale * (q @ k.T)
-    s = np.where(visible, s, -np.inf)
+    # The score matrix is updated in place (same operations, same order) to
+    # avoid fresh [n, N] temporaries, whose first touch dominates at 100K+ keys.
+    s = q @ k.T
+    s *= scale
+    s[~np.asarray(visible, bool)] = -np.inf
     m = s.max(axis=1, keepdims=True)
     empty = ~np.isfinite(m[:, 0])
     m = np.where(np.isfinite(m), m, 0.0)
-    p = np.exp(s - m)
+    np.subtract(s, m, out=s)
+    p = np.exp(s, out=s)
     l = p.sum(axis=1)
     o = (p @ v) / np.where(empty, 1.0, l)[:, None]
     o[empty] = 0.0

@@ -21,11 +21,16 @@ from . import attention, bf16, rope
 def repos_runs(kpool, runs, base, layout="interleaved", out=None):
     """Apply a flush run list [(src, dst, lo, hi, delta)] to a copy of kpool.
 
-    Every run reads rows [lo, hi) of page src in every layer and head of the
-    pool as it was before the flush, rotates them by delta in float64, rounds
-    to bfloat16 and writes them to the same rows of page dst.  ``out=kpool``
-    updates the pool in place: no run reads a row another run writes (a
-    destination page is either the run's own source or a fresh copy).
+    Every run reads rows [lo, hi) of page src in every layer and head, rotates
+    them by delta in float64, rounds to bfloat16 and writes them to the same
+    rows of page dst.  Runs are applied one after another in list order.
+    Without ``out`` every run reads the pool as it was before the flush.  With
+    ``out=kpool`` the pool is updated in place and a run reads what earlier
+    runs left: a flush of two sequences sharing a page lists the copy of that
+    page (copy-on-write for the first sharer) before the in-place rotation of
+    the same page (for the last sharer), so the copy reads the unrotated rows
+    and the result equals the out-of-place one.  No two runs of a flush write
+    the same row.
     """
     if out is None:
         out = np.array(kpool, dtype=np.float64, copy=True)

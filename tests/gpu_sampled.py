@@ -177,8 +177,26 @@ class SampledCase:
             n_checked += len(idxs)
         return n_checked
 
+    def sample_rows(self, q_len, n_random, rng):
+        """Query rows to check in one segment: the first and last row of every 128-row query tile
+        (a tile holds 128 / G tokens of one kv group, G = query heads per kv head), so every
+        work item of the launch over the segment -- split across CTAs or not -- has checked
+        rows, plus n_random further rows drawn without replacement."""
+        s = self.w.shape
+        per_tile = 128 // (s.n_q_heads // s.n_kv_heads)
+        starts = np.arange(0, q_len, per_tile)
+        edge = np.concatenate([starts, np.minimum(starts + per_tile, q_len) - 1])
+        rest = np.setdiff1d(np.arange(q_len), edge)
+        pick = rng.choice(rest, size=min(n_random, rest.size), replace=False)
+        return np.unique(np.concatenate([edge, pick]))
+
     def check_attention(self, layer, rows_per_segment, rng, segments=None):
-        """Sampled query rows of the given segments: GPU output vs float64 oracle over the full visible list."""
+        """Sampled query rows of the given segments (see sample_rows): GPU output vs the float64
+        oracle, every row against the segment's full visible list.  The oracle is evaluated one
+        query head at a time in a thread pool (numpy releases the GIL in its kernels)."""
+        import os
+        from concurrent.futures import ThreadPoolExecutor
+        from oracle import attention
         s, w = self.w.shape, self.w
         q32 = synth.q_array(w, layer)
         nq = q32.shape[0]
@@ -189,7 +207,9 @@ class SampledCase:
         torch.cuda.synchronize()
         assert self.eng.check_device_error(self.stream) == 0
         segs = range(len(w.segments)) if segments is None else segments
-        worst = 0.0
+        group = s.n_q_heads // s.n_kv_heads
+        n_threads = max(1, min(16, os.cpu_count() or 1))
+        worst, n_rows = 0.0, 0
         for si in segs:
             g = w.segments[si]
             name = g["seq"]
@@ -204,16 +224,24 @@ class SampledCase:
             _, K, V, _ = self.expected(name, vis, layer)   # [kv][H][d]
             if s.mla:
                 K = np.concatenate([V, K], axis=-1)
-            rows = np.unique(np.concatenate([[0, g["q_len"] - 1],
-                                             rng.choice(g["q_len"], size=min(rows_per_segment, g["q_len"]),
-                                                        replace=False)]))
+            rows = self.sample_rows(g["q_len"], rows_per_segment, rng)
             qb = bf16.round_bf16(q32[g["q_row0"]:g["q_row0"] + g["q_len"]].astype(np.float64))
-            from oracle import attention
-            want_o, want_lse = attention.segment_attention(qb, K, V, s.scale, rows=rows)
-            got_o = o[g["q_row0"] + torch.from_numpy(rows).cuda()].double().cpu().numpy()
-            got_lse = lse[g["q_row0"] + torch.from_numpy(rows).cuda()].double().cpu().numpy()
+
+            def one_head(h):
+                kv = h // group
+                return attention.segment_attention(qb[:, h:h + 1], K[:, kv:kv + 1], V[:, kv:kv + 1], s.scale,
+                                                   rows=rows)
+
+            with ThreadPoolExecutor(n_threads) as ex:
+                parts = list(ex.map(one_head, range(s.n_q_heads)))
+            want_o = np.concatenate([p[0] for p in parts], axis=1)
+            want_lse = np.concatenate([p[1] for p in parts], axis=1)
+            idx = g["q_row0"] + torch.from_numpy(rows).cuda()
+            got_o = o[idx].double().cpu().numpy()
+            got_lse = lse[idx].double().cpu().numpy()
             err = float(np.abs(got_o - want_o).max())
             worst = max(worst, err)
             assert err <= 2e-2, (si, err)
             assert np.abs(got_lse - want_lse).max() <= 2e-2
-        return worst
+            n_rows += len(rows)
+        return worst, n_rows

@@ -2,11 +2,15 @@
 
 * eight 64K-token sessions sharing a 4K prefix, 32 layers (~72 GB of pools):
   sampled rotated rows of every session and layer; attention on layers 0 and
-  31 for sampled query rows of first / middle / last segments;
+  31 for three segment classes -- a session's first segment (shortest
+  history, nothing hidden), a middle one, a session's last (longest history,
+  most hidden spans);
 * the Llama-3.1-70B-shaped 128K cache, 80 layers (~54 GB of pools): the
   in-place full-cache sweep with shifts up to +-64K, sampled rows; attention
-  of four of the 32 branch segments on layers 0 and 79;
+  on layers 0 and 79 for the branches hiding the fewest and the most spans
+  and the first and last branch;
 * 16 DeepSeek-V2-Lite MLA sessions, 27 layers: the splice's K_pe rotation;
+  attention of three sessions, every query row;
 * the benchmark's compaction: the post-drop branch of the 32K trajectory over
   32 layers, shifts still pending (fused into the copy): sampled K rows
   against the oracle's rotation, sampled V rows bit-identical, attention over
@@ -14,6 +18,10 @@
 * the post-drop 32K turn's attention-mass launch as the benchmark runs it
   (2,048 queries x 32 heads over 24,479 visible entries, automatic K-tile
   ranges): every token against the float64 oracle.
+Attention samples (tests/gpu_sampled.py): in every checked segment, at least
+256 random query rows (every row when there are fewer) plus the first and last
+row of each query tile, so each work item of the launch, split or not, is
+checked; each row against the segment's full visible KV, all query heads.
 Bars as in the other GPU tests (rotated keys: one bf16 ulp plus the float32
 rotation allowance, >= 99.9% bit-identical; attention: 2e-2 max-abs)."""
 import gc
@@ -58,8 +66,17 @@ def test_sessions_64k_full_size_sampled():
     n_rot, worst = c.check_repos(4096, rng)
     assert n_rot > 1000
     last = len(w.segments) - 1
+    by_seq = {}
+    for i, g in enumerate(w.segments):
+        by_seq.setdefault(g["seq"], []).append(i)
+    seqs = sorted(by_seq)
+    first = next(by_seq[q][0] for q in seqs if not w.segments[by_seq[q][0]]["hide"])
+    middle = by_seq[seqs[len(seqs) // 2]][len(by_seq[seqs[len(seqs) // 2]]) // 2]
+    final = max((by_seq[q][-1] for q in seqs), key=lambda i: (len(w.segments[i]["hide"]), i))
+    assert w.segments[final]["hide"]
     for layer in (0, w.shape.n_layers - 1):
-        c.check_attention(layer, 12, rng, segments=[0, last // 2, last])
+        _, n = c.check_attention(layer, 256, rng, segments=[first, middle, final])
+        assert n >= 3 * 256
     release(c)
 
 
@@ -71,8 +88,11 @@ def test_llama70b_128k_full_size_sampled():
     rng = np.random.default_rng(12)
     n_rot, worst = c.check_repos(4096, rng)
     assert n_rot > 1000
+    n_hidden = [sum(b - a for a, b in g["hide"]) for g in w.segments]
+    segs = sorted({0, len(w.segments) - 1, int(np.argmin(n_hidden)), int(np.argmax(n_hidden))})
     for layer in (0, w.shape.n_layers - 1):
-        c.check_attention(layer, 8, rng, segments=[0, 13, 22, 31])
+        _, n = c.check_attention(layer, 256, rng, segments=segs)
+        assert n >= len(segs) * 256
     release(c)
 
 
@@ -85,7 +105,8 @@ def test_mla_16_sessions_full_size_sampled():
     n_rot, worst = c.check_repos(4096, rng)
     assert n_rot > 1000
     for layer in (0, w.shape.n_layers - 1):
-        c.check_attention(layer, 16, rng, segments=[0, 7, 15])
+        _, n = c.check_attention(layer, 256, rng, segments=[0, 7, 15])
+        assert n == 3 * 256      # every query row of the three sessions
     release(c)
 
 
@@ -112,5 +133,6 @@ def test_compaction_32k_branch_full_size_sampled():
     assert c.check_values(2048, rng) > 1000
     w.segments = remap_segments(w, states, c.names)
     for layer in (0, w.shape.n_layers - 1):
-        c.check_attention(layer, 12, rng)
+        _, n = c.check_attention(layer, 256, rng)
+        assert n >= 256
     release(c)

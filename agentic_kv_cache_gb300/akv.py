@@ -11,7 +11,8 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libakv.so")
+# AKV_CHECKED=1 selects the build with device-side descriptor checks (see build.py)
+LIB_PATH = os.path.join(_HERE, "libakv_checked.so" if os.environ.get("AKV_CHECKED", "") == "1" else "libakv.so")
 
 OK, ERR_ARG, ERR_RANGE, ERR_NO_PAGES, ERR_OVERFLOW, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_DEVICE = 0, 1, 2, 4, 5, 6, 7, 8
 STATUS_NAMES = {0: "OK", 1: "ARG", 2: "RANGE", 4: "NO_PAGES", 5: "OVERFLOW", 6: "CUDA", 7: "DEVICE_TIMEOUT",
@@ -113,6 +114,8 @@ def load(path=LIB_PATH):
         "akv_check_device_error": [P, P, pi32],
         "akv_profile_enable": [P, I32],
         "akv_set_attention_split": [P, I32],
+        "akv_debug_wait_limit": [P, ctypes.c_uint64, I32],
+        "akv_debug_corrupt": [P, I32],
         "akv_profile_read": [P, ctypes.POINTER(KernelStats)],
     }
     for name, args in sig.items():
@@ -342,6 +345,16 @@ class Engine:
         """0: automatic split-KV; n >= 1: exactly n KV chunks per work item (1 = never split).
         Applies to attend and attention_mass."""
         self._check(self.lib.akv_set_attention_split(self.h, int(split)))
+
+    def debug_corrupt(self, what):
+        """Checked-build test hook: 1 corrupts the next flush's first run, 2 the next attention
+        launch's first run (after host validation); the plain library raises AKVError(ARG)."""
+        self._check(self.lib.akv_debug_corrupt(self.h, int(what)))
+
+    def debug_wait_limit(self, wait_ns=0, load_cap=-1):
+        """Test hook: limit of the attention kernels' bounded waits (0: the default 4 s) and a cap
+        on the K/V tile copies each CTA issues (-1: none)."""
+        self._check(self.lib.akv_debug_wait_limit(self.h, int(wait_ns), int(load_cap)))
 
     def profile_enable(self, on=True):
         self._check(self.lib.akv_profile_enable(self.h, int(on)))

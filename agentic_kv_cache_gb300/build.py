@@ -5,7 +5,14 @@ Each translation unit is compiled in parallel, then linked into
 library only needs the driver at run time).  Rebuilds only when a source or
 header is newer than the library.
 
-    python -m agentic_kv_cache_gb300.build [--force] [--verbose]
+The checked variant ``libakv_checked.so`` is the same sources compiled with
+-DAKV_CHECKED: every kernel checks the descriptors it reads (pages inside the
+pool, row ranges inside a page, segments and runs inside their tables, query
+rows inside Q) and records AKV_ERR_DEVICE instead of touching memory they do
+not name.  It is built with ``checked=True`` or when the environment sets
+AKV_CHECKED=1, which also makes the binding load it.
+
+    python -m agentic_kv_cache_gb300.build [--force] [--verbose] [--checked]
 """
 import concurrent.futures
 import os
@@ -19,6 +26,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libakv.so")
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "libakv_checked.so")
+
+
+def checked_from_env():
+    return os.environ.get("AKV_CHECKED", "") == "1"
 
 SOURCES = ["engine.cpp", "kv_write.cu", "repos_rotate.cu", "segment_attn.cu", "segment_attn_mla.cu", "repos_noalloc.cu", "compact_copy.cu", "attn_mass.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,15 +54,15 @@ def _inputs():
     return files
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def _compile(src, verbose, extra):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src, verbose, extra, build_dir=BUILD):
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     lang = ["-x", "cu"] if src.endswith(".cu") else ["-x", "c++"]
     cmd = [nvcc()] + ARCH + FLAGS + extra + lang + ["-c", src, "-o", obj]
     if verbose:
@@ -62,24 +75,30 @@ def _compile(src, verbose, extra):
     return obj
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Compile and link libakv.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force=False, verbose=False, extra_flags=(), checked=None):
+    """Compile and link libakv.so (checked: libakv_checked.so, -DAKV_CHECKED; None: from the
+    AKV_CHECKED environment variable); returns its path."""
+    if checked is None:
+        checked = checked_from_env()
+    lib, build_dir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    extra = list(extra_flags) + (["-DAKV_CHECKED"] if checked else [])
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose, list(extra_flags)), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, extra, build_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-lrt", "-ldl", "-lpthread"]
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv,
+                checked=True if "--checked" in sys.argv else None))

@@ -16,6 +16,20 @@ struct DevErr {
   int32_t info[3];
 };
 
+#ifdef __CUDACC__
+// Device-side descriptor checks of the -DAKV_CHECKED build: a failed check
+// records AKV_ERR_DEVICE (8) with where it happened and the kernel skips the
+// work the descriptor names (or, for attention, the whole CTA returns before
+// touching memory).  Never a trap or an assert.  err may be null.
+__device__ __forceinline__ void report_device_error(DevErr* err, int where, int a, int b) {
+  if (err && atomicCAS(&err->code, 0, 8) == 0) {
+    err->info[0] = where;
+    err->info[1] = a;
+    err->info[2] = b;
+  }
+}
+#endif
+
 // One flush run: rows [lo, hi) of K page src are rotated by the shift whose
 // (cos, sin) table row is didx and written to the same rows of page dst
 // (dst == src: in place; dst != src: copy-on-write).
@@ -130,6 +144,11 @@ struct AttnParams {
   int32_t page;
   int32_t width;      // output columns one CTA writes (d_v, or d_v / 2 under MLA)
   int32_t dv;         // output row width (d_v)
+  uint64_t wait_ns;   // limit of every bounded wait (a wait that runs out reports AKV_ERR_DEVICE_TIMEOUT)
+  int32_t load_cap;   // test hook (GQA): K/V tile copies the producer of a CTA issues at most; < 0: no cap
+  int32_t n_segs;     // entries of segs (bounds of the checked build)
+  int32_t n_runs;     // entries of runs
+  int32_t n_q_rows;   // rows of Q, O and lse
 };
 
 // Attention-mass pass (GQA): one CTA per (segment, kv head, query tile);
@@ -152,7 +171,33 @@ struct MassParams {
   int32_t hq;
   int32_t group;
   int32_t page;
+  int32_t n_segs;     // bounds of the checked build
+  int32_t n_runs;
+  int32_t n_q_rows;
+  int32_t pad;
 };
+
+#if defined(__CUDACC__) && defined(AKV_CHECKED)
+// Checked build: the descriptors one attention work item reads name a
+// segment of the table, a run range inside the run table whose runs name
+// existing pages and a non-empty row range of one page, and query rows inside
+// Q.  Threads of a CTA split the run checks by `lane` of `lanes`.
+__device__ __forceinline__ bool attn_item_ok(const AttnWork& w, const AttnSeg* segs, const AttnRun* runs, int n_segs,
+                                             int n_runs, int n_q_rows, int n_pages, int page, int lane, int lanes) {
+  if (w.seg < 0 || w.seg >= n_segs || w.t0 < 0 || w.t0 > w.t1 || w.qt0 < 0) return false;
+  const AttnSeg sg = segs[w.seg];
+  if (sg.run_off < 0 || sg.n_runs < 1 || sg.run_off + sg.n_runs > n_runs || sg.q_row0 < 0 || sg.q_len < 0 ||
+      sg.q_row0 + sg.q_len > n_q_rows || sg.kv_len < sg.q_len)
+    return false;
+  bool ok = true;
+  for (int i = lane; i < sg.n_runs && ok; i += lanes) {
+    const AttnRun r = runs[sg.run_off + i];
+    const int lo = r.lohi & 0xffff, hi = r.lohi >> 16;
+    ok = r.kp >= 0 && r.kp < n_pages && r.vp >= 0 && r.vp < n_pages && lo < hi && hi <= page && r.es >= 0;
+  }
+  return ok;
+}
+#endif
 
 // Floats of one partial slot: tiles x 128 rows x (width + 2).
 __host__ __device__ inline int64_t partial_floats(int tiles, int width) { return int64_t(tiles) * 128 * (width + 2); }
@@ -160,24 +205,24 @@ __host__ __device__ inline int64_t partial_floats(int tiles, int width) { return
 // Launchers; each returns the launch's cudaError_t.
 cudaError_t launch_kv_write(const void* src_k, void* pool_k, const int32_t* rows_k, int dim_k, const void* src_v,
                             void* pool_v, const int32_t* rows_v, int dim_v, int64_t n, int n_layers, int heads,
-                            int page, int64_t n_pages, int n_sm, cudaStream_t st);
+                            int page, int64_t n_pages, int n_sm, DevErr* err, cudaStream_t st);
 
 cudaError_t launch_compact_copy(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int d_v, int page, int64_t n_pages, bool half,
-                                int n_sm, cudaStream_t st);
+                                int n_sm, DevErr* err, cudaStream_t st);
 
 cudaError_t launch_attn_mass(const MassParams& p, int dim, cudaStream_t st);
 
 cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int page, int64_t n_pages,
-                                bool half_layout, cudaStream_t st);
+                                bool half_layout, DevErr* err, cudaStream_t st);
 
 // Float32 debug mode of repos_rotate: rotated rows of each run go to
 // out[L][total_rows][H][d_rot] (rows of run r start at row_off[r]); the pool
 // is only read.
 cudaError_t launch_repos_rotate_f32(const void* kpool, const RunDesc* runs, const float2* cs, const int32_t* row_off,
                                     int64_t total_rows, float* out, int n_runs, int n_layers, int heads, int d_rot,
-                                    int page, int64_t n_pages, bool half_layout, cudaStream_t st);
+                                    int page, int64_t n_pages, bool half_layout, DevErr* err, cudaStream_t st);
 
 // dim: d_rot = d_v (GQA, 64 or 128).
 cudaError_t launch_segment_attn(const AttnParams& p, int dim, cudaStream_t st);

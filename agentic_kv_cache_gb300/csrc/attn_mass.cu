@@ -370,6 +370,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_mass_kernel(const __grid_con
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kBars + 8 * kMNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kBars + 8 * kMNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#ifdef AKV_CHECKED
+  {  // the whole CTA returns together, before any barrier or TMEM use
+    const bool ok = int(blockIdx.x) < p.n_work && p.work[blockIdx.x].kvh >= 0 &&
+                    p.work[blockIdx.x].kvh < p.hq / p.group &&
+                    attn_item_ok(p.work[blockIdx.x], p.segs, p.runs, p.n_segs, p.n_runs, p.n_q_rows, p.n_pages,
+                                 p.page, int(threadIdx.x), int(blockDim.x));
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) report_device_error(p.err, 12, int(blockIdx.x), 0);
+      return;
+    }
+  }
+#endif
   const AttnWork w = p.work[blockIdx.x];
   const AttnSeg seg = p.segs[w.seg];
   if (threadIdx.x == 0) {

@@ -35,7 +35,8 @@ template <int D, bool kHalf, int kPart>
 __global__ void __launch_bounds__(kThreads, kPart == 1 ? 4 : 3) compact_copy_kernel(uint4* __restrict__ kpool, uint4* __restrict__ vpool,
                                                                const CopyRun* __restrict__ runs,
                                                                const float2* __restrict__ cs, int n_runs, int n_layers,
-                                                               int heads, int page, int64_t n_pages, int vv_shift) {
+                                                               int heads, int page, int64_t n_pages, int vv_shift,
+                                                               DevErr* err) {
   constexpr int VK = D / 8;                  // 16-byte vectors per K row
   constexpr int W = kHalf ? VK / 2 : VK;     // K work items per row: vectors, or (v, v + VK/2) pairs
   constexpr int kInFlight = kPart == 1 ? 8 : 4;
@@ -46,6 +47,17 @@ __global__ void __launch_bounds__(kThreads, kPart == 1 ? 4 : 3) compact_copy_ker
     const int r = int(u % n_runs);
     const int64_t layer = u / n_runs;
     const CopyRun cr = runs[r];
+#ifdef AKV_CHECKED
+    // pages exist, both slot ranges lie inside one page, the shift row is valid or -1
+    if (!(cr.src_k >= 0 && cr.src_k < n_pages && cr.src_v >= 0 && cr.src_v < n_pages && cr.dst_k >= 0 &&
+          cr.dst_k < n_pages && cr.dst_v >= 0 && cr.dst_v < n_pages && cr.n > 0 && cr.src_lo >= 0 &&
+          cr.dst_lo >= 0 && cr.src_lo + cr.n <= page && cr.dst_lo + cr.n <= page && cr.didx >= -1)) {
+      if (threadIdx.x == 0) report_device_error(err, 3 + kPart, r, int(layer));
+      continue;  // the whole CTA skips this unit
+    }
+#else
+    (void)err;
+#endif
     // ---- K rows: rotated when the run carries a shift, else copied.
     if constexpr (kPart == 0) {
       const uint4* src = kpool + (layer * n_pages + cr.src_k) * kpage + cr.src_lo * VK;
@@ -124,16 +136,16 @@ __global__ void __launch_bounds__(kThreads, kPart == 1 ? 4 : 3) compact_copy_ker
 
 template <int D, bool kHalf>
 cudaError_t launch_variant(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs, int n_layers,
-                           int heads, int page, int64_t n_pages, int dv, int n_sm, cudaStream_t st) {
+                           int heads, int page, int64_t n_pages, int dv, int n_sm, DevErr* err, cudaStream_t st) {
   int vv_shift = 0;
   while ((8 << vv_shift) < dv) ++vv_shift;
   if ((8 << vv_shift) != dv) return cudaErrorInvalidValue;  // d_v must be 8 x a power of two
   const int64_t units = int64_t(n_layers) * n_runs;
   const int grid = int(units < int64_t(n_sm) * 8 ? units : int64_t(n_sm) * 8);
   compact_copy_kernel<D, kHalf, 0><<<grid, kThreads, 0, st>>>(static_cast<uint4*>(kpool), static_cast<uint4*>(vpool),
-                                                              runs, cs, n_runs, n_layers, heads, page, n_pages, vv_shift);
+                                                              runs, cs, n_runs, n_layers, heads, page, n_pages, vv_shift, err);
   compact_copy_kernel<D, kHalf, 1><<<grid, kThreads, 0, st>>>(static_cast<uint4*>(kpool), static_cast<uint4*>(vpool),
-                                                              runs, cs, n_runs, n_layers, heads, page, n_pages, vv_shift);
+                                                              runs, cs, n_runs, n_layers, heads, page, n_pages, vv_shift, err);
   return cudaGetLastError();
 }
 
@@ -141,15 +153,15 @@ cudaError_t launch_variant(void* kpool, void* vpool, const CopyRun* runs, const 
 
 cudaError_t launch_compact_copy(void* kpool, void* vpool, const CopyRun* runs, const float2* cs, int n_runs,
                                 int n_layers, int heads, int d_rot, int d_v, int page, int64_t n_pages, bool half,
-                                int n_sm, cudaStream_t st) {
+                                int n_sm, DevErr* err, cudaStream_t st) {
   if (n_runs <= 0) return cudaSuccess;
   if (d_v % 8 != 0) return cudaErrorInvalidValue;
   if (d_rot == 64)
-    return half ? launch_variant<64, true>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, st)
-                : launch_variant<64, false>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, st);
+    return half ? launch_variant<64, true>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, err, st)
+                : launch_variant<64, false>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, err, st);
   if (d_rot == 128)
-    return half ? launch_variant<128, true>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, st)
-                : launch_variant<128, false>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, st);
+    return half ? launch_variant<128, true>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, err, st)
+                : launch_variant<128, false>(kpool, vpool, runs, cs, n_runs, n_layers, heads, page, n_pages, d_v, n_sm, err, st);
   return cudaErrorInvalidValue;
 }
 

@@ -388,6 +388,9 @@ struct akv_ctx {
   int n_sm = 148;          // SMs of the device, for split decisions
   int mla_slots = 148;     // MLA kernel CTAs resident at once (CTA pairs x 2)
   int split_override = 0;  // 0: choose the split factor; n >= 1: use n
+  int32_t corrupt_next = 0;           // checked-build test hook (akv_debug_corrupt)
+  uint64_t wait_ns = 4000000000ull;  // limit of the attention kernels' bounded waits
+  int32_t load_cap = -1;              // test hook: cap on a CTA's K/V tile copies (GQA attention)
   CUtensorMap k_map{}, v_map{}, k_tile_map{}, v_tile_map{};
   bool maps_ok = false;
 
@@ -541,7 +544,7 @@ struct akv_ctx {
     begin_timed(kKvWrite, double(kbytes + vbytes) * 2.0, 0.0, st, t, 1);
     cuda_check(akv::launch_kv_write(kd, kpool, static_cast<int32_t*>(dk), cfg.d_rot, vd, vpool,
                                     static_cast<int32_t*>(dv), cfg.d_v, n, cfg.n_layers, cfg.n_kv_heads,
-                                    cfg.page_size, cfg.n_pages, n_sm, st),
+                                    cfg.page_size, cfg.n_pages, n_sm, dev_err, st),
                "kv_write launch");
     end_timed(t, st);
     up.done(st);
@@ -810,7 +813,8 @@ struct akv_ctx {
     begin_timed(kCompact, bytes, 0.0, st, tm, 2);  // key launch + value launch
     cuda_check(akv::launch_compact_copy(kpool, vpool, static_cast<akv::CopyRun*>(druns), static_cast<float2*>(dcs),
                                         int(runs.size()), cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.d_v,
-                                        cfg.page_size, cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, n_sm, st),
+                                        cfg.page_size, cfg.n_pages, cfg.rope_layout == AKV_ROPE_HALF, n_sm, dev_err,
+                                        st),
                "compact_copy launch");
     end_timed(tm, st);
     up.done(st);
@@ -880,6 +884,10 @@ struct akv_ctx {
       for (size_t i = n_copy; i < runs.size() && !conflict; ++i) conflict = mk.test(runs[i].dst);
     }
     std::vector<float2> cs = angle_table(deltas);
+    if (corrupt_next == 1) {  // checked-build test hook: a row range past the page
+      runs[0].lohi = (runs[0].lohi & 0xffff) | ((cfg.page_size + 1) << 16);
+      corrupt_next = 0;
+    }
     void* druns = nullptr;
     void* dcs = nullptr;
     up.upload({{runs.data(), runs.size() * sizeof(akv::RunDesc), &druns}, {cs.data(), cs.size() * sizeof(float2), &dcs}},
@@ -892,7 +900,7 @@ struct akv_ctx {
     auto launch = [&](int first, int n) {
       cuda_check(akv::launch_repos_rotate(kpool, static_cast<akv::RunDesc*>(druns) + first, static_cast<float2*>(dcs),
                                           n, cfg.n_layers, cfg.n_kv_heads, cfg.d_rot, cfg.page_size, cfg.n_pages,
-                                          cfg.rope_layout == AKV_ROPE_HALF, st),
+                                          cfg.rope_layout == AKV_ROPE_HALF, dev_err, st),
                  "repos_rotate launch");
     };
     if (conflict) {
@@ -952,7 +960,7 @@ struct akv_ctx {
     cuda_check(akv::launch_repos_rotate_f32(kpool, static_cast<akv::RunDesc*>(druns), static_cast<float2*>(dcs),
                                             static_cast<int32_t*>(doff), rows, out, n_runs, cfg.n_layers,
                                             cfg.n_kv_heads, cfg.d_rot, cfg.page_size, cfg.n_pages,
-                                            cfg.rope_layout == AKV_ROPE_HALF, st),
+                                            cfg.rope_layout == AKV_ROPE_HALF, dev_err, st),
                "repos_rotate f32 launch");
     up.done(st);
   }
@@ -1272,8 +1280,17 @@ struct akv_ctx {
   // partial results the last one to finish merges.  A cut never leaves a
   // piece of an item shorter than kMinSteps steps.  akv_set_attention_split
   // (n >= 1) instead cuts every item into n equal parts, one CTA per unit.
+  //
+  // A launch with many items per CTA (many segments) is first laid out for L2
+  // reuse: items are sorted by kv head, then sequence, segment and query tile
+  // (items of one kv head of one sequence, or of forks sharing its pages, read
+  // the same K/V), then dealt in that order, each to the CTA with the least
+  // work so far, and the CTAs' lists are laid end to end before the cut.  The
+  // CTAs running at the same time then all work on one or two such groups, so
+  // each K/V tile is fetched from HBM about once per group instead of once per
+  // item.  Units then run in that order inside each CTA.
   void plan_persistent(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts,
-                       std::vector<int32_t>& cta_units) {
+                       std::vector<int32_t>& cta_units, const std::vector<int32_t>& seg_seq) {
     if (split_override > 0) {
       std::vector<akv::AttnWork> units;
       for (auto& w : work) {
@@ -1298,6 +1315,7 @@ struct akv_ctx {
     constexpr int64_t kUnitCost = 1;   // start + epilogue of a unit, in query-tile steps (measured: 1 to 14 within 0.6 %, 1 best)
     constexpr int64_t kMinSteps = 4;   // shortest piece of an item worth a unit
     constexpr int64_t kMinCtaCost = 48;
+    constexpr int64_t kGroupedItemsPerCta = 4;  // from this many items per CTA on, lay items out by K/V group
     // cost of the first j steps of item w (O(1): each query tile feeds its first n steps)
     auto prefix = [](const akv::AttnWork& w, int64_t j) {
       return std::min<int64_t>(j, w.n_a) + std::min<int64_t>(j, w.n_b);
@@ -1305,9 +1323,37 @@ struct akv_ctx {
     int64_t total = 0;
     for (auto& w : work) total += kUnitCost + prefix(w, w.t1);
     const int64_t n_cta = std::max<int64_t>(1, std::min<int64_t>(n_sm, total / kMinCtaCost));
-    total += (n_cta - 1) * kUnitCost;  // each cut starts one more unit
+    const bool grouped = int64_t(work.size()) >= kGroupedItemsPerCta * n_cta;
+    if (grouped) {
+      std::vector<size_t> idx(work.size());
+      for (size_t i = 0; i < idx.size(); ++i) idx[i] = i;
+      std::stable_sort(idx.begin(), idx.end(), [&](size_t a, size_t b) {
+        const akv::AttnWork &x = work[a], &y = work[b];
+        const int32_t sx = seg_seq[size_t(x.seg)], sy = seg_seq[size_t(y.seg)];
+        if (x.kvh != y.kvh) return x.kvh < y.kvh;
+        if (sx != sy) return sx < sy;
+        if (x.seg != y.seg) return x.seg < y.seg;
+        return x.qt0 < y.qt0;
+      });
+      std::vector<std::vector<size_t>> lists;
+      lists.resize(static_cast<size_t>(n_cta));
+      std::priority_queue<std::pair<int64_t, int64_t>, std::vector<std::pair<int64_t, int64_t>>, std::greater<>> load;
+      for (int64_t c = 0; c < n_cta; ++c) load.emplace(0, c);
+      for (size_t i : idx) {
+        auto [l, c] = load.top();
+        load.pop();
+        lists[size_t(c)].push_back(i);
+        load.emplace(l + kUnitCost + prefix(work[i], work[i].t1), c);
+      }
+      std::vector<akv::AttnWork> dealt;
+      dealt.reserve(work.size());
+      for (const auto& l : lists)
+        for (size_t i : l) dealt.push_back(work[i]);
+      work.swap(dealt);
+    }
     std::vector<akv::AttnWork> units;
     std::vector<int32_t> item_of;  // unit -> item index
+    total += (n_cta - 1) * kUnitCost;  // each cut starts one more unit
     units.reserve(work.size() + size_t(n_cta));
     item_of.reserve(work.size() + size_t(n_cta));
     cta_units.assign(1, 0);
@@ -1356,13 +1402,13 @@ struct akv_ctx {
       if (close_at_end && cta < n_cta - 1) close_cta();
     }
     if (cta_units.back() != int32_t(units.size())) close_cta();
-    // Order inside each CTA: the piece that starts an item (at KV step 0)
-    // first, then the piece that ends an item cut by the previous CTA, then
-    // whole items.  With items of similar length every CTA then reads the
-    // same KV step of its item at about the same time (three phases in all),
-    // so the K/V tiles a step needs are fetched from HBM once and served to
-    // the other CTAs from L2.
-    {
+    // Order inside each CTA (a few items per CTA): the piece that starts an
+    // item (at KV step 0) first, then the piece that ends an item cut by the
+    // previous CTA, then whole items.  With items of similar length every CTA
+    // then reads the same KV step of its item at about the same time (three
+    // phases in all), so the K/V tiles a step needs are fetched from HBM once
+    // and served to the other CTAs from L2.
+    if (!grouped) {
       std::vector<akv::AttnWork> ordered;
       std::vector<int32_t> ordered_item;
       ordered.reserve(units.size());
@@ -1504,7 +1550,9 @@ struct akv_ctx {
     if (mla) {
       plan_split(work, comb, n_parts);
     } else {
-      plan_persistent(work, comb, n_parts, cta_units);
+      std::vector<int32_t> seg_seq(static_cast<size_t>(n_segs));
+      for (int32_t i = 0; i < n_segs; ++i) seg_seq[size_t(i)] = segs[i].seq;
+      plan_persistent(work, comb, n_parts, cta_units, seg_seq);
     }
     if (mla) {
       if (cfg.d_v != 512 || cfg.d_rot != 64)
@@ -1552,6 +1600,10 @@ struct akv_ctx {
     void* dcs = nullptr;
     const std::vector<float2> cs = rotate ? angle_table(shifts) : std::vector<float2>();
     if (!rotate) run_didx.clear();
+    if (corrupt_next == 2) {  // checked-build test hook: a K page outside the pool
+      runs[0].kp = cfg.n_pages;
+      corrupt_next = 0;
+    }
     up.upload({{runs.data(), runs.size() * sizeof(akv::AttnRun), &druns},
                {tab.data(), tab.size() * sizeof(akv::AttnSeg), &dsegs},
                {work.data(), work.size() * sizeof(akv::AttnWork), &dwork},
@@ -1578,6 +1630,11 @@ struct akv_ctx {
     p.page = cfg.page_size;
     p.width = mla ? cfg.d_v / 2 : cfg.d_v;
     p.dv = cfg.d_v;
+    p.wait_ns = wait_ns;
+    p.load_cap = load_cap;
+    p.n_segs = int32_t(tab.size());
+    p.n_runs = int32_t(runs.size());
+    p.n_q_rows = int32_t(n_q_rows);
     p.fused = rotate ? 1 : 0;
     p.run_didx = rotate ? static_cast<const int32_t*>(ddidx) : nullptr;
     p.cs = rotate ? static_cast<const float2*>(dcs) : nullptr;
@@ -1864,6 +1921,9 @@ struct akv_ctx {
     p.err = dev_err;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.n_work = int32_t(work.size());
+    p.n_segs = int32_t(tab.size());
+    p.n_runs = int32_t(runs.size());
+    p.n_q_rows = int32_t(n_q_rows);
     p.layer = layer;
     p.n_pages = cfg.n_pages;
     p.hq = cfg.n_q_heads;
@@ -2206,6 +2266,26 @@ akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split) {
   return guard(ctx, [&] {
     if (split < 0 || split > 8) fail(AKV_ERR_ARG, "split must be 0 (automatic) or 1..8");
     ctx->split_override = split;
+  });
+}
+
+akv_status akv_debug_wait_limit(akv_ctx* ctx, uint64_t wait_ns, int32_t load_cap) {
+  return guard(ctx, [&] {
+    if (load_cap < -1) fail(AKV_ERR_ARG, "load_cap must be -1 (no cap) or >= 0");
+    ctx->wait_ns = wait_ns ? wait_ns : 4000000000ull;
+    ctx->load_cap = load_cap;
+  });
+}
+
+akv_status akv_debug_corrupt(akv_ctx* ctx, int32_t what) {
+  return guard(ctx, [&] {
+#ifdef AKV_CHECKED
+    if (what < 0 || what > 2) fail(AKV_ERR_ARG, "what must be 0, 1 (flush) or 2 (attend)");
+    ctx->corrupt_next = what;
+#else
+    (void)what;
+    fail(AKV_ERR_ARG, "descriptor corruption needs the checked build (libakv_checked.so)");
+#endif
   });
 }
 

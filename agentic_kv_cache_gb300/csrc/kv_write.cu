@@ -28,7 +28,7 @@ struct KvSide {
 
 template <typename I>
 __global__ void __launch_bounds__(256) kv_write_kernel(KvSide k, KvSide v, I n, int n_layers, int heads, int page,
-                                                       int64_t n_pages) {
+                                                       int64_t n_pages, DevErr* err) {
   const KvSide s = blockIdx.y == 0 ? k : v;
   const I vpr = I(s.vec_per_row);
   const I total = I(n_layers) * n * I(heads) * vpr;
@@ -43,6 +43,12 @@ __global__ void __launch_bounds__(256) kv_write_kernel(KvSide k, KvSide v, I n, 
     const I t = rest % n;
     const I l = rest / n;
     const int32_t r = __ldg(s.rows + t);
+#ifdef AKV_CHECKED
+    if (r < 0 || int64_t(r) >= n_pages * page) {  // skip the row: it names no slot of the pool
+      report_device_error(err, 2, int(t), r);
+      continue;
+    }
+#endif
     const int32_t pg = r / page, slot = r % page;
     const uint4 x = __ldcs(s.src + i);
     __stcs(s.pool + int64_t(l) * layer_vecs + int64_t(pg) * page_vecs + int64_t(h) * row_vecs +
@@ -55,7 +61,7 @@ __global__ void __launch_bounds__(256) kv_write_kernel(KvSide k, KvSide v, I n, 
 
 cudaError_t launch_kv_write(const void* src_k, void* pool_k, const int32_t* rows_k, int dim_k, const void* src_v,
                             void* pool_v, const int32_t* rows_v, int dim_v, int64_t n, int n_layers, int heads,
-                            int page, int64_t n_pages, int n_sm, cudaStream_t st) {
+                            int page, int64_t n_pages, int n_sm, DevErr* err, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   if (dim_k % 8 || dim_v % 8) return cudaErrorInvalidValue;
   const int64_t total = int64_t(n_layers) * n * heads * (std::max(dim_k, dim_v) / 8);
@@ -64,9 +70,9 @@ cudaError_t launch_kv_write(const void* src_k, void* pool_k, const int32_t* rows
   const KvSide v{static_cast<const uint4*>(src_v), static_cast<uint4*>(pool_v), rows_v, dim_v / 8};
   const dim3 grid(unsigned(blocks), 2);
   if (total < (int64_t(1) << 31) - int64_t(blocks) * 256)
-    kv_write_kernel<int32_t><<<grid, 256, 0, st>>>(k, v, int32_t(n), n_layers, heads, page, n_pages);
+    kv_write_kernel<int32_t><<<grid, 256, 0, st>>>(k, v, int32_t(n), n_layers, heads, page, n_pages, err);
   else
-    kv_write_kernel<int64_t><<<grid, 256, 0, st>>>(k, v, n, n_layers, heads, page, n_pages);
+    kv_write_kernel<int64_t><<<grid, 256, 0, st>>>(k, v, n, n_layers, heads, page, n_pages, err);
   return cudaGetLastError();
 }
 

@@ -172,10 +172,11 @@ extern "C" AKV_API akv_status akv_repos_rotate_noalloc(void* k_pool, int32_t n_l
   }
   const int32_t first_n = conflict ? n_copy : n_runs;
   if (akv::launch_repos_rotate(k_pool, dev_runs, dev_cs, first_n, n_layers, n_kv_heads, d_rot, page_size, n_pages,
-                               rope_layout == AKV_ROPE_HALF, st) != cudaSuccess)
+                               rope_layout == AKV_ROPE_HALF, nullptr, st) != cudaSuccess)
     return AKV_ERR_CUDA;
   if (conflict && akv::launch_repos_rotate(k_pool, dev_runs + n_copy, dev_cs, n_runs - n_copy, n_layers, n_kv_heads,
-                                           d_rot, page_size, n_pages, rope_layout == AKV_ROPE_HALF, st) != cudaSuccess)
+                                           d_rot, page_size, n_pages, rope_layout == AKV_ROPE_HALF, nullptr,
+                                           st) != cudaSuccess)
     return AKV_ERR_CUDA;
   return AKV_OK;
 }

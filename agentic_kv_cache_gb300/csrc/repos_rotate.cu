@@ -35,6 +35,15 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
+#ifdef AKV_CHECKED
+// A run descriptor names existing pages and a non-empty row range of one page.
+__device__ __forceinline__ bool run_ok(const RunDesc& rd, int page, int64_t n_pages) {
+  const int lo = rd.lohi & 0xffff, hi = rd.lohi >> 16;
+  return rd.src >= 0 && rd.src < n_pages && rd.dst >= 0 && rd.dst < n_pages && lo < hi && hi <= page &&
+         rd.didx >= 0;
+}
+#endif
+
 // Where a rotated 16-byte vector goes: back into the pool as bf16 (the
 // product path), or, in the float32 debug mode, into a dense float32 array
 // [L][rows][H][D] so the rotation can be checked before rounding.
@@ -49,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) repos_interleaved_kernel(uint4* __re
                                                                    const RunDesc* __restrict__ runs,
                                                                    const float2* __restrict__ cs, int n_runs,
                                                                    int n_layers, int heads, int page,
-                                                                   int64_t n_pages, F32Out f32) {
+                                                                   int64_t n_pages, F32Out f32, DevErr* err) {
   constexpr int V = D / 8;  // vectors per row
   const int64_t page_vecs = int64_t(heads) * page * V;
   const int64_t layer_vecs = page_vecs * n_pages;
@@ -59,6 +68,14 @@ __global__ void __launch_bounds__(kThreads) repos_interleaved_kernel(uint4* __re
     const int64_t layer = u / n_runs;
     const RunDesc rd = runs[r];
     const int lo = rd.lohi & 0xffff, n = (rd.lohi >> 16) - lo;
+#ifdef AKV_CHECKED
+    if (!run_ok(rd, page, n_pages)) {  // the whole CTA skips this unit
+      if (threadIdx.x == 0) report_device_error(err, 1, r, int(layer));
+      continue;
+    }
+#else
+    (void)err;
+#endif
     const float2* cs_row = cs + int64_t(rd.didx) * (D / 2);
     const uint4* src = pool + layer * layer_vecs + rd.src * page_vecs;
     uint4* dst = pool + layer * layer_vecs + rd.dst * page_vecs;
@@ -102,7 +119,8 @@ template <int D, bool F32>
 __global__ void __launch_bounds__(kThreads) repos_half_kernel(uint4* __restrict__ pool,
                                                             const RunDesc* __restrict__ runs,
                                                             const float2* __restrict__ cs, int n_runs, int n_layers,
-                                                            int heads, int page, int64_t n_pages, F32Out f32) {
+                                                            int heads, int page, int64_t n_pages, F32Out f32,
+                                                            DevErr* err) {
   constexpr int V = D / 8;
   constexpr int HV = V / 2;  // vector pairs per row: (v, v + V/2)
   const int64_t page_vecs = int64_t(heads) * page * V;
@@ -113,6 +131,14 @@ __global__ void __launch_bounds__(kThreads) repos_half_kernel(uint4* __restrict_
     const int64_t layer = u / n_runs;
     const RunDesc rd = runs[r];
     const int lo = rd.lohi & 0xffff, n = (rd.lohi >> 16) - lo;
+#ifdef AKV_CHECKED
+    if (!run_ok(rd, page, n_pages)) {  // the whole CTA skips this unit
+      if (threadIdx.x == 0) report_device_error(err, 1, r, int(layer));
+      continue;
+    }
+#else
+    (void)err;
+#endif
     const float2* cs_row = cs + int64_t(rd.didx) * (D / 2);
     const uint4* src = pool + layer * layer_vecs + rd.src * page_vecs;
     uint4* dst = pool + layer * layer_vecs + rd.dst * page_vecs;
@@ -150,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) repos_half_kernel(uint4* __restrict_
 
 template <bool F32>
 cudaError_t launch(void* kpool, const RunDesc* runs, const float2* cs, int n_runs, int n_layers, int heads,
-                   int d_rot, int page, int64_t n_pages, bool half_layout, F32Out f32, cudaStream_t st) {
+                   int d_rot, int page, int64_t n_pages, bool half_layout, F32Out f32, DevErr* err, cudaStream_t st) {
   if (n_runs <= 0) return cudaSuccess;
   int sms = 152;
   int dev = 0;
@@ -162,10 +188,10 @@ cudaError_t launch(void* kpool, const RunDesc* runs, const float2* cs, int n_run
   case DIM:                                                                                                    \
     if (half_layout)                                                                                           \
       repos_half_kernel<DIM, F32><<<blocks, kThreads, 0, st>>>(p, runs, cs, n_runs, n_layers, heads, page,     \
-                                                               n_pages, f32);                                  \
+                                                               n_pages, f32, err);                             \
     else                                                                                                       \
       repos_interleaved_kernel<DIM, F32><<<blocks, kThreads, 0, st>>>(p, runs, cs, n_runs, n_layers, heads,    \
-                                                                      page, n_pages, f32);                    \
+                                                                      page, n_pages, f32, err);               \
     break;
   switch (d_rot) {
     AKV_REPOS_CASE(16)
@@ -183,16 +209,17 @@ cudaError_t launch(void* kpool, const RunDesc* runs, const float2* cs, int n_run
 }  // namespace
 
 cudaError_t launch_repos_rotate(void* kpool, const RunDesc* runs, const float2* cs, int n_runs, int n_layers,
-                                int heads, int d_rot, int page, int64_t n_pages, bool half_layout, cudaStream_t st) {
+                                int heads, int d_rot, int page, int64_t n_pages, bool half_layout, DevErr* err,
+                                cudaStream_t st) {
   return launch<false>(kpool, runs, cs, n_runs, n_layers, heads, d_rot, page, n_pages, half_layout,
-                       F32Out{nullptr, nullptr, 0}, st);
+                       F32Out{nullptr, nullptr, 0}, err, st);
 }
 
 cudaError_t launch_repos_rotate_f32(const void* kpool, const RunDesc* runs, const float2* cs, const int32_t* row_off,
                                     int64_t total_rows, float* out, int n_runs, int n_layers, int heads, int d_rot,
-                                    int page, int64_t n_pages, bool half_layout, cudaStream_t st) {
+                                    int page, int64_t n_pages, bool half_layout, DevErr* err, cudaStream_t st) {
   return launch<true>(const_cast<void*>(kpool), runs, cs, n_runs, n_layers, heads, d_rot, page, n_pages,
-                      half_layout, F32Out{out, row_off, total_rows}, st);
+                      half_layout, F32Out{out, row_off, total_rows}, err, st);
 }
 
 }  // namespace akv

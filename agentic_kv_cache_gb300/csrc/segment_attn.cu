@@ -30,8 +30,9 @@
 //     QK that overwrites S, and one thread's MMAs execute in issue order).
 //     While one warpgroup computes exponentials the tensor core runs the other
 //     tile's MMAs;
-//   * every wait is bounded; on time-out the CTA records AKV_ERR_DEVICE_TIMEOUT
-//     in the device error word, drains its copies and MMAs, frees TMEM, exits.
+//   * every wait is bounded (p.wait_ns, 4 s unless a test lowers it); on
+//     time-out the CTA records AKV_ERR_DEVICE_TIMEOUT in the device error
+//     word, drains its copies and MMAs, frees TMEM, exits.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -51,7 +52,6 @@ constexpr int kRotThreads = 64;
 constexpr int kTileKeys = 128;
 constexpr int kRows = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;  // AKV_ERR_DEVICE_TIMEOUT
 constexpr int32_t kErrDevice = 8;   // AKV_ERR_DEVICE
@@ -110,15 +110,20 @@ __device__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, vol
   const int layer_base = p.layer * p.n_pages;
   int armed[kSlots] = {0, 0, 0, 0};
   int ld0 = 0, q_loads = 0;
-  bool ok = true;
-  for (int u = u0; u < u1 && ok; ++u) {
+  bool ok = true, capped = false;
+  // Test hook: with p.load_cap >= 0 the producer issues at most that many
+  // K/V tile copies and then stops (no error of its own); the waits of the
+  // MMA thread and the softmax on the missing tiles then run out after
+  // p.wait_ns and report AKV_ERR_DEVICE_TIMEOUT.
+  int n_copies = 0;
+  for (int u = u0; u < u1 && ok && !capped; ++u) {
     const AttnWork w = p.work[u];
     const AttnSeg seg = p.segs[w.seg];
     // KV tiles [t0, t1) of this unit; local tile j is global tile t0 + j
     const int span = w.t1 - w.t0;
     const int n_max = max(min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span));
     const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
-    if (u > u0 && !(ok = ptx::mbar_wait(bar(kBarQFree), (u - u0 - 1) & 1, abort_flag, kWaitLimitNs))) break;
+    if (u > u0 && !(ok = ptx::mbar_wait(bar(kBarQFree), (u - u0 - 1) & 1, abort_flag, p.wait_ns))) break;
     ptx::mbar_arrive_expect_tx(bar(kBarQ), (w.n_b > 0 ? 2 : 1) * L::kTile);
     for (int t = 0; t < (w.n_b > 0 ? 2 : 1); ++t)
       for (int kb = 0; kb < L::kBlocks; ++kb)
@@ -151,9 +156,14 @@ __device__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, vol
     };
     fetch(0, kpg, vpg);
     for (int l = 0; l < 2 * n_max; ++l) {
+      if (p.load_cap >= 0 && n_copies >= p.load_cap) {
+        capped = true;
+        break;
+      }
+      ++n_copies;
       const int ld = ld0 + l, j = l >> 1, is_v = l & 1, slot = ld % kSlots, use = ld / kSlots;
       if (!is_v && j + 1 < n_max) fetch(j + 1, nkp, nvp);
-      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -220,14 +230,14 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
   // a slot's tile may be read once TMA has landed it (and, with fused rotation, once K is rotated)
   auto ready_bar = [&](int ld) { return bar((kFused ? kBarRdy0 : kBarFull0) + ld % kSlots); };
   int ld0 = 0, cs0 = 0, cs1 = 0;
-  bool ok = true;
+  bool ok = true, issued = false;  // a commit is only issued after this thread's first MMA
   const uint64_t qd0 = ptx::smem_desc(sbase + L::kQ, 16, 1024), qd1 = ptx::smem_desc(sbase + L::kQ + L::kTile, 16, 1024);
   for (int u = u0; u < u1 && ok; ++u) {
     const AttnWork w = p.work[u];
     const int span = w.t1 - w.t0;  // local tile counts of this KV range
     const int nt0 = min(max(w.n_a - w.t0, 0), span), nt1 = min(max(w.n_b - w.t0, 0), span);
     const int n_max = max(nt0, nt1);
-    if (!(ok = ptx::mbar_wait(bar(kBarQ), (u - u0) & 1, abort_flag, kWaitLimitNs))) break;
+    if (!(ok = ptx::mbar_wait(bar(kBarQ), (u - u0) & 1, abort_flag, p.wait_ns))) break;
     for (int j = 0; j <= n_max && ok; ++j) {
       bool k_ready = false, v_ready = false;
 #pragma unroll
@@ -237,16 +247,17 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
         if (ok && j >= 1 && j - 1 < nt) {
           if (!v_ready) {
             const int ld = ld0 + 2 * (j - 1) + 1;
-            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, p.wait_ns);
             v_ready = true;
           }
-          if (ok) ok = ptx::mbar_wait(bar(kBarP0 + t), (cs + j - 1) & 1, abort_flag, kWaitLimitNs);
+          if (ok) ok = ptx::mbar_wait(bar(kBarP0 + t), (cs + j - 1) & 1, abort_flag, p.wait_ns);
           if (ok) {
             ptx::tc_fence_after();
             const uint64_t vd = ptx::smem_desc(sbase + L::kSlot + slot_of(ld0 + 2 * (j - 1) + 1) * L::kTile,
                                                L::kBlockBytes, 1024);
             // P: 16 keys = 8 packed TMEM columns per step; V: 16 key rows = 2 KiB per step
             ptx::mma_bf16_tmem_a(tO, tS, vd, idesc_pv, j > 1);
+            issued = true;
 #pragma unroll
             for (int ks = 1; ks < kTileKeys / 16; ++ks)
               ptx::mma_bf16_tmem_a(tO, tS + 8u * ks, ptx::desc_advance(vd, ks * 16 * 128), idesc_pv, 1);
@@ -256,7 +267,7 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
         if (ok && j < nt) {
           if (!k_ready) {
             const int ld = ld0 + 2 * j;
-            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, kWaitLimitNs);
+            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, p.wait_ns);
             k_ready = true;
             ptx::tc_fence_after();
           }
@@ -269,6 +280,7 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
               const uint32_t off = (ks >> 2) * L::kBlockBytes + (ks & 3) * 32;
               ptx::mma_bf16(tS, ptx::desc_advance(qd, off), ptx::desc_advance(kd, off), idesc_qk, ks > 0);
             }
+            issued = true;
             ptx::mma_commit(bar(kBarS0 + t));
           }
         }
@@ -287,8 +299,10 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
     *abort_flag = 1;
   }
   // Every MMA issued above has completed before TMEM is released.
-  ptx::mma_commit(bar(kBarFin));
-  ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs);
+  if (issued) {
+    ptx::mma_commit(bar(kBarFin));
+    ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs);
+  }
 }
 
 // ------------------------------------------------------------ K rotation
@@ -319,7 +333,7 @@ __device__ void rotate_k(const AttnParams& p, int u0, int u1, uint32_t sbase, ui
     const int n_max = max(min(max(w.n_a - w.t0, 0), span), min(max(w.n_b - w.t0, 0), span));
     for (int l = 0; l < 2 * n_max; ++l) {
       const int ld = ld0 + l, slot = ld % kSlots;
-      if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot), (ld / kSlots) & 1, abort_flag, kWaitLimitNs))) break;
+      if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot), (ld / kSlots) & 1, abort_flag, p.wait_ns))) break;
       if ((l & 1) == 0) {
         uint8_t* tile = smem + L::kSlot + slot * L::kTile;
 #pragma unroll 1
@@ -435,7 +449,7 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     if (ri0 < seg.n_runs) run_cur = run_le[2 * ri0 + 1];
   }
   for (int j = 0; j < n_t; ++j) {
-    ok = ptx::mbar_wait(bar(kBarS0 + t), (ph ^ j) & 1, abort_flag, kWaitLimitNs);
+    ok = ptx::mbar_wait(bar(kBarS0 + t), (ph ^ j) & 1, abort_flag, p.wait_ns);
     // Entry index of key column r of tile j (INT_MAX: no entry there);
     // columns are (run c / page, slot c % page) of the tile's runs.  The run
     // of the next tile is fetched now so its latency hides behind this tile.
@@ -549,7 +563,7 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     ptx::mbar_arrive(bar(kBarP0 + t));
   }
   if (ok) {
-    ok = ptx::mbar_wait(bar(kBarO0 + t), (ph >> 1) & 1, abort_flag, kWaitLimitNs);
+    ok = ptx::mbar_wait(bar(kBarO0 + t), (ph >> 1) & 1, abort_flag, p.wait_ns);
     ok = ptx::bar_red_and(bar_id, 128, ok);
   }
   if (!ok) {
@@ -631,6 +645,21 @@ __global__ void __launch_bounds__(kFused ? kThreadsFused : kThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int u0 = p.cta_units ? p.cta_units[blockIdx.x] : int(blockIdx.x);
   const int u1 = p.cta_units ? p.cta_units[blockIdx.x + 1] : int(blockIdx.x) + 1;
+#ifdef AKV_CHECKED
+  {  // every thread takes part, so the whole CTA returns together, before any barrier or TMEM use
+    bool ok = u0 >= 0 && u0 <= u1 && u1 <= p.n_work;
+    for (int u = u0; u < u1 && ok; ++u) {
+      const AttnWork w = p.work[u];
+      ok = w.kvh >= 0 && w.kvh < p.hq / p.group &&
+           attn_item_ok(w, p.segs, p.runs, p.n_segs, p.n_runs, p.n_q_rows, p.n_pages, p.page, int(threadIdx.x),
+                        int(blockDim.x));
+    }
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) report_device_error(p.err, 10, int(blockIdx.x), u0);
+      return;
+    }
+  }
+#endif
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)

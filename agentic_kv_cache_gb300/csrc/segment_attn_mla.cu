@@ -50,7 +50,6 @@ constexpr uint32_t kQChunk = 128 * 128;      // 128 rows x 64 bf16
 constexpr uint32_t kUnit = 64 * 128;         // 64 keys x 64 bf16: one copy
 constexpr uint32_t kSlot = 2 * kUnit;        // one round: two copies
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 100000000ull;
 constexpr int32_t kErrTimeout = 7;
 constexpr uint16_t kBoth = 0x3;  // CTA mask of the pair
@@ -195,7 +194,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
   auto round = [&](int kind, int j, const TilePages& tp) {
     if (ok && rd % kProducers == who) {
       const int slot = rd % kRing, use = rd / kRing;
-      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, kWaitLimitNs)) {
+      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, p.wait_ns)) {
         ok = false;
       } else {
         const uint32_t dst = sbase + kSlots + slot * kSlot;
@@ -268,11 +267,11 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
   const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);
   int rd = 0;
   bool issued = false;  // a commit is only issued after this thread's first MMA
-  bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, kWaitLimitNs);
+  bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, p.wait_ns);
   ptx::tc_fence_after();
   auto next_round = [&]() -> uint32_t {  // wait for round rd; its slot address
     const int slot = rd % kRing;
-    ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kRing) & 1, abort_flag, kWaitLimitNs);
+    ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kRing) & 1, abort_flag, p.wait_ns);
     ptx::tc_fence_after();
     return sbase + kSlots + slot * kSlot;
   };
@@ -311,7 +310,7 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
   for (int j = 0; j < n && ok; ++j) {
     if (j + 1 < n) qk(j + 1);
     if (!ok) break;
-    if (!(ok = ptx::mbar_wait_cl(bar(kBarP), j & 1, abort_flag, kWaitLimitNs))) break;
+    if (!(ok = ptx::mbar_wait_cl(bar(kBarP), j & 1, abort_flag, p.wait_ns))) break;
     ptx::tc_fence_after();
     const uint32_t tP = tmem + 128u * (j & 1);  // P of tile j, packed over S
 #pragma unroll 1
@@ -371,7 +370,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
   }
   for (int j = 0; j < n; ++j) {
     const uint32_t tS = tmem + 128u * (j & 1);
-    ok = ptx::mbar_wait(bar(kBarS0 + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs);
+    ok = ptx::mbar_wait(bar(kBarS0 + (j & 1)), (j >> 1) & 1, abort_flag, p.wait_ns);
     if (!ptx::bar_red_and(1, 128, ok)) {
       ok = false;
       break;
@@ -449,7 +448,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
       ptx::tmem_store32(tS + lane_addr, q);
     }
     if (j > 0) {  // O stable (PV of tile j-1 done) before any rescale
-      ok = ptx::mbar_wait(bar(kBarO), (j - 1) & 1, abort_flag, kWaitLimitNs);
+      ok = ptx::mbar_wait(bar(kBarO), (j - 1) & 1, abort_flag, p.wait_ns);
       if (!ptx::bar_red_and(1, 128, ok)) {
         ok = false;
         break;
@@ -475,7 +474,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
       ptx::mbar_arrive_cluster(lead_p);
   }
   if (ok && n > 0) {
-    ok = ptx::mbar_wait(bar(kBarO), (n - 1) & 1, abort_flag, kWaitLimitNs);
+    ok = ptx::mbar_wait(bar(kBarO), (n - 1) & 1, abort_flag, p.wait_ns);
     ok = ptx::bar_red_and(1, 128, ok);
   }
   if (!ok) {
@@ -539,6 +538,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ptx::cluster_ctarank();
+#ifdef AKV_CHECKED
+  {  // both CTAs of the pair check the same two items, so the pair returns together, before any cluster barrier
+    const int b0 = int(blockIdx.x) & ~1;
+    bool ok = b0 + 1 < p.n_work;
+    for (int k = 0; k < 2 && ok; ++k)
+      ok = attn_item_ok(p.work[b0 + k], p.segs, p.runs, p.n_segs, p.n_runs, p.n_q_rows, p.n_pages, p.page,
+                        int(threadIdx.x), int(blockDim.x));
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) report_device_error(p.err, 11, int(blockIdx.x), 0);
+      return;
+    }
+  }
+#endif
   const AttnWork w = p.work[blockIdx.x];
   const AttnSeg seg = p.segs[w.seg];
   if (threadIdx.x == 0) {

@@ -152,12 +152,12 @@ class ClockSampler:
 class Turn:
     """The engine, the resident 32K-token trajectory and the per-step inputs."""
 
-    def __init__(self, seed=0, host_inputs=False, attn_split=0, n_new=2048):
+    def __init__(self, seed=0, host_inputs=False, attn_split=0, n_new=2048, n_layers=1):
         import torch
         from agentic_kv_cache_gb300 import akv, build, runner, synth
         build.build()
         self.torch, self.akv, self.runner = torch, akv, runner
-        self.w = w = synth.llama8b_32k(seed=seed, fork=True, n_new=n_new)
+        self.w = w = synth.llama8b_32k(seed=seed, fork=True, n_new=n_new, n_layers=n_layers)
         s = w.shape
         self.cfg = akv.config_from_shape(s, w.n_pages)
         self.pools = akv.make_pools(self.cfg)
@@ -170,7 +170,7 @@ class Turn:
         self.names = runner.run_ops(self.eng, w, kv_source=src, ops=self.setup_ops, stream=self.stream)
         new_op = next(op for op in self.step_ops if op[0] == "append")
         self.new_k, self.new_v = src(new_op[3], new_op[2])
-        q32 = synth.q_array(w)
+        q32 = synth.q_array(w, 0)
         self.q = torch.from_numpy(q32).cuda().to(torch.bfloat16)
         self.nq = q32.shape[0]
         self.o = torch.empty((self.nq, s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
@@ -189,7 +189,8 @@ class Turn:
                             stream=self.stream)
         segs = self.runner.engine_segments(self.w, names)
         q, o = (self.h_q, self.h_o) if host else (self.q, self.o)
-        self.eng.attend(0, segs, q, self.nq, o, None, self.w.shape.scale, stream=self.stream, fused=fused)
+        for layer in range(self.w.shape.n_layers):
+            self.eng.attend(layer, segs, q, self.nq, o, None, self.w.shape.scale, stream=self.stream, fused=fused)
         self.eng.seq_free(names["F"])
 
     def flush_l2(self):
@@ -359,6 +360,170 @@ def compaction(steps=4, warmup=1, n_layers=32):
     return {"workload": f"llama8b_32k post-drop branch, {n_layers} layers", "fragmentation_before": frag,
             "ms_per_compaction": ms, "bytes_per_compaction": stats["bytes"] / calls, "GB/s": gbs,
             "frac_of_hbm": gbs / load_peaks()[0]}
+
+
+def turn_all_layers(steps=5, warmup=3, n_layers=32):
+    """The headline turn with every layer of the Llama-3.1-8B shape (32 layers): the same fork,
+    20 drops + composed suffix repos, append of 2,048 tokens, one flush (all 32 layers) and segment
+    attention of the 2,048 queries in each of the 32 layers (one Q reused per layer).  This is the
+    TTFT-equivalent of the post-drop turn over the whole model's cache."""
+    import torch
+    t = Turn(n_layers=n_layers)
+    for _ in range(warmup):
+        t.step()
+        t.flush_l2()
+    torch.cuda.synchronize()
+    t.eng.profile_enable(True)
+    ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(t.stream)
+        t.step()
+        b.record(t.stream)
+        t.flush_l2()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    stats = t.eng.profile_read()
+    t.eng.profile_enable(False)
+    assert t.eng.check_device_error(t.stream) == 0
+    del t
+    torch.cuda.empty_cache()
+    hbm, bf16_peak, _, _ = load_peaks()
+    att, rep = stats["segment_attn"], stats["repos_rotate"]
+    att_tf = att["flops"] / max(att["ms"], 1e-9) / 1e9
+    rep_gbs = rep["bytes"] / max(rep["ms"], 1e-9) / 1e6
+    return {"workload": f"llama8b_32k post-drop turn, {n_layers} layers", "ttft_equiv_ms": statistics.median(ms),
+            "attn_ms_per_layer": att["ms"] / max(att["launches"], 1), "attn_TFLOP/s": att_tf,
+            "attn_frac_of_bf16_dense": att_tf / bf16_peak, "flush_ms": rep["ms"] / steps,
+            "flush_bytes": rep["bytes"] / steps, "repos_GB/s": rep_gbs, "repos_frac_of_hbm": rep_gbs / hbm,
+            "kv_write_ms": stats["kv_write"]["ms"] / steps}
+
+
+def sessions_turn(steps=2, warmup=1, n_layers=32):
+    """Eight 64K-token sessions sharing a 4K prefix, 32 layers of the Llama-3.1-8B shape.  A step is
+    one turn of all eight: each session gets a branch (a fork sharing its pages), its 1-4 drop +
+    repos directives (shifts of either sign, composed per token) and its 4-16 x 512 new tokens
+    (kv_write, all layers); one flush rotates every shifted retained key of every branch in all 32
+    layers into copy-on-write pages (repos_rotate); then one segment-batch attention launch per layer
+    covers all 4-16 segments of all eight sessions (512 queries each, nested hidden spans), 32
+    layers; the branches are released.  Inputs (new K/V, one Q reused per layer) are resident."""
+    import torch
+    from agentic_kv_cache_gb300 import akv, runner, synth
+    w = synth.sessions_64k(n_layers=n_layers)
+    s = w.shape
+    per = {}
+    for op in w.ops:
+        if op[0] == "append" and op[3].startswith("hist"):
+            per[op[1]] = op[2]
+    extra = sum(-(-n // s.page_size) + 1 for n in per.values())   # copy-on-write K pages of the branches
+    cfg = akv.config_from_shape(s, w.n_pages + extra + 64)
+    pools = akv.make_pools(cfg)
+    eng = akv.Engine(cfg, pools)
+    st = torch.cuda.current_stream()
+    src = runner.torch_device_kv_source(w)
+    setup, turn = [], []
+    for op in w.ops:
+        if op[0] in ("drop", "repos") or (op[0] == "append" and op[3].startswith("new")):
+            turn.append(op)
+        else:
+            setup.append(op)
+    names = runner.run_ops(eng, w, kv_source=src, ops=setup, stream=st)
+    kv = {op[3]: src(op[3], op[2]) for op in turn if op[0] == "append"}
+    nq = w.n_queries
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(11)
+    q = torch.randn((nq, s.n_q_heads, s.d_rot), generator=gen, device="cuda").to(torch.bfloat16)
+    o = torch.empty((nq, s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
+    seq_len = {n: eng.seq_len(names[n]) for n in per}
+    torch.cuda.synchronize()
+
+    def step():
+        br = {n: eng.seq_fork(names[n], seq_len[n]) for n in per}
+        runner.run_ops(eng, w, kv_source=lambda key, n: kv[key], ops=turn, names=br, stream=st)
+        eng.flush(-1, stream=st)
+        segs = runner.engine_segments(w, br)
+        for layer in range(s.n_layers):
+            eng.attend(layer, segs, q, nq, o, None, s.scale, stream=st)
+        for n in per:
+            eng.seq_free(br[n])
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    eng.profile_enable(True)
+    ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        step()
+        b.record(st)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    stats = eng.profile_read()
+    eng.profile_enable(False)
+    assert eng.check_device_error(st) == 0
+    del eng, pools, kv, q, o
+    torch.cuda.empty_cache()
+    hbm, bf16_peak, bf16_sus, _ = load_peaks()
+    att, rep, kvw = stats["segment_attn"], stats["repos_rotate"], stats["kv_write"]
+    att_tf = att["flops"] / max(att["ms"], 1e-9) / 1e9
+    rep_gbs = rep["bytes"] / max(rep["ms"], 1e-9) / 1e6
+    return {"workload": f"sessions_64k: 8 sessions x 64K tokens sharing a 4K prefix, {n_layers} layers, 32 q / 8 kv heads, "
+                        f"d 128; {len(w.segments)} segments x 512 queries; directives per session 1-4",
+            "segments": len(w.segments), "queries": nq, "ms_per_turn": statistics.median(ms),
+            "attn_ms_per_layer": att["ms"] / max(att["launches"], 1),
+            "attn_flops_per_layer": att["flops"] / max(att["launches"], 1), "attn_TFLOP/s": att_tf,
+            "attn_frac_of_bf16_dense": att_tf / bf16_peak,
+            "attn_frac_of_bf16_sustained": att_tf / bf16_sus if bf16_sus else None,
+            "flush_ms": rep["ms"] / steps, "flush_bytes": rep["bytes"] / steps, "repos_GB/s": rep_gbs,
+            "repos_frac_of_hbm": rep_gbs / hbm, "rotated_token_layers_per_s": rep["bytes"] / 4096 / max(rep["ms"], 1e-9) * 1e3,
+            "kv_write_ms": kvw["ms"] / steps}
+
+
+def branches_128k(n_layers=80, reps=1):
+    """Segment-batch attention on the Llama-3.1-70B-shaped 128K cache (80 layers, 64 q / 8 kv heads,
+    d 128): the 64 spans repositioned in place (shifts in +-64K), then 32 branches (forks sharing every
+    page) each append 1,024 new tokens and attend as one segment hiding a seeded quarter of the spans;
+    one launch per layer covers the 32 segments (32K query rows over ~100K visible keys each).  Every
+    layer is timed once (one Q reused per layer)."""
+    import torch
+    from agentic_kv_cache_gb300 import akv, runner, synth
+    w = synth.llama70b_128k(n_layers=n_layers)
+    s = w.shape
+    cfg = akv.config_from_shape(s, w.n_pages)
+    pools = akv.make_pools(cfg)
+    eng = akv.Engine(cfg, pools)
+    st = torch.cuda.current_stream()
+    names = runner.run_ops(eng, w, kv_source=runner.torch_device_kv_source(w), stream=st)
+    nq = w.n_queries
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(12)
+    q = torch.randn((nq, s.n_q_heads, s.d_rot), generator=gen, device="cuda").to(torch.bfloat16)
+    o = torch.empty((nq, s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
+    segs = runner.engine_segments(w, names)
+    eng.attend(0, segs, q, nq, o, None, s.scale, stream=st)
+    torch.cuda.synchronize()
+    eng.profile_enable(True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        for layer in range(n_layers):
+            eng.attend(layer, segs, q, nq, o, None, s.scale, stream=st)
+    b.record(st)
+    torch.cuda.synchronize()
+    att = eng.profile_read()["segment_attn"]
+    eng.profile_enable(False)
+    assert eng.check_device_error(st) == 0
+    del eng, pools, q, o
+    torch.cuda.empty_cache()
+    _, bf16_peak, bf16_sus, _ = load_peaks()
+    tf = att["flops"] / max(att["ms"], 1e-9) / 1e9
+    return {"workload": f"llama70b_128k: 32 branches x 1,024 queries over 131,072 keys (a quarter of the spans "
+                        f"hidden per branch), 64 q / 8 kv heads, d 128, {n_layers} layers",
+            "ms_all_layers": a.elapsed_time(b) / reps, "attn_ms_per_layer": att["ms"] / max(att["launches"], 1),
+            "attn_flops_per_layer": att["flops"] / max(att["launches"], 1), "attn_TFLOP/s": tf,
+            "attn_frac_of_bf16_dense": tf / bf16_peak,
+            "attn_frac_of_bf16_sustained": tf / bf16_sus if bf16_sus else None}
 
 
 def mass_pass(t, reps=5):
@@ -601,6 +766,9 @@ def gpu_arm(args, rank, world):
     if not args.no_sweep:
         line["repos_rotate_sweep"] = repos_sweep(steps=4, n_layers=args.sweep_layers)
     if not args.no_extra:
+        line["turn_32_layers"] = turn_all_layers()
+        line["sessions_64k_turn"] = sessions_turn()
+        line["llama70b_128k_attention"] = branches_128k()
         line["mla_dsv2lite_turn"] = mla_turns()
         line["compact_copy"] = compaction()
     if world == 1 and not args.no_cpu_baseline:
@@ -816,6 +984,10 @@ def main():
                     help="run only the MLA turn at concurrency C (for profiling)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the re-prefill equivalent and the MLA per-concurrency turns")
+    ap.add_argument("--only-leg", default="", choices=["", "turn32", "sessions", "branches128k"],
+                    help="run only one measurement leg (for profiling): the 32-layer 32K turn, the 8 x 64K "
+                         "sessions turn, or the 128K branches' attention")
+    ap.add_argument("--leg-layers", type=int, default=0, help="layers of the --only-leg workload (0: full)")
     ap.add_argument("--attn-split", type=int, default=0,
                     help="KV chunks per attention work item: 0 chooses automatically, 1 never splits")
     args = ap.parse_args()
@@ -828,6 +1000,20 @@ def main():
         from agentic_kv_cache_gb300 import build
         build.build()
         print(json.dumps(mla_turns((args.only_mla,), steps=args.steps, warmup=args.warmup)), flush=True)
+        return
+    if args.only_leg:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        from agentic_kv_cache_gb300 import build
+        build.build()
+        L = args.leg_layers
+        if args.only_leg == "turn32":
+            out = turn_all_layers(steps=args.steps, warmup=args.warmup, n_layers=L or 32)
+        elif args.only_leg == "sessions":
+            out = sessions_turn(steps=args.steps, warmup=args.warmup, n_layers=L or 32)
+        else:
+            out = branches_128k(n_layers=L or 80)
+        print(json.dumps(out), flush=True)
         return
     if args.only_sweep:
         import torch

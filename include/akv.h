@@ -411,6 +411,33 @@ AKV_API akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* c
  * many chunks per item (1 = never split). */
 AKV_API akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split);
 
+/* Test hook for the bounded waits of the attention kernels (no counterpart
+ * on the pages: every device-side wait gives up after a time limit, records
+ * AKV_ERR_DEVICE_TIMEOUT in the device error word, drains its copies and
+ * tensor-core work, frees its TMEM and exits, so a stuck launch reports an
+ * error instead of hanging the GPU).  wait_ns: the limit of every wait in
+ * later akv_attend / akv_attend_fused launches (0 restores the default,
+ * 4 s).  load_cap >= 0 (GQA layout only): the copy-issuing thread of each CTA
+ * issues at most that many K/V tile copies and then stops, so the waits for
+ * the missing tiles run out; -1 (default) removes the cap.  A test sets a
+ * short limit and a cap, checks akv_check_device_error for
+ * AKV_ERR_DEVICE_TIMEOUT and that the context still works after restoring
+ * (0, -1).  AKV_ERR_ARG for load_cap < -1. */
+AKV_API akv_status akv_debug_wait_limit(akv_ctx* ctx, uint64_t wait_ns, int32_t load_cap);
+
+/* Test hook of the checked build (libakv_checked.so, compiled with
+ * -DAKV_CHECKED; no counterpart on the pages).  That build adds device-side
+ * descriptor checks to every kernel: a descriptor naming a page outside the
+ * pool, a row range outside a page, a segment or run outside its table or
+ * query rows outside Q makes the kernel record AKV_ERR_DEVICE in the device
+ * error word and skip the work it names (attention: the CTA returns before
+ * touching memory), never a trap.  Host validation normally keeps such
+ * descriptors away from the device, so this call corrupts one after it:
+ * what = 1, the next flush's first run gets a row range ending past its page;
+ * what = 2, the next attention launch's first run gets a K page outside the
+ * pool; 0 cancels.  The plain library returns AKV_ERR_ARG. */
+AKV_API akv_status akv_debug_corrupt(akv_ctx* ctx, int32_t what);
+
 /* Enable (1) or disable (0) per-launch CUDA-event timing of the context's
  * kernels; enabling clears the statistics. */
 AKV_API akv_status akv_profile_enable(akv_ctx* ctx, int32_t on);

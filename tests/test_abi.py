@@ -91,3 +91,16 @@ def test_metadata_only_attend_plans_without_device(lib):
     e.attend(0, [dict(seq=s, kv_end=64, q_len=4)], None, 4, None)   # flushes; no data touched
     assert (e.export_state(s)["delta"] == 0).all()
     assert len(e.last_flush_runs()) == 4
+
+
+def test_checked_build_exports_every_symbol_and_plain_build_refuses_the_hook(lib):
+    # the -DAKV_CHECKED variant (device-side descriptor checks) builds and exports the same ABI;
+    # its corruption hook is refused by the plain library
+    path = build.build(checked=True)
+    raw = ctypes.CDLL(path)
+    for n in declared_symbols():
+        getattr(raw, n)
+    eng = akv.Engine(cfg(), None)
+    with pytest.raises(akv.AKVError) as e:
+        eng.debug_corrupt(1)
+    assert e.value.code == "ARG"

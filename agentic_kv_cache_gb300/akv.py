@@ -116,6 +116,7 @@ def load(path=LIB_PATH):
         "akv_set_attention_split": [P, I32],
         "akv_debug_wait_limit": [P, ctypes.c_uint64, I32],
         "akv_debug_corrupt": [P, I32],
+        "akv_set_output_stream": [P, P],
         "akv_profile_read": [P, ctypes.POINTER(KernelStats)],
     }
     for name, args in sig.items():
@@ -345,6 +346,11 @@ class Engine:
         """0: automatic split-KV; n >= 1: exactly n KV chunks per work item (1 = never split).
         Applies to attend and attention_mass."""
         self._check(self.lib.akv_set_attention_split(self.h, int(split)))
+
+    def set_output_stream(self, stream=None):
+        """Copy host results (o, lse, mass) on `stream` (a torch stream or raw handle) after the
+        call's kernels, so they overlap later calls; None: on the call's own stream."""
+        self._check(self.lib.akv_set_output_stream(self.h, _stream(stream) if stream is not None else None))
 
     def debug_corrupt(self, what):
         """Checked-build test hook: 1 corrupts the next flush's first run, 2 the next attention

@@ -383,6 +383,8 @@ struct akv_ctx {
   akv::DevErr* dev_err = nullptr;
   Uploader up;
   Staging st_k, st_v, st_q, st_o, st_lse;
+  cudaStream_t out_st = nullptr;     // akv_set_output_stream: where results are copied to host memory
+  cudaEvent_t out_ready = nullptr;
   cudaStream_t copy_st = nullptr;  // host-to-device copies of inputs and descriptor tables
   Staging partial;         // split-KV partial results (device only)
   int n_sm = 148;          // SMs of the device, for split decisions
@@ -1656,15 +1658,31 @@ struct akv_ctx {
     up.done(st);
     if (n_parts > 0) partial.release(st);
     if (st_q.dev && !is_device_ptr(q)) st_q.release(st);
+    const cudaStream_t ost = output_stream(st);
     if (o_host) {
-      cuda_check(cudaMemcpyAsync(o, od, obytes, cudaMemcpyDeviceToHost, st), "O copy to host");
-      st_o.release(st);
+      cuda_check(cudaMemcpyAsync(o, od, obytes, cudaMemcpyDeviceToHost, ost), "O copy to host");
+      st_o.release(ost);
     }
     if (lse_host) {
-      cuda_check(cudaMemcpyAsync(lse, lsed, size_t(n_q_rows) * cfg.n_q_heads * 4, cudaMemcpyDeviceToHost, st),
+      cuda_check(cudaMemcpyAsync(lse, lsed, size_t(n_q_rows) * cfg.n_q_heads * 4, cudaMemcpyDeviceToHost, ost),
                  "LSE copy to host");
-      st_lse.release(st);
+      st_lse.release(ost);
     }
+  }
+
+  // Stream for copies of results to host memory: the caller's stream, or the
+  // output stream set by akv_set_output_stream, which first waits for
+  // everything enqueued on the caller's stream so far (the kernel that wrote
+  // the result).  Then a result copy overlaps the caller's next kernels.
+  cudaStream_t output_stream(cudaStream_t st) {
+    if (!out_st || out_st == st) return st;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cuda_check(cudaStreamIsCapturing(st, &cs), "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone) return st;
+    if (!out_ready) cuda_check(cudaEventCreateWithFlags(&out_ready, cudaEventDisableTiming), "cudaEventCreate");
+    cuda_check(cudaEventRecord(out_ready, st), "cudaEventRecord");
+    cuda_check(cudaStreamWaitEvent(out_st, out_ready, 0), "cudaStreamWaitEvent");
+    return out_st;
   }
 
   // ---------------------------------------------------------- radix tree
@@ -1937,8 +1955,9 @@ struct akv_ctx {
     if (st_q.dev && !is_device_ptr(q)) st_q.release(st);
     if (st_lse.dev && !is_device_ptr(lse)) st_lse.release(st);
     if (m_host) {
-      cuda_check(cudaMemcpyAsync(mass, md, size_t(mass_len) * 4, cudaMemcpyDeviceToHost, st), "mass copy to host");
-      st_o.release(st);
+      const cudaStream_t ost = output_stream(st);
+      cuda_check(cudaMemcpyAsync(mass, md, size_t(mass_len) * 4, cudaMemcpyDeviceToHost, ost), "mass copy to host");
+      st_o.release(ost);
     }
   }
 
@@ -2016,6 +2035,10 @@ struct akv_ctx {
     st_q.destroy();
     st_o.destroy();
     st_lse.destroy();
+    if (out_ready) {
+      cudaEventDestroy(out_ready);
+      out_ready = nullptr;
+    }
     partial.destroy();
     for (auto& t : timed) {
       cudaEventDestroy(t.a);
@@ -2275,6 +2298,10 @@ akv_status akv_debug_wait_limit(akv_ctx* ctx, uint64_t wait_ns, int32_t load_cap
     ctx->wait_ns = wait_ns ? wait_ns : 4000000000ull;
     ctx->load_cap = load_cap;
   });
+}
+
+akv_status akv_set_output_stream(akv_ctx* ctx, void* stream) {
+  return guard(ctx, [&] { ctx->out_st = static_cast<cudaStream_t>(stream); });
 }
 
 akv_status akv_debug_corrupt(akv_ctx* ctx, int32_t what) {

@@ -16,6 +16,7 @@ independent sessions (weak scaling, no data-path collective); the time is the
 max over ranks.
 """
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -657,37 +658,71 @@ def gpu_arm(args, rank, world):
         t.step()
         t.flush_l2()
     assert t.eng.check_device_error(t.stream) == 0
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier()
-    t.eng.profile_enable(True)
-    for i in range(args.steps):
-        ev[i][0].record(t.stream)
-        t.step()
-        ev[i][1].record(t.stream)
-        t.flush_l2()
-    barrier()
-    stats = t.eng.profile_read()
-    t.eng.profile_enable(False)
-    assert t.eng.check_device_error(t.stream) == 0
-    ms = [a.elapsed_time(b) for a, b in ev]
+
+    # Timed steps: CUDA events around each turn on the turn's stream, the L2
+    # flush between turns outside them.  Python's garbage collector is off
+    # during timed loops (host noise of the harness, not of the library).
+    # The library's per-launch events are off here: each acts as a barrier on
+    # the stream (~13 us per turn); kernel durations come from a second pass.
+    def timed_steps(profile):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier()
+        if profile:
+            t.eng.profile_enable(True)
+        host_s = 0.0
+        gc.disable()
+        for i in range(args.steps):
+            ev[i][0].record(t.stream)
+            h0 = time.perf_counter()
+            t.step()
+            host_s += time.perf_counter() - h0
+            ev[i][1].record(t.stream)
+            t.flush_l2()
+        gc.enable()
+        barrier()
+        st = None
+        if profile:
+            st = t.eng.profile_read()
+            t.eng.profile_enable(False)
+        assert t.eng.check_device_error(t.stream) == 0
+        return [a.elapsed_time(b) for a, b in ev], host_s * 1e3 / args.steps, st
+
+    ms, host_ms, _ = timed_steps(False)
     total_ms = sum(ms)
+    ms_prof, _, stats = timed_steps(True)
 
     # End to end through the C ABI with pinned host buffers: turns run back to
     # back as a serving loop would run them (the host prepares turn i + 1 while
     # the GPU runs turn i); every turn copies its K, V and Q from pinned host
-    # memory and its output back to pinned host memory, and the L2 flush
-    # between turns is inside the timed region.  The latency of one turn on
-    # its own (synchronised before and after) is reported beside it.
-    for _ in range(2):
-        t.step(host=True)
-        t.flush_l2()
-    barrier()
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        t.step(host=True)
-        t.flush_l2()
-    barrier()
-    e2e_total = (time.perf_counter() - t0) * 1e3
+    # memory (on the library's copy stream) and its output back to pinned host
+    # memory on an output stream (akv_set_output_stream), so turn i's output
+    # copy overlaps turn i + 1's kernels; all of it is inside the timed region.
+    # No L2 flush between these turns: a turn touches ~225 MB (the branch's
+    # K/V, its copy-on-write pages, Q, O and the new K/V), more than the
+    # 129 MB L2.  The same loop with the 512 MiB flush between turns (timed)
+    # and the latency of one turn on its own are reported beside it.
+    copy_back = torch.cuda.Stream()
+    t.eng.set_output_stream(copy_back)
+
+    def e2e_loop(flush):
+        for _ in range(2):
+            t.step(host=True)
+            if flush:
+                t.flush_l2()
+        barrier()
+        gc.disable()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            t.step(host=True)
+            if flush:
+                t.flush_l2()
+        barrier()
+        e = (time.perf_counter() - t0) * 1e3
+        gc.enable()
+        return e
+
+    e2e_total = e2e_loop(False)
+    e2e_flushed = e2e_loop(True)
     lat_ms = []
     for i in range(max(3, min(args.steps, 10))):
         t.flush_l2()
@@ -700,7 +735,7 @@ def gpu_arm(args, rank, world):
     clk.stop()
 
     if dist:
-        total_ms, e2e_total = max_over_ranks([total_ms, e2e_total], "cuda")
+        total_ms, e2e_total, e2e_flushed = max_over_ranks([total_ms, e2e_total, e2e_flushed], "cuda")
     if rank != 0:
         return None
 
@@ -743,12 +778,19 @@ def gpu_arm(args, rank, world):
                                "ms_per_launch": att_ms, "flops_per_launch": att_flops},
         "kv_write": {"ms_per_step": kvw["ms"] / args.steps, "GB/s": kvw["bytes"] / max(kvw["ms"], 1e-9) / 1e6},
         "ttft_equiv_ms": total_ms / args.steps,
+        "ms_per_step_median": statistics.median(ms),
+        "host_ms_per_step": host_ms,
+        "kernel_timing": "kernel durations, shares and rooflines from a second pass of the same steps with CUDA "
+                         f"events around every launch ({sum(ms_prof) / args.steps:.4f} ms per turn with them)",
         "kernel_share": {k: v / max(sum(share.values()), 1e-9) for k, v in share.items()},
         "roofline": roof,
         "gpu_launches": int(sum(v["launches"] for v in stats.values())),
         "clocks": clk.summary(),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_total / args.steps, "mode": "turns back to back, L2 flush between turns timed",
+                "ms_per_step": e2e_total / args.steps,
+                "mode": "turns back to back through the C ABI, inputs from and outputs to pinned host memory; "
+                        "no L2 flush (a turn touches ~225 MB > 129 MB L2); output copies on an output stream",
+                "ms_per_step_l2_flushed": e2e_flushed / args.steps,
                 "latency_ms_one_turn": lat_ms[len(lat_ms) // 2]},
     }
     if not args.no_extra:

@@ -402,6 +402,18 @@ AKV_API akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_
  * is cleared after reading.  Returns the same status as *code. */
 AKV_API akv_status akv_check_device_error(akv_ctx* ctx, void* stream, int32_t* code);
 
+/* Where results are copied to host memory.  By default (stream NULL) a host
+ * output of akv_attend / akv_attend_fused (o, lse) or akv_attention_mass
+ * (mass) is copied on the call's own stream, so synchronising that stream
+ * covers it.  With an output stream set, the copy is enqueued on `stream`
+ * (a cudaStream_t) after everything enqueued on the call's stream so far, so
+ * it overlaps the kernels of later calls; the caller then synchronises the
+ * output stream (or an event recorded on it) before reading a host output.
+ * The device staging of a result is reused two calls later, after its copy
+ * has completed.  While the call's stream is being captured into a graph,
+ * results are copied on it.  The stream must stay valid while set. */
+AKV_API akv_status akv_set_output_stream(akv_ctx* ctx, void* stream);
+
 /* Split-KV control for akv_attend and akv_attention_mass.  0 (default): the
  * engine cuts long work items into chunks of KV tiles when that fills the
  * GPU's waves of SMs better; in akv_attend the CTA that finishes an item's

@@ -1,6 +1,7 @@
 """Host buffers through the C ABI: inputs staged into library memory on the
 library's copy stream (ahead of the caller's stream, which waits for each
-copy), outputs copied back on the caller's stream.
+copy), outputs copied back on the caller's stream -- or, with an output stream
+set (akv_set_output_stream), on that stream, overlapping the next turn.
 
 Post-drop turns run back to back on one stream with no synchronisation
 between them, as a serving loop runs them: every turn forks the trajectory,
@@ -34,7 +35,8 @@ class Side:
         self.names = runner.run_ops(self.eng, w, kv_source=src, ops=setup_ops, stream=self.stream)
 
 
-def test_back_to_back_host_turns_match_device_turns():
+@pytest.mark.parametrize("out_stream", [False, True])
+def test_back_to_back_host_turns_match_device_turns(out_stream):
     w = synth.llama8b_32k(total=4096, n_new=300, fork=True)
     s = w.shape
     fork_at = next(i for i, op in enumerate(w.ops) if op[0] == "fork")
@@ -57,6 +59,9 @@ def test_back_to_back_host_turns_match_device_turns():
 
     dev = Side(w, src, setup_ops)
     host = Side(w, src, setup_ops)
+    if out_stream:
+        copy_back = torch.cuda.Stream()
+        host.eng.set_output_stream(copy_back)
     torch.cuda.synchronize()
 
     def turn(side, t, k, v, q, o, lse):

@@ -1195,6 +1195,97 @@ struct akv_ctx {
     }
   }
 
+  // Persistent schedule for the MLA kernel (automatic split): the pair items
+  // (work entries 2k, 2k + 1: one KV range, one output half) are laid end to
+  // end in their order (consecutive items of one segment share its K/V in L2)
+  // as sequences of KV tiles, plus a start cost per unit, and cut into one
+  // equal-cost piece per resident CTA pair (stream-K).  An item crossing a cut
+  // becomes several units whose partials the last to finish merges; no piece
+  // is shorter than kMlaMinTiles (the cut moves instead) and no item is cut
+  // into more than 8 parts (fewer pairs are used until none is).  Pair b runs
+  // units [cta_units[b], cta_units[b + 1]) (unit u = work entries 2u, 2u + 1).
+  static constexpr int64_t kMlaMinTiles = 4;
+  void plan_mla_persistent(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts,
+                           std::vector<int32_t>& cta_units) {
+    const int64_t pair_slots = std::max(1, mla_slots / 2);
+    const size_t n_items = work.size() / 2;
+    const int64_t unit_cost = int64_t(kMlaUnitCost);
+    auto span_of = [&](size_t k) { return int64_t(std::max(1, work[2 * k].n_a)); };
+    int64_t items_cost = 0;
+    for (size_t k = 0; k < n_items; ++k) items_cost += unit_cost + span_of(k);
+    struct Piece {
+      size_t item;
+      int32_t t0, t1;
+    };
+    std::vector<Piece> pieces;
+    std::vector<int32_t> n_of;
+    int64_t n_pairs = std::max<int64_t>(1, std::min<int64_t>(pair_slots, items_cost / (4 * unit_cost)));
+    for (;; --n_pairs) {
+      pieces.clear();
+      cta_units.assign(1, 0);
+      const int64_t total = items_cost + (n_pairs - 1) * unit_cost;  // each cut starts one more unit
+      int64_t acc = 0, pair = 0;
+      auto boundary = [&]() { return (pair + 1) * total / n_pairs; };
+      auto close_pair = [&]() {
+        cta_units.push_back(int32_t(pieces.size()));
+        ++pair;
+      };
+      for (size_t k = 0; k < n_items; ++k) {
+        const int64_t span = span_of(k);
+        int64_t start = 0;
+        acc += unit_cost;
+        int64_t base = acc;  // acc = base + j after j tiles of this item
+        bool close_at_end = false;
+        while (pair < n_pairs - 1 && base + span >= boundary()) {
+          const int64_t j = std::max(boundary() - base, start + kMlaMinTiles);  // tiles up to the cut
+          if (span - j < kMlaMinTiles) {
+            close_at_end = true;  // finish the item in this pair
+            break;
+          }
+          pieces.push_back(Piece{k, int32_t(start), int32_t(j)});
+          close_pair();
+          start = j;
+          base += unit_cost;  // the next piece starts a unit
+        }
+        pieces.push_back(Piece{k, int32_t(start), int32_t(span)});
+        acc = base + span;
+        if (close_at_end && pair < n_pairs - 1) close_pair();
+      }
+      if (cta_units.back() != int32_t(pieces.size())) close_pair();
+      n_of.assign(n_items, 0);
+      int32_t most = 0;
+      for (const Piece& pc : pieces) most = std::max(most, ++n_of[pc.item]);
+      if (most <= 8 || n_pairs == 1) break;
+    }
+    // partial slots and ticket counters of the items cut into several units
+    // (a shadow writes nothing, so owns no parts)
+    std::vector<int32_t> base_of(work.size(), -1), comb_of(work.size(), -1), next_of(n_items, 0);
+    for (size_t k = 0; k < n_items; ++k) {
+      if (n_of[k] < 2) continue;
+      for (size_t m = 0; m < 2; ++m) {
+        if (work[2 * k + m].kvh & akv::kShadow) continue;
+        comb.push_back(akv::CombineItem{n_parts, n_of[k], {0, 0}});
+        base_of[2 * k + m] = n_parts;
+        comb_of[2 * k + m] = int32_t(comb.size()) - 1;
+        n_parts += n_of[k];
+      }
+    }
+    std::vector<akv::AttnWork> units;
+    units.reserve(2 * pieces.size());
+    for (const Piece& pc : pieces) {
+      const int32_t idx = next_of[pc.item]++;
+      for (size_t m = 0; m < 2; ++m) {
+        akv::AttnWork e = work[2 * pc.item + m];
+        e.t0 = pc.t0;
+        e.t1 = pc.t1;
+        e.part = base_of[2 * pc.item + m] >= 0 ? base_of[2 * pc.item + m] + idx : -1;
+        e.comb = comb_of[2 * pc.item + m];
+        units.push_back(e);
+      }
+    }
+    work.swap(units);
+  }
+
   // K-tile ranges of the attention-mass pass.  The lse is final, so a pair
   // item's K tiles can be cut into ranges that run as separate CTAs and add
   // into the same outputs, with no merge.  Every item is cut into S equal
@@ -1550,7 +1641,10 @@ struct akv_ctx {
     std::vector<int32_t> cta_units;  // GQA: persistent schedule, CTA b runs units [cta_units[b], cta_units[b+1])
     int32_t n_parts = 0;
     if (mla) {
-      plan_split(work, comb, n_parts);
+      if (split_override > 0)
+        plan_split(work, comb, n_parts);
+      else
+        plan_mla_persistent(work, comb, n_parts, cta_units);
     } else {
       std::vector<int32_t> seg_seq(static_cast<size_t>(n_segs));
       for (int32_t i = 0; i < n_segs; ++i) seg_seq[size_t(i)] = segs[i].seq;

@@ -22,6 +22,13 @@
 // copies count on the even CTA's barriers); warp 1: TMEM allocation and, in
 // the even CTA, the single-thread MMA issuer; warps 2-5: softmax of the CTA's
 // own rows.  Every wait is bounded.
+//
+// A pair runs a list of units (persistent schedule: the engine cuts the work
+// end to end into one equal piece per resident pair, so a unit may be part
+// of an item whose partials the last part merges).  The ring position and the
+// S / P / O phases continue across units; after a unit's last QK^T MMA the
+// even CTA commits to both CTAs' Q-free barrier, on which each CTA reloads
+// its Q tile for the next unit.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -43,7 +50,6 @@ constexpr int kPe = 64;        // K_pe width
 constexpr int kQChunks = (kLat + kPe) / 64;  // 9 chunks of the QK contraction
 constexpr int kQKRounds = 5;                 // latent chunks in pairs, then K_pe
 constexpr int kPVRounds = 2;                 // one per O quarter
-constexpr int kPerTile = kQKRounds + kPVRounds;
 constexpr int kRing = 5;
 constexpr int kMaxRuns = 8;  // runs per 128-key tile: 128 / page, page >= 16
 constexpr uint32_t kQChunk = 128 * 128;      // 128 rows x 64 bf16
@@ -57,8 +63,8 @@ constexpr uint16_t kBoth = 0x3;  // CTA mask of the pair
 // shared memory layout (bytes)
 constexpr uint32_t kQ = 0;                           // 9 chunks of Q
 constexpr uint32_t kSlots = kQ + kQChunks * kQChunk;  // ring of 16 KiB slots
-constexpr uint32_t kColE = kSlots + kRing * kSlot;    // int32[128]
-constexpr uint32_t kBars = kColE + 128 * 4;
+constexpr uint32_t kColE = kSlots + kRing * kSlot;    // int32[2][128], by tile parity
+constexpr uint32_t kBars = kColE + 2 * 128 * 4;
 constexpr uint32_t kBytes = kBars + 256;
 static_assert(kBytes + 1024 <= 232448, "shared memory");
 
@@ -69,7 +75,7 @@ static_assert(kBytes + 1024 <= 232448, "shared memory");
 // and commits, whose CTA-scope waits are much cheaper on the producer's and
 // the MMA thread's per-unit path.
 enum Bar { kBarQ = 0, kBarFull0, kBarEmpty0 = kBarFull0 + kRing, kBarS0 = kBarEmpty0 + kRing, kBarP = kBarS0 + 2,
-           kBarO, kBarFin, kNumBars };
+           kBarO, kBarQFree, kBarFin, kNumBars };
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 
 __device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
@@ -146,29 +152,27 @@ __device__ __forceinline__ TilePages tile_pages(const int2 (&kv)[kMaxRuns], int 
   return t;
 }
 
-__device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint32_t sbase,
-                                        uint32_t rank, int who, volatile int* abort_flag) {
+__device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t rank, int who,
+                                        volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
   const int rpu = p.page >= 64 ? 1 : 64 / p.page;  // runs per 64-key half
-  const int half = w.n_b;                           // which 256 output columns
   const uint32_t lead_full0 = ptx::mapa(bar(kBarFull0), 0);
+  const uint32_t lead_q = ptx::mapa(bar(kBarQ), 0);
+  const int layer_base = p.layer * p.n_pages;
   if (who == 0) {
     ptx::prefetch_tensormap(&p.q_map);
     ptx::prefetch_tensormap(&p.k_map);
     ptx::prefetch_tensormap(&p.v_map);
     ptx::prefetch_tensormap(&p.k_tile_map);
     ptx::prefetch_tensormap(&p.v_tile_map);
-    const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
-    const uint32_t lead_q = ptx::mapa(bar(kBarQ), 0);
-    if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * kQChunks * kQChunk);
-    for (int c = 0; c < kQChunks; ++c)
-      ptx::tma_load_3d_pair(sbase + kQ + c * kQChunk, &p.q_map, lead_q, c * 64, 0, q_tok0);
   }
-  const int layer_base = p.layer * p.n_pages;
-  const int n_loc = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
-  const int2 first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
+  // the unit being streamed (read by the lambdas below)
+  AttnWork w = p.work[2 * u0 + int(rank)];
+  AttnSeg seg = p.segs[w.seg];
+  int2 first = make_int2(0, 0);
+  int half = 0;  // which 256 output columns
   bool ok = true;
   // One 64-key x 64-column block: keys of half kh of local tile j (pages tp),
   // columns col of K_pe (pe) or of the latent.
@@ -189,7 +193,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
       }
     }
   };
-  int rd = 0;
+  int rd = 0;  // rounds of the key stream so far, over all units
   // Round `kind` (< kQKRounds: QK round, else PV round kind - kQKRounds) of local tile j.
   auto round = [&](int kind, int j, const TilePages& tp) {
     if (ok && rd % kProducers == who) {
@@ -217,32 +221,52 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
     }
     ++rd;
   };
-  int2 raw[kMaxRuns];
-  load_runs(p, seg, w.t0, rpt, first, raw);
-  TilePages cur = tile_pages(raw, p.page, rpu, layer_base), nxt = cur;
-  if (n_loc > 1) {
-    load_runs(p, seg, w.t0 + 1, rpt, first, raw);
-    nxt = tile_pages(raw, p.page, rpu, layer_base);
-  }
-  for (int m = 0; m < kQKRounds; ++m) round(m, 0, cur);
-  for (int b = 0; b < n_loc && ok; ++b) {
-    // runs of tile b + 2 are loaded here and used a block later
-    if (b + 2 < n_loc) load_runs(p, seg, w.t0 + b + 2, rpt, first, raw);
-    if (b + 1 < n_loc)
-      for (int m = 0; m < kQKRounds; ++m) round(m, b + 1, nxt);
-    for (int q = 0; q < kPVRounds; ++q) round(kQKRounds + q, b, cur);
-    cur = nxt;
-    if (b + 2 < n_loc) nxt = tile_pages(raw, p.page, rpu, layer_base);
+  int q_loads = 0;
+  for (int u = u0; u < u1 && ok; ++u) {
+    w = p.work[2 * u + int(rank)];
+    seg = p.segs[w.seg];
+    half = w.n_b;
+    first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
+    const int n_loc = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
+    if (who == 0) {
+      // Q tiles of this unit, once the previous unit's last QK MMA has released
+      // both CTAs' Q buffers (a multicast commit to each CTA's Q-free barrier).
+      if (u > u0 && !(ok = ptx::mbar_wait(bar(kBarQFree), (u - u0 - 1) & 1, abort_flag, p.wait_ns))) break;
+      const int q_tok0 = seg.q_row0 + w.qt0 * tpt;
+      if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * kQChunks * kQChunk);
+      for (int c = 0; c < kQChunks; ++c)
+        ptx::tma_load_3d_pair(sbase + kQ + c * kQChunk, &p.q_map, lead_q, c * 64, 0, q_tok0);
+      ++q_loads;
+    }
+    int2 raw[kMaxRuns];
+    load_runs(p, seg, w.t0, rpt, first, raw);
+    TilePages cur = tile_pages(raw, p.page, rpu, layer_base), nxt = cur;
+    if (n_loc > 1) {
+      load_runs(p, seg, w.t0 + 1, rpt, first, raw);
+      nxt = tile_pages(raw, p.page, rpu, layer_base);
+    }
+    if (n_loc > 0)
+      for (int m = 0; m < kQKRounds; ++m) round(m, 0, cur);
+    for (int b = 0; b < n_loc && ok; ++b) {
+      // runs of tile b + 2 are loaded here and used a block later
+      if (b + 2 < n_loc) load_runs(p, seg, w.t0 + b + 2, rpt, first, raw);
+      if (b + 1 < n_loc)
+        for (int m = 0; m < kQKRounds; ++m) round(m, b + 1, nxt);
+      for (int q = 0; q < kPVRounds; ++q) round(kQKRounds + q, b, cur);
+      cur = nxt;
+      if (b + 2 < n_loc) nxt = tile_pages(raw, p.page, rpu, layer_base);
+    }
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 10, who);
     *abort_flag = 1;
   }
   if (who != 0) return;
-  // Drain (one thread): every round consumed (so every copy into this CTA has
-  // landed) and every multicast commit to this CTA's ring barriers arrived.
-  const int total = kPerTile * n_loc;
-  if (rank == 0) ptx::mbar_wait_drain(bar(kBarQ), 0, kDrainLimitNs);
+  // Drain (one thread): every round issued so far consumed (so every copy
+  // into this CTA has landed) and every multicast commit to this CTA's ring
+  // barriers arrived; the Q barrier's last phase completed.
+  const int total = rd;
+  if (rank == 0 && q_loads) ptx::mbar_wait_drain(bar(kBarQ), (q_loads - 1) & 1, kDrainLimitNs);
 #pragma unroll 1
   for (int s = 0; s < kRing; ++s) {
     const int uses = total > s ? (total - s + kRing - 1) / kRing : 0;
@@ -257,18 +281,16 @@ __device__ __forceinline__ void produce(const AttnParams& p, const AttnWork& w, 
 // keys, 64 from each CTA).  PV: O quarter q (128 columns) += P (256 rows x
 // 128 keys, from each CTA's TMEM) x V (128 keys x 128 columns, 64 from each
 // CTA).
-__device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w, uint32_t sbase, uint32_t tmem,
+__device__ __forceinline__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
                                           volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(2 * kRows, kKeys, false);
   constexpr uint32_t idesc_pv = ptx::idesc_bf16(2 * kRows, 128, true);
   const uint32_t tO = tmem + 256;
-  const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);
   int rd = 0;
   bool issued = false;  // a commit is only issued after this thread's first MMA
-  bool ok = ptx::mbar_wait(bar(kBarQ), 0, abort_flag, p.wait_ns);
-  ptx::tc_fence_after();
+  bool ok = true;
   auto next_round = [&]() -> uint32_t {  // wait for round rd; its slot address
     const int slot = rd % kRing;
     ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kRing) & 1, abort_flag, p.wait_ns);
@@ -289,8 +311,10 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
     for (int ks = 1; ks < 4; ++ks)
       ptx::mma_bf16_pair(tS, ptx::desc_advance(qd, ks * 32), ptx::desc_advance(kd, ks * 32), idesc_qk, 1);
   };
-  auto qk = [&](int j) {
-    const uint32_t tS = tmem + 128u * (j & 1);
+  // S of global tile gt (tiles of earlier units included: the S, P and O
+  // phases continue across units) into S buffer gt & 1.
+  auto qk = [&](int gt) {
+    const uint32_t tS = tmem + 128u * (gt & 1);
 #pragma unroll 1
     for (int m = 0; m < kQKRounds && ok; ++m) {
       const uint32_t kt = next_round();
@@ -304,27 +328,48 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
       issued = true;
       release();
     }
-    if (ok) ptx::mma_commit_pair_mc(bar(kBarS0 + (j & 1)), kBoth);
+    if (ok) ptx::mma_commit_pair_mc(bar(kBarS0 + (gt & 1)), kBoth);
   };
-  if (ok && n > 0) qk(0);
-  for (int j = 0; j < n && ok; ++j) {
-    if (j + 1 < n) qk(j + 1);
-    if (!ok) break;
-    if (!(ok = ptx::mbar_wait_cl(bar(kBarP), j & 1, abort_flag, p.wait_ns))) break;
+  int g = 0;  // tiles of earlier units
+  for (int u = u0; u < u1 && ok; ++u) {
+    const AttnWork w = p.work[2 * u];
+    const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);
+    const bool more = u + 1 < u1;
+    if (!(ok = ptx::mbar_wait(bar(kBarQ), (u - u0) & 1, abort_flag, p.wait_ns))) break;
     ptx::tc_fence_after();
-    const uint32_t tP = tmem + 128u * (j & 1);  // P of tile j, packed over S
-#pragma unroll 1
-    for (int q = 0; q < kPVRounds && ok; ++q) {
-      const uint32_t vt = next_round();
-      if (!ok) break;
-      const uint64_t vd = ptx::smem_desc(vt, kSlot, 1024);
-      ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP, vd, idesc_pv, j > 0);
-#pragma unroll
-      for (int ks = 1; ks < kKeys / 16; ++ks)
-        ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
-      release();
+    // After the unit's last QK MMA both CTAs may reload their Q tiles.
+    auto q_free = [&](int j) {
+      if (ok && more && j == n - 1) ptx::mma_commit_pair_mc(bar(kBarQFree), kBoth);
+    };
+    if (n > 0) {
+      qk(g);
+      q_free(0);
     }
-    if (ok) ptx::mma_commit_pair_mc(bar(kBarO), kBoth);
+    for (int j = 0; j < n && ok; ++j) {
+      if (j + 1 < n) {
+        qk(g + j + 1);
+        q_free(j + 1);
+      }
+      if (!ok) break;
+      if (!(ok = ptx::mbar_wait_cl(bar(kBarP), (g + j) & 1, abort_flag, p.wait_ns))) break;
+      ptx::tc_fence_after();
+      const uint32_t tP = tmem + 128u * ((g + j) & 1);  // P of tile j, packed over S
+#pragma unroll 1
+      for (int q = 0; q < kPVRounds && ok; ++q) {
+        const uint32_t vt = next_round();
+        if (!ok) break;
+        const uint64_t vd = ptx::smem_desc(vt, kSlot, 1024);
+        // the unit's first PV overwrites O: the softmax threads arrived on P
+        // only after reading out the previous unit's O
+        ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP, vd, idesc_pv, j > 0);
+#pragma unroll
+        for (int ks = 1; ks < kKeys / 16; ++ks)
+          ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
+        release();
+      }
+      if (ok) ptx::mma_commit_pair_mc(bar(kBarO), kBoth);
+    }
+    g += n;
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 11, 0);
@@ -337,9 +382,8 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, const AttnWork& w
 }
 
 // ----------------------------------------------------------------- softmax
-__device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, const AttnSeg& seg, uint8_t* smem,
-                                        uint32_t sbase, uint32_t tmem, uint32_t rank, volatile int* abort_flag) {
-  const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
+__device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uint8_t* smem, uint32_t sbase,
+                                        uint32_t tmem, uint32_t rank, volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int quad = (threadIdx.x / 32) & 3;  // warps 2..5 -> TMEM lane quadrants 2, 3, 0, 1
@@ -349,17 +393,21 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
   const uint32_t tO = tmem + 256;
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
   const int t_loc = r / G, g = r % G;
-  const int qi = w.qt0 * tpt + t_loc;
-  const bool row_valid = qi < seg.q_len;
-  const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
   const float sl2 = p.scale_log2;
-  int* colE = reinterpret_cast<int*>(smem + kColE);
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
   const int sl_own = r & (p.page - 1);
   const uint32_t lead_p = ptx::mapa(bar(kBarP), 0);  // P barrier of the even CTA
-  float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
+  int gbase = 0;  // tiles of earlier units: the S, P and O phases continue across units
+  for (int u = u0; u < u1; ++u) {
+  const AttnWork w = p.work[2 * u + int(rank)];
+  const AttnSeg seg = p.segs[w.seg];
+  const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
+  const int qi = w.qt0 * tpt + t_loc;
+  const bool row_valid = qi < seg.q_len;
+  const int lim = seg.kv_len - seg.q_len + (row_valid ? qi : seg.q_len - 1);
+  float m_run = -INFINITY, l_run = 0.f;
   // (lohi, es) of the run holding key column r of the current tile, fetched one tile ahead;
   // lo = hi = 0 past the segment's last run, so no slot matches
   const int2* run_le = reinterpret_cast<const int2*>(p.runs + seg.run_off);
@@ -369,12 +417,16 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     if (ri0 < seg.n_runs) run_cur = run_le[2 * ri0 + 1];
   }
   for (int j = 0; j < n; ++j) {
-    const uint32_t tS = tmem + 128u * (j & 1);
-    ok = ptx::mbar_wait(bar(kBarS0 + (j & 1)), (j >> 1) & 1, abort_flag, p.wait_ns);
+    const int gt = gbase + j;
+    const uint32_t tS = tmem + 128u * (gt & 1);
+    ok = ptx::mbar_wait(bar(kBarS0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.wait_ns);
     if (!ptx::bar_red_and(1, 128, ok)) {
       ok = false;
       break;
     }
+    // Column entries go to the buffer of this tile's parity: the other buffer
+    // may still be read by a thread finishing the previous tile.
+    int* colE = reinterpret_cast<int*>(smem + kColE) + (gt & 1) * 128;
     int e = INT_MAX;  // entry index of key column r (INT_MAX: none)
     {
       const int lo = run_cur.x & 0xffff, hi = run_cur.x >> 16;
@@ -448,7 +500,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
       ptx::tmem_store32(tS + lane_addr, q);
     }
     if (j > 0) {  // O stable (PV of tile j-1 done) before any rescale
-      ok = ptx::mbar_wait(bar(kBarO), (j - 1) & 1, abort_flag, p.wait_ns);
+      ok = ptx::mbar_wait(bar(kBarO), (gt - 1) & 1, abort_flag, p.wait_ns);
       if (!ptx::bar_red_and(1, 128, ok)) {
         ok = false;
         break;
@@ -474,7 +526,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
       ptx::mbar_arrive_cluster(lead_p);
   }
   if (ok && n > 0) {
-    ok = ptx::mbar_wait(bar(kBarO), (n - 1) & 1, abort_flag, p.wait_ns);
+    ok = ptx::mbar_wait(bar(kBarO), (gbase + n - 1) & 1, abort_flag, p.wait_ns);
     ok = ptx::bar_red_and(1, 128, ok);
   }
   if (!ok) {
@@ -483,9 +535,11 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     return;
   }
   ptx::tc_fence_after();
-  if (w.kvh & kShadow) return;  // stand-in for a missing query tile: computes, writes nothing
+  // A shadow (stand-in for a missing query tile) computes and writes nothing.
+  // The next unit's first PV overwrites O only after this unit's O is read
+  // out here: this thread arrives on its first P after the epilogue.
   const int half = w.n_b;
-  if (w.part >= 0) {
+  if (!(w.kvh & kShadow) && w.part >= 0) {
     // Split part: unnormalised O half, running max and sum, [column][row] layout.
     float* base = p.partial + w.part * partial_floats(1, 256) + r;
 #pragma unroll 1
@@ -501,30 +555,33 @@ __device__ __forceinline__ void softmax(const AttnParams& p, const AttnWork& w, 
     merge_if_last<256>(p, w, 0, r, 1,
                        row_valid ? static_cast<__nv_bfloat16*>(p.o) + row * kLat + 256 * half : nullptr,
                        row_valid && p.lse && half == 0 ? p.lse + row : nullptr);
-    return;
-  }
-  const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-  __nv_bfloat16* orow =
-      static_cast<__nv_bfloat16*>(p.o) + (int64_t(seg.q_row0 + qi) * p.hq + g) * kLat + 256 * half;
+  } else if (!(w.kvh & kShadow)) {
+    const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+    __nv_bfloat16* orow =
+        static_cast<__nv_bfloat16*>(p.o) + (int64_t(seg.q_row0 + qi) * p.hq + g) * kLat + 256 * half;
 #pragma unroll 1
-  for (int c = 0; c < 256 / 32; ++c) {
-    uint32_t o[32];
-    ptx::tmem_load32(tO + lane_addr + c * 32, o);
-    if (row_valid) {
+    for (int c = 0; c < 256 / 32; ++c) {
+      uint32_t o[32];
+      ptx::tmem_load32(tO + lane_addr + c * 32, o);
+      if (row_valid) {
 #pragma unroll
-      for (int k = 0; k < 32; k += 8) {
-        uint4 v;
-        v.x = pack_bf16(__uint_as_float(o[k + 0]) * inv, __uint_as_float(o[k + 1]) * inv);
-        v.y = pack_bf16(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
-        v.z = pack_bf16(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
-        v.w = pack_bf16(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
-        *reinterpret_cast<uint4*>(orow + c * 32 + k) = v;
+        for (int k = 0; k < 32; k += 8) {
+          uint4 v;
+          v.x = pack_bf16(__uint_as_float(o[k + 0]) * inv, __uint_as_float(o[k + 1]) * inv);
+          v.y = pack_bf16(__uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+          v.z = pack_bf16(__uint_as_float(o[k + 4]) * inv, __uint_as_float(o[k + 5]) * inv);
+          v.w = pack_bf16(__uint_as_float(o[k + 6]) * inv, __uint_as_float(o[k + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + c * 32 + k) = v;
+        }
       }
     }
+    if (row_valid && p.lse && half == 0) {
+      const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      p.lse[int64_t(seg.q_row0 + qi) * p.hq + g] = lse;
+    }
   }
-  if (row_valid && p.lse && half == 0) {
-    const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
-    p.lse[int64_t(seg.q_row0 + qi) * p.hq + g] = lse;
+  ptx::tc_fence_before();  // the O reads above precede this thread's next arrive on P
+  gbase += n;
   }
 }
 
@@ -538,12 +595,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + 8 * kNumBars + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ptx::cluster_ctarank();
+  // The pair runs units [u0, u1); unit u is work entries 2u (even CTA) and 2u + 1.
+  const int pair = int(blockIdx.x) >> 1;
+  const int u0 = p.cta_units ? p.cta_units[pair] : pair;
+  const int u1 = p.cta_units ? p.cta_units[pair + 1] : pair + 1;
 #ifdef AKV_CHECKED
-  {  // both CTAs of the pair check the same two items, so the pair returns together, before any cluster barrier
-    const int b0 = int(blockIdx.x) & ~1;
-    bool ok = b0 + 1 < p.n_work;
-    for (int k = 0; k < 2 && ok; ++k)
-      ok = attn_item_ok(p.work[b0 + k], p.segs, p.runs, p.n_segs, p.n_runs, p.n_q_rows, p.n_pages, p.page,
+  {  // both CTAs of the pair check the same items, so the pair returns together, before any cluster barrier
+    bool ok = u0 >= 0 && u0 < u1 && 2 * u1 <= p.n_work;
+    for (int k = 2 * u0; ok && k < 2 * u1; ++k)
+      ok = attn_item_ok(p.work[k], p.segs, p.runs, p.n_segs, p.n_runs, p.n_q_rows, p.n_pages, p.page,
                         int(threadIdx.x), int(blockDim.x));
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) report_device_error(p.err, 11, int(blockIdx.x), 0);
@@ -551,8 +611,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 #endif
-  const AttnWork w = p.work[blockIdx.x];
-  const AttnSeg seg = p.segs[w.seg];
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, i == kBarP ? 2 * 128 : 1);
     *abort_flag = 0;
@@ -568,11 +626,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp == 0 || warp >= 6) {
-    if (lane == 0) produce(p, w, seg, sbase, rank, warp == 0 ? 0 : warp - 5, abort_flag);
+    if (lane == 0) produce(p, u0, u1, sbase, rank, warp == 0 ? 0 : warp - 5, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) issue_mma(p, w, sbase, tmem, abort_flag);
+    if (lane == 0 && rank == 0) issue_mma(p, u0, u1, sbase, tmem, abort_flag);
   } else {
-    softmax(p, w, seg, smem, sbase, tmem, rank, abort_flag);
+    softmax(p, u0, u1, smem, sbase, tmem, rank, abort_flag);
   }
   ptx::tc_fence_before();
   __syncwarp();
@@ -607,10 +665,11 @@ int segment_attn_mla_slots() {
 cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st) {
   if (p.n_work <= 0) return cudaSuccess;
   if (p.n_work % 2) return cudaErrorInvalidValue;  // CTA pairs
+  const int grid = p.cta_units ? 2 * p.n_cta : p.n_work;  // persistent: one CTA pair per unit list
   const int smem = int(kBytes) + 1024;
   cudaError_t e = cudaFuncSetAttribute(segment_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  segment_attn_mla_kernel<<<p.n_work, kThreads, smem, st>>>(p);
+  segment_attn_mla_kernel<<<grid, kThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -28,6 +28,13 @@ class AKVError(RuntimeError):
         self.code = STATUS_NAMES.get(status, str(status))
 
 
+EDIT_DROP, EDIT_REPOS = 1, 2
+
+
+class EditOp(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("delta", ctypes.c_int32), ("s", ctypes.c_int64), ("e", ctypes.c_int64)]
+
+
 class Config(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("d_rot", ctypes.c_int32), ("d_v", ctypes.c_int32),
@@ -95,6 +102,7 @@ def load(path=LIB_PATH):
         "akv_append": [P, I32, I64, P, P, P, P],
         "akv_drop": [P, I32, I64, I64],
         "akv_repos": [P, I32, I64, I64, I32],
+        "akv_edit": [P, I32, ctypes.POINTER(EditOp), I32],
         "akv_splice": [P, I32, I64, I64, I64, P, P, P, P],
         "akv_flush": [P, I32, P],
         "akv_attend": [P, I32, ctypes.POINTER(Segment), I32, P, I64, P, P, F32, P],
@@ -221,6 +229,18 @@ class Engine:
 
     def repos(self, seq, s, e, delta):
         self._check(self.lib.akv_repos(self.h, seq, s, e, delta))
+
+    def edit(self, seq, ops):
+        """A list of ("drop", s, e) / ("repos", s, e, delta) directives in one call, all or nothing."""
+        arr = (EditOp * max(len(ops), 1))()
+        for i, op in enumerate(ops):
+            if op[0] == "drop":
+                arr[i] = EditOp(EDIT_DROP, 0, op[1], op[2])
+            elif op[0] == "repos":
+                arr[i] = EditOp(EDIT_REPOS, op[3], op[1], op[2])
+            else:
+                arr[i] = EditOp(0, 0, op[1], op[2])  # rejected by the library
+        self._check(self.lib.akv_edit(self.h, seq, arr, len(ops)))
 
     def splice(self, seq, s, e, n_stub, k=None, v=None, pos=None, stream=None):
         keep, pp = _i32_array(pos, n_stub)

@@ -649,6 +649,47 @@ struct akv_ctx {
     grow_bound(sid, std::abs(int64_t(delta)));
   }
 
+  // A list of drop / repos directives for one sequence, in order, all or
+  // nothing: every span is checked first (drops and repositions do not change
+  // the sequence's length); when the running bound shows no token can leave
+  // int32 every reposition is an O(1) record and nothing else can fail;
+  // otherwise the sequence's state is saved and restored if a later entry
+  // fails its overflow check.
+  void edit(int32_t sid, const akv_edit_op* ops, int32_t n) {
+    if (n < 0 || (n > 0 && !ops)) fail(AKV_ERR_ARG, "bad edit list");
+    auto& toks = seq_raw(sid);
+    int64_t shift_sum = 0;
+    for (int32_t i = 0; i < n; ++i) {
+      const akv_edit_op& o = ops[i];
+      if (o.kind != AKV_EDIT_DROP && o.kind != AKV_EDIT_REPOS) fail(AKV_ERR_ARG, "edit %d: unknown kind %d", i, o.kind);
+      check_span(toks, o.s, o.e, o.kind == AKV_EDIT_DROP ? "drop" : "repos");
+      if (o.kind == AKV_EDIT_REPOS) shift_sum += std::abs(int64_t(o.delta));
+    }
+    const bool safe = bound[sid] + shift_sum <= kI32Max;
+    std::vector<Tok> saved_toks;
+    std::vector<Pend> saved_pend;
+    const int64_t saved_bound = bound[sid];
+    if (!safe) {
+      saved_toks = toks;
+      saved_pend = pend[sid];
+    }
+    try {
+      for (int32_t i = 0; i < n; ++i) {
+        if (ops[i].kind == AKV_EDIT_DROP)
+          drop(sid, ops[i].s, ops[i].e);
+        else
+          repos(sid, ops[i].s, ops[i].e, ops[i].delta);
+      }
+    } catch (...) {
+      if (!safe) {
+        seqs[sid] = std::move(saved_toks);
+        pend[sid] = std::move(saved_pend);
+        bound[sid] = saved_bound;
+      }
+      throw;
+    }
+  }
+
   void splice(int32_t sid, int64_t s, int64_t e, int64_t n_stub, const void* k, const void* v, const int32_t* pos,
               cudaStream_t st) {
     auto& toks = seq(sid);
@@ -2232,6 +2273,10 @@ akv_status akv_drop(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e) {
 
 akv_status akv_repos(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int32_t delta) {
   return guard(ctx, [&] { ctx->repos(seq, s, e, delta); });
+}
+
+akv_status akv_edit(akv_ctx* ctx, int32_t seq, const akv_edit_op* ops, int32_t n_ops) {
+  return guard(ctx, [&] { ctx->edit(seq, ops, n_ops); });
 }
 
 akv_status akv_splice(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int64_t n_stub, const void* k_stub,

@@ -37,10 +37,22 @@ def torch_device_kv_source(w, device="cuda"):
 
 
 def run_ops(engine, w, kv_source=None, stream=None, ops=None, names=None):
-    """Replay ops on the engine; kv_source(key, n) -> (k, v) or None for metadata-only engines."""
+    """Replay ops on the engine; kv_source(key, n) -> (k, v) or None for metadata-only engines.
+    Consecutive drop / repos ops on one sequence go to the engine as one akv_edit call."""
     names = {} if names is None else names
-    for op in (w.ops if ops is None else ops):
+    ops = list(w.ops if ops is None else ops)
+    i = 0
+    while i < len(ops):
+        op = ops[i]
         kind = op[0]
+        if kind in ("drop", "repos"):
+            j = i
+            while j < len(ops) and ops[j][0] in ("drop", "repos") and ops[j][1] == op[1]:
+                j += 1
+            engine.edit(names[op[1]], [(o[0],) + tuple(o[2:]) for o in ops[i:j]])
+            i = j
+            continue
+        i += 1
         if kind == "alloc":
             names[op[1]] = engine.seq_alloc()
         elif kind == "fork":
@@ -48,10 +60,6 @@ def run_ops(engine, w, kv_source=None, stream=None, ops=None, names=None):
         elif kind == "append":
             k, v = kv_source(op[3], op[2]) if kv_source else (None, None)
             engine.append(names[op[1]], op[2], k, v, stream=stream)
-        elif kind == "drop":
-            engine.drop(names[op[1]], op[2], op[3])
-        elif kind == "repos":
-            engine.repos(names[op[1]], op[2], op[3], op[4])
         elif kind == "splice":
             k, v = kv_source(op[5], op[4]) if kv_source else (None, None)
             engine.splice(names[op[1]], op[2], op[3], op[4], k, v, stream=stream)

@@ -208,6 +208,21 @@ AKV_API akv_status akv_drop(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e);
  * keys are rotated once, by the composed shift, at the next flush. */
 AKV_API akv_status akv_repos(akv_ctx* ctx, int32_t seq, int64_t s, int64_t e, int32_t delta);
 
+/* A turn's list of drop / repos directives for one sequence in one call
+ * ([Leyline] "Method": directives arrive as a list and compose by addition).
+ * Equivalent to calling akv_drop / akv_repos once per entry, in order, but
+ * all or nothing: on an error (AKV_ERR_ARG for an unknown kind, AKV_ERR_RANGE
+ * for a span outside the sequence, AKV_ERR_OVERFLOW) no entry is applied. */
+#define AKV_EDIT_DROP 1
+#define AKV_EDIT_REPOS 2
+typedef struct akv_edit_op {
+  int32_t kind;   /* AKV_EDIT_DROP or AKV_EDIT_REPOS */
+  int32_t delta;  /* shift of a repos (ignored for a drop) */
+  int64_t s;      /* span [s, e), logical token indices */
+  int64_t e;
+} akv_edit_op;
+AKV_API akv_status akv_edit(akv_ctx* ctx, int32_t seq, const akv_edit_op* ops, int32_t n_ops);
+
 /* Leyline AMORTIZE splice ([Leyline] "Method", D = (s, e, R, AMORTIZE)):
  * remove tokens [s, e) from the sequence, insert n_stub stub tokens at s
  * (written to fresh pages), and shift every later token by

@@ -65,6 +65,37 @@ def test_errors_leave_state_unchanged(lib):
     assert (before[1][0] == after[1][0]).all() and (before[1][1] == after[1][1]).all()
 
 
+def test_edit_list_is_all_or_nothing_and_equals_single_calls(lib):
+    # akv_edit: a turn's drop / repos list in one call; a failing entry anywhere leaves every
+    # earlier entry unapplied (overflow needs the saved-state path: the bound is near int32)
+    e = akv.Engine(cfg(n_pages=16))
+    s = e.seq_alloc()
+    e.append(s, 100)
+    e.repos(s, 0, 100, 2 ** 31 - 200)          # positions near the int32 limit
+    before = e.export_state(s)
+    bad = [[("drop", 10, 20), ("repos", 20, 50, 3), ("drop", 5, 101)],               # span outside
+           [("repos", 0, 10, -4), ("drop", 30, 40), ("repos", 50, 60, 150)],         # overflow
+           [("drop", 1, 2), ("bogus", 1, 2)]]                                        # unknown kind
+    for ops, code in zip(bad, ["RANGE", "OVERFLOW", "ARG"]):
+        with pytest.raises(akv.AKVError) as x:
+            e.edit(s, ops)
+        assert x.value.code == code
+        after = e.export_state(s)
+        for k in before:
+            assert (before[k] == after[k]).all(), (code, k)
+    # the same list through akv_edit and through single calls gives the same state
+    ops = [("drop", 10, 20), ("repos", 20, 100, -10), ("drop", 40, 45), ("repos", 50, 100, 7), ("repos", 0, 5, -3)]
+    a, b = akv.Engine(cfg(n_pages=16)), akv.Engine(cfg(n_pages=16))
+    for eng in (a, b):
+        eng.append(eng.seq_alloc(), 100)
+    a.edit(0, ops)
+    for op in ops:
+        (b.drop(0, *op[1:]) if op[0] == "drop" else b.repos(0, *op[1:]))
+    sa, sb = a.export_state(0), b.export_state(0)
+    for k in sa:
+        assert (sa[k] == sb[k]).all(), k
+
+
 def test_segment_validation(lib):
     e = akv.Engine(cfg())
     s = e.seq_alloc()

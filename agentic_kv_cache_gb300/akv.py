@@ -125,6 +125,7 @@ def load(path=LIB_PATH):
         "akv_debug_wait_limit": [P, ctypes.c_uint64, I32],
         "akv_debug_corrupt": [P, I32],
         "akv_set_output_stream": [P, P],
+        "akv_last_attention_plan": [P, P, I64, pi64, P, I64, pi64, I32],
         "akv_profile_read": [P, ctypes.POINTER(KernelStats)],
     }
     for name, args in sig.items():
@@ -366,6 +367,19 @@ class Engine:
         """0: automatic split-KV; n >= 1: exactly n KV chunks per work item (1 = never split).
         Applies to attend and attention_mass."""
         self._check(self.lib.akv_set_attention_split(self.h, int(split)))
+
+    def last_attention_plan(self, n_sm=0):
+        """Metadata-only contexts: (units [n, 9] int32, cta_units int32[n_cta + 1] or empty) of the
+        last attend; n_sm > 0 sets the SM count later plans assume."""
+        n, nc = ctypes.c_int64(), ctypes.c_int64()
+        self._check(self.lib.akv_last_attention_plan(self.h, None, 0, ctypes.byref(n), None, 0, ctypes.byref(nc),
+                                                     int(n_sm)))
+        units = np.zeros((n.value, 9), np.int32)
+        cta = np.zeros((nc.value + 1 if nc.value else 0,), np.int32)
+        self._check(self.lib.akv_last_attention_plan(self.h, units.ctypes.data, n.value, ctypes.byref(n),
+                                                     cta.ctypes.data if cta.size else None, cta.size,
+                                                     ctypes.byref(nc), 0))
+        return units, cta
 
     def set_output_stream(self, stream=None):
         """Copy host results (o, lse, mass) on `stream` (a torch stream or raw handle) after the

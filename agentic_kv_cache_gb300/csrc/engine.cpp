@@ -387,6 +387,8 @@ struct akv_ctx {
   cudaEvent_t out_ready = nullptr;
   cudaStream_t copy_st = nullptr;  // host-to-device copies of inputs and descriptor tables
   Staging partial;         // split-KV partial results (device only)
+  std::vector<akv::AttnWork> last_work;  // metadata-only contexts: the last attention plan
+  std::vector<int32_t> last_cta_units;
   int n_sm = 148;          // SMs of the device, for split decisions
   int mla_slots = 148;     // MLA kernel CTAs resident at once (CTA pairs x 2)
   int split_override = 0;  // 0: choose the split factor; n >= 1: use n
@@ -1261,10 +1263,13 @@ struct akv_ctx {
     std::vector<Piece> pieces;
     std::vector<int32_t> n_of;
     int64_t n_pairs = std::max<int64_t>(1, std::min<int64_t>(pair_slots, items_cost / (4 * unit_cost)));
-    for (;; --n_pairs) {
+    // The cut positions assume a total cost; a cut that lands on an item
+    // boundary starts no extra unit, so the total is re-estimated from the
+    // cut just made until it settles (else the last pair gets the remainder).
+    int64_t total = items_cost + (n_pairs - 1) * unit_cost;
+    for (int pass = 0;; ++pass) {
       pieces.clear();
       cta_units.assign(1, 0);
-      const int64_t total = items_cost + (n_pairs - 1) * unit_cost;  // each cut starts one more unit
       int64_t acc = 0, pair = 0;
       auto boundary = [&]() { return (pair + 1) * total / n_pairs; };
       auto close_pair = [&]() {
@@ -1296,7 +1301,15 @@ struct akv_ctx {
       n_of.assign(n_items, 0);
       int32_t most = 0;
       for (const Piece& pc : pieces) most = std::max(most, ++n_of[pc.item]);
-      if (most <= 8 || n_pairs == 1) break;
+      if (most > 8 && n_pairs > 1) {  // too many parts for the merge: fewer pairs
+        --n_pairs;
+        total = items_cost + (n_pairs - 1) * unit_cost;
+        pass = -1;
+        continue;
+      }
+      const int64_t actual = items_cost + (int64_t(pieces.size()) - int64_t(n_items)) * unit_cost;
+      if (actual == total || pass >= 3) break;
+      total = actual;
     }
     // partial slots and ticket counters of the items cut into several units
     // (a shadow writes nothing, so owns no parts)
@@ -1676,10 +1689,9 @@ struct akv_ctx {
       if (rotate && cfg.layout == AKV_LAYOUT_MLA)
         fail(AKV_ERR_ARG, "fused rotation is implemented for the GQA layout; flush, then attend");
     }
-    if (meta) return;
     const bool mla = cfg.layout == AKV_LAYOUT_MLA;
     std::vector<akv::CombineItem> comb;
-    std::vector<int32_t> cta_units;  // GQA: persistent schedule, CTA b runs units [cta_units[b], cta_units[b+1])
+    std::vector<int32_t> cta_units;  // persistent schedule: CTA (MLA: pair) b runs units [cta_units[b], cta_units[b+1])
     int32_t n_parts = 0;
     if (mla) {
       if (split_override > 0)
@@ -1690,6 +1702,11 @@ struct akv_ctx {
       std::vector<int32_t> seg_seq(static_cast<size_t>(n_segs));
       for (int32_t i = 0; i < n_segs; ++i) seg_seq[size_t(i)] = segs[i].seq;
       plan_persistent(work, comb, n_parts, cta_units, seg_seq);
+    }
+    if (meta) {  // the plan is kept for inspection (akv_last_attention_plan); no device work
+      last_work = work;
+      last_cta_units = cta_units;
+      return;
     }
     if (mla) {
       if (cfg.d_v != 512 || cfg.d_rot != 64)
@@ -2436,6 +2453,27 @@ akv_status akv_debug_wait_limit(akv_ctx* ctx, uint64_t wait_ns, int32_t load_cap
     if (load_cap < -1) fail(AKV_ERR_ARG, "load_cap must be -1 (no cap) or >= 0");
     ctx->wait_ns = wait_ns ? wait_ns : 4000000000ull;
     ctx->load_cap = load_cap;
+  });
+}
+
+akv_status akv_last_attention_plan(akv_ctx* ctx, int32_t* units, int64_t cap, int64_t* n_units, int32_t* cta_units,
+                                   int64_t cta_cap, int64_t* n_cta, int32_t n_sm) {
+  return guard(ctx, [&] {
+    if (!ctx->meta) fail(AKV_ERR_ARG, "the plan is kept by metadata-only contexts");
+    if (n_sm > 0) {  // the device size later plans assume
+      ctx->n_sm = n_sm;
+      ctx->mla_slots = n_sm & ~1;
+    }
+    const int64_t n = int64_t(ctx->last_work.size());
+    if (n_units) *n_units = n;
+    for (int64_t i = 0; i < std::min(n, cap) && units; ++i) {
+      const akv::AttnWork& w = ctx->last_work[size_t(i)];
+      const int32_t row[9] = {w.seg, w.kvh, w.qt0, w.n_a, w.n_b, w.t0, w.t1, w.part, w.comb};
+      std::memcpy(units + 9 * i, row, sizeof row);
+    }
+    const int64_t nc = ctx->last_cta_units.empty() ? 0 : int64_t(ctx->last_cta_units.size()) - 1;
+    if (n_cta) *n_cta = nc;
+    for (int64_t i = 0; i <= nc && i < cta_cap && cta_units; ++i) cta_units[i] = ctx->last_cta_units[size_t(i)];
   });
 }
 

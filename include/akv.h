@@ -410,6 +410,19 @@ AKV_API akv_status akv_last_flush_runs(akv_ctx* ctx, int32_t* out, int64_t cap, 
 AKV_API akv_status akv_segment_runs(akv_ctx* ctx, const akv_segment* seg, int32_t* out, int64_t cap,
                             int64_t* n_runs, int64_t* kv_len);
 
+/* Schedule of the last akv_attend of a metadata-only context (pools NULL:
+ * the planners run, nothing is launched), for checking the schedule on hosts
+ * without a GPU.  units: 9 int32 per work entry (segment, kv head or MLA
+ * flags, first query tile, KV tiles of query tile A, of tile B or the MLA
+ * output half, first and end KV tile of the entry, partial slot or -1, merge
+ * item or -1), at most `cap` entries; cta_units: the persistent schedule's
+ * boundaries (CTA -- MLA: CTA pair -- b runs entries or pair units
+ * [cta_units[b], cta_units[b + 1])), at most cta_cap values; *n_cta = 0 when
+ * the launch has one unit per CTA.  n_sm > 0 sets the SM count later plans
+ * assume (0 keeps it).  AKV_ERR_ARG on a context with pools. */
+AKV_API akv_status akv_last_attention_plan(akv_ctx* ctx, int32_t* units, int64_t cap, int64_t* n_units,
+                                           int32_t* cta_units, int64_t cta_cap, int64_t* n_cta, int32_t n_sm);
+
 /* --- device status and measurement --------------------------------------- */
 
 /* Synchronise `stream` and read the device error word of the context's

@@ -1241,12 +1241,15 @@ struct akv_ctx {
   // Persistent schedule for the MLA kernel (automatic split): the pair items
   // (work entries 2k, 2k + 1: one KV range, one output half) are laid end to
   // end in their order (consecutive items of one segment share its K/V in L2)
-  // as sequences of KV tiles, plus a start cost per unit, and cut into one
-  // equal-cost piece per resident CTA pair (stream-K).  An item crossing a cut
-  // becomes several units whose partials the last to finish merges; no piece
-  // is shorter than kMlaMinTiles (the cut moves instead) and no item is cut
-  // into more than 8 parts (fewer pairs are used until none is).  Pair b runs
-  // units [cta_units[b], cta_units[b + 1]) (unit u = work entries 2u, 2u + 1).
+  // as sequences of KV tiles, each unit costing its tiles plus a start cost.
+  // A pair's list takes units in that order until the next would exceed a
+  // budget B, cutting the item at the budget (stream-K); the plan is the fill
+  // with the smallest B that fits the resident CTA pairs, which minimises the
+  // busiest pair's cost (the launch's length) among in-order fills.  An item
+  // crossing a cut becomes several units whose partials the last to finish
+  // merges; no piece is shorter than kMlaMinTiles (the cut moves back
+  // instead) and no item is cut into more than 8 parts.  Pair b runs units
+  // [cta_units[b], cta_units[b + 1]) (unit u = work entries 2u, 2u + 1).
   static constexpr int64_t kMlaMinTiles = 4;
   void plan_mla_persistent(std::vector<akv::AttnWork>& work, std::vector<akv::CombineItem>& comb, int32_t& n_parts,
                            std::vector<int32_t>& cta_units) {
@@ -1261,56 +1264,53 @@ struct akv_ctx {
       int32_t t0, t1;
     };
     std::vector<Piece> pieces;
-    std::vector<int32_t> n_of;
-    int64_t n_pairs = std::max<int64_t>(1, std::min<int64_t>(pair_slots, items_cost / (4 * unit_cost)));
-    // The cut positions assume a total cost; a cut that lands on an item
-    // boundary starts no extra unit, so the total is re-estimated from the
-    // cut just made until it settles (else the last pair gets the remainder).
-    int64_t total = items_cost + (n_pairs - 1) * unit_cost;
-    for (int pass = 0;; ++pass) {
+    const int64_t n_pairs = std::max<int64_t>(1, std::min<int64_t>(pair_slots, items_cost / (4 * unit_cost)));
+    // in-order fill under budget B; false when it needs more than n_pairs
+    // pairs or an item more than 8 parts
+    auto fill = [&](int64_t budget) {
       pieces.clear();
       cta_units.assign(1, 0);
-      int64_t acc = 0, pair = 0;
-      auto boundary = [&]() { return (pair + 1) * total / n_pairs; };
-      auto close_pair = [&]() {
-        cta_units.push_back(int32_t(pieces.size()));
-        ++pair;
-      };
+      int64_t room = budget;
       for (size_t k = 0; k < n_items; ++k) {
         const int64_t span = span_of(k);
         int64_t start = 0;
-        acc += unit_cost;
-        int64_t base = acc;  // acc = base + j after j tiles of this item
-        bool close_at_end = false;
-        while (pair < n_pairs - 1 && base + span >= boundary()) {
-          const int64_t j = std::max(boundary() - base, start + kMlaMinTiles);  // tiles up to the cut
-          if (span - j < kMlaMinTiles) {
-            close_at_end = true;  // finish the item in this pair
+        int32_t parts = 0;
+        for (;;) {
+          const int64_t rest = span - start;
+          if (unit_cost + rest <= room) {
+            pieces.push_back(Piece{k, int32_t(start), int32_t(span)});
+            room -= unit_cost + rest;
             break;
           }
-          pieces.push_back(Piece{k, int32_t(start), int32_t(j)});
-          close_pair();
-          start = j;
-          base += unit_cost;  // the next piece starts a unit
+          int64_t take = room - unit_cost;
+          if (rest - take < kMlaMinTiles) take = rest - kMlaMinTiles;
+          const bool cut = take >= kMlaMinTiles && parts < 7;
+          if (cut) {
+            pieces.push_back(Piece{k, int32_t(start), int32_t(start + take)});
+            start += take;
+            ++parts;
+          } else if (room == budget) {
+            return false;  // a fresh pair can take nothing of this item
+          }
+          cta_units.push_back(int32_t(pieces.size()));
+          if (int64_t(cta_units.size()) > n_pairs) return false;
+          room = budget;
         }
-        pieces.push_back(Piece{k, int32_t(start), int32_t(span)});
-        acc = base + span;
-        if (close_at_end && pair < n_pairs - 1) close_pair();
       }
-      if (cta_units.back() != int32_t(pieces.size())) close_pair();
-      n_of.assign(n_items, 0);
-      int32_t most = 0;
-      for (const Piece& pc : pieces) most = std::max(most, ++n_of[pc.item]);
-      if (most > 8 && n_pairs > 1) {  // too many parts for the merge: fewer pairs
-        --n_pairs;
-        total = items_cost + (n_pairs - 1) * unit_cost;
-        pass = -1;
-        continue;
-      }
-      const int64_t actual = items_cost + (int64_t(pieces.size()) - int64_t(n_items)) * unit_cost;
-      if (actual == total || pass >= 3) break;
-      total = actual;
+      if (cta_units.back() != int32_t(pieces.size())) cta_units.push_back(int32_t(pieces.size()));
+      return int64_t(cta_units.size()) - 1 <= n_pairs;
+    };
+    int64_t lo = std::max<int64_t>(unit_cost + 1, items_cost / n_pairs), hi = items_cost;  // fill(hi) holds
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (fill(mid))
+        hi = mid;
+      else
+        lo = mid + 1;
     }
+    fill(hi);
+    std::vector<int32_t> n_of(n_items, 0);
+    for (const Piece& pc : pieces) ++n_of[pc.item];
     // partial slots and ticket counters of the items cut into several units
     // (a shadow writes nothing, so owns no parts)
     std::vector<int32_t> base_of(work.size(), -1), comb_of(work.size(), -1), next_of(n_items, 0);

@@ -5,9 +5,10 @@ A metadata-only context runs the planners and keeps the last plan
 schedule must satisfy: each work item's KV tiles are covered exactly once by
 its units; an item cut into several units has one partial slot per unit and
 one merge item; no item is cut into more than 8 parts; the persistent lists
-partition the units and give the CTAs (MLA: CTA pairs) equal work; every MLA
-unit reads at least one tile and its two entries (a CTA pair) agree.  The GPU
-tests check the results of the same plans against the oracle."""
+partition the units and give the CTAs equal work (MLA: no CTA pair far above
+the mean); every MLA unit reads at least one tile and its two entries (a CTA
+pair) agree.  The GPU tests check the results of the same plans against the
+oracle."""
 from collections import defaultdict
 
 import numpy as np
@@ -95,7 +96,9 @@ def test_mla_persistent_schedule(concurrency):
     assert 1 <= n_pairs <= N_SM // 2 and cta[-1] == len(pairs) and np.all(np.diff(cta) >= 1)
     cost = np.array([sum(MLA_UNIT_COST + int(p[0][6] - p[0][5]) for p in pairs[cta[b]:cta[b + 1]])
                      for b in range(n_pairs)])
-    assert cost.max() - cost.min() <= 4 * (4 + MLA_UNIT_COST), (cost.min(), cost.max())
+    # the launch lasts as long as its busiest pair: within a start cost and two minimum pieces of
+    # the mean (a pair closes early only when the next piece could not be cut at least 4 tiles long)
+    assert cost.max() <= cost.sum() / n_pairs + MLA_UNIT_COST + 2 * 4, (cost.max(), cost.sum() / n_pairs)
     if concurrency == 1:
         assert n_pairs == N_SM // 2               # every resident pair has work
 

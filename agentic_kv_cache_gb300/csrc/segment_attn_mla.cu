@@ -20,8 +20,9 @@
 // back over the consumed S columns as bf16 pairs) and the 256-column O half.
 // Warps 0, 6, 7: TMA producers taking rounds of the key stream in turn (their
 // copies count on the even CTA's barriers); warp 1: TMEM allocation and, in
-// the even CTA, the single-thread MMA issuer; warps 2-5: softmax of the CTA's
-// own rows.  Every wait is bounded.
+// the even CTA, the thread issuing the QK^T MMAs; warp 8 (even CTA): the thread
+// issuing the PV MMAs; warps 2-5: softmax of the CTA's own rows.  Every wait
+// is bounded.
 //
 // A pair runs a list of units (persistent schedule: the engine cuts the work
 // end to end into one equal piece per resident pair, so a unit may be part
@@ -41,8 +42,7 @@
 namespace akv {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kProducers = 3;  // warps 0, 6 and 7 issue the copies, taking rounds in turn
+constexpr int kThreads = 288;
 constexpr int kKeys = 128;     // keys per KV tile (the pair MMA's N for QK^T)
 constexpr int kRows = 128;     // rows per CTA; the pair covers 256
 constexpr int kLat = 512;      // latent width
@@ -50,7 +50,13 @@ constexpr int kPe = 64;        // K_pe width
 constexpr int kQChunks = (kLat + kPe) / 64;  // 9 chunks of the QK contraction
 constexpr int kQKRounds = 5;                 // latent chunks in pairs, then K_pe
 constexpr int kPVRounds = 2;                 // one per O quarter
-constexpr int kRing = 5;
+// Two rings of 16 KiB slots, one per MMA thread: each ring has one consumer,
+// which takes its rounds in order, and no more producers than slots, so a
+// wait on a slot's barrier phase can never see the phase of an older use.
+constexpr int kQKSlots = 3;     // QK^T rounds, filled by warps 0 and 6 in turn
+constexpr int kQKProducers = 2;
+constexpr int kPVSlots = 2;     // PV rounds, filled by warp 7
+static_assert(kQKProducers <= kQKSlots, "a ring needs at least as many slots as producers");
 constexpr int kMaxRuns = 8;  // runs per 128-key tile: 128 / page, page >= 16
 constexpr uint32_t kQChunk = 128 * 128;      // 128 rows x 64 bf16
 constexpr uint32_t kUnit = 64 * 128;         // 64 keys x 64 bf16: one copy
@@ -62,8 +68,9 @@ constexpr uint16_t kBoth = 0x3;  // CTA mask of the pair
 
 // shared memory layout (bytes)
 constexpr uint32_t kQ = 0;                           // 9 chunks of Q
-constexpr uint32_t kSlots = kQ + kQChunks * kQChunk;  // ring of 16 KiB slots
-constexpr uint32_t kColE = kSlots + kRing * kSlot;    // int32[2][128], by tile parity
+constexpr uint32_t kSlots = kQ + kQChunks * kQChunk;  // QK^T ring, then PV ring (16 KiB slots)
+constexpr uint32_t kVSlots = kSlots + kQKSlots * kSlot;
+constexpr uint32_t kColE = kVSlots + kPVSlots * kSlot;  // int32[2][128], by tile parity
 constexpr uint32_t kBars = kColE + 2 * 128 * 4;
 constexpr uint32_t kBytes = kBars + 256;
 static_assert(kBytes + 1024 <= 232448, "shared memory");
@@ -74,9 +81,24 @@ static_assert(kBytes + 1024 <= 232448, "shared memory");
 // scope (thread arrivals from the peer); the others are completed by copies
 // and commits, whose CTA-scope waits are much cheaper on the producer's and
 // the MMA thread's per-unit path.
-enum Bar { kBarQ = 0, kBarFull0, kBarEmpty0 = kBarFull0 + kRing, kBarS0 = kBarEmpty0 + kRing, kBarP = kBarS0 + 2,
-           kBarO, kBarQFree, kBarFin, kNumBars };
-static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+enum Bar {
+  kBarQ = 0,
+  kBarFull0,                           // + QK^T slot
+  kBarEmpty0 = kBarFull0 + kQKSlots,   // + QK^T slot
+  kBarVFull0 = kBarEmpty0 + kQKSlots,  // + PV slot
+  kBarVEmpty0 = kBarVFull0 + kPVSlots,
+  kBarS0 = kBarVEmpty0 + kPVSlots,  // + S buffer
+  kBarP = kBarS0 + 2,
+  kBarO,
+  kBarQFree,
+  kBarFin,   // the QK^T thread's MMAs done
+  kBarPVd0,  // + S buffer: the PV that read P from that buffer is done
+  kBarFin2 = kBarPVd0 + 2,  // the PV thread's MMAs done
+  kBarProd,  // both QK^T producers have published their last round per slot (count 2)
+  kNumBars
+};
+// after the barriers: abort flag, TMEM address, the QK^T producers' last round per slot
+static_assert(kNumBars * 8 + 8 + kQKProducers * kQKSlots * 4 <= 256, "barrier area");
 
 __device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
   if (atomicCAS(&err->code, 0, code) == 0) {
@@ -93,12 +115,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 // The key stream is cut into rounds, each one ring slot filled by one or two
 // copies counted on one barrier (a copy and its barrier cost a producer thread
-// far more than the bytes, so rounds are large and three threads issue them).
-// Order = the MMA thread's: QK rounds of tile 0, then for each tile j: QK
-// rounds of tile j+1 (if any), PV rounds of tile j.  QK round m < 4: latent
-// chunks 2m and 2m+1 of the CTA's own 64 keys; m = 4: its K_pe chunk.  PV
-// round q: latent columns 256 half + 128 q + 64 rank of all 128 keys (two
-// copies, one per key half).  Round rd uses slot rd % kRing.
+// far more than the bytes, so rounds are large and two threads issue the
+// QK^T rounds).  QK^T ring: per tile, round m < 4 holds latent chunks 2m and
+// 2m+1 of the CTA's own 64 keys, m = 4 its K_pe chunk; QK^T round qr (counted
+// over all units) uses slot qr % kQKSlots.  PV ring: per tile, round q holds
+// latent columns 256 half + 128 q + 64 rank of all 128 keys (two copies, one
+// per key half); PV round vr uses slot vr % kPVSlots.
 
 // Pages of one KV tile per 64-key half h: the K_pe and latent pages of the
 // half's first run and whether the half's pages are consecutive (then one
@@ -152,16 +174,22 @@ __device__ __forceinline__ TilePages tile_pages(const int2 (&kv)[kMaxRuns], int 
   return t;
 }
 
-__device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t rank, int who,
-                                        volatile int* abort_flag) {
+// One producer thread.  pv: the PV ring (warp 7); else the QK^T ring, rounds
+// taken in turn by who = 0 (warp 0, which also loads the Q tiles) and who = 1.
+__device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t rank, bool pv,
+                                        int who, volatile int* abort_flag, volatile int* prod_last) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
   const int rpu = p.page >= 64 ? 1 : 64 / p.page;  // runs per 64-key half
-  const uint32_t lead_full0 = ptx::mapa(bar(kBarFull0), 0);
+  const int n_slots = pv ? kPVSlots : kQKSlots, stride = pv ? 1 : kQKProducers;
+  const int full0 = pv ? kBarVFull0 : kBarFull0, empty0 = pv ? kBarVEmpty0 : kBarEmpty0;
+  const uint32_t ring = sbase + (pv ? kVSlots : kSlots);
+  const uint32_t lead_full0 = ptx::mapa(bar(full0), 0);
   const uint32_t lead_q = ptx::mapa(bar(kBarQ), 0);
+  const bool loads_q = !pv && who == 0;
   const int layer_base = p.layer * p.n_pages;
-  if (who == 0) {
+  if (loads_q) {
     ptx::prefetch_tensormap(&p.q_map);
     ptx::prefetch_tensormap(&p.k_map);
     ptx::prefetch_tensormap(&p.v_map);
@@ -193,34 +221,39 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
       }
     }
   };
-  int rd = 0;  // rounds of the key stream so far, over all units
-  // Round `kind` (< kQKRounds: QK round, else PV round kind - kQKRounds) of local tile j.
-  auto round = [&](int kind, int j, const TilePages& tp) {
-    if (ok && rd % kProducers == who) {
-      const int slot = rd % kRing, use = rd / kRing;
-      if (use >= 1 && !ptx::mbar_wait(bar(kBarEmpty0 + slot), (use - 1) & 1, abort_flag, p.wait_ns)) {
+  int rd = 0;  // rounds of this ring so far, over all units
+  int last[kQKSlots] = {-1, -1, -1};  // the last round this thread issued into each slot
+  // Round m of local tile j: QK^T round m (< kQKRounds) or PV round m.
+  auto round = [&](int m, int j, const TilePages& tp) {
+    if (ok && rd % stride == who) {
+      const int slot = rd % n_slots, use = rd / n_slots;
+      if (use >= 1 && !ptx::mbar_wait(bar(empty0 + slot), (use - 1) & 1, abort_flag, p.wait_ns)) {
         ok = false;
       } else {
-        const uint32_t dst = sbase + kSlots + slot * kSlot;
+#pragma unroll
+        for (int s = 0; s < kQKSlots; ++s)
+          if (s == slot) last[s] = rd;
+        const uint32_t dst = ring + slot * kSlot;
         const uint32_t fb = lead_full0 + 8u * uint32_t(slot);
         const int kr = int(rank);
-        if (kind < kQKRounds - 1) {
-          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), 2 * kSlot);
-          copy(dst, fb, false, kr, 128 * kind, j, tp);
-          copy(dst + kUnit, fb, false, kr, 128 * kind + 64, j, tp);
-        } else if (kind == kQKRounds - 1) {
-          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), 2 * kUnit);
-          copy(dst, fb, true, kr, 0, j, tp);
-        } else {
-          const int col = 256 * half + 128 * (kind - kQKRounds) + 64 * kr;
-          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(kBarFull0 + slot), 2 * kSlot);
+        if (pv) {
+          const int col = 256 * half + 128 * m + 64 * kr;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(full0 + slot), 2 * kSlot);
           copy(dst, fb, false, 0, col, j, tp);
           copy(dst + kUnit, fb, false, 1, col, j, tp);
+        } else if (m < kQKRounds - 1) {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(full0 + slot), 2 * kSlot);
+          copy(dst, fb, false, kr, 128 * m, j, tp);
+          copy(dst + kUnit, fb, false, kr, 128 * m + 64, j, tp);
+        } else {
+          if (rank == 0) ptx::mbar_arrive_expect_tx(bar(full0 + slot), 2 * kUnit);
+          copy(dst, fb, true, kr, 0, j, tp);
         }
       }
     }
     ++rd;
   };
+  const int n_rounds = pv ? kPVRounds : kQKRounds;
   int q_loads = 0;
   for (int u = u0; u < u1 && ok; ++u) {
     w = p.work[2 * u + int(rank)];
@@ -228,7 +261,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
     half = w.n_b;
     first = *reinterpret_cast<const int2*>(p.runs + seg.run_off);
     const int n_loc = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);  // local tile j is global tile t0 + j
-    if (who == 0) {
+    if (loads_q) {
       // Q tiles of this unit, once the previous unit's last QK MMA has released
       // both CTAs' Q buffers (a multicast commit to each CTA's Q-free barrier).
       if (u > u0 && !(ok = ptx::mbar_wait(bar(kBarQFree), (u - u0 - 1) & 1, abort_flag, p.wait_ns))) break;
@@ -238,69 +271,70 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
         ptx::tma_load_3d_pair(sbase + kQ + c * kQChunk, &p.q_map, lead_q, c * 64, 0, q_tok0);
       ++q_loads;
     }
+    // runs of tile j + 1 are loaded while tile j's rounds are issued
     int2 raw[kMaxRuns];
     load_runs(p, seg, w.t0, rpt, first, raw);
-    TilePages cur = tile_pages(raw, p.page, rpu, layer_base), nxt = cur;
-    if (n_loc > 1) {
-      load_runs(p, seg, w.t0 + 1, rpt, first, raw);
-      nxt = tile_pages(raw, p.page, rpu, layer_base);
-    }
-    if (n_loc > 0)
-      for (int m = 0; m < kQKRounds; ++m) round(m, 0, cur);
-    for (int b = 0; b < n_loc && ok; ++b) {
-      // runs of tile b + 2 are loaded here and used a block later
-      if (b + 2 < n_loc) load_runs(p, seg, w.t0 + b + 2, rpt, first, raw);
-      if (b + 1 < n_loc)
-        for (int m = 0; m < kQKRounds; ++m) round(m, b + 1, nxt);
-      for (int q = 0; q < kPVRounds; ++q) round(kQKRounds + q, b, cur);
-      cur = nxt;
-      if (b + 2 < n_loc) nxt = tile_pages(raw, p.page, rpu, layer_base);
+    for (int j = 0; j < n_loc && ok; ++j) {
+      const TilePages tp = tile_pages(raw, p.page, rpu, layer_base);
+      if (j + 1 < n_loc) load_runs(p, seg, w.t0 + j + 1, rpt, first, raw);
+      for (int m = 0; m < n_rounds; ++m) round(m, j, tp);
     }
   }
   if (!ok) {
-    raise_error(p.err, kErrTimeout, blockIdx.x, 10, who);
+    raise_error(p.err, kErrTimeout, blockIdx.x, 10, pv ? 2 : who);
     *abort_flag = 1;
   }
-  if (who != 0) return;
-  // Drain (one thread): every round issued so far consumed (so every copy
-  // into this CTA has landed) and every multicast commit to this CTA's ring
-  // barriers arrived; the Q barrier's last phase completed.
-  const int total = rd;
-  if (rank == 0 && q_loads) ptx::mbar_wait_drain(bar(kBarQ), (q_loads - 1) & 1, kDrainLimitNs);
-#pragma unroll 1
-  for (int s = 0; s < kRing; ++s) {
-    const int uses = total > s ? (total - s + kRing - 1) / kRing : 0;
-    if (!uses) continue;
-    if (rank == 0) ptx::mbar_wait_drain(bar(kBarFull0 + s), (uses - 1) & 1, kDrainLimitNs);
-    ptx::mbar_wait_drain(bar(kBarEmpty0 + s), (uses - 1) & 1, kDrainLimitNs);
+  // Drain (one producer per ring): every round of the ring issued so far has
+  // landed (the Full barriers, in the even CTA, count both CTAs' bytes) and
+  // been consumed (the consumer's multicast commit has reached this CTA's
+  // Empty barrier), and the Q barrier's last phase completed.  A slot is
+  // drained at the last round any producer issued into it: no later phase
+  // exists, so the parity wait cannot match an older or a newer phase.
+  if (!pv) {
+#pragma unroll
+    for (int s = 0; s < kQKSlots; ++s) prod_last[who * kQKSlots + s] = last[s];
+    ptx::mbar_arrive(bar(kBarProd));
+    if (who != 0) return;
+    if (!ptx::mbar_wait_drain(bar(kBarProd), 0, kDrainLimitNs)) raise_error(p.err, kErrTimeout, blockIdx.x, 15, 0);
+#pragma unroll
+    for (int s = 0; s < kQKSlots; ++s)
+      for (int q = 1; q < kQKProducers; ++q) last[s] = max(last[s], prod_last[q * kQKSlots + s]);
   }
+  bool drained = true;
+  if (loads_q && rank == 0 && q_loads) drained = ptx::mbar_wait_drain(bar(kBarQ), (q_loads - 1) & 1, kDrainLimitNs);
+#pragma unroll
+  for (int s = 0; s < kQKSlots; ++s) {
+    if (last[s] < 0) continue;
+    const uint32_t parity = uint32_t(last[s] / n_slots) & 1u;
+    if (rank == 0) drained = ptx::mbar_wait_drain(bar(full0 + s), parity, kDrainLimitNs) && drained;
+    drained = ptx::mbar_wait_drain(bar(empty0 + s), parity, kDrainLimitNs) && drained;
+  }
+  if (!drained) raise_error(p.err, kErrTimeout, blockIdx.x, 14, pv ? 2 : who);  // copies may still be in flight
 }
 
 // --------------------------------------------------------------------- MMA
-// Even CTA only.  QK^T: D (S, 128 columns per CTA) = Q (256 rows) x K (128
-// keys, 64 from each CTA).  PV: O quarter q (128 columns) += P (256 rows x
-// 128 keys, from each CTA's TMEM) x V (128 keys x 128 columns, 64 from each
-// CTA).
-__device__ __forceinline__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
-                                          volatile int* abort_flag) {
+// Even CTA only, two issuing threads.  A thread's tensor-core queue is short
+// and every shared-memory access it makes between MMAs (a barrier wait above
+// all) leaves the tensor pipe idle for about 200 clocks; with the QK^T and the
+// PV MMAs issued by different threads, one thread's MMAs fill the other's
+// waits.  QK^T: D (S, 128 columns per CTA) = Q (256 rows) x K (128 keys, 64
+// from each CTA).  PV: O quarter q (128 columns) += P (256 rows x 128 keys,
+// from each CTA's TMEM) x V (128 keys x 128 columns, 64 from each CTA).
+
+// Local tiles of a unit (local tile j is global tile t0 + j).
+__device__ __forceinline__ int unit_tiles(const AttnWork& w) { return min(max(w.n_a - w.t0, 0), w.t1 - w.t0); }
+
+// QK^T thread.  S of global tile gt (tiles of earlier units included: the S,
+// P and O phases continue across units) goes to S buffer gt & 1, which holds
+// P(gt - 2) until that tile's PV is done.  After a unit's last QK^T MMA both
+// CTAs may reload their Q tiles.
+__device__ __forceinline__ void issue_qk(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
+                                         volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   constexpr uint32_t idesc_qk = ptx::idesc_bf16(2 * kRows, kKeys, false);
-  constexpr uint32_t idesc_pv = ptx::idesc_bf16(2 * kRows, 128, true);
-  const uint32_t tO = tmem + 256;
-  int rd = 0;
   bool issued = false;  // a commit is only issued after this thread's first MMA
   bool ok = true;
-  auto next_round = [&]() -> uint32_t {  // wait for round rd; its slot address
-    const int slot = rd % kRing;
-    ok = ok && ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kRing) & 1, abort_flag, p.wait_ns);
-    ptx::tc_fence_after();
-    return sbase + kSlots + slot * kSlot;
-  };
-  auto release = [&]() {
-    ptx::mma_commit_pair_mc(bar(kBarEmpty0 + rd % kRing), kBoth);
-    ++rd;
-  };
   // Descriptors are built once and advanced by constants (only the start
   // address changes).
   const uint64_t qd0 = ptx::smem_desc(sbase + kQ, 16, 1024);
@@ -311,65 +345,38 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, int u0, int u1, u
     for (int ks = 1; ks < 4; ++ks)
       ptx::mma_bf16_pair(tS, ptx::desc_advance(qd, ks * 32), ptx::desc_advance(kd, ks * 32), idesc_qk, 1);
   };
-  // S of global tile gt (tiles of earlier units included: the S, P and O
-  // phases continue across units) into S buffer gt & 1.
-  auto qk = [&](int gt) {
-    const uint32_t tS = tmem + 128u * (gt & 1);
-#pragma unroll 1
-    for (int m = 0; m < kQKRounds && ok; ++m) {
-      const uint32_t kt = next_round();
-      if (!ok) break;
-      if (m < kQKRounds - 1) {
-        chunk(tS, 2 * m, kt);
-        chunk(tS, 2 * m + 1, kt + kUnit);
-      } else {
-        chunk(tS, kQChunks - 1, kt);
-      }
-      issued = true;
-      release();
-    }
-    if (ok) ptx::mma_commit_pair_mc(bar(kBarS0 + (gt & 1)), kBoth);
-  };
-  int g = 0;  // tiles of earlier units
+  int g = 0, rd0 = 0;  // tiles and key-stream rounds of earlier units
   for (int u = u0; u < u1 && ok; ++u) {
-    const AttnWork w = p.work[2 * u];
-    const int n = min(max(w.n_a - w.t0, 0), w.t1 - w.t0);
+    const int n = unit_tiles(p.work[2 * u]);
     const bool more = u + 1 < u1;
     if (!(ok = ptx::mbar_wait(bar(kBarQ), (u - u0) & 1, abort_flag, p.wait_ns))) break;
-    ptx::tc_fence_after();
-    // After the unit's last QK MMA both CTAs may reload their Q tiles.
-    auto q_free = [&](int j) {
-      if (ok && more && j == n - 1) ptx::mma_commit_pair_mc(bar(kBarQFree), kBoth);
-    };
-    if (n > 0) {
-      qk(g);
-      q_free(0);
-    }
     for (int j = 0; j < n && ok; ++j) {
-      if (j + 1 < n) {
-        qk(g + j + 1);
-        q_free(j + 1);
+      const int gt = g + j;
+      if (gt >= 2 && !(ok = ptx::mbar_wait(bar(kBarPVd0 + (gt & 1)), ((gt >> 1) - 1) & 1, abort_flag, p.wait_ns)))
+        break;
+      const uint32_t tS = tmem + 128u * (gt & 1);
+      int rd = rd0 + kQKRounds * j;  // QK^T ring round
+#pragma unroll 1
+      for (int m = 0; m < kQKRounds; ++m, ++rd) {
+        const int slot = rd % kQKSlots;
+        if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kQKSlots) & 1, abort_flag, p.wait_ns))) break;
+        ptx::tc_fence_after();
+        const uint32_t kt = sbase + kSlots + slot * kSlot;
+        if (m < kQKRounds - 1) {
+          chunk(tS, 2 * m, kt);
+          chunk(tS, 2 * m + 1, kt + kUnit);
+        } else {
+          chunk(tS, kQChunks - 1, kt);
+        }
+        issued = true;
+        ptx::mma_commit_pair_mc(bar(kBarEmpty0 + slot), kBoth);
       }
       if (!ok) break;
-      if (!(ok = ptx::mbar_wait_cl(bar(kBarP), (g + j) & 1, abort_flag, p.wait_ns))) break;
-      ptx::tc_fence_after();
-      const uint32_t tP = tmem + 128u * ((g + j) & 1);  // P of tile j, packed over S
-#pragma unroll 1
-      for (int q = 0; q < kPVRounds && ok; ++q) {
-        const uint32_t vt = next_round();
-        if (!ok) break;
-        const uint64_t vd = ptx::smem_desc(vt, kSlot, 1024);
-        // the unit's first PV overwrites O: the softmax threads arrived on P
-        // only after reading out the previous unit's O
-        ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP, vd, idesc_pv, j > 0);
-#pragma unroll
-        for (int ks = 1; ks < kKeys / 16; ++ks)
-          ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
-        release();
-      }
-      if (ok) ptx::mma_commit_pair_mc(bar(kBarO), kBoth);
+      ptx::mma_commit_pair_mc(bar(kBarS0 + (gt & 1)), kBoth);
+      if (more && j == n - 1) ptx::mma_commit_pair_mc(bar(kBarQFree), kBoth);
     }
     g += n;
+    rd0 += kQKRounds * n;
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 11, 0);
@@ -377,7 +384,59 @@ __device__ __forceinline__ void issue_mma(const AttnParams& p, int u0, int u1, u
   }
   if (issued) {
     ptx::mma_commit_pair(bar(kBarFin));
-    ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs);
+    if (!ptx::mbar_wait_drain(bar(kBarFin), 0, kDrainLimitNs)) raise_error(p.err, kErrTimeout, blockIdx.x, 16, 0);
+  }
+}
+
+// PV thread.  PV of global tile gt reads P from S buffer gt & 1 once the
+// softmax threads of both CTAs have written it; the commit after it releases
+// that buffer to the QK^T thread (and O to the softmax threads).  A unit's
+// first PV overwrites O: the softmax threads arrived on its P only after
+// reading out the previous unit's O.
+__device__ __forceinline__ void issue_pv(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
+                                         volatile int* abort_flag) {
+  const uint32_t bars = sbase + kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  constexpr uint32_t idesc_pv = ptx::idesc_bf16(2 * kRows, 128, true);
+  const uint32_t tO = tmem + 256;
+  bool issued = false;
+  bool ok = true;
+  int g = 0, rd0 = 0;
+  for (int u = u0; u < u1 && ok; ++u) {
+    const int n = unit_tiles(p.work[2 * u]);
+    for (int j = 0; j < n && ok; ++j) {
+      const int gt = g + j;
+      if (!(ok = ptx::mbar_wait_cl(bar(kBarP), gt & 1, abort_flag, p.wait_ns))) break;
+      ptx::tc_fence_after();
+      const uint32_t tP = tmem + 128u * (gt & 1);  // P of tile gt, packed over S
+      int rd = rd0 + kPVRounds * j;  // PV ring round
+#pragma unroll 1
+      for (int q = 0; q < kPVRounds; ++q, ++rd) {
+        const int slot = rd % kPVSlots;
+        if (!(ok = ptx::mbar_wait(bar(kBarVFull0 + slot), (rd / kPVSlots) & 1, abort_flag, p.wait_ns))) break;
+        ptx::tc_fence_after();
+        const uint64_t vd = ptx::smem_desc(sbase + kVSlots + slot * kSlot, kSlot, 1024);
+        ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP, vd, idesc_pv, j > 0);
+#pragma unroll
+        for (int ks = 1; ks < kKeys / 16; ++ks)
+          ptx::mma_bf16_tmem_a_pair(tO + 128u * q, tP + 8u * ks, ptx::desc_advance(vd, ks * 2048), idesc_pv, 1);
+        issued = true;
+        ptx::mma_commit_pair_mc(bar(kBarVEmpty0 + slot), kBoth);
+      }
+      if (!ok) break;
+      ptx::mma_commit_pair_mc(bar(kBarO), kBoth);
+      ptx::mma_commit_pair(bar(kBarPVd0 + (gt & 1)));
+    }
+    g += n;
+    rd0 += kPVRounds * n;
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 13, 0);
+    *abort_flag = 1;
+  }
+  if (issued) {
+    ptx::mma_commit_pair(bar(kBarFin2));
+    if (!ptx::mbar_wait_drain(bar(kBarFin2), 0, kDrainLimitNs)) raise_error(p.err, kErrTimeout, blockIdx.x, 17, 0);
   }
 }
 
@@ -593,6 +652,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t bars = sbase + kBars;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBars + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBars + 8 * kNumBars + 4);
+  volatile int* prod_last = reinterpret_cast<volatile int*>(smem + kBars + 8 * kNumBars + 8);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = ptx::cluster_ctarank();
   // The pair runs units [u0, u1); unit u is work entries 2u (even CTA) and 2u + 1.
@@ -612,7 +672,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 #endif
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) ptx::mbar_init(bars + 8u * i, i == kBarP ? 2 * 128 : 1);
+    for (int i = 0; i < kNumBars; ++i)
+      ptx::mbar_init(bars + 8u * i, i == kBarP ? 2 * 128 : (i == kBarProd ? kQKProducers : 1));
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -625,10 +686,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();  // the pair's TMEM is allocated in both CTAs before the first MMA
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp == 0 || warp >= 6) {
-    if (lane == 0) produce(p, u0, u1, sbase, rank, warp == 0 ? 0 : warp - 5, abort_flag);
+  if (warp == 0 || warp == 6 || warp == 7) {
+    if (lane == 0) produce(p, u0, u1, sbase, rank, warp == 7, warp == 6 ? 1 : 0, abort_flag, prod_last);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) issue_mma(p, u0, u1, sbase, tmem, abort_flag);
+    if (lane == 0 && rank == 0) issue_qk(p, u0, u1, sbase, tmem, abort_flag);
+  } else if (warp == 8) {
+    if (lane == 0 && rank == 0) issue_pv(p, u0, u1, sbase, tmem, abort_flag);
   } else {
     softmax(p, u0, u1, smem, sbase, tmem, rank, abort_flag);
   }

@@ -239,7 +239,13 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
     const int n_max = max(nt0, nt1);
     if (!(ok = ptx::mbar_wait(bar(kBarQ), (u - u0) & 1, abort_flag, p.wait_ns))) break;
     for (int j = 0; j <= n_max && ok; ++j) {
-      bool k_ready = false, v_ready = false;
+      bool v_ready = false;
+      // K_j is waited for before P_A(j-1): the thread would wait for P_A
+      // anyway, and a wait between PV_A and QK_A idles the tensor pipe.
+      if (j < n_max) {
+        const int ld = ld0 + 2 * j;
+        ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, p.wait_ns);
+      }
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const int nt = t ? nt1 : nt0, cs = t ? cs1 : cs0;
@@ -265,12 +271,7 @@ __device__ void issue_mma(const AttnParams& p, int u0, int u1, uint32_t sbase, u
           }
         }
         if (ok && j < nt) {
-          if (!k_ready) {
-            const int ld = ld0 + 2 * j;
-            ok = ptx::mbar_wait(ready_bar(ld), full_parity(ld), abort_flag, p.wait_ns);
-            k_ready = true;
-            ptx::tc_fence_after();
-          }
+          ptx::tc_fence_after();
           if (ok) {
             const uint64_t kd = ptx::smem_desc(sbase + L::kSlot + slot_of(ld0 + 2 * j) * L::kTile, 16, 1024);
             const uint64_t qd = t ? qd1 : qd0;
@@ -449,11 +450,11 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     if (ri0 < seg.n_runs) run_cur = run_le[2 * ri0 + 1];
   }
   for (int j = 0; j < n_t; ++j) {
-    ok = ptx::mbar_wait(bar(kBarS0 + t), (ph ^ j) & 1, abort_flag, p.wait_ns);
     // Entry index of key column r of tile j (INT_MAX: no entry there);
-    // columns are (run c / page, slot c % page) of the tile's runs.  The run
-    // of the next tile is fetched now so its latency hides behind this tile.
-    // The entries go to the buffer of this tile's parity: the other buffer may
+    // columns are (run c / page, slot c % page) of the tile's runs.  It needs
+    // no score, so it is formed before S_t(j) is waited for, and the run of
+    // the next tile is fetched now so its latency hides behind this tile.  The
+    // entries go to the buffer of this tile's parity: the other buffer may
     // still be read by a thread finishing tile j - 1.
     int* colE = colE_base + (j & 1) * 128;
     int e = INT_MAX;
@@ -464,6 +465,7 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       const int ri = (w.t0 + j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
+    ok = ptx::mbar_wait(bar(kBarS0 + t), (ph ^ j) & 1, abort_flag, p.wait_ns);
     // One barrier per tile: every thread's S arrived and every column has an
     // entry; only when that fails does a second one tell a time-out from masking.
     const bool all_valid = ptx::bar_red_and(bar_id, 128, ok && e != INT_MAX);

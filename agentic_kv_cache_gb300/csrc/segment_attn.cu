@@ -478,26 +478,25 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
     // holds the tile's largest entry index.
     const bool need_mask = !all_valid || colE[kTileKeys - 1] > lim;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
-    // One pass over the two 64-column halves of S: each half is read from TMEM
-    // once, its max taken (three-input max, two scores per instruction), and
-    // P = exp2(s * scale * log2 e - m) formed with the running max m, packed to
-    // bf16 pairs and stored over the S columns already read (keys 2c, 2c+1 ->
-    // column c), where the PV MMA reads it as its A operand.  m is raised only
-    // when a half's max exceeds it by more than 2^8 (lazy rescale); if the
-    // second half raises it, the first half's P and sum are scaled down.  The
-    // scale-and-shift and the row sum run on float pairs.
+    // One pass over the row: the 128 scores are read from TMEM with one load
+    // (one wait), the row max is taken (three-input max, two scores per
+    // instruction), and P = exp2(s * scale * log2 e - m) is formed with the
+    // running max m, packed to bf16 pairs in place (pair c, keys 2c and 2c+1,
+    // goes to register c, whose score is already used) and stored with one
+    // 64-column store over the S columns, where the PV MMA reads it as its A
+    // operand.  m is raised only when the row max exceeds it by more than 2^8
+    // (lazy rescale).  The scale-and-shift and the row sum run on float pairs.
     const float2 sl2v = make_float2(sl2, sl2);
-    float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // two pair accumulators: no spills at 168 registers
-    float m_use = m_run, alpha = 1.0f, a_first = 1.0f;
+    float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float m_use = m_run, alpha = 1.0f;
     bool resc = false;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t u[64];
-      ptx::tmem_load64(tS + lane_addr + h * 64, u);
+    {
+      uint32_t u[128];
+      ptx::tmem_load128(tS + lane_addr, u);
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int4 e4 = ce4[h * 16 + c];
+        for (int c = 0; c < 32; ++c) {
+          const int4 e4 = ce4[c];
           if (e4.x > lim) u[4 * c + 0] = 0xff800000u;  // -inf
           if (e4.y > lim) u[4 * c + 1] = 0xff800000u;
           if (e4.z > lim) u[4 * c + 2] = 0xff800000u;
@@ -506,46 +505,27 @@ __device__ bool softmax_tile(const AttnParams& p, const AttnWork& w, const AttnS
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < 32; ++c)
         mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[4 * c]), __uint_as_float(u[4 * c + 1]));
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < 32; ++c)
         mx[c & 3] = ptx::max3(mx[c & 3], __uint_as_float(u[4 * c + 2]), __uint_as_float(u[4 * c + 3]));
       const float mh = fmaxf(ptx::max3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
       if (mh > m_use + 8.0f) {
-        const float a = m_use == -INFINITY ? 0.f : ptx::ex2_approx(m_use - mh);
-        if (h == 1) {  // rare: the first half was formed with the smaller max
-          sum[0] = make_float2(sum[0].x * a, sum[0].y * a);
-          sum[1] = make_float2(sum[1].x * a, sum[1].y * a);
-          a_first = a;  // its P is scaled once this half is stored (fewer live registers)
-        }
-        alpha *= a;
+        alpha = m_use == -INFINITY ? 0.f : ptx::ex2_approx(m_use - mh);
         m_use = mh;
         resc = true;
       }
       const float msub = m_use == -INFINITY ? 0.f : m_use;
       const float2 negm = make_float2(-msub, -msub);
-      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 64; ++c) {
         const float2 x = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2v, negm);
         const float2 pr = make_float2(ptx::ex2_approx(x.x), ptx::ex2_approx(x.y));
         sum[c & 1] = __fadd2_rn(sum[c & 1], pr);
-        pk[c] = pack_bf16(pr.x, pr.y);
+        u[c] = pack_bf16(pr.x, pr.y);
       }
-      ptx::tmem_store32(tS + lane_addr + h * 32, pk);
-    }
-    // P of the first half, scaled to the raised max.  TMEM loads and stores are
-    // warp-collective: the whole warp takes this branch (other lanes scale by 1).
-    if (__any_sync(0xffffffffu, a_first != 1.0f)) {
-      uint32_t q[32];
-      ptx::tmem_load32(tS + lane_addr, q);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q[c]));
-        q[c] = pack_bf16(f.x * a_first, f.y * a_first);
-      }
-      ptx::tmem_store32(tS + lane_addr, q);
+      ptx::tmem_store64(tS + lane_addr, u);
     }
     // O_T is stable here (S_T(j) completes after PV_T(j-1)); PV_T(j) waits for P below.
     if (j > 0 && __any_sync(0xffffffffu, resc)) {

@@ -1686,8 +1686,6 @@ struct akv_ctx {
         run_didx[r] = it->second;
       }
       rotate = !shifts.empty();
-      if (rotate && cfg.layout == AKV_LAYOUT_MLA)
-        fail(AKV_ERR_ARG, "fused rotation is implemented for the GQA layout; flush, then attend");
     }
     const bool mla = cfg.layout == AKV_LAYOUT_MLA;
     std::vector<akv::CombineItem> comb;

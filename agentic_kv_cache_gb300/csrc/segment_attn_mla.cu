@@ -21,8 +21,9 @@
 // Warps 0, 6, 7: TMA producers taking rounds of the key stream in turn (their
 // copies count on the even CTA's barriers); warp 1: TMEM allocation and, in
 // the even CTA, the thread issuing the QK^T MMAs; warp 8 (even CTA): the thread
-// issuing the PV MMAs; warps 2-5: softmax of the CTA's own rows.  Every wait
-// is bounded.
+// issuing the PV MMAs; warps 2-5: softmax of the CTA's own rows; warps 9-10,
+// with fused rotation only: the K_pe rotation of the CTA's key half.  Every
+// wait is bounded.
 //
 // A pair runs a list of units (persistent schedule: the engine cuts the work
 // end to end into one equal piece per resident pair, so a unit may be part
@@ -37,12 +38,14 @@
 
 #include "akv_internal.h"
 #include "attn_merge.cuh"
+#include "rope_rot.cuh"
 #include "sm100_ptx.cuh"
 
 namespace akv {
 namespace {
 
-constexpr int kThreads = 288;
+constexpr int kThreads = 352;
+constexpr int kRotWarps = 2;  // fused rotation: warps 9 and 10, one K_pe row per lane
 constexpr int kKeys = 128;     // keys per KV tile (the pair MMA's N for QK^T)
 constexpr int kRows = 128;     // rows per CTA; the pair covers 256
 constexpr int kLat = 512;      // latent width
@@ -53,7 +56,7 @@ constexpr int kPVRounds = 2;                 // one per O quarter
 // Two rings of 16 KiB slots, one per MMA thread: each ring has one consumer,
 // which takes its rounds in order, and no more producers than slots, so a
 // wait on a slot's barrier phase can never see the phase of an older use.
-constexpr int kQKSlots = 3;     // QK^T rounds, filled by warps 0 and 6 in turn
+constexpr int kQKSlots = 3;     // QK^T rounds, filled by warps 0 and 6 (by position in the tile)
 constexpr int kQKProducers = 2;
 constexpr int kPVSlots = 2;     // PV rounds, filled by warp 7
 static_assert(kQKProducers <= kQKSlots, "a ring needs at least as many slots as producers");
@@ -95,7 +98,9 @@ enum Bar {
   kBarPVd0,  // + S buffer: the PV that read P from that buffer is done
   kBarFin2 = kBarPVd0 + 2,  // the PV thread's MMAs done
   kBarProd,  // both QK^T producers have published their last round per slot (count 2)
-  kNumBars
+  kBarPeFull0,  // + QK^T slot, fused rotation: this CTA's K_pe copy landed (each CTA its own)
+  kBarRdy0 = kBarPeFull0 + kQKSlots,  // + QK^T slot, fused rotation: both CTAs' K_pe rotated (even CTA, 128 lanes)
+  kNumBars = kBarRdy0 + kQKSlots
 };
 // after the barriers: abort flag, TMEM address, the QK^T producers' last round per slot
 static_assert(kNumBars * 8 + 8 + kQKProducers * kQKSlots * 4 <= 256, "barrier area");
@@ -174,15 +179,21 @@ __device__ __forceinline__ TilePages tile_pages(const int2 (&kv)[kMaxRuns], int 
   return t;
 }
 
-// One producer thread.  pv: the PV ring (warp 7); else the QK^T ring, rounds
-// taken in turn by who = 0 (warp 0, which also loads the Q tiles) and who = 1.
+// One producer thread.  pv: the PV ring (warp 7); else the QK^T ring, whose
+// rounds are owned by position in the tile: rounds 0, 2 and K_pe by who = 0
+// (warp 0, which also loads the Q tiles), rounds 1 and 3 by who = 1, so each
+// owns a round in every 3 consecutive ones (the ring's slot count).  With
+// fused rotation each CTA's K_pe copy lands on a barrier of its own CTA (the
+// rotation warp waits there) and the ring's Full barrier takes a plain arrive
+// in its place, so its phases stay in step.
+template <bool kFused>
 __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t rank, bool pv,
                                         int who, volatile int* abort_flag, volatile int* prod_last) {
   const uint32_t bars = sbase + kBars;
   auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
   const int G = p.group, tpt = kRows / G, rpt = kKeys / p.page;
   const int rpu = p.page >= 64 ? 1 : 64 / p.page;  // runs per 64-key half
-  const int n_slots = pv ? kPVSlots : kQKSlots, stride = pv ? 1 : kQKProducers;
+  const int n_slots = pv ? kPVSlots : kQKSlots;
   const int full0 = pv ? kBarVFull0 : kBarFull0, empty0 = pv ? kBarVEmpty0 : kBarEmpty0;
   const uint32_t ring = sbase + (pv ? kVSlots : kSlots);
   const uint32_t lead_full0 = ptx::mapa(bar(full0), 0);
@@ -204,28 +215,37 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
   bool ok = true;
   // One 64-key x 64-column block: keys of half kh of local tile j (pages tp),
   // columns col of K_pe (pe) or of the latent.
-  auto copy = [&](uint32_t dst, uint32_t fb, bool pe, int kh, int col, int j, const TilePages& tp) {
+  // local: the copy completes on barrier fb of this CTA (else on the even CTA's).
+  auto copy = [&](uint32_t dst, uint32_t fb, bool pe, int kh, int col, int j, const TilePages& tp, bool local = false) {
+    auto load = [&](uint32_t d, const CUtensorMap* map, int c0, int c1, int c3) {
+      if (local)
+        ptx::tma_load_4d(d, map, fb, c0, c1, 0, c3);
+      else
+        ptx::tma_load_4d_pair(d, map, fb, c0, c1, 0, c3);
+    };
     const int pg = pe ? (kh ? tp.k1 : tp.k0) : (kh ? tp.v1 : tp.v0);
     const bool cons = (tp.cons >> ((pe ? 0 : 2) + kh)) & 1u;
     if (p.page > 64) {  // one page per tile, the block is its half kh
-      ptx::tma_load_4d_pair(dst, pe ? &p.k_tile_map : &p.v_tile_map, fb, col, 64 * kh, 0, pg);
+      load(dst, pe ? &p.k_tile_map : &p.v_tile_map, col, 64 * kh, pg);
     } else if (cons) {
-      ptx::tma_load_4d_pair(dst, pe ? &p.k_tile_map : &p.v_tile_map, fb, col, 0, 0, pg);
+      load(dst, pe ? &p.k_tile_map : &p.v_tile_map, col, 0, pg);
     } else {  // pages of the half one by one (copied pages of a fork)
       const CUtensorMap* map = pe ? &p.k_map : &p.v_map;
       for (int g = 0; g < rpu; ++g) {
         const int ri = (w.t0 + j) * rpt + kh * rpu + g;
         int2 kv = first;
         if (ri < seg.n_runs) kv = *reinterpret_cast<const int2*>(p.runs + seg.run_off + ri);
-        ptx::tma_load_4d_pair(dst + g * p.page * 128, map, fb, col, 0, 0, layer_base + (pe ? kv.x : kv.y));
+        load(dst + g * p.page * 128, map, col, 0, layer_base + (pe ? kv.x : kv.y));
       }
     }
   };
   int rd = 0;  // rounds of this ring so far, over all units
-  int last[kQKSlots] = {-1, -1, -1};  // the last round this thread issued into each slot
+  int last[kQKSlots] = {-1, -1, -1};     // the last round this thread issued into each slot
+  int last_pe[kQKSlots] = {-1, -1, -1};  // fused rotation: the last K_pe round (local barrier) per slot
   // Round m of local tile j: QK^T round m (< kQKRounds) or PV round m.
   auto round = [&](int m, int j, const TilePages& tp) {
-    if (ok && rd % stride == who) {
+    const bool mine = pv || ((m == 1 || m == 3) == (who == 1));
+    if (ok && mine) {
       const int slot = rd % n_slots, use = rd / n_slots;
       if (use >= 1 && !ptx::mbar_wait(bar(empty0 + slot), (use - 1) & 1, abort_flag, p.wait_ns)) {
         ok = false;
@@ -245,6 +265,13 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
           if (rank == 0) ptx::mbar_arrive_expect_tx(bar(full0 + slot), 2 * kSlot);
           copy(dst, fb, false, kr, 128 * m, j, tp);
           copy(dst + kUnit, fb, false, kr, 128 * m + 64, j, tp);
+        } else if (kFused) {
+          if (rank == 0) ptx::mbar_arrive(bar(full0 + slot));  // the phase only: the copy completes locally
+          ptx::mbar_arrive_expect_tx(bar(kBarPeFull0 + slot), kUnit);
+          copy(dst, bar(kBarPeFull0 + slot), true, kr, 0, j, tp, true);
+#pragma unroll
+          for (int s = 0; s < kQKSlots; ++s)
+            if (s == slot) last_pe[s] = rd;
         } else {
           if (rank == 0) ptx::mbar_arrive_expect_tx(bar(full0 + slot), 2 * kUnit);
           copy(dst, fb, true, kr, 0, j, tp);
@@ -309,6 +336,12 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
     if (rank == 0) drained = ptx::mbar_wait_drain(bar(full0 + s), parity, kDrainLimitNs) && drained;
     drained = ptx::mbar_wait_drain(bar(empty0 + s), parity, kDrainLimitNs) && drained;
   }
+  // K_pe copies of fused rotation: round 5T + 4 of tile T is the (T / 3)-th use of its slot.
+#pragma unroll
+  for (int s = 0; s < kQKSlots; ++s)
+    if (last_pe[s] >= 0)
+      drained = ptx::mbar_wait_drain(bar(kBarPeFull0 + s), uint32_t((last_pe[s] / kQKRounds) / kQKSlots) & 1u,
+                                     kDrainLimitNs) && drained;
   if (!drained) raise_error(p.err, kErrTimeout, blockIdx.x, 14, pv ? 2 : who);  // copies may still be in flight
 }
 
@@ -327,7 +360,9 @@ __device__ __forceinline__ int unit_tiles(const AttnWork& w) { return min(max(w.
 // QK^T thread.  S of global tile gt (tiles of earlier units included: the S,
 // P and O phases continue across units) goes to S buffer gt & 1, which holds
 // P(gt - 2) until that tile's PV is done.  After a unit's last QK^T MMA both
-// CTAs may reload their Q tiles.
+// CTAs may reload their Q tiles.  With fused rotation the K_pe round is read
+// once both CTAs' rotation warps have rotated it (the ready barrier).
+template <bool kFused>
 __device__ __forceinline__ void issue_qk(const AttnParams& p, int u0, int u1, uint32_t sbase, uint32_t tmem,
                                          volatile int* abort_flag) {
   const uint32_t bars = sbase + kBars;
@@ -359,7 +394,11 @@ __device__ __forceinline__ void issue_qk(const AttnParams& p, int u0, int u1, ui
 #pragma unroll 1
       for (int m = 0; m < kQKRounds; ++m, ++rd) {
         const int slot = rd % kQKSlots;
-        if (!(ok = ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kQKSlots) & 1, abort_flag, p.wait_ns))) break;
+        if (kFused && m == kQKRounds - 1)  // the (gt / 3)-th K_pe round in this slot
+          ok = ptx::mbar_wait_cl(bar(kBarRdy0 + slot), (gt / kQKSlots) & 1, abort_flag, p.wait_ns);
+        else
+          ok = ptx::mbar_wait(bar(kBarFull0 + slot), (rd / kQKSlots) & 1, abort_flag, p.wait_ns);
+        if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t kt = sbase + kSlots + slot * kSlot;
         if (m < kQKRounds - 1) {
@@ -437,6 +476,85 @@ __device__ __forceinline__ void issue_pv(const AttnParams& p, int u0, int u1, ui
   if (issued) {
     ptx::mma_commit_pair(bar(kBarFin2));
     if (!ptx::mbar_wait_drain(bar(kBarFin2), 0, kDrainLimitNs)) raise_error(p.err, kErrTimeout, blockIdx.x, 17, 0);
+  }
+}
+
+// ------------------------------------------------------------ K_pe rotation
+// Fused rotation ([Leyline] "Method": under MLA only K_pe carries position;
+// [AKV-blog] section 4: rotate keys on their way to the tensor core instead of
+// writing them back).  Two warps per CTA (part 0, 1: 32 rows each, one per
+// lane) take the K_pe round of every tile in order once their CTA's copy has
+// landed, rotate each of its 64 key rows whose run carries a pending shift by
+// R(delta * theta_j) in shared memory -- the arithmetic and angle table of
+// repos_rotate, so the bits equal the materialised key -- make the writes
+// visible to the tensor core and arrive (every lane; the odd CTA remotely) on
+// the even CTA's ready barrier.
+__device__ __forceinline__ void rotate_pe(const AttnParams& p, int u0, int u1, uint8_t* smem, uint32_t sbase,
+                                          uint32_t rank, int part, volatile int* abort_flag) {
+  const uint32_t bars = sbase + kBars;
+  auto bar = [&](int i) { return bars + 8u * uint32_t(i); };
+  const int lane = threadIdx.x % 32, rpt = kKeys / p.page;
+  int page_shift = 4;
+  while ((1 << page_shift) < p.page) ++page_shift;
+  bool ok = true;
+  int g = 0;  // tiles of earlier units
+  for (int u = u0; u < u1 && ok; ++u) {
+    const AttnWork w = p.work[2 * u + int(rank)];
+    const AttnSeg seg = p.segs[w.seg];
+    const int n = unit_tiles(w);
+    for (int j = 0; j < n; ++j) {
+      const int gt = g + j, slot = (kQKRounds * gt + kQKRounds - 1) % kQKSlots;
+      if (!(ok = ptx::mbar_wait(bar(kBarPeFull0 + slot), (gt / kQKSlots) & 1, abort_flag, p.wait_ns))) break;
+      uint8_t* tile = smem + kSlots + slot * kSlot;
+      {
+        const int row = 32 * part + lane;  // this CTA's key 64 rank + row of the tile
+        const int ri = (w.t0 + j) * rpt + ((64 * int(rank) + row) >> page_shift);
+        const int didx = ri < seg.n_runs ? p.run_didx[seg.run_off + ri] : -1;
+        if (didx >= 0) {
+        const float2* cs = p.cs + int64_t(didx) * (kPe / 2);
+        auto at = [&](int v) {  // 16-byte vector v of the row (128-byte swizzle)
+          return reinterpret_cast<uint4*>(tile + row * 128 + (((v & 7) ^ (row & 7)) << 4));
+        };
+        if (!p.rope_half) {
+#pragma unroll
+          for (int v = 0; v < kPe / 8; ++v) {  // pairs 4v .. 4v + 3
+            uint4* q = at(v);
+            const uint4 x = *q;
+            const float4 a = __ldg(reinterpret_cast<const float4*>(cs + 4 * v));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(cs + 4 * v + 2));
+            *q = make_uint4(pack_rot(rot2(x.x, a.x, a.y)), pack_rot(rot2(x.y, a.z, a.w)), pack_rot(rot2(x.z, b.x, b.y)),
+                            pack_rot(rot2(x.w, b.z, b.w)));
+          }
+        } else {
+#pragma unroll
+          for (int v = 0; v < kPe / 16; ++v) {  // dims 8v .. 8v + 7 pair with dims kPe/2 + 8v ..
+            uint4* qa = at(v);
+            uint4* qb = at(v + kPe / 16);
+            const uint4 a = *qa, b = *qb;
+            const float4* c4 = reinterpret_cast<const float4*>(cs + 8 * v);
+            const float4 c01 = __ldg(c4), c23 = __ldg(c4 + 1), c45 = __ldg(c4 + 2), c67 = __ldg(c4 + 3);
+            float2 ya[4], yb[4];
+            rot_halves(a.x, b.x, c01.x, c01.y, c01.z, c01.w, ya[0], yb[0]);
+            rot_halves(a.y, b.y, c23.x, c23.y, c23.z, c23.w, ya[1], yb[1]);
+            rot_halves(a.z, b.z, c45.x, c45.y, c45.z, c45.w, ya[2], yb[2]);
+            rot_halves(a.w, b.w, c67.x, c67.y, c67.z, c67.w, ya[3], yb[3]);
+            *qa = make_uint4(pack_rot(ya[0]), pack_rot(ya[1]), pack_rot(ya[2]), pack_rot(ya[3]));
+            *qb = make_uint4(pack_rot(yb[0]), pack_rot(yb[1]), pack_rot(yb[2]), pack_rot(yb[3]));
+          }
+        }
+        }
+      }
+      ptx::fence_proxy_async_smem();  // generic-proxy writes -> tensor-core (async proxy) reads
+      if (rank == 0)
+        ptx::mbar_arrive(bar(kBarRdy0 + slot));
+      else
+        ptx::mbar_arrive_cluster(ptx::mapa(bar(kBarRdy0 + slot), 0));
+    }
+    g += n;
+  }
+  if (!ok) {
+    raise_error(p.err, kErrTimeout, blockIdx.x, 18, 2 * int(rank) + part);
+    *abort_flag = 1;
   }
 }
 
@@ -644,6 +762,7 @@ __device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uin
   }
 }
 
+template <bool kFused>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     segment_attn_mla_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -673,7 +792,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      ptx::mbar_init(bars + 8u * i, i == kBarP ? 2 * 128 : (i == kBarProd ? kQKProducers : 1));
+      ptx::mbar_init(bars + 8u * i, i == kBarP                               ? 2 * 128
+                                    : i == kBarProd                          ? kQKProducers
+                                    : (i >= kBarRdy0 && i < kBarRdy0 + kQKSlots) ? 2 * 32 * kRotWarps
+                                                                               : 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -687,11 +809,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp == 0 || warp == 6 || warp == 7) {
-    if (lane == 0) produce(p, u0, u1, sbase, rank, warp == 7, warp == 6 ? 1 : 0, abort_flag, prod_last);
+    if (lane == 0) produce<kFused>(p, u0, u1, sbase, rank, warp == 7, warp == 6 ? 1 : 0, abort_flag, prod_last);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) issue_qk(p, u0, u1, sbase, tmem, abort_flag);
+    if (lane == 0 && rank == 0) issue_qk<kFused>(p, u0, u1, sbase, tmem, abort_flag);
   } else if (warp == 8) {
     if (lane == 0 && rank == 0) issue_pv(p, u0, u1, sbase, tmem, abort_flag);
+  } else if (warp == 9 || warp == 10) {
+    if (kFused) rotate_pe(p, u0, u1, smem, sbase, rank, warp - 9, abort_flag);
   } else {
     softmax(p, u0, u1, smem, sbase, tmem, rank, abort_flag);
   }
@@ -711,29 +835,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // wave size.  0 if the occupancy query fails.
 int segment_attn_mla_slots() {
   const int smem = int(kBytes) + 1024;
-  if (cudaFuncSetAttribute(segment_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(segment_attn_mla_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, segment_attn_mla_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, segment_attn_mla_kernel<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return 2 * clusters;
 }
 
+namespace {
+template <bool kFused>
+cudaError_t launch_mla_variant(const AttnParams& p, int grid, int smem, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(segment_attn_mla_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  segment_attn_mla_kernel<kFused><<<grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_segment_attn_mla(const AttnParams& p, cudaStream_t st) {
   if (p.n_work <= 0) return cudaSuccess;
   if (p.n_work % 2) return cudaErrorInvalidValue;  // CTA pairs
   const int grid = p.cta_units ? 2 * p.n_cta : p.n_work;  // persistent: one CTA pair per unit list
   const int smem = int(kBytes) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(segment_attn_mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  segment_attn_mla_kernel<<<grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return p.fused ? launch_mla_variant<true>(p, grid, smem, st) : launch_mla_variant<false>(p, grid, smem, st);
 }
 
 }  // namespace akv

@@ -323,6 +323,73 @@ def fused_vs_materialised(t, steps=10, warmup=3):
     return out
 
 
+def mla_fused_rotation(concurrencies=(1, 8), n_news=(16, 256), steps=4, warmup=2):
+    """The DeepSeek-V2-Lite MLA turn (27 layers) two ways: flush (K_pe of every token after the
+    splice rotated into copy-on-write pages) then attend, or akv_attend_fused (K_pe rotated in
+    shared memory inside the pair kernel, the shift left pending).  Per concurrency C and new-token
+    count: GPU time per turn from CUDA events on the stream, the attention kernel's own time and
+    algorithmic TFLOP/s."""
+    import torch
+    from agentic_kv_cache_gb300 import akv, runner, synth
+    out = {}
+    for C in concurrencies:
+        for n_new in n_news:
+            w = synth.mla_dsv2lite(concurrency=C, n_new=n_new)
+            s = w.shape
+            cfg = akv.config_from_shape(s, w.n_pages + C * (17408 // 64 + 8))
+            pools = akv.make_pools(cfg)
+            eng = akv.Engine(cfg, pools)
+            st = torch.cuda.current_stream()
+            src = runner.torch_device_kv_source(w)
+            setup = [op for op in w.ops if op[0] == "alloc" or (op[0] == "append" and op[3].startswith("prompt"))]
+            names = runner.run_ops(eng, w, kv_source=src, ops=setup, stream=st)
+            turn = [op for op in w.ops if op[0] == "splice" or (op[0] == "append" and op[3].startswith("new"))]
+            kv = {op[5] if op[0] == "splice" else op[3]: src(op[5] if op[0] == "splice" else op[3],
+                                                             op[4] if op[0] == "splice" else op[2]) for op in turn}
+            q = torch.from_numpy(synth.q_array(w)).cuda().to(torch.bfloat16)
+            o = torch.empty((q.shape[0], s.n_q_heads, s.d_v), dtype=torch.bfloat16, device="cuda")
+            prompt = next(op for op in w.ops if op[0] == "append")[2]
+
+            def step(fused):
+                br = {f"C{c}": eng.seq_fork(names[f"C{c}"], prompt) for c in range(C)}
+                runner.run_ops(eng, w, kv_source=lambda key, n: kv[key], ops=turn, names=br, stream=st)
+                if not fused:
+                    for c in range(C):
+                        eng.flush(br[f"C{c}"], stream=st)
+                segs = runner.engine_segments(w, br)
+                for layer in range(s.n_layers):
+                    eng.attend(layer, segs, q, q.shape[0], o, None, s.scale, stream=st, fused=fused)
+                for c in range(C):
+                    eng.seq_free(br[f"C{c}"])
+
+            res = {}
+            for fused in (False, True):
+                for _ in range(warmup):
+                    step(fused)
+                torch.cuda.synchronize()
+                eng.profile_enable(True)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                for _ in range(steps):
+                    step(fused)
+                b.record(st)
+                torch.cuda.synchronize()
+                stats = eng.profile_read()
+                eng.profile_enable(False)
+                assert eng.check_device_error(st) == 0
+                att, rep = stats["segment_attn"], stats["repos_rotate"]
+                res["fused" if fused else "materialised"] = {
+                    "ms_per_turn": a.elapsed_time(b) / steps,
+                    "attn_ms_per_layer": att["ms"] / max(att["launches"], 1),
+                    "attn_TFLOP/s": att["flops"] / max(att["ms"], 1e-9) / 1e9,
+                    "repos_ms_per_turn": rep["ms"] / steps,
+                }
+            out[f"C{C}_q{n_new}"] = res
+            del eng, pools
+            torch.cuda.empty_cache()
+    return out
+
+
 def compaction(steps=4, warmup=1, n_layers=32):
     """akv_compact on the post-drop branch of the 32K trajectory with every layer of a
     Llama-3.1-8B-shaped model (32 layers): ~24.5K visible tokens copied into dense pages, the
@@ -802,6 +869,7 @@ def gpu_arm(args, rank, world):
         torch.cuda.empty_cache()
         t = Turn(seed=rank, attn_split=args.attn_split, n_new=16)
         fz["turn_16_queries"] = fused_vs_materialised(t)
+        fz["mla_dsv2lite"] = mla_fused_rotation()
         line["fused_rotation"] = fz
     del t
     torch.cuda.empty_cache()
@@ -1026,7 +1094,7 @@ def main():
                     help="run only the MLA turn at concurrency C (for profiling)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the re-prefill equivalent and the MLA per-concurrency turns")
-    ap.add_argument("--only-leg", default="", choices=["", "turn32", "sessions", "branches128k"],
+    ap.add_argument("--only-leg", default="", choices=["", "turn32", "sessions", "branches128k", "mlafused"],
                     help="run only one measurement leg (for profiling): the 32-layer 32K turn, the 8 x 64K "
                          "sessions turn, or the 128K branches' attention")
     ap.add_argument("--leg-layers", type=int, default=0, help="layers of the --only-leg workload (0: full)")
@@ -1053,6 +1121,8 @@ def main():
             out = turn_all_layers(steps=args.steps, warmup=args.warmup, n_layers=L or 32)
         elif args.only_leg == "sessions":
             out = sessions_turn(steps=args.steps, warmup=args.warmup, n_layers=L or 32)
+        elif args.only_leg == "mlafused":
+            out = mla_fused_rotation(steps=args.steps, warmup=args.warmup)
         else:
             out = branches_128k(n_layers=L or 80)
         print(json.dumps(out), flush=True)

@@ -1,6 +1,7 @@
 """akv_attend_fused on the GPU: the rotation applied to K tiles inside the
 attention kernel, pending shifts left pending ([AKV-blog] section 4, keys
-rotated on their way to the tensor core instead of materialised in HBM).
+rotated on their way to the tensor core instead of materialised in HBM; under
+MLA only K_pe is rotated, [Leyline] "Method").
 
 Bars: the same as segment_batch_attn (bf16 output vs the float64 oracle on the
 oracle's materialised keys within max-abs 2e-2, LSE within 2e-2); the pools are
@@ -99,14 +100,18 @@ def test_fused_without_pending_shift_equals_attend():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-def test_fused_mla_with_pending_shift_is_refused():
-    from gpu_case import Case
+@pytest.mark.parametrize("page", [16, 64, 128])
+def test_fused_mla_spliced_session(page):
+    # MLA: K_pe of the tokens after the spliced span rotated inside the pair kernel, the latent as stored
+    import dataclasses
     w = synth.mla_dsv2lite(n_layers=1, concurrency=1, prompt=3000, span=700, stub=20, n_new=100)
-    c = Case(w)
-    c.run_ops()
-    k0 = c.pools[0].clone()
-    with pytest.raises(akv.AKVError) as e:
-        c.attend_gpu(fused=True)
-    assert e.value.code == "ARG"
-    torch.cuda.synchronize()
-    assert torch.equal(c.pools[0], k0)
+    w.shape = dataclasses.replace(w.shape, page_size=page)
+    w.n_pages = w.n_pages * 64 // page + 64  # the workload's pool is sized for 64-token pages
+    fused_case(w)
+
+
+def test_fused_mla_half_layout_and_sessions():
+    import dataclasses
+    w = synth.mla_dsv2lite(n_layers=1, concurrency=3, prompt=2500, span=600, stub=16, n_new=70)
+    w.shape = dataclasses.replace(w.shape, rope_layout="half")
+    fused_case(w)

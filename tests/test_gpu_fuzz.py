@@ -114,6 +114,12 @@ def test_random_fused_histories_match_oracle(seed):
     fused_case(random_workload(100 + seed, False, force_repos=True))
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_random_fused_mla_histories_match_oracle(seed):
+    from test_gpu_fused import fused_case
+    fused_case(random_workload(300 + seed, True, force_repos=True))
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_random_histories_attention_mass(seed):
     from test_gpu_mass import mass_case

@@ -332,9 +332,8 @@ AKV_API akv_status akv_attention_mass(akv_ctx* ctx, int32_t layer, const akv_seg
  * float32 arithmetic and (cos, sin) table as akv_flush, so its bf16 bits equal
  * the materialised key's; runs then also break where the shift changes, so
  * tile composition (and float rounding order) can differ from akv_attend.
- * GQA layout only: under MLA with pending shifts it returns AKV_ERR_ARG
- * (flush, then akv_attend).  Without pending shifts it is akv_attend without
- * the flush. */
+ * Under MLA only K_pe is rotated ([Leyline] "Method"); the latent is read as
+ * stored.  Without pending shifts it is akv_attend without the flush. */
 AKV_API akv_status akv_attend_fused(akv_ctx* ctx, int32_t layer, const akv_segment* segs, int32_t n_segs,
                             const void* q, int64_t n_q_rows, void* o, float* lse, float scale,
                             void* stream);

@@ -394,7 +394,7 @@ struct akv_ctx {
   int split_override = 0;  // 0: choose the split factor; n >= 1: use n
   int32_t corrupt_next = 0;           // checked-build test hook (akv_debug_corrupt)
   uint64_t wait_ns = 4000000000ull;  // limit of the attention kernels' bounded waits
-  int32_t load_cap = -1;              // test hook: cap on a CTA's K/V tile copies (GQA attention)
+  int32_t load_cap = -1;              // test hook: cap on a CTA's K/V copies (attention: GQA tiles, MLA rounds)
   CUtensorMap k_map{}, v_map{}, k_tile_map{}, v_tile_map{};
   bool maps_ok = false;
 

@@ -240,12 +240,19 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
     }
   };
   int rd = 0;  // rounds of this ring so far, over all units
+  // Test hook: with p.load_cap >= 0 this thread issues at most that many
+  // rounds and then stops (no error of its own); the waits for the missing
+  // rounds run out after p.wait_ns and report AKV_ERR_DEVICE_TIMEOUT.
+  int n_issued = 0;
+  bool capped = false;
   int last[kQKSlots] = {-1, -1, -1};     // the last round this thread issued into each slot
   int last_pe[kQKSlots] = {-1, -1, -1};  // fused rotation: the last K_pe round (local barrier) per slot
   // Round m of local tile j: QK^T round m (< kQKRounds) or PV round m.
   auto round = [&](int m, int j, const TilePages& tp) {
     const bool mine = pv || ((m == 1 || m == 3) == (who == 1));
-    if (ok && mine) {
+    if (ok && mine && !capped && p.load_cap >= 0 && n_issued >= p.load_cap) capped = true;
+    if (ok && mine && !capped) {
+      ++n_issued;
       const int slot = rd % n_slots, use = rd / n_slots;
       if (use >= 1 && !ptx::mbar_wait(bar(empty0 + slot), (use - 1) & 1, abort_flag, p.wait_ns)) {
         ok = false;
@@ -282,7 +289,7 @@ __device__ __forceinline__ void produce(const AttnParams& p, int u0, int u1, uin
   };
   const int n_rounds = pv ? kPVRounds : kQKRounds;
   int q_loads = 0;
-  for (int u = u0; u < u1 && ok; ++u) {
+  for (int u = u0; u < u1 && ok && !capped; ++u) {
     w = p.work[2 * u + int(rank)];
     seg = p.segs[w.seg];
     half = w.n_b;

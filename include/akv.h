@@ -456,9 +456,9 @@ AKV_API akv_status akv_set_attention_split(akv_ctx* ctx, int32_t split);
  * tensor-core work, frees its TMEM and exits, so a stuck launch reports an
  * error instead of hanging the GPU).  wait_ns: the limit of every wait in
  * later akv_attend / akv_attend_fused launches (0 restores the default,
- * 4 s).  load_cap >= 0 (GQA layout only): the copy-issuing thread of each CTA
- * issues at most that many K/V tile copies and then stops, so the waits for
- * the missing tiles run out; -1 (default) removes the cap.  A test sets a
+ * 4 s).  load_cap >= 0: each copy-issuing thread of a CTA issues at most
+ * that many K/V copies (GQA: tiles; MLA: ring rounds) and then stops, so the
+ * waits for the missing ones run out; -1 (default) removes the cap.  A test sets a
  * short limit and a cap, checks akv_check_device_error for
  * AKV_ERR_DEVICE_TIMEOUT and that the context still works after restoring
  * (0, -1).  AKV_ERR_ARG for load_cap < -1. */

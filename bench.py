@@ -1012,8 +1012,9 @@ class OracleTurn:
         self.kp[:, idx[:, 0], :, idx[:, 2]] = kb.transpose(1, 0, 2, 3)
         self.vp[:, idx[:, 1], :, idx[:, 2]] = vb.transpose(1, 0, 2, 3)
 
-    def step(self, rows):
-        """Run one turn (attention on `rows` sampled query rows); returns (seconds per full turn, parts)."""
+    def step(self, rows, offset=0):
+        """Run one turn (attention on `rows` query rows, evenly spaced from `offset`); returns (seconds
+        per full turn, parts)."""
         s, m = self.w.shape, self.model
         names = dict(self.names)
         t0 = time.perf_counter()
@@ -1033,7 +1034,11 @@ class OracleTurn:
         t0 = time.perf_counter()
         self.kernels.repos_runs(self.kp, runs, s.rope_base, s.rope_layout, out=self.kp)
         t_rep = time.perf_counter() - t0
-        sample = np.linspace(0, g["q_len"] - 1, rows).astype(np.int64)
+        stride = g["q_len"] // rows
+        if stride >= 2:  # every stride-th row from a rotating offset
+            sample = np.arange(rows, dtype=np.int64) * stride + offset % stride
+        else:            # most rows: spread evenly over the segment (later rows see more keys)
+            sample = np.linspace(0, g["q_len"] - 1, rows).astype(np.int64)
         # attention = gather of the segment's KV (once per turn) + per-row work (scaled to all rows)
         t0 = time.perf_counter()
         k = self.kernels.gather(self.kp, 0, seg_runs, 0).astype(np.float64)
@@ -1060,13 +1065,17 @@ def cpu_baseline(seconds=15.0):
             "seconds_per_turn": est, "parts": parts}
 
 
+REF_ROWS = 128  # query rows of the reference arm's attention sample per step
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
     ot = OracleTurn()
-    for _ in range(args.warmup):
-        ot.step(rows=16)
-    times = [ot.step(rows=16)[0] for _ in range(args.steps)]
+    for i in range(args.warmup):
+        ot.step(rows=REF_ROWS, offset=i)
+    # each step takes a different slice of the query rows: after 2048 / REF_ROWS steps every row was timed
+    times = [ot.step(rows=REF_ROWS, offset=args.warmup + i)[0] for i in range(args.steps)]
     total = sum(times)
     value = args.steps / total
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -1074,8 +1083,9 @@ def reference_arm(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "n/a (host)", "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": "per step: full bookkeeping and repos, attention on 16 of 2048 query rows "
-                                       "scaled to the full turn"},
+                             "sample": f"per step: full bookkeeping and repos, attention on {REF_ROWS} of 2048 query "
+                                       f"rows (every {2048 // REF_ROWS}th, offset by the step number, so successive "
+                                       f"steps time different rows) scaled to the full turn"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

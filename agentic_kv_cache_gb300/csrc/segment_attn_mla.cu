@@ -15,22 +15,22 @@
 // (M = 256, N = 128) and each CTA supplies half of its B operand: for QK^T the
 // 64 keys of its half of the 128-key tile, for PV 64 of the 128 output columns
 // of each quarter.  Per SM that halves the key bytes streamed per MMA clock;
-// a 5-slot ring of 16 KiB rounds (80 KiB) sits beside the resident 144 KiB Q
-// tile.  TMEM (allocated for the pair): S0, S1 (double-buffered, P written
-// back over the consumed S columns as bf16 pairs) and the 256-column O half.
-// Warps 0, 6, 7: TMA producers taking rounds of the key stream in turn (their
-// copies count on the even CTA's barriers); warp 1: TMEM allocation and, in
-// the even CTA, the thread issuing the QK^T MMAs; warp 8 (even CTA): the thread
-// issuing the PV MMAs; warps 2-5: softmax of the CTA's own rows; warps 9-10,
-// with fused rotation only: the K_pe rotation of the CTA's key half.  Every
-// wait is bounded.
+// two rings of 16 KiB rounds (QK^T: 3 slots, PV: 2 slots; 80 KiB) sit beside
+// the resident 144 KiB Q tile.  TMEM (allocated for the pair): S0, S1
+// (double-buffered, P written back over the consumed S columns as bf16 pairs)
+// and the 256-column O half.  Warps 0 and 6: TMA producers of the QK^T ring,
+// warp 7: of the PV ring (their copies count on the even CTA's barriers);
+// warp 1: TMEM allocation and, in the even CTA, the thread issuing the QK^T
+// MMAs; warp 8 (even CTA): the thread issuing the PV MMAs; warps 2-5: softmax
+// of the CTA's own rows; warps 9-10, with fused rotation only: the K_pe
+// rotation of the CTA's key half.  Every wait is bounded.
 //
 // A pair runs a list of units (persistent schedule: the engine cuts the work
-// end to end into one equal piece per resident pair, so a unit may be part
-// of an item whose partials the last part merges).  The ring position and the
-// S / P / O phases continue across units; after a unit's last QK^T MMA the
-// even CTA commits to both CTAs' Q-free barrier, on which each CTA reloads
-// its Q tile for the next unit.
+// end to end by the smallest per-pair budget that fits the resident pairs,
+// so a unit may be part of an item whose partials the last part merges).  The
+// ring positions and the S / P / O phases continue across units; after a
+// unit's last QK^T MMA the even CTA commits to both CTAs' Q-free barrier, on
+// which each CTA reloads its Q tile for the next unit.
 #include <cuda_bf16.h>
 
 #include <climits>

@@ -63,8 +63,8 @@ struct MLayout {
   static constexpr uint32_t kP = kSlot + kRing * kTile;    // one probability tile per query tile
   static constexpr uint32_t kPTile = 2 * kBlockBytes;      // 2 x 64-key blocks
   static constexpr uint32_t kOnes = kP + 2 * kPTile;       // one 128 x 64 block of bf16 ones
-  static constexpr uint32_t kColE = kOnes + kBlockBytes;   // int32 [2 query tiles][128]
-  static constexpr uint32_t kBars = kColE + 2 * 128 * 4;
+  static constexpr uint32_t kColE = kOnes + kBlockBytes;   // int32 [2 query tiles][2 buffers][128]
+  static constexpr uint32_t kBars = kColE + 2 * 2 * 128 * 4;
   static constexpr uint32_t kBytes = kBars + 256;
 };
 
@@ -256,7 +256,8 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
   const float lse2 = row_valid ? p.lse[int64_t(seg.q_row0 + qi) * p.hq + int64_t(w.kvh) * G + g] * 1.4426950408889634f
                                : INFINITY;
   const float2 sl2v = make_float2(p.scale_log2, p.scale_log2), neg = make_float2(-lse2, -lse2);
-  int* colE = reinterpret_cast<int*>(smem + L::kColE) + 128 * t;
+  int* const colE_base = reinterpret_cast<int*>(smem + L::kColE) + 256 * t;  // two buffers, by tile parity
+  int* colE = colE_base;
   uint8_t* P = smem + L::kP + t * L::kPTile;
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
@@ -308,11 +309,11 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
           make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
   };
   for (int j = 0; j < n && ok; ++j) {
-    ok = ptx::mbar_wait(bar(kMS0 + t), j & 1, abort_flag, kWaitLimitNs);
-    if (!ptx::bar_red_and(bar_id, 128, ok)) {
-      ok = false;
-      break;
-    }
+    // Entry and token of key column r of tile j need no score, so they are
+    // formed before S is waited for (the token lookup's latency hides behind
+    // the wait); the entries go to the buffer of this tile's parity: the other
+    // buffer may still be read by a thread finishing tile j - 1.
+    colE = colE_base + (j & 1) * 128;
     int e = INT_MAX;  // entry index of key column r of tile j
     int tok = -1;     // its logical token
     {
@@ -323,7 +324,14 @@ __device__ void m_softmax(const MassParams& p, const AttnWork& w, const AttnSeg&
       const int ri = (rg.t0 + j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
-    const bool all_valid = ptx::bar_red_and(bar_id, 128, e != INT_MAX);
+    ok = ptx::mbar_wait(bar(kMS0 + t), j & 1, abort_flag, kWaitLimitNs);
+    // One barrier per tile: every thread's S arrived and every column has an
+    // entry; only when that fails does a second one tell a time-out from masking.
+    const bool all_valid = ptx::bar_red_and(bar_id, 128, ok && e != INT_MAX);
+    if (!all_valid && !ptx::bar_red_and(bar_id, 128, ok)) {
+      ok = false;
+      break;
+    }
     ptx::tc_fence_after();
     const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
     uint32_t pk0[32], pk1[32];

@@ -64,8 +64,9 @@ void cuda_check(cudaError_t e, const char* what) {
   if (e != cudaSuccess) fail(AKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-struct Tok {
-  int32_t kp, vp, slot, pos, delta;
+struct Tok {  // 20 bytes: every pass over a sequence streams these records
+  int32_t kp, vp, pos, delta;
+  int16_t slot;  // < page_size <= 128
   uint8_t vis;
   int64_t eff() const { return int64_t(pos) + delta; }
 };
@@ -436,15 +437,22 @@ struct akv_ctx {
     if (p.size() == 1) {
       for (int64_t i = p[0].s; i < p[0].e; ++i) toks[i].delta += p[0].d;
     } else {
-      std::vector<int64_t> diff(toks.size() + 1, 0);
+      // Sweep over the spans' sorted end points: between two consecutive
+      // points every token gets the same sum of shifts; only spans with a
+      // nonzero sum are touched.
+      std::vector<std::pair<int64_t, int64_t>> ev;
+      ev.reserve(2 * p.size());
       for (const Pend& r : p) {
-        diff[size_t(r.s)] += r.d;
-        diff[size_t(r.e)] -= r.d;
+        ev.emplace_back(r.s, r.d);
+        ev.emplace_back(r.e, -int64_t(r.d));
       }
+      std::sort(ev.begin(), ev.end());
       int64_t acc = 0;
-      for (size_t i = 0; i < toks.size(); ++i) {
-        acc += diff[i];
-        if (acc) toks[i].delta += int32_t(acc);
+      for (size_t k = 0; k + 1 < ev.size(); ++k) {
+        acc += ev[k].second;
+        if (acc == 0) continue;
+        const int32_t a = int32_t(acc);
+        for (int64_t i = ev[k].first; i < ev[k + 1].first; ++i) toks[size_t(i)].delta += a;
       }
     }
     p.clear();
@@ -596,7 +604,7 @@ struct akv_ctx {
         slot = 0;
         room = cfg.page_size - 1;
       }
-      toks.push_back(Tok{kp, vp, slot, p[i], 0, 1});
+      toks.push_back(Tok{kp, vp, p[i], 0, int16_t(slot), 1});
       bound[sid] = std::max<int64_t>(bound[sid], std::abs(int64_t(p[i])));
       krow[i] = kp * cfg.page_size + slot;
       vrow[i] = vp * cfg.page_size + slot;
@@ -737,7 +745,7 @@ struct akv_ctx {
         kp = K.alloc();
         vp = V.alloc();
       }
-      stub[i] = Tok{kp, vp, slot, p[i], 0, 1};
+      stub[i] = Tok{kp, vp, p[i], 0, int16_t(slot), 1};
       krow[i] = kp * cfg.page_size + slot;
       vrow[i] = vp * cfg.page_size + slot;
     }
@@ -840,7 +848,7 @@ struct akv_ctx {
         runs.push_back(akv::CopyRun{t.kp, t.vp, dk, dv, t.slot, ds, 1, di});
       }
       const int32_t pos = int32_t(t.eff());
-      out.push_back(Tok{dk, dv, ds, pos, 0, 1});
+      out.push_back(Tok{dk, dv, pos, 0, int16_t(ds), 1});
       b = std::max<int64_t>(b, std::abs(int64_t(pos)));
     }
     for (int32_t q : kps) K.dec(q);
@@ -870,8 +878,12 @@ struct akv_ctx {
   void moving_pages(const std::vector<Tok>& toks, std::vector<int32_t>& order) {
     mk.next();
     order.clear();
+    int32_t last = -1;  // consecutive tokens mostly share their page
     for (const Tok& t : toks)
-      if (t.vis && t.delta != 0 && mk.test_set(t.kp)) order.push_back(t.kp);
+      if (t.vis && t.delta != 0 && t.kp != last) {
+        last = t.kp;
+        if (mk.test_set(t.kp)) order.push_back(t.kp);
+      }
   }
 
   void flush(const std::vector<int32_t>& ids, cudaStream_t st) {
@@ -1046,15 +1058,22 @@ struct akv_ctx {
       flat.insert(flat.end(), {c_src, c_dst, c_lo, c_hi, c_delta});
       open = false;
     };
+    int32_t last = -1, last_dst = -1;  // page of the previous token, its destination
+    bool last_copied = false;
     for (Tok& t : toks) {
-      const bool copied = mk.test(t.kp);
+      if (t.kp != last) {  // consecutive tokens mostly share their page
+        last = t.kp;
+        last_copied = mk.test(t.kp);
+        last_dst = page_dst[t.kp];  // meaningful for moving pages only
+      }
+      const bool copied = last_copied;
       const bool emit = t.vis && (t.delta != 0 || copied);
       if (!emit) {
         if (copied) mv.test_set(t.kp);  // a dropped token stays behind in the copied page
         close();
         continue;
       }
-      const int32_t d = page_dst[t.kp];  // emitted tokens sit in moving pages
+      const int32_t d = last_dst;  // emitted tokens sit in moving pages
       if (open && c_src == t.kp && c_dst == d && c_delta == t.delta && t.slot == c_hi) {
         ++c_hi;
       } else {

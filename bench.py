@@ -1104,9 +1104,10 @@ def main():
                     help="run only the MLA turn at concurrency C (for profiling)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the re-prefill equivalent and the MLA per-concurrency turns")
-    ap.add_argument("--only-leg", default="", choices=["", "turn32", "sessions", "branches128k", "mlafused"],
+    ap.add_argument("--only-leg", default="", choices=["", "turn32", "sessions", "branches128k", "mlafused", "fused32"],
                     help="run only one measurement leg (for profiling): the 32-layer 32K turn, the 8 x 64K "
-                         "sessions turn, or the 128K branches' attention")
+                         "sessions turn, the 128K branches' attention, fused vs materialised rotation on "
+                         "the MLA turn or on the 32K turn (2,048 and 16 queries)")
     ap.add_argument("--leg-layers", type=int, default=0, help="layers of the --only-leg workload (0: full)")
     ap.add_argument("--attn-split", type=int, default=0,
                     help="KV chunks per attention work item: 0 chooses automatically, 1 never splits")
@@ -1133,6 +1134,10 @@ def main():
             out = sessions_turn(steps=args.steps, warmup=args.warmup, n_layers=L or 32)
         elif args.only_leg == "mlafused":
             out = mla_fused_rotation(steps=args.steps, warmup=args.warmup)
+        elif args.only_leg == "fused32":
+            out = {"turn_2048_queries": fused_vs_materialised(Turn(seed=0), args.steps, args.warmup)}
+            torch.cuda.empty_cache()
+            out["turn_16_queries"] = fused_vs_materialised(Turn(seed=0, n_new=16), args.steps, args.warmup)
         else:
             out = branches_128k(n_layers=L or 80)
         print(json.dumps(out), flush=True)

@@ -188,6 +188,53 @@ def test_random_operations_match_oracle(seed):
         assert np.array_equal(ke, ko) and np.array_equal(ve, vo), (step, op)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_batched_repositions_fold_like_the_oracle(seed):
+    """Several repositions recorded before any read fold into the tokens at once
+    (the engine sweeps the spans' sorted end points).  Batches of 2-10 spans
+    that overlap, cancel to a zero sum over part of the sequence, share end
+    points or are empty, with drops between them, then a flush: the state
+    after the fold and the flush run list equal the oracle's, which applies
+    each reposition to its tokens one by one."""
+    rng = np.random.default_rng(700 + seed)
+    P = 16
+    cfg = dict(layout=0, n_layers=1, n_q_heads=4, n_kv_heads=1, d_rot=64, d_v=64, page_size=P, n_pages=96,
+               rope_layout=0, rope_base=1e4)
+    eng, model = akv.Engine(cfg), CacheModel(96, P)
+    s = eng.seq_alloc()
+    assert model.seq_alloc() == s
+    apply_both(eng, model, "append", (s, 600))
+    for batch in range(8):
+        n = len(model.seqs[s])
+        ends = np.sort(rng.integers(0, n + 1, size=4))  # shared end points across the batch's spans
+        for _ in range(int(rng.integers(2, 11))):
+            kind = rng.random()
+            if kind < 0.15:
+                a = int(rng.integers(0, n + 1))
+                apply_both(eng, model, "drop", (s, a, int(rng.integers(a, n + 1))))
+                continue
+            if kind < 0.5:
+                a, b = sorted(int(x) for x in rng.choice(ends, size=2))
+            else:
+                a = int(rng.integers(0, n + 1))
+                b = int(rng.integers(a, n + 1))
+            d = int(rng.integers(-700, 700))
+            apply_both(eng, model, "repos", (s, a, b, d))
+            if rng.random() < 0.3:  # the same span undone: a zero sum where nothing else covers it
+                apply_both(eng, model, "repos", (s, a, b, -d))
+        a, b = eng.export_state(s), model.state(s)
+        for k in b:
+            assert np.array_equal(a[k], np.asarray(b[k], np.int32)), (batch, k)
+        if batch % 2:
+            runs_o = model.flush([s])
+            eng.flush(s)
+            if runs_o:
+                assert np.array_equal(eng.last_flush_runs(), np.asarray(runs_o, np.int32).reshape(-1, 5))
+            a, b = eng.export_state(s), model.state(s)
+            for k in b:
+                assert np.array_equal(a[k], np.asarray(b[k], np.int32)), (batch, "flushed", k)
+
+
 @pytest.mark.parametrize("name,make", WORKLOADS, ids=[n for n, _ in WORKLOADS])
 def test_compaction_matches_oracle(name, make):
     # every live sequence compacted in turn after the workload's operations (pending shifts

@@ -75,7 +75,7 @@ constexpr uint32_t kSlots = kQ + kQChunks * kQChunk;  // QK^T ring, then PV ring
 constexpr uint32_t kVSlots = kSlots + kQKSlots * kSlot;
 constexpr uint32_t kColE = kVSlots + kPVSlots * kSlot;  // int32[2][128], by tile parity
 constexpr uint32_t kBars = kColE + 2 * 128 * 4;
-constexpr uint32_t kBytes = kBars + 256;
+constexpr uint32_t kBytes = kBars + 512;
 static_assert(kBytes + 1024 <= 232448, "shared memory");
 
 // Full and Q count both CTAs' bytes and live in the even CTA; Empty, S and O
@@ -91,9 +91,9 @@ enum Bar {
   kBarVFull0 = kBarEmpty0 + kQKSlots,  // + PV slot
   kBarVEmpty0 = kBarVFull0 + kPVSlots,
   kBarS0 = kBarVEmpty0 + kPVSlots,  // + S buffer
-  kBarP = kBarS0 + 2,
-  kBarO,
-  kBarQFree,
+  kBarP0 = kBarS0 + 2,  // + tile parity (two, so a CTA a tile ahead never completes the other's phase)
+  kBarO0 = kBarP0 + 2,  // + tile parity: PV of that tile done (O stable)
+  kBarQFree = kBarO0 + 2,
   kBarFin,   // the QK^T thread's MMAs done
   kBarPVd0,  // + S buffer: the PV that read P from that buffer is done
   kBarFin2 = kBarPVd0 + 2,  // the PV thread's MMAs done
@@ -103,7 +103,7 @@ enum Bar {
   kNumBars = kBarRdy0 + kQKSlots
 };
 // after the barriers: abort flag, TMEM address, the QK^T producers' last round per slot
-static_assert(kNumBars * 8 + 8 + kQKProducers * kQKSlots * 4 <= 256, "barrier area");
+static_assert(kNumBars * 8 + 8 + kQKProducers * kQKSlots * 4 <= 512, "barrier area");
 
 __device__ __forceinline__ void raise_error(DevErr* err, int32_t code, int a, int b, int c) {
   if (atomicCAS(&err->code, 0, code) == 0) {
@@ -452,7 +452,7 @@ __device__ __forceinline__ void issue_pv(const AttnParams& p, int u0, int u1, ui
     const int n = unit_tiles(p.work[2 * u]);
     for (int j = 0; j < n && ok; ++j) {
       const int gt = g + j;
-      if (!(ok = ptx::mbar_wait_cl(bar(kBarP), gt & 1, abort_flag, p.wait_ns))) break;
+      if (!(ok = ptx::mbar_wait_cl(bar(kBarP0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.wait_ns))) break;
       ptx::tc_fence_after();
       const uint32_t tP = tmem + 128u * (gt & 1);  // P of tile gt, packed over S
       int rd = rd0 + kPVRounds * j;  // PV ring round
@@ -470,7 +470,7 @@ __device__ __forceinline__ void issue_pv(const AttnParams& p, int u0, int u1, ui
         ptx::mma_commit_pair_mc(bar(kBarVEmpty0 + slot), kBoth);
       }
       if (!ok) break;
-      ptx::mma_commit_pair_mc(bar(kBarO), kBoth);
+      ptx::mma_commit_pair_mc(bar(kBarO0 + (gt & 1)), kBoth);
       ptx::mma_commit_pair(bar(kBarPVd0 + (gt & 1)));
     }
     g += n;
@@ -581,7 +581,8 @@ __device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uin
   int page_shift = 4;
   while ((1 << page_shift) < p.page) ++page_shift;
   const int sl_own = r & (p.page - 1);
-  const uint32_t lead_p = ptx::mapa(bar(kBarP), 0);  // P barrier of the even CTA
+  const uint32_t lead_p0 = ptx::mapa(bar(kBarP0), 0);  // P barriers of the even CTA
+  const uint32_t lead_p1 = ptx::mapa(bar(kBarP0 + 1), 0);
   bool ok = true;
   int gbase = 0;  // tiles of earlier units: the S, P and O phases continue across units
   for (int u = u0; u < u1; ++u) {
@@ -603,13 +604,9 @@ __device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uin
   for (int j = 0; j < n; ++j) {
     const int gt = gbase + j;
     const uint32_t tS = tmem + 128u * (gt & 1);
-    ok = ptx::mbar_wait(bar(kBarS0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.wait_ns);
-    if (!ptx::bar_red_and(1, 128, ok)) {
-      ok = false;
-      break;
-    }
-    // Column entries go to the buffer of this tile's parity: the other buffer
-    // may still be read by a thread finishing the previous tile.
+    // Column entries need no score, so they are formed before S is waited for;
+    // they go to the buffer of this tile's parity: the other buffer may still
+    // be read by a thread finishing the previous tile.
     int* colE = reinterpret_cast<int*>(smem + kColE) + (gt & 1) * 128;
     int e = INT_MAX;  // entry index of key column r (INT_MAX: none)
     {
@@ -619,7 +616,16 @@ __device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uin
       const int ri = (w.t0 + j + 1) * rpt + (r >> page_shift);
       run_cur = ri < seg.n_runs ? run_le[2 * ri + 1] : make_int2(0, 0);
     }
-    const bool all_valid = ptx::bar_red_and(1, 128, e != INT_MAX);
+    // One barrier per tile: every thread's S arrived (and no warp's O wait of
+    // the previous tile ran out) and every column has an entry; only when that
+    // fails does a second one tell a failure from masking, and then every
+    // thread leaves together.
+    const bool s_ok = ok && ptx::mbar_wait(bar(kBarS0 + (gt & 1)), (gt >> 1) & 1, abort_flag, p.wait_ns);
+    const bool all_valid = ptx::bar_red_and(1, 128, s_ok && e != INT_MAX);
+    if (!all_valid && !ptx::bar_red_and(1, 128, s_ok)) {
+      ok = false;
+      break;
+    }
     ptx::tc_fence_after();
     const bool need_mask = !all_valid || colE[kKeys - 1] > lim;
     const int4* ce4 = reinterpret_cast<const int4*>(colE);
@@ -683,14 +689,24 @@ __device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uin
       }
       ptx::tmem_store32(tS + lane_addr, q);
     }
-    if (j > 0) {  // O stable (PV of tile j-1 done) before any rescale
-      ok = ptx::mbar_wait(bar(kBarO), (gt - 1) & 1, abort_flag, p.wait_ns);
-      if (!ptx::bar_red_and(1, 128, ok)) {
-        ok = false;
-        break;
-      }
+    // A warp that raised its running max rescales its rows of O, which must be
+    // stable first (PV of tile j-1 done), before it arrives on P; the other
+    // warps arrive first and wait after, so P of tile j reaches the PV thread
+    // while PV of tile j-1 may still run (PV of tile j queues behind it on the
+    // same thread).  That later wait costs nothing: S of tile j+1 needs PV of
+    // tile j-1 done anyway.  O and P have one barrier per tile parity and
+    // every warp waits for every tile's O in order, so no parity wait can
+    // alias: the barrier of tile j-1 cannot complete tile j+1 before this
+    // warp arrives on P of tile j+1.  A wait that runs out leaves ok false
+    // for the next tile's barrier (or the unit's end), where every thread
+    // learns of it.
+    bool o_waited = j == 0;
+    if (j > 0 && __any_sync(0xffffffffu, resc)) {
+      const bool o_ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(kBarO0 + ((gt - 1) & 1)), ((gt - 1) >> 1) & 1,
+                                                               abort_flag, p.wait_ns));
+      o_waited = true;
       ptx::tc_fence_after();
-      if (__any_sync(0xffffffffu, resc)) {
+      if (o_ok) {  // TMEM loads / stores are warp-collective: the whole warp takes this branch
 #pragma unroll 1
         for (int c = 0; c < 256 / 32; ++c) {
           uint32_t o[32];
@@ -699,19 +715,24 @@ __device__ __forceinline__ void softmax(const AttnParams& p, int u0, int u1, uin
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
           ptx::tmem_store32(tO + lane_addr + c * 32, o);
         }
+      } else {
+        ok = false;
       }
     }
     l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
     m_run = m_use;
     ptx::tc_fence_before();
     if (rank == 0)
-      ptx::mbar_arrive(bar(kBarP));
+      ptx::mbar_arrive(bar(kBarP0 + (gt & 1)));
     else
-      ptx::mbar_arrive_cluster(lead_p);
+      ptx::mbar_arrive_cluster((gt & 1) ? lead_p1 : lead_p0);
+    if (!o_waited && !ptx::mbar_wait(bar(kBarO0 + ((gt - 1) & 1)), ((gt - 1) >> 1) & 1, abort_flag, p.wait_ns))
+      ok = false;
   }
-  if (ok && n > 0) {
-    ok = ptx::mbar_wait(bar(kBarO), (gbase + n - 1) & 1, abort_flag, p.wait_ns);
-    ok = ptx::bar_red_and(1, 128, ok);
+  if (n > 0) {  // every thread takes this barrier: ok may differ between warps here
+    const int gl = gbase + n - 1;
+    const bool o_ok = ok && ptx::mbar_wait(bar(kBarO0 + (gl & 1)), (gl >> 1) & 1, abort_flag, p.wait_ns);
+    ok = ptx::bar_red_and(1, 128, o_ok);
   }
   if (!ok) {
     raise_error(p.err, kErrTimeout, blockIdx.x, 12, 0);
@@ -799,7 +820,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      ptx::mbar_init(bars + 8u * i, i == kBarP                               ? 2 * 128
+      ptx::mbar_init(bars + 8u * i, i == kBarP0 || i == kBarP0 + 1           ? 2 * 128
                                     : i == kBarProd                          ? kQKProducers
                                     : (i >= kBarRdy0 && i < kBarRdy0 + kQKSlots) ? 2 * 32 * kRotWarps
                                                                                : 1);

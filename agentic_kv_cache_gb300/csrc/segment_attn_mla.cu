@@ -30,7 +30,11 @@
 // so a unit may be part of an item whose partials the last part merges).  The
 // ring positions and the S / P / O phases continue across units; after a
 // unit's last QK^T MMA the even CTA commits to both CTAs' Q-free barrier, on
-// which each CTA reloads its Q tile for the next unit.
+// which each CTA reloads its Q tile for the next unit.  The softmax threads
+// signal P of a tile before PV of the previous tile has completed, unless
+// their warp rescales O, so the PV thread queues consecutive PVs back to back;
+// P and O therefore have one barrier per tile parity (the CTAs of the pair may
+// be a tile apart on P).
 #include <cuda_bf16.h>
 
 #include <climits>
